@@ -1,0 +1,176 @@
+"""CPU oracle for C = alpha*A*B + beta*C (bf16 in, fp64 sum, one rounding out).
+
+TEST INFRASTRUCTURE.  Only the test suite, the package smoke check and the
+benchmark's CPU-baseline / reference leg may import this module.  The CUDA
+library never imports, links or calls it, and it shares no code with the CUDA
+library: the arithmetic lives in ``gemm_oracle.c`` (plain C, compiled with gcc)
+and this file only marshals numpy arrays into it.
+
+Every function cites the passage it follows in ``gemm_oracle.c``'s header:
+the product and layouts from the H100 work log "在 H100 上超越 cuBLAS：一份工作日志"
+(sections "Simon 博客的快速回顾" and "实验设置"), and the alpha/beta update
+from the "DeepGEMM" article, section 1.1.
+
+Parity pins for this oracle live in ``tests/test_oracle_pins.py``.  The fp32
+accumulation order of the GPU is a hardware choice; it is covered only by the
+tolerance, not by a pin ("parity unpinned" beyond the tolerance).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gemm_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_lock = threading.Lock()
+
+
+def lib_path(mutant: int = 0, build_dir: Optional[str] = None) -> str:
+    d = build_dir or _BUILD
+    name = "liboracle.so" if mutant == 0 else f"liboracle_mut{mutant}.so"
+    return os.path.join(d, name)
+
+
+def build(mutant: int = 0, build_dir: Optional[str] = None, force: bool = False) -> str:
+    """Compile the oracle with gcc (plain -O2, no fast-math, so every double
+    operation rounds as written).  Returns the path of the shared object."""
+    out = lib_path(mutant, build_dir)
+    with _lock:
+        if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
+            return out
+        os.makedirs(os.path.dirname(out), exist_ok=True)
+        tmp = out + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+               "-fno-fast-math", "-ffp-contract=off",
+               f"-DORACLE_MUTANT={int(mutant)}", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, out)
+    return out
+
+
+class Oracle:
+    """ctypes view of one compiled oracle (the real one or a planted mutant)."""
+
+    def __init__(self, path: str):
+        self.path = path
+        L = ctypes.CDLL(path)
+        i64, p = ctypes.c_int64, ctypes.c_void_p
+        L.oracle_gemm_f64.argtypes = [i64, i64, i64, p, i64, p, i64, p, i64, ctypes.c_int,
+                                      ctypes.c_float, ctypes.c_float, p, ctypes.c_int]
+        L.oracle_gemm_f64.restype = ctypes.c_int
+        L.oracle_gemm_sampled_f64.argtypes = [i64, i64, i64, p, i64, p, i64, p, i64, ctypes.c_int,
+                                              ctypes.c_float, ctypes.c_float, i64, p, p, p]
+        L.oracle_gemm_sampled_f64.restype = ctypes.c_int
+        L.oracle_round_bf16.argtypes = [ctypes.c_double]
+        L.oracle_round_bf16.restype = ctypes.c_uint16
+        L.oracle_round_bf16_array.argtypes = [p, p, i64]
+        L.oracle_round_f32_array.argtypes = [p, p, i64]
+        L.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+        L.oracle_bf16_to_double.restype = ctypes.c_double
+        L.oracle_threads.argtypes = [ctypes.c_int]
+        L.oracle_threads.restype = ctypes.c_int
+        L.oracle_mutant_id.restype = ctypes.c_int
+        self._L = L
+
+    # -- helpers -------------------------------------------------------------
+    @staticmethod
+    def _ptr(a: Optional[np.ndarray]):
+        return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+    @staticmethod
+    def _cin(C_in, beta):
+        # C_in is handed to the C code whenever the caller supplies it; the C
+        # code itself decides (by the definition) not to read it when beta == 0.
+        if C_in is None:
+            return None, 0, 0
+        C_in = np.ascontiguousarray(C_in)
+        if C_in.dtype == np.uint16:
+            return C_in, C_in.shape[1], 1
+        if C_in.dtype == np.float32:
+            return C_in, C_in.shape[1], 0
+        raise TypeError("C_in must be float32 or bf16 bits (uint16)")
+
+    @property
+    def mutant(self) -> int:
+        return self._L.oracle_mutant_id()
+
+    def threads(self, n: int = 0) -> int:
+        return self._L.oracle_threads(n)
+
+    # -- the definition --------------------------------------------------------
+    def gemm_f64(self, M: int, N: int, K: int, A: np.ndarray, B: np.ndarray,
+                 C_in: Optional[np.ndarray] = None, alpha: float = 1.0, beta: float = 0.0,
+                 threads: int = 0) -> np.ndarray:
+        """D = alpha*A*B + beta*C_in in fp64.
+
+        A: uint16 bf16 bits, shape (M, lda).  B: uint16, shape (N, ldb) (column
+        j of B is row j).  C_in: (N, ldc) float32 or uint16 bf16 bits.
+        Returns D as an (N, M) float64 array: D_arr[j, i] = D[i, j].
+        """
+        A = np.ascontiguousarray(A, dtype=np.uint16)
+        B = np.ascontiguousarray(B, dtype=np.uint16)
+        assert A.shape[0] == M and B.shape[0] == N
+        lda = A.shape[1] if A.ndim == 2 else K
+        ldb = B.shape[1] if B.ndim == 2 else K
+        cin, ldc, cin_bf16 = self._cin(C_in, beta)
+        D = np.empty((N, M), dtype=np.float64)
+        rc = self._L.oracle_gemm_f64(M, N, K, self._ptr(A), lda, self._ptr(B), ldb,
+                                     self._ptr(cin), max(ldc, M), cin_bf16,
+                                     float(alpha), float(beta), self._ptr(D), int(threads))
+        if rc != 0:
+            raise ValueError("oracle_gemm_f64: bad arguments")
+        return D
+
+    def gemm_sampled_f64(self, M: int, N: int, K: int, A: np.ndarray, B: np.ndarray,
+                         rows: np.ndarray, cols: np.ndarray,
+                         C_in: Optional[np.ndarray] = None, alpha: float = 1.0,
+                         beta: float = 0.0) -> np.ndarray:
+        A = np.ascontiguousarray(A, dtype=np.uint16)
+        B = np.ascontiguousarray(B, dtype=np.uint16)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        cols = np.ascontiguousarray(cols, dtype=np.int64)
+        cin, ldc, cin_bf16 = self._cin(C_in, beta)
+        out = np.empty(rows.shape[0], dtype=np.float64)
+        rc = self._L.oracle_gemm_sampled_f64(M, N, K, self._ptr(A), A.shape[1], self._ptr(B),
+                                             B.shape[1], self._ptr(cin), max(ldc, M), cin_bf16,
+                                             float(alpha), float(beta), rows.shape[0],
+                                             self._ptr(rows), self._ptr(cols), self._ptr(out))
+        if rc != 0:
+            raise ValueError("oracle_gemm_sampled_f64: bad arguments")
+        return out
+
+    def round_bf16(self, d: np.ndarray) -> np.ndarray:
+        d = np.ascontiguousarray(d, dtype=np.float64)
+        out = np.empty(d.shape, dtype=np.uint16)
+        self._L.oracle_round_bf16_array(self._ptr(d), self._ptr(out), d.size)
+        return out
+
+    def round_f32(self, d: np.ndarray) -> np.ndarray:
+        d = np.ascontiguousarray(d, dtype=np.float64)
+        out = np.empty(d.shape, dtype=np.float32)
+        self._L.oracle_round_f32_array(self._ptr(d), self._ptr(out), d.size)
+        return out
+
+    def round_out(self, d: np.ndarray, out_dtype: int) -> np.ndarray:
+        """out_dtype 0 -> float32 array, 1 -> uint16 bf16 bits."""
+        return self.round_f32(d) if out_dtype == 0 else self.round_bf16(d)
+
+    def bf16_to_double(self, bits: int) -> float:
+        return self._L.oracle_bf16_to_double(bits)
+
+
+_default: Optional[Oracle] = None
+
+
+def get() -> Oracle:
+    """The real (unmutated) oracle, compiled on first use."""
+    global _default
+    if _default is None:
+        _default = Oracle(build())
+    return _default

@@ -1,0 +1,244 @@
+/*
+ * CPU oracle for the bf16 GEMM  C_out = alpha * A * B + beta * C_in.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
+ * definition that the CUDA library is checked against.  It shares no code,
+ * header, table or constant with the CUDA library, and only the tests, the
+ * package's smoke check and the benchmark's CPU-baseline leg may load it.
+ *
+ * What it computes (the definition, written out):
+ *
+ *   S[i,j]     = sum_{k=0}^{K-1} A[i,k] * B[k,j]            (k ascending, fp64)
+ *   D[i,j]     = alpha * S[i,j] + beta * C_in[i,j]          (fp64; the beta
+ *                term is skipped entirely when beta == 0, so C_in is not read)
+ *   C_out[i,j] = round_out(D[i,j])                          (one rounding)
+ *
+ * Sources:
+ *  - The product C[m,n] = A[m,k] x B[k,n] and the layouts -- A row-major,
+ *    B and C column-major, bf16 -- are from the H100 work log
+ *    "在 H100 上超越 cuBLAS：一份工作日志", sections "Simon 博客的快速回顾"
+ *    (recap of the blocked GEMM structure) and "实验设置" (experimental
+ *    setup).
+ *  - The alpha/beta form C = alpha*A*B + beta*C is from the "DeepGEMM"
+ *    article (demingchina.com), section 1.1; its extracted formula lost the
+ *    "=" and "+" signs, and we read it as the standard BLAS update.
+ *  - fp32 accumulation of low-precision products is the precision contract of
+ *    the same article, section 3.1; the oracle accumulates in fp64, which is
+ *    at least as accurate, so the GPU's fp32 sum is compared against the
+ *    exact-up-to-fp64 value.
+ *
+ * Indexing: A[i,k] = A[i*lda + k], B[k,j] = B[j*ldb + k], C[i,j] = C[j*ldc + i].
+ * bf16 values are the upper 16 bits of an IEEE binary32 and decode exactly to
+ * double.  Every product of two bf16 values is exact in double.
+ *
+ * round_out: fp32 output rounds the double to nearest-even binary32; bf16
+ * output rounds the double directly (once) to nearest-even bf16.
+ *
+ * Planted mistakes: when compiled with -DORACLE_MUTANT=n (n > 0) one
+ * deliberate error is switched on.  The test suite builds these variants to
+ * prove that its pins catch every such error; the normal build has n = 0.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+
+/* ---- number formats --------------------------------------------------- */
+
+/* bf16 -> double: bf16 is the upper half of a binary32, so widening the bit
+ * pattern gives the exact float, and float -> double is exact. */
+static double bf16_to_double(uint16_t h) {
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+double oracle_bf16_to_double(uint16_t h) { return bf16_to_double(h); }
+
+/* double -> bf16, round to nearest, ties to even, in one step.
+ * bf16 has 8 exponent bits (like binary32) and 7 stored fraction bits, so the
+ * spacing of representable values in the binade [2^e, 2^(e+1)) is 2^(e-7),
+ * and below the smallest normal 2^-126 the spacing stays 2^-133.  Dividing by
+ * that spacing is an exact power-of-two scaling; nearbyint() in the default
+ * rounding mode rounds to the nearest integer with ties to even. */
+uint16_t oracle_round_bf16(double x) {
+    if (isnan(x)) return (uint16_t)(signbit(x) ? 0xFFC0u : 0x7FC0u);
+    if (isinf(x)) return (uint16_t)(signbit(x) ? 0xFF80u : 0x7F80u);
+    if (x == 0.0) return (uint16_t)(signbit(x) ? 0x8000u : 0x0000u);
+    int e;
+    (void)frexp(fabs(x), &e);       /* |x| = m * 2^e, m in [0.5, 1)      */
+    int lead = e - 1;               /* 2^lead <= |x| < 2^(lead+1)        */
+    if (lead < -126) lead = -126;   /* subnormal range: fixed spacing    */
+    double q = ldexp(1.0, lead - 7);
+#if ORACLE_MUTANT == 7
+    double r = trunc(x / q) * q;    /* planted: truncation instead of RNE */
+#else
+    double r = nearbyint(x / q) * q;
+#endif
+    if (fabs(r) >= ldexp(1.0, 128)) /* beyond the largest finite bf16    */
+        return (uint16_t)(signbit(x) ? 0xFF80u : 0x7F80u);
+    float f = (float)r;             /* exact: r has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
+/* double -> binary32, round to nearest even (C's conversion in the default
+ * rounding mode). */
+float oracle_round_f32(double x) { return (float)x; }
+
+void oracle_round_bf16_array(const double* x, uint16_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_round_bf16(x[i]);
+}
+
+void oracle_round_f32_array(const double* x, float* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_round_f32(x[i]);
+}
+
+/* ---- one output element ------------------------------------------------ */
+
+typedef struct {
+    int64_t M, N, K;
+    const uint16_t* A; int64_t lda;
+    const uint16_t* B; int64_t ldb;
+    const void* Cin; int64_t ldc; int cin_bf16; /* C_in dtype: 0 fp32, 1 bf16 */
+    double alpha, beta;
+} problem_t;
+
+static double c_in_at(const problem_t* p, int64_t i, int64_t j) {
+#if ORACLE_MUTANT == 8
+    int64_t idx = i * p->N + j;     /* planted: C_in read row-major */
+#else
+    int64_t idx = j * p->ldc + i;
+#endif
+    if (p->cin_bf16) return bf16_to_double(((const uint16_t*)p->Cin)[idx]);
+    return (double)((const float*)p->Cin)[idx];
+}
+
+static double element(const problem_t* p, int64_t i, int64_t j) {
+#if ORACLE_MUTANT == 10
+    float s = 0.0f;                 /* planted: fp32 accumulation */
+#else
+    double s = 0.0;
+#endif
+#if ORACLE_MUTANT == 5
+    const int64_t kend = p->K > 0 ? p->K - 1 : 0;   /* planted: drops the last term */
+#else
+    const int64_t kend = p->K;
+#endif
+    for (int64_t k = 0; k < kend; ++k) {
+#if ORACLE_MUTANT == 1
+        double a = bf16_to_double(p->A[k * p->M + i]);   /* planted: A as column-major */
+#else
+        double a = bf16_to_double(p->A[i * p->lda + k]);
+#endif
+#if ORACLE_MUTANT == 2
+        double b = bf16_to_double(p->B[k * p->N + j]);   /* planted: B as row-major */
+#else
+        double b = bf16_to_double(p->B[j * p->ldb + k]);
+#endif
+        s += a * b;
+    }
+#if ORACLE_MUTANT == 4
+    double d = p->beta * (double)s;                     /* planted: alpha and beta swapped */
+    if (p->beta != 0.0) d += p->alpha * c_in_at(p, i, j);
+#elif ORACLE_MUTANT == 3
+    double d = p->alpha * (double)s;                    /* planted: beta term dropped */
+#elif ORACLE_MUTANT == 6
+    double d = p->alpha * (double)s;                    /* planted: wrong sign */
+    if (p->beta != 0.0) d -= p->beta * c_in_at(p, i, j);
+#elif ORACLE_MUTANT == 9
+    double d = p->alpha * (double)s;                    /* planted: reads C even when beta == 0 */
+    if (p->Cin != NULL) d += p->beta * c_in_at(p, i, j);
+#else
+    double d = p->alpha * (double)s;
+    if (p->beta != 0.0) d += p->beta * c_in_at(p, i, j);
+#endif
+    return d;
+}
+
+/* ---- full matrix, threaded over columns ------------------------------- */
+
+typedef struct {
+    const problem_t* p;
+    int64_t j0, j1;
+    double* D; /* column-major, leading dimension M */
+} job_t;
+
+static void* run_columns(void* arg) {
+    job_t* job = (job_t*)arg;
+    const problem_t* p = job->p;
+    for (int64_t j = job->j0; j < job->j1; ++j)
+        for (int64_t i = 0; i < p->M; ++i)
+            job->D[j * p->M + i] = element(p, i, j);
+    return NULL;
+}
+
+static int pick_threads(int nthreads, int64_t units) {
+    if (nthreads <= 0) {
+        long n = sysconf(_SC_NPROCESSORS_ONLN);
+        nthreads = n > 0 ? (int)n : 1;
+    }
+    if (nthreads > 256) nthreads = 256;
+    if ((int64_t)nthreads > units) nthreads = (int)(units > 0 ? units : 1);
+    return nthreads;
+}
+
+int oracle_threads(int nthreads) { return pick_threads(nthreads, 1 << 30); }
+
+/* D (column-major M x N, leading dimension M) = alpha*A*B + beta*C_in in fp64.
+ * Returns 0 on success, -1 on a bad argument. */
+int oracle_gemm_f64(int64_t M, int64_t N, int64_t K,
+                    const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                    const void* Cin, int64_t ldc, int cin_bf16,
+                    float alpha, float beta, double* D, int nthreads) {
+    if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || ldc < M) return -1;
+    if (beta != 0.0f && Cin == NULL) return -1;
+    problem_t p = {M, N, K, A, lda, B, ldb, Cin, ldc, cin_bf16, (double)alpha, (double)beta};
+    if (M == 0 || N == 0) return 0;
+    int nt = pick_threads(nthreads, N);
+    pthread_t tid[256];
+    int spawned[256];
+    job_t jobs[256];
+    int64_t per = (N + nt - 1) / nt;
+    for (int t = 0; t < nt; ++t) {
+        jobs[t].p = &p;
+        jobs[t].j0 = t * per < N ? t * per : N;
+        jobs[t].j1 = (t + 1) * per < N ? (t + 1) * per : N;
+        jobs[t].D = D;
+        spawned[t] = 0;
+        if (t < nt - 1 && pthread_create(&tid[t], NULL, run_columns, &jobs[t]) == 0)
+            spawned[t] = 1;
+        else
+            run_columns(&jobs[t]);  /* the last slice, or a failed spawn, runs here */
+    }
+    for (int t = 0; t < nt; ++t)
+        if (spawned[t]) pthread_join(tid[t], NULL);
+    return 0;
+}
+
+/* The same definition at selected (row, col) positions only. */
+int oracle_gemm_sampled_f64(int64_t M, int64_t N, int64_t K,
+                            const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                            const void* Cin, int64_t ldc, int cin_bf16,
+                            float alpha, float beta,
+                            int64_t count, const int64_t* rows, const int64_t* cols,
+                            double* out) {
+    if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || ldc < M) return -1;
+    if (beta != 0.0f && Cin == NULL) return -1;
+    problem_t p = {M, N, K, A, lda, B, ldb, Cin, ldc, cin_bf16, (double)alpha, (double)beta};
+    for (int64_t s = 0; s < count; ++s) {
+        if (rows[s] < 0 || rows[s] >= M || cols[s] < 0 || cols[s] >= N) return -1;
+        out[s] = element(&p, rows[s], cols[s]);
+    }
+    return 0;
+}
+
+int oracle_mutant_id(void) { return ORACLE_MUTANT; }

@@ -1,0 +1,73 @@
+"""Comparison rules shared by the parity tests.
+
+* fp32 output: |C - C_ref| <= 1e-3 * sqrt(K) * max(1, |C_ref|), elementwise.
+* bf16 output: the two bit patterns, mapped to an ordered integer line, are at
+  most 1 apart (within one bf16 ulp of the oracle's single rounding).
+* Integer-valued inputs: bit-exact.
+
+C_ref is the oracle's fp64 value D (for fp32 output) or its bf16 rounding.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def bf16_ordered(bits: np.ndarray) -> np.ndarray:
+    """Map bf16 bit patterns to integers that increase with the value.
+    +0 and -0 both map to 0; negative values map below zero."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.int32)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def bf16_ulp_distance(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
+    return np.abs(bf16_ordered(a_bits) - bf16_ordered(b_bits))
+
+
+def f32_tolerance(ref: np.ndarray, K: int) -> np.ndarray:
+    return 1e-3 * np.sqrt(max(K, 1)) * np.maximum(1.0, np.abs(ref))
+
+
+def check_f32(got: np.ndarray, ref_f64: np.ndarray, K: int, what: str = "") -> None:
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref_f64, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    if got.size == 0:
+        return
+    err = np.abs(got - ref)
+    tol = f32_tolerance(ref, K)
+    bad = ~(err <= tol)  # NaN counts as bad
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError(f"{what}: {int(bad.sum())} of {got.size} fp32 outputs out of "
+                             f"tolerance; first {idx.tolist()} got {got[bad][:5]} ref {ref[bad][:5]}")
+
+
+def check_bf16(got_bits: np.ndarray, ref_bits: np.ndarray, what: str = "", max_ulp: int = 1) -> None:
+    got_bits = np.asarray(got_bits, dtype=np.uint16)
+    ref_bits = np.asarray(ref_bits, dtype=np.uint16)
+    assert got_bits.shape == ref_bits.shape
+    if got_bits.size == 0:
+        return
+    d = bf16_ulp_distance(got_bits, ref_bits)
+    bad = d > max_ulp
+    nan_got = (got_bits & 0x7FFF) > 0x7F80
+    bad |= nan_got
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError(f"{what}: {int(bad.sum())} of {got_bits.size} bf16 outputs more than "
+                             f"{max_ulp} ulp away; first {idx.tolist()} got "
+                             f"{[hex(x) for x in got_bits[bad][:5]]} ref {[hex(x) for x in ref_bits[bad][:5]]}")
+
+
+def check_exact(got: np.ndarray, ref: np.ndarray, what: str = "") -> None:
+    got = np.asarray(got)
+    ref = np.asarray(ref)
+    if got.dtype == np.uint16 or ref.dtype == np.uint16:
+        eq = got.astype(np.uint16) == ref.astype(np.uint16)
+    else:
+        eq = got.astype(np.float64) == ref.astype(np.float64)
+    if not eq.all():
+        idx = np.argwhere(~eq)[:5]
+        raise AssertionError(f"{what}: {int((~eq).sum())} of {got.size} outputs not bit-exact; "
+                             f"first {idx.tolist()} got {got[~eq][:5]} ref {ref[~eq][:5]}")

@@ -1,0 +1,256 @@
+"""Pins for the CPU oracle: checks against facts fixed by the pages' definition
+and by mathematics, not by the oracle itself.
+
+The pages print no worked numerical example, so the pins are:
+  * exact brute force with Python integers on integer-valued bf16 inputs,
+  * numpy's float64 matmul (an independent library routine) on N(0,1) inputs,
+  * identity and permutation matrices, all-ones and rank-1 closed forms,
+  * the bf16 rounding table in tests/golden/bf16_encodings.txt, derived by
+    hand from the bf16 format, plus torch's fp32 -> bf16 conversion where the
+    value is exactly a float,
+  * beta == 0 never reading C, K == 0, and the N(0, K) statistics of the
+    product of N(0,1) matrices.
+
+Each pin is a plain function of an ``Oracle`` so that ``test_planted_mistakes``
+can run the same pins against oracle builds with one deliberate error each
+and show that every error is caught.
+"""
+from __future__ import annotations
+
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import gemm_inputs as gi
+import oracle as oracle_mod
+from tests import parity
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _u16(t):
+    return gi.as_u16(t)
+
+
+def _cin_np(case):
+    if case.C_in is None:
+        return None
+    if case.C_in.dtype == torch.bfloat16:
+        return _u16(case.C_in)
+    return case.C_in.numpy()
+
+
+def _as_int(bits: np.ndarray) -> np.ndarray:
+    """Integer-valued bf16 bits -> Python-int object array, decoded by the
+    format (no oracle code): value = (-1)^s * 1.f * 2^(e-127)."""
+    out = np.empty(bits.shape, dtype=object)
+    flat = bits.reshape(-1)
+    res = out.reshape(-1)
+    for n, b in enumerate(flat):
+        b = int(b)
+        s, e, f = b >> 15, (b >> 7) & 0xFF, b & 0x7F
+        if e == 0 and f == 0:
+            v = Fraction(0)
+        else:
+            v = Fraction(128 + f, 128) * (Fraction(2) ** (e - 127))
+        res[n] = -v if s else v
+    return out
+
+
+def _run(o, case):
+    return o.gemm_f64(case.M, case.N, case.K, _u16(case.A), _u16(case.B), _cin_np(case),
+                      case.alpha, case.beta)
+
+
+# ---------------------------------------------------------------- pins ------
+
+def pin_integer_bruteforce(o):
+    """Integer inputs: every product and partial sum is an exact integer, so
+    the oracle's D must equal the exact rational alpha*sum + beta*C."""
+    shapes = [(5, 7, 9, 1.0, 0.0), (3, 2, 17, 2.0, 0.5), (6, 4, 3, -1.5, 0.5),
+              (1, 9, 12, 1.0, -2.0), (9, 1, 1, 0.25, 1.0)]
+    for n, (M, N, K, alpha, beta) in enumerate(shapes):
+        case = gi.make_case(f"int{n}", M, N, K, alpha=alpha, beta=beta, out_dtype=gi.OUT_F32,
+                            seed=100 + n, kind="integer", lda=K + 3, ldb=K + 5, ldc=M + 2)
+        D = _run(o, case)
+        A = _as_int(_u16(case.A)[:, :K])
+        B = _as_int(_u16(case.B)[:, :K])  # row j = column j of B
+        Cin = None if case.C_in is None else case.C_in.numpy()
+        for i in range(M):
+            for j in range(N):
+                s = sum((A[i, k] * B[j, k] for k in range(K)), Fraction(0))
+                want = Fraction(alpha) * s
+                if beta != 0.0:
+                    want += Fraction(beta) * Fraction(float(Cin[j, i]))
+                assert D[j, i] == float(want), (n, i, j, D[j, i], want)
+
+
+def pin_numpy_f64(o):
+    """N(0,1) inputs: numpy's float64 matmul computes the same sum in another
+    order; the two agree within the fp64 summation error bound."""
+    M, N, K = 37, 29, 300
+    case = gi.make_case("np", M, N, K, alpha=1.25, beta=0.5, out_dtype=gi.OUT_F32, seed=7,
+                        lda=K + 8, ldb=K + 16, ldc=M + 3)
+    D = _run(o, case)
+    A = case.A[:, :K].to(torch.float64).numpy()
+    B = case.B[:, :K].to(torch.float64).numpy()
+    C = case.C_in[:, :M].to(torch.float64).numpy()
+    ref = 1.25 * (B @ A.T) + 0.5 * C            # (N, M) layout, like D
+    bound = 2 * K * 2.0 ** -52 * (np.abs(B) @ np.abs(A).T) * 1.25 + 1e-300
+    assert np.all(np.abs(D - ref) <= bound + 2.0 ** -52 * np.abs(ref)), np.max(np.abs(D - ref))
+
+
+def pin_identity_and_permutation(o):
+    """A = I gives D = B exactly; B = I gives A laid out column-major; a row
+    permutation of I permutes the rows of B."""
+    K = 24
+    Bcase = gi.make_case("b", K, 11, K, seed=3, out_dtype=gi.OUT_F32, lda=K, ldb=K + 8)
+    eye = torch.eye(K, dtype=torch.bfloat16)
+    D = o.gemm_f64(K, 11, K, _u16(eye), _u16(Bcase.B))
+    B64 = Bcase.B[:, :K].to(torch.float64).numpy()     # (N, K): B64[j, k] = B[k, j]
+    assert np.array_equal(D, B64)                      # D[j, i] = B[i, j]
+    Acase = gi.make_case("a", 13, K, K, seed=4, out_dtype=gi.OUT_F32, lda=K + 8, ldb=K)
+    D = o.gemm_f64(13, K, K, _u16(Acase.A), _u16(eye))
+    A64 = Acase.A[:, :K].to(torch.float64).numpy()     # (M, K)
+    assert np.array_equal(D, A64.T)                    # D[j, i] = A[i, j]
+    perm = np.random.default_rng(5).permutation(K)
+    P = torch.zeros((K, K), dtype=torch.bfloat16)
+    P[np.arange(K), perm] = 1.0                        # P[i, perm[i]] = 1
+    D = o.gemm_f64(K, 11, K, _u16(P), _u16(Bcase.B))
+    assert np.array_equal(D, B64[:, perm])             # D[i, j] = B[perm[i], j]
+
+
+def pin_closed_forms(o):
+    """All-ones: D = alpha*K + beta*C.  Rank one: A[i,k] = u_i w_k,
+    B[k,j] = w_k v_j gives D = u_i v_j sum_k w_k^2 (all small powers of two,
+    so exact)."""
+    M, N, K = 7, 5, 33
+    ones_a = torch.ones((M, K), dtype=torch.bfloat16)
+    ones_b = torch.ones((N, K), dtype=torch.bfloat16)
+    C = gi.integer_out(N, M, 9, gi.OUT_F32)
+    D = o.gemm_f64(M, N, K, _u16(ones_a), _u16(ones_b), C.numpy(), 3.0, -0.5)
+    assert np.array_equal(D, 3.0 * K - 0.5 * C.numpy().astype(np.float64))
+    u = np.array([1, -2, 4, 0.5, -1, 8, 2], dtype=np.float64)
+    v = np.array([2, 1, -0.25, 4, -1], dtype=np.float64)
+    w = np.array([(-1) ** k * 2.0 ** (k % 5 - 2) for k in range(K)])
+    A = torch.tensor(np.outer(u, w), dtype=torch.bfloat16)
+    B = torch.tensor(np.outer(v, w), dtype=torch.bfloat16)  # row j = column j
+    D = o.gemm_f64(M, N, K, _u16(A), _u16(B))
+    assert np.array_equal(D, np.outer(v, u) * float(np.sum(w * w)))
+
+
+def pin_bf16_rounding(o):
+    """One RNE rounding from double straight to bf16: hand-derived table,
+    then torch's fp32 -> bf16 conversion on values that are exactly floats."""
+    path = os.path.join(GOLDEN, "bf16_encodings.txt")
+    for line in open(path):
+        line = line.split("#")[0].split()
+        if not line:
+            continue
+        x, want = float.fromhex(line[0]), int(line[1], 16)
+        got = int(o.round_bf16(np.array([x]))[0])
+        assert got == want, (line[0], hex(got), hex(want))
+    vals = torch.randn(20000, generator=torch.Generator().manual_seed(11)) * 1000
+    vals = torch.cat([vals, torch.randn(5000, generator=torch.Generator().manual_seed(12)) * 1e-38])
+    want = vals.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = o.round_bf16(vals.to(torch.float64).numpy())
+    assert np.array_equal(got, want)
+    f = o.round_f32(np.array([1.0 + 2.0 ** -24, 1.0 + 3 * 2.0 ** -24, 1e39]))
+    assert f[0] == np.float32(1.0) and f[1] == np.float32(1.0 + 2.0 ** -22) and np.isinf(f[2])
+
+
+def pin_beta_zero_ignores_c(o):
+    """beta == 0: C_in is not read, so a C full of NaN leaves no trace."""
+    case = gi.make_case("nan", 9, 6, 20, seed=13, out_dtype=gi.OUT_F32)
+    C = np.full((6, 9), np.nan, dtype=np.float32)
+    D = o.gemm_f64(9, 6, 20, _u16(case.A), _u16(case.B), C, 1.0, 0.0)
+    assert np.all(np.isfinite(D))
+    D0 = o.gemm_f64(9, 6, 20, _u16(case.A), _u16(case.B))
+    assert np.array_equal(D, D0)
+
+
+def pin_k_zero(o):
+    """K == 0: the empty sum is 0, so D = beta * C_in."""
+    C = gi.integer_out(4, 3, 17, gi.OUT_F32).numpy()
+    A = np.zeros((3, 8), dtype=np.uint16)
+    B = np.zeros((4, 8), dtype=np.uint16)
+    D = o.gemm_f64(3, 4, 0, A, B, C, 1.0, 0.5)
+    assert np.array_equal(D, 0.5 * C.astype(np.float64))
+    assert np.array_equal(o.gemm_f64(3, 4, 0, A, B), np.zeros((4, 3)))
+
+
+def pin_statistics(o):
+    """A, B with i.i.d. N(0,1) entries: each entry of A*B has mean 0 and
+    variance K, so the sample standard deviation is close to sqrt(K)."""
+    case = gi.make_case("st", 192, 160, 256, seed=19, out_dtype=gi.OUT_F32)
+    D = _run(o, case)
+    assert abs(D.std() / np.sqrt(256) - 1.0) < 0.03, D.std()
+    assert abs(D.mean()) < 0.1 * np.sqrt(256)
+
+
+def pin_sampled_matches_full(o):
+    """The per-entry routine and the full routine evaluate the same
+    definition; at sampled positions they agree bit for bit, and the rounding
+    routine agrees with the full output."""
+    case = gi.make_case("smp", 33, 47, 70, alpha=0.75, beta=-1.0, seed=23, out_dtype=gi.OUT_BF16,
+                        lda=72, ldb=80, ldc=40)
+    D = _run(o, case)
+    rows, cols = gi.sample_indices(33, 47, 50, 1)
+    s = o.gemm_sampled_f64(33, 47, 70, _u16(case.A), _u16(case.B), rows, cols, _cin_np(case),
+                           case.alpha, case.beta)
+    assert np.array_equal(s, D[cols, rows])
+
+
+PINS = [pin_integer_bruteforce, pin_numpy_f64, pin_identity_and_permutation, pin_closed_forms,
+        pin_bf16_rounding, pin_beta_zero_ignores_c, pin_k_zero, pin_statistics,
+        pin_sampled_matches_full]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(oracle_lib, pin):
+    pin(oracle_lib)
+
+
+MUTANTS = {
+    1: "A read as column-major",
+    2: "B read as row-major",
+    3: "beta term dropped",
+    4: "alpha and beta swapped",
+    5: "last k term dropped",
+    6: "beta term subtracted",
+    7: "bf16 rounding truncates",
+    8: "C_in read as row-major",
+    9: "C_in read when beta == 0",
+    10: "fp32 accumulation",
+}
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS), ids=[MUTANTS[m] for m in sorted(MUTANTS)])
+def test_planted_mistakes_are_caught(tmp_path_factory, mutant):
+    """Each oracle build with one planted error fails at least one pin."""
+    d = str(tmp_path_factory.mktemp("mutants"))
+    o = oracle_mod.Oracle(oracle_mod.build(mutant=mutant, build_dir=d))
+    assert o.mutant == mutant
+    failed = []
+    for pin in PINS:
+        try:
+            with np.errstate(all="ignore"):
+                pin(o)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"planted mistake '{MUTANTS[mutant]}' passed every pin"
+
+
+def test_ulp_distance_rules():
+    """The bf16 comparison maps both zeros to 0 and counts ulps across 0."""
+    d = parity.bf16_ulp_distance(np.array([0x0000, 0x3F80, 0x0001, 0x7F7F], dtype=np.uint16),
+                                 np.array([0x8000, 0x3F81, 0x8001, 0x7F80], dtype=np.uint16))
+    assert d.tolist() == [0, 1, 2, 1]
+    with pytest.raises(AssertionError):
+        parity.check_bf16(np.array([0x3F80], np.uint16), np.array([0x3F82], np.uint16))
+    with pytest.raises(AssertionError):
+        parity.check_f32(np.array([1.0 + 0.05]), np.array([1.0]), K=1)
+    parity.check_f32(np.array([1.0 + 0.0009]), np.array([1.0]), K=1)
