@@ -1,0 +1,414 @@
+#!/usr/bin/env python3
+"""Benchmark: bf16 GEMM TFLOP/s (2*M*N*K / time) on GB300, one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config s4k|s8k|edge|skinny|s256]
+
+A step is one C = alpha*A*B + beta*C over the configured workload (default:
+M = N = K = 4096, bf16 inputs, fp32 accumulation, bf16 output, A row-major,
+B and C column-major, N(0,1) inputs — the H100 work log's headline shape).
+
+Timing: W untimed warm-up steps, then K timed steps between a barrier plus
+torch.cuda.synchronize() on both sides.  The 96 MiB working set of the 4096
+case fits in the 126 MiB L2, so a 512 MiB buffer is written between timed
+steps (untimed) and each GEMM is timed alone with CUDA events on its stream.
+With N > 1 (torchrun), every rank multiplies its own independent matrices on
+its own GPU (no collective on the data path), the max over ranks is taken
+and `value` is the aggregate over all ranks.
+
+`--impl reference` times the CPU oracle (the plain C definition) on a bounded
+column slab of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "bf16 GEMM TFLOP/s (2MNK/t) at 4096³/8192³ on 1 GB300; % of dense BF16 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FLUSH_BYTES = 512 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def profile_traffic(kernel_tag: str):
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
+    summary, or None if the kernel source changed since it was captured."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    h = hashlib.sha256()
+    for rel in ("tensor_core_matmul_gb300/csrc/gemm_kernel.cuh", "tensor_core_matmul_gb300/csrc/ptx.cuh",
+                "tensor_core_matmul_gb300/csrc/tcgemm.cu"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    src = h.hexdigest()[:16]
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 3 and parts[0] == kernel_tag and parts[1] == src:
+            return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_ours(args) -> None:
+    import torch
+
+    import gemm_inputs as gi
+    import tensor_core_matmul_gb300 as tc
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    case = gi.config_case(args.config)
+    M, N, K = case.M, case.N, case.K
+    A = case.A.to(dev)
+    B = case.B.to(dev)
+    C = (case.C_in.to(dev) if case.C_in is not None
+         else torch.zeros((N, case.ldc), dtype=case.out_torch_dtype(), device=dev))
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def gemm():
+        tc.gemm_bf16(A, B, C, case.alpha, case.beta, M=M, N=N, K=K, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        gemm()
+    torch.cuda.synchronize(dev)
+    st, where = tc.check_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} during warm-up (role {where})")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.25)  # let the sampler take a first reading
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    n_launch0 = tc.launch_count()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)          # evict A, B, C from L2 (untimed)
+        starts[i].record(stream)
+        gemm()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if pg:
+        pg.barrier()
+    launches = tc.launch_count() - n_launch0
+    clocks = sampler.stop()
+    st, where = tc.check_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} in the timed region (role {where})")
+
+    times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_s = sum(times_ms) / 1e3
+    if pg:
+        t = torch.tensor([total_s], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_s = float(t.item())
+    flops = case.flops
+    value = world * flops * args.steps / total_s / 1e12
+    ms_per_step = total_s / args.steps * 1e3
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    achieved = flops / (total_s / args.steps) / 1e12
+    traffic = profile_traffic(f"gemm_{args.config}")
+    plan = tc.plan(M, N, K, 0, torch.cuda.get_device_properties(dev).multi_processor_count)
+    variant = tc.pick_variant(M, N, K, torch.cuda.get_device_properties(dev).multi_processor_count)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(args, case, dev, stream)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(case, target_s=args.cpu_seconds)
+
+    if rank == 0:
+        out = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "TFLOP/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic",
+            "config": {
+                "workload": f"gemm {args.config}: M={M} N={N} K={K}, bf16 A row-major x B col-major, "
+                            f"fp32 accumulate, {'bf16' if case.out_dtype else 'fp32'} C col-major, "
+                            f"alpha={case.alpha} beta={case.beta}, N(0,1) inputs",
+                "M": M, "N": N, "K": K,
+                "l2": f"flushed between timed steps ({FLUSH_BYTES >> 20} MiB write, untimed)",
+                "kernel": {"variant": {1: "1cta", 2: "2cta"}.get(variant, str(variant)), **plan},
+                "parallelism": f"independent problem per GPU x{world}",
+                "wall_s_timed_loop": round(wall, 3),
+            },
+            "roofline": {
+                "bound": "tensor",
+                "achieved": round(achieved, 2),
+                "peak": peak,
+                "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": traffic,
+                "peak_source": f"{peak_src} bf16_tflops (cuBLAS burst, MEASURED_PEAKS.json)"
+                               if peak_src == "measured" else "fallback 1.9 PFLOP/s bf16 burst",
+                "nominal_dense_bf16_tflops": 2250.0,
+                "frac_of_nominal": round(achieved / 2250.0, 4),
+            },
+            "clocks": clocks,
+            "e2e": e2e,
+            "gpu_launches": int(launches),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(out), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+def measure_e2e(args, case, dev, stream) -> dict:
+    """Same metric through the public API with host buffers: every step copies
+    A and B from pinned host memory, runs the GEMM and copies C back."""
+    import torch
+
+    import tensor_core_matmul_gb300 as tc
+    hA = case.A.pin_memory()
+    hB = case.B.pin_memory()
+    C0 = (case.C_in if case.C_in is not None
+          else torch.zeros((case.N, case.ldc), dtype=case.out_torch_dtype()))
+    hC_in = C0.pin_memory()
+    hC = torch.empty_like(hC_in).pin_memory()
+    dA = torch.empty_like(case.A, device=dev)
+    dB = torch.empty_like(case.B, device=dev)
+    dC = torch.empty_like(hC_in, device=dev)
+    has_beta = case.beta != 0.0
+    steps = max(3, min(args.steps, args.e2e_steps))
+
+    def step():
+        dA.copy_(hA, non_blocking=True)
+        dB.copy_(hB, non_blocking=True)
+        if has_beta:
+            dC.copy_(hC_in, non_blocking=True)
+        tc.gemm_bf16(dA, dB, dC, case.alpha, case.beta, M=case.M, N=case.N, K=case.K, stream=stream)
+        hC.copy_(dC, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize(dev)
+    t = s.elapsed_time(e) / 1e3
+    h2d = hA.numel() * 2 + hB.numel() * 2 + (hC_in.numel() * hC_in.element_size() if has_beta else 0)
+    d2h = hC.numel() * hC.element_size()
+    return {"value": round(case.flops * steps / t / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
+            "ms_per_step": round(t / steps * 1e3, 4)}
+
+
+def oracle_slab(case, ncols: int, threads: int = 0) -> float:
+    """Seconds for the oracle to compute columns [0, ncols) of C."""
+    import numpy as np
+
+    import gemm_inputs as gi
+    import oracle
+    o = oracle.get()
+    A = gi.as_u16(case.A)
+    B = gi.as_u16(case.B)[:ncols]
+    cin = None
+    if case.C_in is not None:
+        cin = case.C_in[:ncols]
+        cin = gi.as_u16(cin) if cin.dtype.is_floating_point and cin.element_size() == 2 else cin.numpy()
+    t0 = time.perf_counter()
+    o.gemm_f64(case.M, ncols, case.K, A, np.ascontiguousarray(B), cin, case.alpha, case.beta, threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(case, target_s: float) -> dict:
+    import oracle
+    cores = oracle.get().threads(0)
+    ncal = max(1, min(case.N, cores))
+    t = oracle_slab(case, ncal)
+    per_col = t / ncal
+    ncols = int(max(1, min(case.N, round(target_s / max(per_col, 1e-9)))))
+    ncols = max(ncols, min(case.N, cores))
+    t = oracle_slab(case, ncols)
+    flops = 2 * case.M * ncols * case.K
+    return {"value": round(flops / t / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"columns 0..{ncols - 1} of C ({case.M}x{ncols}x{case.K}, {flops / 1e9:.1f} GFLOP), "
+                      f"{t:.1f} s on {cores} threads; fp64 k-ascending definition"}
+
+
+def run_reference(args) -> None:
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    import oracle
+
+    import gemm_inputs as gi
+    case = gi.config_case(args.config)
+    cores = oracle.get().threads(0)
+    # Size each step's column slab so the whole run takes about args.ref_seconds.
+    ncal = max(1, min(case.N, cores))
+    per_col = oracle_slab(case, ncal) / ncal
+    total_steps = args.steps + args.warmup
+    ncols = int(max(1, min(case.N, round(args.ref_seconds / total_steps / max(per_col, 1e-9)))))
+    for _ in range(args.warmup):
+        oracle_slab(case, ncols)
+    t = 0.0
+    for _ in range(args.steps):
+        t += oracle_slab(case, ncols)
+    flops = 2 * case.M * ncols * case.K
+    value = flops * args.steps / t / 1e12
+    out = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t / args.steps * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"gemm {args.config}: M={case.M} N={case.N} K={case.K}; each step computes "
+                               f"columns 0..{ncols - 1} of C with the CPU oracle",
+                   "M": case.M, "N": case.N, "K": case.K},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{ncols} columns of C per step ({case.M}x{ncols}x{case.K})"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="s4k", choices=["s256", "s4k", "s8k", "edge", "skinny"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

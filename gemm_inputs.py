@@ -189,3 +189,23 @@ def sample_indices(M: int, N: int, count: int, seed: int) -> tuple[np.ndarray, n
         rows.append(i)
         cols.append(j)
     return np.asarray(rows, dtype=np.int64), np.asarray(cols, dtype=np.int64)
+
+
+def cell_sample_indices(M: int, N: int, cell_m: int, cell_n: int, per_cell: int,
+                        seed: int) -> tuple[np.ndarray, np.ndarray]:
+    """``per_cell`` random (row, col) positions inside every cell of a
+    cell_m x cell_n grid laid over the M x N output, plus the corners, so that
+    every tile of any tiling with tiles that are multiples of the cell is
+    sampled."""
+    rng = np.random.default_rng(seed)
+    rows, cols = [], []
+    for i0 in range(0, M, cell_m):
+        hi = min(M, i0 + cell_m)
+        for j0 in range(0, N, cell_n):
+            hj = min(N, j0 + cell_n)
+            rows.extend(rng.integers(i0, hi, size=per_cell).tolist())
+            cols.extend(rng.integers(j0, hj, size=per_cell).tolist())
+    for (i, j) in [(0, 0), (M - 1, 0), (0, N - 1), (M - 1, N - 1)]:
+        rows.append(i)
+        cols.append(j)
+    return np.asarray(rows, dtype=np.int64), np.asarray(cols, dtype=np.int64)

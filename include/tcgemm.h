@@ -1,0 +1,135 @@
+/*
+ * tcgemm — bf16 GEMM with fp32 accumulation on tcgen05 tensor cores (sm_103a).
+ *
+ *   C = alpha * A * B + beta * C
+ *
+ * The operation is the matrix product C[m,n] = A[m,k] x B[k,n] of the H100 work
+ * log "在 H100 上超越 cuBLAS：一份工作日志" (section "Simon 博客的快速回顾"), with
+ * the layouts of its section "实验设置": bf16 inputs, A row-major, B and C
+ * column-major.  The alpha/beta update is the BLAS form named in the "DeepGEMM"
+ * article (demingchina.com), section 1.1; fp32 accumulation is that article's
+ * precision contract (section 3.1).
+ *
+ * Layouts (element (i,j) of each matrix):
+ *   A: M x K, row-major,    A[i,k] at ((const bf16*)A)[i*lda + k], lda >= K
+ *   B: K x N, column-major, B[k,j] at ((const bf16*)B)[j*ldb + k], ldb >= K
+ *   C: M x N, column-major, C[i,j] at ((T*)C)[j*ldc + i],          ldc >= M
+ * where bf16 is the 16-bit brain-float format and T is float (out_dtype
+ * TCGEMM_OUT_F32) or bf16 (TCGEMM_OUT_BF16).  With beta != 0, C is read first
+ * and has the output type; with beta == 0, C is never read (NaN in C is fine).
+ *
+ * Pointers: A, B and C are device pointers (CUDA global memory) on the current
+ * device.  The caller owns every buffer and the stream; the library keeps no
+ * reference to any of them after the call returns.  `stream` is a cudaStream_t
+ * passed as void* (NULL means the legacy default stream).
+ *
+ * Rules checked on the host before anything is launched (error return, nothing
+ * written):
+ *   - M, N, K >= 0 and below 2^31; lda >= max(K,1), ldb >= max(K,1), ldc >= max(M,1);
+ *   - A, B, C 16-byte aligned; lda*2, ldb*2 and ldc*sizeof(T) multiples of 16
+ *     bytes (the tensor-memory-accelerator copy rules)   -> TCGEMM_ERR_ALIGNMENT;
+ *   - C does not overlap A or B                           -> TCGEMM_ERR_INVALID_ARG;
+ *   - the current device is compute capability 10.3      -> TCGEMM_ERR_UNSUPPORTED_DEVICE.
+ * M == 0 or N == 0 is a no-op.  K == 0 sets C = beta*C (0 when beta == 0).
+ *
+ * Asynchrony: calls enqueue work on `stream` and return.  Launch failures return
+ * TCGEMM_ERR_CUDA.  A device-side wait that exceeds its time limit (a hang
+ * guard; it never fires in a correct run) is reported through
+ * tcgemm_check_device_status().  Concurrent calls from several host threads are
+ * safe.
+ */
+#ifndef TCGEMM_H
+#define TCGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TCGEMM_OUT_F32 = 0,
+    TCGEMM_OUT_BF16 = 1
+} tcgemm_dtype_t;
+
+typedef enum {
+    TCGEMM_OK = 0,
+    TCGEMM_ERR_INVALID_ARG = 1,
+    TCGEMM_ERR_ALIGNMENT = 2,
+    TCGEMM_ERR_UNSUPPORTED_DEVICE = 3,
+    TCGEMM_ERR_CUDA = 4,
+    TCGEMM_ERR_TIMEOUT = 5
+} tcgemm_status_t;
+
+/* Kernel variants (see gemm_bf16_variant).  TCGEMM_VARIANT_AUTO picks by shape. */
+typedef enum {
+    TCGEMM_VARIANT_AUTO = 0,
+    TCGEMM_VARIANT_1CTA = 1,  /* one CTA per SM, 128 x 256 tiles, cta_group::1 MMA   */
+    TCGEMM_VARIANT_2CTA = 2   /* CTA pairs, 256 x 256 tiles, cta_group::2 MMA (M=256) */
+} tcgemm_variant_t;
+
+/* C = alpha*A*B + beta*C as described above.  Returns TCGEMM_OK once the work
+ * is enqueued. */
+int gemm_bf16(int64_t M, int64_t N, int64_t K,
+              const void* A, int64_t lda,
+              const void* B, int64_t ldb,
+              void* C, int64_t ldc,
+              float alpha, float beta, int out_dtype, void* stream);
+
+/* Same operation with an explicit kernel variant (tcgemm_variant_t); used by
+ * tests and tuning to run every variant on the same shapes.  Same rules and
+ * errors as gemm_bf16; an unknown variant is TCGEMM_ERR_INVALID_ARG. */
+int gemm_bf16_variant(int64_t M, int64_t N, int64_t K,
+                      const void* A, int64_t lda,
+                      const void* B, int64_t ldb,
+                      void* C, int64_t ldc,
+                      float alpha, float beta, int out_dtype, void* stream, int variant);
+
+/* The variant gemm_bf16 would run for this shape on a device with `num_sms`
+ * streaming multiprocessors.  Host only; needs no GPU. */
+int tcgemm_pick_variant(int64_t M, int64_t N, int64_t K, int num_sms);
+
+/* Host-only description of the launch gemm_bf16_variant would make, for tests
+ * and tools: out[0] = grid size (CTAs), out[1] = CTAs per cluster, out[2] =
+ * tile rows (tiles_m), out[3] = tile columns (tiles_n), out[4] = tile height,
+ * out[5] = tile width, out[6] = k-blocks per tile, out[7] = dynamic shared
+ * memory bytes.  `out` must hold 8 values.  Returns TCGEMM_OK or
+ * TCGEMM_ERR_INVALID_ARG.  Needs no GPU. */
+int tcgemm_plan(int64_t M, int64_t N, int64_t K, int variant, int num_sms, int64_t* out);
+
+/* Tile visiting order used by the persistent kernels (host copy of the device
+ * function): writes the tile row and column of order index t = 0..count-1
+ * into tm[t], tn[t].  Needs no GPU. */
+int tcgemm_tile_order(int tiles_m, int tiles_n, int group_m, int64_t count, int32_t* tm, int32_t* tn);
+
+/* Human-readable name of a status code (static string). */
+const char* tcgemm_status_string(int status);
+
+/* Detail of the last failed call on this host thread (static per-thread
+ * buffer, empty when there was none). */
+const char* tcgemm_last_error(void);
+
+/* Synchronises `stream`, then reads and clears the device status word of the
+ * current device.  Returns TCGEMM_ERR_TIMEOUT if a kernel gave up a wait since
+ * the last check (*where_out, if not NULL, receives the role that timed out:
+ * 1 producer, 2 MMA, 3 epilogue, 4 drain, 5 self test), TCGEMM_ERR_CUDA if the
+ * synchronisation failed, else TCGEMM_OK. */
+int tcgemm_check_device_status(void* stream, uint32_t* where_out);
+
+/* Launches a one-thread kernel that waits on a barrier nothing arrives on and
+ * gives up after `timeout_ns` nanoseconds, then returns
+ * tcgemm_check_device_status() — TCGEMM_ERR_TIMEOUT when the hang guard
+ * works.  Touches no user memory. */
+int tcgemm_selftest_timeout(void* stream, uint64_t timeout_ns);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t tcgemm_launch_count(void);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int tcgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TCGEMM_H */

@@ -67,6 +67,8 @@ class Oracle:
         L.oracle_gemm_sampled_f64.argtypes = [i64, i64, i64, p, i64, p, i64, p, i64, ctypes.c_int,
                                               ctypes.c_float, ctypes.c_float, i64, p, p, p]
         L.oracle_gemm_sampled_f64.restype = ctypes.c_int
+        L.oracle_absdot_sampled_f64.argtypes = [i64, i64, i64, p, i64, p, i64, i64, p, p, p]
+        L.oracle_absdot_sampled_f64.restype = ctypes.c_int
         L.oracle_round_bf16.argtypes = [ctypes.c_double]
         L.oracle_round_bf16.restype = ctypes.c_uint16
         L.oracle_round_bf16_array.argtypes = [p, p, i64]
@@ -143,6 +145,21 @@ class Oracle:
                                              self._ptr(rows), self._ptr(cols), self._ptr(out))
         if rc != 0:
             raise ValueError("oracle_gemm_sampled_f64: bad arguments")
+        return out
+
+    def absdot_sampled_f64(self, M: int, N: int, K: int, A: np.ndarray, B: np.ndarray,
+                           rows: np.ndarray, cols: np.ndarray) -> np.ndarray:
+        """G[i,j] = sum_k |A[i,k] * B[k,j]| at the given positions (fp64), the
+        scale of the fp32-accumulation error bound."""
+        A = np.ascontiguousarray(A, dtype=np.uint16)
+        B = np.ascontiguousarray(B, dtype=np.uint16)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        cols = np.ascontiguousarray(cols, dtype=np.int64)
+        out = np.empty(rows.shape[0], dtype=np.float64)
+        rc = self._L.oracle_absdot_sampled_f64(M, N, K, self._ptr(A), A.shape[1], self._ptr(B), B.shape[1],
+                                               rows.shape[0], self._ptr(rows), self._ptr(cols), self._ptr(out))
+        if rc != 0:
+            raise ValueError("oracle_absdot_sampled_f64: bad arguments")
         return out
 
     def round_bf16(self, d: np.ndarray) -> np.ndarray:

@@ -110,6 +110,7 @@ typedef struct {
     const uint16_t* B; int64_t ldb;
     const void* Cin; int64_t ldc; int cin_bf16; /* C_in dtype: 0 fp32, 1 bf16 */
     double alpha, beta;
+    int absolute;       /* 1: sum |A[i,k]*B[k,j]| instead (error model, no alpha/beta) */
 } problem_t;
 
 static double c_in_at(const problem_t* p, int64_t i, int64_t j) {
@@ -144,8 +145,9 @@ static double element(const problem_t* p, int64_t i, int64_t j) {
 #else
         double b = bf16_to_double(p->B[j * p->ldb + k]);
 #endif
-        s += a * b;
+        s += p->absolute ? fabs(a * b) : a * b;
     }
+    if (p->absolute) return (double)s;
 #if ORACLE_MUTANT == 4
     double d = p->beta * (double)s;                     /* planted: alpha and beta swapped */
     if (p->beta != 0.0) d += p->alpha * c_in_at(p, i, j);
@@ -201,7 +203,7 @@ int oracle_gemm_f64(int64_t M, int64_t N, int64_t K,
                     float alpha, float beta, double* D, int nthreads) {
     if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || ldc < M) return -1;
     if (beta != 0.0f && Cin == NULL) return -1;
-    problem_t p = {M, N, K, A, lda, B, ldb, Cin, ldc, cin_bf16, (double)alpha, (double)beta};
+    problem_t p = {M, N, K, A, lda, B, ldb, Cin, ldc, cin_bf16, (double)alpha, (double)beta, 0};
     if (M == 0 || N == 0) return 0;
     int nt = pick_threads(nthreads, N);
     pthread_t tid[256];
@@ -233,7 +235,24 @@ int oracle_gemm_sampled_f64(int64_t M, int64_t N, int64_t K,
                             double* out) {
     if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || ldc < M) return -1;
     if (beta != 0.0f && Cin == NULL) return -1;
-    problem_t p = {M, N, K, A, lda, B, ldb, Cin, ldc, cin_bf16, (double)alpha, (double)beta};
+    problem_t p = {M, N, K, A, lda, B, ldb, Cin, ldc, cin_bf16, (double)alpha, (double)beta, 0};
+    for (int64_t s = 0; s < count; ++s) {
+        if (rows[s] < 0 || rows[s] >= M || cols[s] < 0 || cols[s] >= N) return -1;
+        out[s] = element(&p, rows[s], cols[s]);
+    }
+    return 0;
+}
+
+/* Error model for the fp32-accumulation bound: G[i,j] = sum_k |A[i,k]*B[k,j]|
+ * in fp64, at selected positions.  A recursive fp32 sum of these K products,
+ * in any order, differs from the exact sum by at most about
+ * K * 2^-24 * G[i,j] (the classical bound for floating-point summation). */
+int oracle_absdot_sampled_f64(int64_t M, int64_t N, int64_t K,
+                              const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                              int64_t count, const int64_t* rows, const int64_t* cols,
+                              double* out) {
+    if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K) return -1;
+    problem_t p = {M, N, K, A, lda, B, ldb, NULL, M, 0, 1.0, 0.0, 1};
     for (int64_t s = 0; s < count; ++s) {
         if (rows[s] < 0 || rows[s] >= M || cols[s] < 0 || cols[s] >= N) return -1;
         out[s] = element(&p, rows[s], cols[s]);

@@ -1,0 +1,16 @@
+"""bf16 GEMM on GB300 tensor cores (tcgen05 + TMA + TMEM), behind a C ABI.
+
+    C = alpha * A * B + beta * C      A row-major, B and C column-major,
+                                      bf16 inputs, fp32 accumulation,
+                                      fp32 or bf16 output.
+
+The CUDA library (``_lib/libtcgemm.so``, built from ``csrc/``) does all the
+work; ``binding`` only marshals arguments.  Build with ``_build.build()``.
+"""
+from .binding import (OUT_BF16, OUT_F32, VARIANT_1CTA, VARIANT_2CTA, VARIANT_AUTO, TcgemmError,
+                      check_device_status, gemm_bf16, gemm_bf16_raw, launch_count, lib, pick_variant,
+                      plan, selftest_timeout, tile_order, version)
+
+__all__ = ["OUT_BF16", "OUT_F32", "VARIANT_1CTA", "VARIANT_2CTA", "VARIANT_AUTO", "TcgemmError",
+           "check_device_status", "gemm_bf16", "gemm_bf16_raw", "launch_count", "lib", "pick_variant",
+           "plan", "selftest_timeout", "tile_order", "version"]

@@ -1,0 +1,171 @@
+"""ctypes binding of the tcgemm C ABI (include/tcgemm.h).
+
+Argument marshalling only: every step of the GEMM runs in the CUDA library.
+There is no fallback: if libtcgemm.so is missing or fails to load, every call
+raises.  Torch is used for device memory and streams.
+
+Storage convention for torch tensors (matching the C ABI's layouts):
+  A: (M, lda) bf16       -> A[i, k]   (row-major M x K)
+  B: (N, ldb) bf16       -> B[k, j] is B_t[j, k] (column-major K x N)
+  C: (N, ldc) fp32/bf16  -> C[i, j] is C_t[j, i] (column-major M x N)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from . import _build
+
+OUT_F32 = 0
+OUT_BF16 = 1
+VARIANT_AUTO, VARIANT_1CTA, VARIANT_2CTA = 0, 1, 2
+
+STATUS = {0: "TCGEMM_OK", 1: "TCGEMM_ERR_INVALID_ARG", 2: "TCGEMM_ERR_ALIGNMENT",
+          3: "TCGEMM_ERR_UNSUPPORTED_DEVICE", 4: "TCGEMM_ERR_CUDA", 5: "TCGEMM_ERR_TIMEOUT"}
+
+
+class TcgemmError(RuntimeError):
+    def __init__(self, status: int, detail: str = ""):
+        self.status = status
+        super().__init__(f"{STATUS.get(status, status)}: {detail}")
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return os.environ.get("TCGEMM_LIB", _build.LIB_PATH)
+
+
+def lib() -> ctypes.CDLL:
+    """Load libtcgemm.so (built in-tree by __graft_entry__.build() or
+    tensor_core_matmul_gb300._build.build()).  Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libtcgemm.so not found at {path}; build it first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    L = ctypes.CDLL(path)
+    i64, p, f32, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int
+    gemm_args = [i64, i64, i64, p, i64, p, i64, p, i64, f32, f32, i32, p]
+    L.gemm_bf16.argtypes = gemm_args
+    L.gemm_bf16.restype = i32
+    L.gemm_bf16_variant.argtypes = gemm_args + [i32]
+    L.gemm_bf16_variant.restype = i32
+    L.tcgemm_pick_variant.argtypes = [i64, i64, i64, i32]
+    L.tcgemm_pick_variant.restype = i32
+    L.tcgemm_plan.argtypes = [i64, i64, i64, i32, i32, ctypes.POINTER(ctypes.c_int64)]
+    L.tcgemm_plan.restype = i32
+    L.tcgemm_tile_order.argtypes = [i32, i32, i32, i64, ctypes.POINTER(ctypes.c_int32),
+                                    ctypes.POINTER(ctypes.c_int32)]
+    L.tcgemm_tile_order.restype = i32
+    L.tcgemm_status_string.argtypes = [i32]
+    L.tcgemm_status_string.restype = ctypes.c_char_p
+    L.tcgemm_last_error.argtypes = []
+    L.tcgemm_last_error.restype = ctypes.c_char_p
+    L.tcgemm_check_device_status.argtypes = [p, ctypes.POINTER(ctypes.c_uint32)]
+    L.tcgemm_check_device_status.restype = i32
+    L.tcgemm_selftest_timeout.argtypes = [p, ctypes.c_uint64]
+    L.tcgemm_selftest_timeout.restype = i32
+    L.tcgemm_launch_count.argtypes = []
+    L.tcgemm_launch_count.restype = ctypes.c_uint64
+    L.tcgemm_version.argtypes = []
+    L.tcgemm_version.restype = i32
+    _lib = L
+    return L
+
+
+def last_error() -> str:
+    return lib().tcgemm_last_error().decode(errors="replace")
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise TcgemmError(status, last_error())
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def gemm_bf16_raw(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int, C: int, ldc: int,
+                  alpha: float, beta: float, out_dtype: int, stream: int, variant: int = 0) -> int:
+    """Pointer-level call; returns the status code (no exception)."""
+    L = lib()
+    if variant == 0:
+        return L.gemm_bf16(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, stream)
+    return L.gemm_bf16_variant(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, stream, variant)
+
+
+def gemm_bf16(A, B, C, alpha: float = 1.0, beta: float = 0.0, *, M: Optional[int] = None,
+              N: Optional[int] = None, K: Optional[int] = None, stream=None, variant: int = 0):
+    """C = alpha * A * B + beta * C on the GPU, tensors in the storage
+    convention above.  M, N, K default to C.shape[1], C.shape[0], A.shape[1]."""
+    import torch
+    if not (A.is_cuda and B.is_cuda and C.is_cuda):
+        raise ValueError("A, B and C must be CUDA tensors")
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise ValueError("A and B must be bfloat16")
+    if C.dtype == torch.float32:
+        out = OUT_F32
+    elif C.dtype == torch.bfloat16:
+        out = OUT_BF16
+    else:
+        raise ValueError("C must be float32 or bfloat16")
+    for t in (A, B, C):
+        if t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError("A, B, C must be 2-D with unit inner stride")
+    M = C.shape[1] if M is None else M
+    N = C.shape[0] if N is None else N
+    K = A.shape[1] if K is None else K
+    if A.shape[0] < M or B.shape[0] < N or C.shape[0] < N:
+        raise ValueError("tensor shapes smaller than M/N")
+    st = gemm_bf16_raw(M, N, K, A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0), C.data_ptr(),
+                       C.stride(0), float(alpha), float(beta), out, _stream_ptr(stream), variant)
+    _check(st)
+    return C
+
+
+def check_device_status(stream=None) -> tuple[int, int]:
+    where = ctypes.c_uint32(0)
+    st = lib().tcgemm_check_device_status(_stream_ptr(stream), ctypes.byref(where))
+    return st, where.value
+
+
+def selftest_timeout(timeout_ns: int, stream=None) -> int:
+    return lib().tcgemm_selftest_timeout(_stream_ptr(stream), int(timeout_ns))
+
+
+def launch_count() -> int:
+    return int(lib().tcgemm_launch_count())
+
+
+def pick_variant(M: int, N: int, K: int, num_sms: int) -> int:
+    return int(lib().tcgemm_pick_variant(M, N, K, num_sms))
+
+
+def plan(M: int, N: int, K: int, variant: int = 0, num_sms: int = 152) -> dict:
+    out = (ctypes.c_int64 * 8)()
+    _check(lib().tcgemm_plan(M, N, K, variant, num_sms, out))
+    keys = ["grid", "cta_group", "tiles_m", "tiles_n", "bm", "bn", "num_kb", "smem"]
+    return dict(zip(keys, [int(v) for v in out]))
+
+
+def tile_order(tiles_m: int, tiles_n: int, group_m: int, count: Optional[int] = None):
+    count = tiles_m * tiles_n if count is None else count
+    tm = (ctypes.c_int32 * count)()
+    tn = (ctypes.c_int32 * count)()
+    _check(lib().tcgemm_tile_order(tiles_m, tiles_n, group_m, count, tm, tn))
+    return list(tm), list(tn)
+
+
+def version() -> int:
+    return int(lib().tcgemm_version())

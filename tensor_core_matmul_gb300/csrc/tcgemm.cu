@@ -1,0 +1,478 @@
+// Host side of the tcgemm C ABI: argument checks, TMA descriptor encoding,
+// variant choice and kernel launch.  See include/tcgemm.h for the contract.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/tcgemm.h"
+#include "gemm_kernel.cuh"
+
+namespace {
+
+thread_local char t_last_error[512];
+
+void set_error(const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_last_error, sizeof t_last_error, fmt, ap);
+    va_end(ap);
+}
+
+std::atomic<uint64_t> g_launches{0};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess) {
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        }
+    });
+    return fn;
+}
+
+uint64_t timeout_ns() {
+    static uint64_t ns = [] {
+        const char* s = std::getenv("TCGEMM_TIMEOUT_MS");
+        double ms = s ? std::atof(s) : 0.0;
+        if (!(ms > 0.0)) ms = 2000.0;
+        return static_cast<uint64_t>(ms * 1e6);
+    }();
+    return ns;
+}
+
+// ------------------------------------------------------------- devices --
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool probed = false;
+    bool supported = false;
+    int sms = 0;
+    int max_pairs = 0;  // co-resident CTA pairs for the 2-CTA kernel
+};
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+// ---------------------------------------------------------------- plans --
+
+struct Plan {
+    int variant = 0;
+    int cta_group = 1;
+    int bm = 128, bn = 256;
+    int tiles_m = 0, tiles_n = 0, num_kb = 0;
+    int grid = 0;
+    int group_m = 1;
+    uint32_t smem = 0;
+};
+
+constexpr int kStages1 = 4;  // 1-CTA: 4 x (16 KB A + 32 KB B)
+constexpr int kStages2 = 6;  // 2-CTA: 6 x (16 KB A + 16 KB B) per CTA
+using Cfg1 = tcg::GemmCfg<1, 256, kStages1>;
+using Cfg2 = tcg::GemmCfg<2, 256, kStages2>;
+
+int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+
+int pick_variant(int64_t M, int64_t N, int64_t K, int sms) {
+    (void)M;
+    (void)N;
+    (void)K;
+    (void)sms;
+    return TCGEMM_VARIANT_1CTA;
+}
+
+bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pairs, Plan& pl) {
+    if (sms <= 0) return false;
+    if (variant == TCGEMM_VARIANT_AUTO) variant = pick_variant(M, N, K, sms);
+    pl.variant = variant;
+    if (variant == TCGEMM_VARIANT_1CTA) {
+        pl.cta_group = 1;
+        pl.bm = Cfg1::kBM;
+        pl.bn = 256;
+        pl.smem = Cfg1::kSmemBytes;
+    } else if (variant == TCGEMM_VARIANT_2CTA) {
+        pl.cta_group = 2;
+        pl.bm = Cfg2::kBM;
+        pl.bn = 256;
+        pl.smem = Cfg2::kSmemBytes;
+    } else {
+        return false;
+    }
+    pl.tiles_m = ceil_div(M, pl.bm);
+    pl.tiles_n = ceil_div(N, pl.bn);
+    pl.num_kb = ceil_div(K, 64);
+    const int64_t tiles = static_cast<int64_t>(pl.tiles_m) * pl.tiles_n;
+    const int64_t clusters = pl.cta_group == 1 ? sms : std::max(1, max_pairs > 0 ? max_pairs : sms / 2);
+    pl.grid = static_cast<int>(std::min<int64_t>(tiles, clusters)) * pl.cta_group;
+    // Band height so that the tiles in flight at once cover a roughly square
+    // patch of C: group_m^2 ~ concurrent tiles * (tile width / tile height).
+    const double ideal = std::sqrt(static_cast<double>(pl.grid / pl.cta_group) * pl.bn / pl.bm);
+    int g = 1;
+    while (g * 2 <= ideal) g *= 2;
+    pl.group_m = std::max(1, std::min(g, pl.tiles_m));
+    return true;
+}
+
+// --------------------------------------------------------- tensor maps --
+
+bool encode_kmajor(CUtensorMap* m, const void* ptr, int64_t k_extent, int64_t rows, int64_t ld,
+                   uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) {
+        set_error("cuTensorMapEncodeTiled is not available from the driver");
+        return false;
+    }
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(k_extent), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
+    cuuint32_t box[2] = {64u, box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled failed (%d) for extent %lld x %lld, ld %lld", static_cast<int>(r),
+                  static_cast<long long>(k_extent), static_cast<long long>(rows), static_cast<long long>(ld));
+        return false;
+    }
+    return true;
+}
+
+// -------------------------------------------------------------- launch --
+
+// The dynamic shared-memory opt-in is a per-kernel attribute; it is set once
+// per device for each kernel instantiation.
+template <int CG, int BN, int ST, typename OutT>
+bool ensure_smem_attr(int dev) {
+    static std::mutex mu;
+    static bool done[kMaxDevices] = {};
+    std::lock_guard<std::mutex> lk(mu);
+    if (done[dev]) return true;
+    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, OutT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(tcg::GemmCfg<CG, BN, ST>::kSmemBytes));
+    if (e != cudaSuccess) {
+        set_error("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        return false;
+    }
+    done[dev] = true;
+    return true;
+}
+
+template <int CG, int BN, int ST, typename OutT>
+int launch_gemm(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, const tcg::GemmParams& gp,
+                cudaStream_t stream, int dev) {
+    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, OutT>;
+    if (!ensure_smem_attr<CG, BN, ST, OutT>(dev)) return TCGEMM_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(pl.grid), 1, 1);
+    cfg.blockDim = dim3(tcg::GemmCfg<CG, BN, ST>::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    cfg.numAttrs = 0;
+    if (CG == 2) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, gp);
+    if (e != cudaSuccess) {
+        set_error("kernel launch: %s", cudaGetErrorString(e));
+        return TCGEMM_ERR_CUDA;
+    }
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return TCGEMM_OK;
+}
+
+int probe_device(int& dev_out, DeviceInfo& info) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        set_error("cudaGetDevice: %s", cudaGetErrorString(e));
+        return TCGEMM_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) {
+        set_error("device ordinal %d out of range", dev);
+        return TCGEMM_ERR_UNSUPPORTED_DEVICE;
+    }
+    dev_out = dev;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.probed) {
+        int major = 0, minor = 0, sms = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        d.supported = (major == 10 && minor == 3);
+        d.sms = sms;
+        d.max_pairs = sms / 2;
+        if (d.supported) {
+            // How many CTA pairs of the 2-CTA kernel can be resident at once
+            // (cluster placement may leave some SMs unpaired).
+            auto kern = tcg::gemm_bf16_tn_kernel<2, 256, kStages2, __nv_bfloat16>;
+            if (ensure_smem_attr<2, 256, kStages2, __nv_bfloat16>(dev)) {
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
+                cfg.blockDim = dim3(Cfg2::kThreads, 1, 1);
+                cfg.dynamicSmemBytes = Cfg2::kSmemBytes;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = 2;
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                int n = 0;
+                if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) d.max_pairs = n;
+                (void)cudaGetLastError();
+            }
+        }
+        d.probed = true;
+    }
+    info = d;
+    if (!d.supported) {
+        set_error("device %d is not compute capability 10.3 (sm_103a)", dev);
+        return TCGEMM_ERR_UNSUPPORTED_DEVICE;
+    }
+    return TCGEMM_OK;
+}
+
+bool overlaps(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    const uintptr_t a1 = a0 + static_cast<uintptr_t>(abytes), b1 = b0 + static_cast<uintptr_t>(bbytes);
+    return a0 < b1 && b0 < a1;
+}
+
+int validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+             const void* C, int64_t ldc, int out_dtype) {
+    const int64_t lim = (int64_t{1} << 31) - 1;
+    if (M < 0 || N < 0 || K < 0 || M > lim || N > lim || K > lim) {
+        set_error("sizes must satisfy 0 <= M, N, K < 2^31 (got %lld, %lld, %lld)", static_cast<long long>(M),
+                  static_cast<long long>(N), static_cast<long long>(K));
+        return TCGEMM_ERR_INVALID_ARG;
+    }
+    if (out_dtype != TCGEMM_OUT_F32 && out_dtype != TCGEMM_OUT_BF16) {
+        set_error("out_dtype must be TCGEMM_OUT_F32 (0) or TCGEMM_OUT_BF16 (1), got %d", out_dtype);
+        return TCGEMM_ERR_INVALID_ARG;
+    }
+    if (lda < std::max<int64_t>(K, 1) || ldb < std::max<int64_t>(K, 1) || ldc < std::max<int64_t>(M, 1)) {
+        set_error("leading dimensions too small: need lda >= K, ldb >= K, ldc >= M (at least 1)");
+        return TCGEMM_ERR_INVALID_ARG;
+    }
+    if (M == 0 || N == 0) return TCGEMM_OK;
+    const int64_t esz = out_dtype == TCGEMM_OUT_F32 ? 4 : 2;
+    if (C == nullptr || (K > 0 && (A == nullptr || B == nullptr))) {
+        set_error("null matrix pointer");
+        return TCGEMM_ERR_INVALID_ARG;
+    }
+    if ((reinterpret_cast<uintptr_t>(C) & 15u) != 0 || ((ldc * esz) & 15) != 0) {
+        set_error("C must be 16-byte aligned with ldc*%lld a multiple of 16 bytes", static_cast<long long>(esz));
+        return TCGEMM_ERR_ALIGNMENT;
+    }
+    if (K > 0) {
+        if ((reinterpret_cast<uintptr_t>(A) & 15u) != 0 || (reinterpret_cast<uintptr_t>(B) & 15u) != 0 ||
+            ((lda * 2) & 15) != 0 || ((ldb * 2) & 15) != 0) {
+            set_error("A and B must be 16-byte aligned with lda*2 and ldb*2 multiples of 16 bytes");
+            return TCGEMM_ERR_ALIGNMENT;
+        }
+        const int64_t cbytes = ((N - 1) * ldc + M) * esz;
+        if (overlaps(C, cbytes, A, ((M - 1) * lda + K) * 2) || overlaps(C, cbytes, B, ((N - 1) * ldb + K) * 2)) {
+            set_error("C overlaps A or B");
+            return TCGEMM_ERR_INVALID_ARG;
+        }
+    }
+    return TCGEMM_OK;
+}
+
+int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+             int64_t ldc, float alpha, float beta, int out_dtype, void* stream_v, int variant) {
+    t_last_error[0] = '\0';
+    if (variant < TCGEMM_VARIANT_AUTO || variant > TCGEMM_VARIANT_2CTA) {
+        set_error("unknown variant %d", variant);
+        return TCGEMM_ERR_INVALID_ARG;
+    }
+    int rc = validate(M, N, K, A, lda, B, ldb, C, ldc, out_dtype);
+    if (rc != TCGEMM_OK) return rc;
+    if (M == 0 || N == 0) return TCGEMM_OK;
+    int dev = 0;
+    DeviceInfo info;
+    rc = probe_device(dev, info);
+    if (rc != TCGEMM_OK) return rc;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+
+    if (K == 0) {
+        const int64_t total = M * N;
+        const int threads = 256;
+        const int64_t blocks = std::min<int64_t>((total + threads - 1) / threads, int64_t{info.sms} * 8);
+        if (out_dtype == TCGEMM_OUT_F32) {
+            tcg::scale_c_kernel<float><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+                static_cast<float*>(C), M, N, ldc, beta);
+        } else {
+            tcg::scale_c_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+                static_cast<__nv_bfloat16*>(C), M, N, ldc, beta);
+        }
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) {
+            set_error("kernel launch: %s", cudaGetErrorString(e));
+            return TCGEMM_ERR_CUDA;
+        }
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        return TCGEMM_OK;
+    }
+
+    Plan pl;
+    if (!make_plan(M, N, K, variant, info.sms, info.max_pairs, pl)) {
+        set_error("no launch plan for this shape and variant");
+        return TCGEMM_ERR_INVALID_ARG;
+    }
+    const uint32_t b_box_rows = static_cast<uint32_t>(pl.bn / pl.cta_group);
+    CUtensorMap ta, tb;
+    if (!encode_kmajor(&ta, A, K, M, lda, 128u) || !encode_kmajor(&tb, B, K, N, ldb, b_box_rows)) {
+        return TCGEMM_ERR_INVALID_ARG;
+    }
+    tcg::GemmParams gp;
+    gp.M = static_cast<int>(M);
+    gp.N = static_cast<int>(N);
+    gp.K = static_cast<int>(K);
+    gp.tiles_m = pl.tiles_m;
+    gp.tiles_n = pl.tiles_n;
+    gp.num_kb = pl.num_kb;
+    gp.group_m = pl.group_m;
+    gp.ldc = ldc;
+    gp.C = C;
+    gp.alpha = alpha;
+    gp.beta = beta;
+    gp.timeout_ns = timeout_ns();
+
+    const bool bf16 = out_dtype == TCGEMM_OUT_BF16;
+    if (pl.cta_group == 1) {
+        return bf16 ? launch_gemm<1, 256, kStages1, __nv_bfloat16>(pl, ta, tb, gp, stream, dev)
+                    : launch_gemm<1, 256, kStages1, float>(pl, ta, tb, gp, stream, dev);
+    }
+    return bf16 ? launch_gemm<2, 256, kStages2, __nv_bfloat16>(pl, ta, tb, gp, stream, dev)
+                : launch_gemm<2, 256, kStages2, float>(pl, ta, tb, gp, stream, dev);
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+              int64_t ldc, float alpha, float beta, int out_dtype, void* stream) {
+    return run_gemm(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, stream, TCGEMM_VARIANT_AUTO);
+}
+
+int gemm_bf16_variant(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                      void* C, int64_t ldc, float alpha, float beta, int out_dtype, void* stream, int variant) {
+    return run_gemm(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, stream, variant);
+}
+
+int tcgemm_pick_variant(int64_t M, int64_t N, int64_t K, int num_sms) { return pick_variant(M, N, K, num_sms); }
+
+int tcgemm_plan(int64_t M, int64_t N, int64_t K, int variant, int num_sms, int64_t* out) {
+    if (out == nullptr || M <= 0 || N <= 0 || K <= 0 || num_sms <= 0) return TCGEMM_ERR_INVALID_ARG;
+    Plan pl;
+    if (!make_plan(M, N, K, variant, num_sms, num_sms / 2, pl)) return TCGEMM_ERR_INVALID_ARG;
+    out[0] = pl.grid;
+    out[1] = pl.cta_group;
+    out[2] = pl.tiles_m;
+    out[3] = pl.tiles_n;
+    out[4] = pl.bm;
+    out[5] = pl.bn;
+    out[6] = pl.num_kb;
+    out[7] = pl.smem;
+    return TCGEMM_OK;
+}
+
+int tcgemm_tile_order(int tiles_m, int tiles_n, int group_m, int64_t count, int32_t* tm, int32_t* tn) {
+    if (tiles_m <= 0 || tiles_n <= 0 || group_m <= 0 || count < 0 || tm == nullptr || tn == nullptr)
+        return TCGEMM_ERR_INVALID_ARG;
+    for (int64_t t = 0; t < count; ++t) {
+        int a, b;
+        tcg::grouped_tile(static_cast<int>(t), tiles_m, tiles_n, group_m, a, b);
+        tm[t] = a;
+        tn[t] = b;
+    }
+    return TCGEMM_OK;
+}
+
+const char* tcgemm_status_string(int status) {
+    switch (status) {
+        case TCGEMM_OK: return "TCGEMM_OK";
+        case TCGEMM_ERR_INVALID_ARG: return "TCGEMM_ERR_INVALID_ARG";
+        case TCGEMM_ERR_ALIGNMENT: return "TCGEMM_ERR_ALIGNMENT";
+        case TCGEMM_ERR_UNSUPPORTED_DEVICE: return "TCGEMM_ERR_UNSUPPORTED_DEVICE";
+        case TCGEMM_ERR_CUDA: return "TCGEMM_ERR_CUDA";
+        case TCGEMM_ERR_TIMEOUT: return "TCGEMM_ERR_TIMEOUT";
+        default: return "TCGEMM_ERR_UNKNOWN";
+    }
+}
+
+const char* tcgemm_last_error(void) { return t_last_error; }
+
+int tcgemm_check_device_status(void* stream, uint32_t* where_out) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        set_error("cudaStreamSynchronize: %s", cudaGetErrorString(e));
+        return TCGEMM_ERR_CUDA;
+    }
+    uint32_t st[4] = {0, 0, 0, 0};
+    e = cudaMemcpyFromSymbol(st, tcg::g_tcgemm_status, sizeof st);
+    if (e != cudaSuccess) {
+        set_error("reading the status word: %s", cudaGetErrorString(e));
+        return TCGEMM_ERR_CUDA;
+    }
+    if (st[0] == 0) return TCGEMM_OK;
+    const uint32_t zero[4] = {0, 0, 0, 0};
+    e = cudaMemcpyToSymbol(tcg::g_tcgemm_status, zero, sizeof zero);
+    if (where_out) *where_out = st[1];
+    set_error("device wait timed out (role %u, block %u)", st[1], st[2]);
+    if (e != cudaSuccess) return TCGEMM_ERR_CUDA;
+    return st[0] == tcg::kStatusTimeout ? TCGEMM_ERR_TIMEOUT : TCGEMM_ERR_CUDA;
+}
+
+int tcgemm_selftest_timeout(void* stream, uint64_t timeout_ns_arg) {
+    int dev = 0;
+    DeviceInfo info;
+    int rc = probe_device(dev, info);
+    if (rc != TCGEMM_OK) return rc;
+    if (timeout_ns_arg == 0 || timeout_ns_arg > 10ull * 1000 * 1000 * 1000) {
+        set_error("self-test timeout must be in (0, 10 s]");
+        return TCGEMM_ERR_INVALID_ARG;
+    }
+    tcg::selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(timeout_ns_arg);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("kernel launch: %s", cudaGetErrorString(e));
+        return TCGEMM_ERR_CUDA;
+    }
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return tcgemm_check_device_status(stream, nullptr);
+}
+
+uint64_t tcgemm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int tcgemm_version(void) { return 100; }
+
+}  // extern "C"

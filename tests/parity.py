@@ -3,6 +3,13 @@
 * fp32 output: |C - C_ref| <= 1e-3 * sqrt(K) * max(1, |C_ref|), elementwise.
 * bf16 output: the two bit patterns, mapped to an ordered integer line, are at
   most 1 apart (within one bf16 ulp of the oracle's single rounding).
+  Where the exact value is so small (cancellation) that the fp32 accumulator's
+  own rounding error exceeds half a bf16 ulp, no fp32-accumulating kernel can
+  meet that bar; there an element is also accepted if
+      |C - D| <= ulp_bf16(D) + K * 2^-24 * G,   G = sum_k |A[i,k] B[k,j]|,
+  the classical worst-case bound for a K-term floating-point sum in any
+  order, plus the output rounding.  At most 0.5% (+2) of the elements may
+  need this second clause, so a real bug cannot hide behind it.
 * Integer-valued inputs: bit-exact.
 
 C_ref is the oracle's fp64 value D (for fp32 output) or its bf16 rounding.
@@ -43,7 +50,25 @@ def check_f32(got: np.ndarray, ref_f64: np.ndarray, K: int, what: str = "") -> N
                              f"tolerance; first {idx.tolist()} got {got[bad][:5]} ref {ref[bad][:5]}")
 
 
-def check_bf16(got_bits: np.ndarray, ref_bits: np.ndarray, what: str = "", max_ulp: int = 1) -> None:
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 values at |x| (2^-133 below the normal range)."""
+    ax = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(ax, 2.0 ** -126)))
+    return np.exp2(e - 7)
+
+
+ACC_UNIT = 2.0 ** -24  # unit roundoff of the fp32 accumulator
+
+
+def check_bf16(got_bits: np.ndarray, ref_bits: np.ndarray, what: str = "", max_ulp: int = 1,
+               fallback=None) -> None:
+    """``fallback(flat_indices) -> (D, G, K)`` supplies the exact value D and
+    G = sum|a*b| at the elements that miss the 1-ulp bar (see module doc)."""
     got_bits = np.asarray(got_bits, dtype=np.uint16)
     ref_bits = np.asarray(ref_bits, dtype=np.uint16)
     assert got_bits.shape == ref_bits.shape
@@ -53,6 +78,14 @@ def check_bf16(got_bits: np.ndarray, ref_bits: np.ndarray, what: str = "", max_u
     bad = d > max_ulp
     nan_got = (got_bits & 0x7FFF) > 0x7F80
     bad |= nan_got
+    if bad.any() and fallback is not None and not nan_got.any():
+        flat = np.flatnonzero(bad)
+        limit = int(0.005 * got_bits.size) + 2
+        if flat.size <= limit:
+            D, G, K = fallback(flat)
+            got = bf16_to_f64(got_bits.reshape(-1)[flat])
+            ok = np.abs(got - D) <= bf16_ulp(D) + K * ACC_UNIT * G
+            bad.reshape(-1)[flat[ok]] = False
     if bad.any():
         idx = np.argwhere(bad)[:5]
         raise AssertionError(f"{what}: {int(bad.sum())} of {got_bits.size} bf16 outputs more than "

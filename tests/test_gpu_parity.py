@@ -1,0 +1,163 @@
+"""GPU parity: the CUDA library, called through the C ABI, against the CPU
+oracle on the same seeded inputs.
+
+Bars: fp32 output within 1e-3*sqrt(K)*max(1,|ref|); bf16 output within one
+bf16 ulp of the oracle's single rounding; integer-valued inputs bit-exact.
+Every run also checks guard bands around C and the ldc padding rows, and
+with beta == 0 the C buffer is pre-filled with NaN (C must not be read).
+"""
+from __future__ import annotations
+
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import gemm_inputs as gi
+from tests import gpu_harness as H
+
+pytestmark = pytest.mark.gpu
+
+import os
+
+# 1-CTA and 2-CTA kernels; TCGEMM_TEST_VARIANTS="1" narrows a run to one of them.
+VARIANTS = [int(v) for v in os.environ.get("TCGEMM_TEST_VARIANTS", "1,2").split(",") if v]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import tensor_core_matmul_gb300 as tc
+    tc.lib()  # fails loudly if the library is missing
+
+
+@pytest.mark.parametrize("variant", [0] + VARIANTS)
+def test_square_256_fp32_full(oracle_lib, variant):
+    case = gi.config_case("s256")
+    g = H.run_case(case, variant)
+    H.compare_full(oracle_lib, case, g.result_np(), what=f"s256 v{variant}")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("out", [gi.OUT_F32, gi.OUT_BF16])
+@pytest.mark.parametrize("beta", [0.0, 0.5])
+def test_integer_bit_exact(oracle_lib, variant, out, beta):
+    """Integer inputs: every partial sum is an exact integer in fp32, so any
+    correct kernel matches the oracle bit for bit (indexing, masks, alpha/beta)."""
+    for n, (M, N, K) in enumerate([(300, 520, 448), (129, 257, 65), (513, 200, 1000)]):
+        case = gi.make_case(f"int{n}", M, N, K, alpha=1.0, beta=beta, out_dtype=out, seed=40 + n,
+                            kind="integer")
+        g = H.run_case(case, variant)
+        H.compare_full(oracle_lib, case, g.result_np(), exact=True, what=f"int {M}x{N}x{K}")
+
+
+SWEEP_MN = [1, 7, 64, 65, 127, 129, 257]
+SWEEP_K = [1, 16, 63, 64, 65, 192, 384]
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_small_shape_sweep(oracle_lib, variant):
+    """Tiny and ragged shapes, odd and even k-block counts (3 and 6 blocks of
+    64), K below one block, every M/N tail."""
+    combos = list(itertools.product(SWEEP_MN, SWEEP_MN, SWEEP_K))
+    rng = np.random.default_rng(5)
+    pick = [combos[i] for i in rng.choice(len(combos), size=60, replace=False)]
+    pick += [(1, 1, 1), (257, 257, 384), (7, 129, 65), (129, 7, 63)]
+    for n, (M, N, K) in enumerate(pick):
+        out = gi.OUT_BF16 if n % 2 else gi.OUT_F32
+        beta = 0.5 if n % 3 == 0 else 0.0
+        case = gi.make_case(f"sw{n}", M, N, K, alpha=1.5, beta=beta, out_dtype=out, seed=200 + n)
+        g = H.run_case(case, variant)
+        H.compare_full(oracle_lib, case, g.result_np(), what=f"sweep {M}x{N}x{K} out{out} b{beta}")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_padded_leading_dimensions(oracle_lib, variant):
+    case = gi.make_case("pad", 200, 300, 136, alpha=-2.0, beta=0.25, out_dtype=gi.OUT_F32, seed=7,
+                        lda=136 + 24, ldb=136 + 8, ldc=200 + 12)
+    g = H.run_case(case, variant)
+    H.compare_full(oracle_lib, case, g.result_np(), what="padded ld")
+
+
+@pytest.mark.parametrize("name", ["s4k", "s8k", "edge", "skinny"])
+def test_configs_sampled(oracle_lib, name):
+    """The full-size workloads in the launch configuration the benchmark times
+    (automatic variant), checked at 2 random points in every 128 x 128 cell of
+    C plus the corners, and at every position of a few whole rows/columns."""
+    case = gi.config_case(name)
+    g = H.run_case(case, 0)
+    got = g.result_np()
+    rows, cols = gi.cell_sample_indices(case.M, case.N, 128, 128, 2, seed=11)
+    H.compare_sampled(oracle_lib, case, got, rows, cols, what=name)
+    for j in [0, case.N // 2 + 3, case.N - 1]:
+        r = np.arange(case.M, dtype=np.int64)
+        H.compare_sampled(oracle_lib, case, got, r, np.full_like(r, j), what=f"{name} col {j}")
+    for i in [0, case.M - 1]:
+        c = np.arange(case.N, dtype=np.int64)
+        H.compare_sampled(oracle_lib, case, got, np.full_like(c, i), c, what=f"{name} row {i}")
+    assert not np.isnan(got.astype(np.float32) if got.dtype != np.uint16 else
+                        ((got & 0x7FFF) > 0x7F80)).any()
+
+
+@pytest.mark.parametrize("name", ["edge", "s8k"])
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_configs_integer_exact_sampled(oracle_lib, name, variant):
+    """The full-size shapes with integer-valued inputs: bit-exact at every
+    sampled position for both kernels."""
+    case = gi.config_case(name, kind="integer")
+    g = H.run_case(case, variant)
+    rows, cols = gi.cell_sample_indices(case.M, case.N, 256, 256, 1, seed=12)
+    H.compare_sampled(oracle_lib, case, g.result_np(), rows, cols, exact=True, what=f"{name} int")
+
+
+def test_k_zero_scales_c(oracle_lib):
+    case = gi.make_case("k0", 70, 33, 0, alpha=1.0, beta=0.5, out_dtype=gi.OUT_F32, seed=3, kind="integer")
+    g = H.run_case(case)
+    H.compare_full(oracle_lib, case, g.result_np(), exact=True, what="K=0")
+    case0 = gi.make_case("k00", 70, 33, 0, alpha=1.0, beta=0.0, out_dtype=gi.OUT_BF16, seed=3)
+    g = H.run_case(case0)
+    assert not g.result_np().any()
+
+
+def test_nonzero_stream_and_repeat(oracle_lib):
+    """Runs on a side stream, twice in a row (the second call reuses every
+    barrier and TMEM path from a clean start)."""
+    case = gi.make_case("st", 384, 640, 320, out_dtype=gi.OUT_BF16, seed=9)
+    s = torch.cuda.Stream()
+    for _ in range(2):
+        with torch.cuda.stream(s):
+            g = H.run_case(case, 0, stream=s)
+        H.compare_full(oracle_lib, case, g.result_np(), what="stream")
+
+
+def test_nan_inf_propagate():
+    """A NaN in A reaches exactly the outputs of its row; an Inf in B reaches
+    exactly the outputs of its column (IEEE propagation, no special casing)."""
+    case = gi.make_case("nan", 130, 260, 96, out_dtype=gi.OUT_F32, seed=21)
+    A = case.A.clone()
+    B = case.B.clone()
+    A[5, 17] = float("nan")
+    B[200, 3] = float("inf")  # column 200 of B
+    case.A, case.B = A, B
+    g = H.run_case(case, 0)
+    got = g.result_np()  # (N, M)
+    assert np.isnan(got[:, 5]).all()
+    col = got[200, :]
+    assert np.isnan(col[5]) and (~np.isfinite(np.delete(col, 5))).all()
+    mask = np.ones_like(got, dtype=bool)
+    mask[:, 5] = False
+    mask[200, :] = False
+    assert np.isfinite(got[mask]).all()
+
+
+def test_hang_guard_selftest():
+    """A wait that nothing satisfies gives up after its limit and reports
+    TCGEMM_ERR_TIMEOUT; the context stays usable afterwards."""
+    import tensor_core_matmul_gb300 as tc
+    st = tc.selftest_timeout(20_000_000)  # 20 ms
+    assert st == 5, st
+    assert tc.check_device_status()[0] == 0  # status word was cleared
+    case = gi.make_case("after", 128, 256, 64, out_dtype=gi.OUT_F32, seed=2, kind="integer")
+    H.run_case(case)

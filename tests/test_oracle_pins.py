@@ -86,6 +86,11 @@ def pin_integer_bruteforce(o):
                 if beta != 0.0:
                     want += Fraction(beta) * Fraction(float(Cin[j, i]))
                 assert D[j, i] == float(want), (n, i, j, D[j, i], want)
+        rows, cols = np.divmod(np.arange(M * N), N)
+        G = o.absdot_sampled_f64(M, N, K, _u16(case.A), _u16(case.B), rows, cols)
+        for s_, (i, j) in enumerate(zip(rows, cols)):
+            want = sum((abs(A[i, k] * B[j, k]) for k in range(K)), Fraction(0))
+            assert G[s_] == float(want), (n, i, j, G[s_], want)
 
 
 def pin_numpy_f64(o):
@@ -140,6 +145,9 @@ def pin_closed_forms(o):
     B = torch.tensor(np.outer(v, w), dtype=torch.bfloat16)  # row j = column j
     D = o.gemm_f64(M, N, K, _u16(A), _u16(B))
     assert np.array_equal(D, np.outer(v, u) * float(np.sum(w * w)))
+    r, c = np.divmod(np.arange(M * N), N)
+    G = o.absdot_sampled_f64(M, N, K, _u16(A), _u16(B), r, c)
+    assert np.array_equal(G, np.abs(u[r] * v[c]) * float(np.sum(w * w)))
 
 
 def pin_bf16_rounding(o):
