@@ -162,7 +162,7 @@ def run_ours(args) -> None:
     stream = torch.cuda.current_stream(dev)
 
     def gemm():
-        tc.gemm_bf16(A, B, C, case.alpha, case.beta, M=M, N=N, K=K, stream=stream)
+        tc.gemm_bf16(A, B, C, case.alpha, case.beta, M=M, N=N, K=K, stream=stream, variant=args.variant)
 
     for _ in range(args.warmup):
         flush.fill_(1)
@@ -211,8 +211,9 @@ def run_ours(args) -> None:
     peak = float(peaks["bf16_tflops"])
     achieved = flops / (total_s / args.steps) / 1e12
     traffic = profile_traffic(f"gemm_{args.config}")
-    plan = tc.plan(M, N, K, 0, torch.cuda.get_device_properties(dev).multi_processor_count)
-    variant = tc.pick_variant(M, N, K, torch.cuda.get_device_properties(dev).multi_processor_count)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    variant = args.variant or tc.pick_variant(M, N, K, sms)
+    plan = tc.plan(M, N, K, variant, sms)
 
     e2e = None
     if not args.no_e2e:
@@ -290,7 +291,8 @@ def measure_e2e(args, case, dev, stream) -> dict:
         dB.copy_(hB, non_blocking=True)
         if has_beta:
             dC.copy_(hC_in, non_blocking=True)
-        tc.gemm_bf16(dA, dB, dC, case.alpha, case.beta, M=case.M, N=case.N, K=case.K, stream=stream)
+        tc.gemm_bf16(dA, dB, dC, case.alpha, case.beta, M=case.M, N=case.N, K=case.K, stream=stream,
+                     variant=args.variant)
         hC.copy_(dC, non_blocking=True)
 
     for _ in range(3):
@@ -396,6 +398,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="s4k", choices=["s256", "s4k", "s8k", "edge", "skinny"])
+    ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 one-CTA, 2 CTA-pair kernel")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")

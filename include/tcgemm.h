@@ -65,7 +65,12 @@ typedef enum {
 typedef enum {
     TCGEMM_VARIANT_AUTO = 0,
     TCGEMM_VARIANT_1CTA = 1,  /* one CTA per SM, 128 x 256 tiles, cta_group::1 MMA   */
-    TCGEMM_VARIANT_2CTA = 2   /* CTA pairs, 256 x 256 tiles, cta_group::2 MMA (M=256) */
+    TCGEMM_VARIANT_2CTA = 2,  /* CTA pairs, 256 x 256 tiles, cta_group::2 MMA (M=256) */
+    TCGEMM_VARIANT_1CTA_MC = 3, /* 4-CTA clusters on 2 x 2 blocks of 128 x 256 tiles; each CTA
+                                  loads half of its A and B tiles and multicasts them to the
+                                  CTA sharing its tile row / tile column */
+    TCGEMM_VARIANT_1CTA_N64 = 4 /* one CTA per SM, narrow 128 x 64 tiles, 9-stage pipeline: the
+                                  choice for M <= 128, where B is streamed from memory once */
 } tcgemm_variant_t;
 
 /* C = alpha*A*B + beta*C as described above.  Returns TCGEMM_OK once the work
@@ -85,6 +90,29 @@ int gemm_bf16_variant(int64_t M, int64_t N, int64_t K,
                       void* C, int64_t ldc,
                       float alpha, float beta, int out_dtype, void* stream, int variant);
 
+/* Same operation with a caller-supplied workspace instead of the library's
+ * own.  Some shapes split the tiles of the last, partial round of work along
+ * K (see tcgemm_workspace_bytes); their fp32 partial tiles and arrival
+ * counters live in the workspace.  `workspace` is device memory of at least
+ * tcgemm_workspace_bytes(M, N, K, variant, SMs) bytes, 256-byte aligned, whose
+ * first 4096 bytes are zero before its first use; the library leaves them
+ * zero after every completed call.  Calls that overlap on the GPU must not
+ * share a workspace.  With a plan that needs none, `workspace` may be NULL.
+ * Too small, misaligned or NULL when needed -> TCGEMM_ERR_INVALID_ARG.
+ * (gemm_bf16 and gemm_bf16_variant use a library-owned workspace per device
+ * and stream instead: about 19.5 MiB, allocated on the first call that needs
+ * one on that stream, so make that first call before any stream capture.) */
+int gemm_bf16_ws(int64_t M, int64_t N, int64_t K,
+                 const void* A, int64_t lda,
+                 const void* B, int64_t ldb,
+                 void* C, int64_t ldc,
+                 float alpha, float beta, int out_dtype, void* stream, int variant,
+                 void* workspace, int64_t workspace_bytes);
+
+/* Workspace bytes the launch for this shape and variant needs on a device
+ * with `num_sms` SMs (0: none).  Host only. */
+int64_t tcgemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int variant, int num_sms);
+
 /* The variant gemm_bf16 would run for this shape on a device with `num_sms`
  * streaming multiprocessors.  Host only; needs no GPU. */
 int tcgemm_pick_variant(int64_t M, int64_t N, int64_t K, int num_sms);
@@ -93,8 +121,14 @@ int tcgemm_pick_variant(int64_t M, int64_t N, int64_t K, int num_sms);
  * and tools: out[0] = grid size (CTAs), out[1] = CTAs per cluster, out[2] =
  * tile rows (tiles_m), out[3] = tile columns (tiles_n), out[4] = tile height,
  * out[5] = tile width, out[6] = k-blocks per tile, out[7] = dynamic shared
- * memory bytes.  `out` must hold 8 values.  Returns TCGEMM_OK or
- * TCGEMM_ERR_INVALID_ARG.  Needs no GPU. */
+ * memory bytes, out[8] = tiles computed whole, out[9] = tiles split along K,
+ * out[10] = pieces per split tile, out[11] = workspace bytes, out[12] = tile
+ * band height of the visiting order, out[13] = variant, out[14] = CTAs per
+ * MMA (cta_group), out[15], out[16] = rows and columns of the unit grid the
+ * visiting order walks (tiles, or 2 x 2 tile blocks for variant 3), out[17] =
+ * 1 when the split tiles are split along N into two half-width tiles (0: along
+ * K).  `out` must hold 18 values.  Returns TCGEMM_OK or TCGEMM_ERR_INVALID_ARG.  Needs no
+ * GPU. */
 int tcgemm_plan(int64_t M, int64_t N, int64_t K, int variant, int num_sms, int64_t* out);
 
 /* Tile visiting order used by the persistent kernels (host copy of the device

@@ -19,7 +19,7 @@ from . import _build
 
 OUT_F32 = 0
 OUT_BF16 = 1
-VARIANT_AUTO, VARIANT_1CTA, VARIANT_2CTA = 0, 1, 2
+VARIANT_AUTO, VARIANT_1CTA, VARIANT_2CTA, VARIANT_1CTA_MC, VARIANT_1CTA_N64 = 0, 1, 2, 3, 4
 
 STATUS = {0: "TCGEMM_OK", 1: "TCGEMM_ERR_INVALID_ARG", 2: "TCGEMM_ERR_ALIGNMENT",
           3: "TCGEMM_ERR_UNSUPPORTED_DEVICE", 4: "TCGEMM_ERR_CUDA", 5: "TCGEMM_ERR_TIMEOUT"}
@@ -55,6 +55,10 @@ def lib() -> ctypes.CDLL:
     L.gemm_bf16.restype = i32
     L.gemm_bf16_variant.argtypes = gemm_args + [i32]
     L.gemm_bf16_variant.restype = i32
+    L.gemm_bf16_ws.argtypes = gemm_args + [i32, p, i64]
+    L.gemm_bf16_ws.restype = i32
+    L.tcgemm_workspace_bytes.argtypes = [i64, i64, i64, i32, i32]
+    L.tcgemm_workspace_bytes.restype = i64
     L.tcgemm_pick_variant.argtypes = [i64, i64, i64, i32]
     L.tcgemm_pick_variant.restype = i32
     L.tcgemm_plan.argtypes = [i64, i64, i64, i32, i32, ctypes.POINTER(ctypes.c_int64)]
@@ -153,10 +157,24 @@ def pick_variant(M: int, N: int, K: int, num_sms: int) -> int:
 
 
 def plan(M: int, N: int, K: int, variant: int = 0, num_sms: int = 152) -> dict:
-    out = (ctypes.c_int64 * 8)()
+    out = (ctypes.c_int64 * 18)()
     _check(lib().tcgemm_plan(M, N, K, variant, num_sms, out))
-    keys = ["grid", "cta_group", "tiles_m", "tiles_n", "bm", "bn", "num_kb", "smem"]
+    keys = ["grid", "cluster", "tiles_m", "tiles_n", "bm", "bn", "num_kb", "smem", "tiles_dp",
+            "tiles_split", "splits", "ws_bytes", "group_m", "variant", "cta_group", "grid_m", "grid_n",
+            "split_n"]
     return dict(zip(keys, [int(v) for v in out]))
+
+
+def workspace_bytes(M: int, N: int, K: int, variant: int = 0, num_sms: int = 152) -> int:
+    return int(lib().tcgemm_workspace_bytes(M, N, K, variant, num_sms))
+
+
+def gemm_bf16_ws_raw(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int, C: int, ldc: int,
+                     alpha: float, beta: float, out_dtype: int, stream: int, variant: int,
+                     workspace: int, workspace_bytes: int) -> int:
+    """Pointer-level call with a caller-owned workspace; returns the status."""
+    return lib().gemm_bf16_ws(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, stream, variant,
+                              workspace, workspace_bytes)
 
 
 def tile_order(tiles_m: int, tiles_n: int, group_m: int, count: Optional[int] = None):

@@ -27,6 +27,18 @@
 //    out-of-range A/B elements with zeros, so they add nothing; the epilogue
 //    masks out-of-range rows and columns of C.
 //
+// Tail splits (not on the pages; the work log's conclusion attributes its
+// remaining per-size gaps to tuning).  When the tile count is not a multiple
+// of the number of persistent CTAs (pairs), the tiles of the last, partial
+// round are split so that more CTAs share that round:
+//  * along N into two half-width tiles (MMA N = BN/2): no workspace, and the
+//    same arithmetic as a whole tile;
+//  * along K into S pieces (problems with fewer tiles than CTAs and a long K):
+//    each piece writes its fp32 partial tile to a workspace slot and bumps a
+//    per-tile counter; the piece that arrives last adds the S partials in
+//    piece order (the result does not depend on arrival order) and runs the
+//    epilogue.  No CTA ever waits for another.
+//
 // Every wait on a barrier is bounded by %globaltimer.  On expiry the waiting
 // thread records TCGEMM_ERR_TIMEOUT in the device status word, raises the
 // CTA's abort flag and leaves its loop; the CTA then drains its own copies and
@@ -109,10 +121,74 @@ __host__ __device__ __forceinline__ void grouped_tile(int t, int tiles_m, int ti
 struct GemmParams {
     int M, N, K;
     int tiles_m, tiles_n, num_kb, group_m;
+    int grid_m, grid_n;  // grid the unit order walks: tiles, or 2 x 2 tile blocks of a multicast cluster
+    int tiles_dp;      // tiles computed whole, round-robin over the clusters
+    int tiles_split;   // trailing tiles split ...
+    int splits;        // ... into this many pieces (1 = no split) ...
+    int split_n;       // ... along N (1, then splits == 2) or along K (0)
     int64_t ldc;
     void* C;
     float alpha, beta;
+    float* ws;               // split partials: [slot][cta rank][BN cols][128 rows] fp32
+    unsigned int* counters;  // one arrival counter per (split tile, cta rank), zero between launches
     uint64_t timeout_ns;
+};
+
+// One unit of work for a cluster: a whole tile, or one K-piece of a split tile.
+struct WorkUnit {
+    int tile;       // index in grouped order
+    int kb0, kb1;   // k-block range [kb0, kb1)
+    int piece;      // piece index (0 for whole tiles)
+    int slot;       // K-split tile index among the split tiles (-1: no partials)
+    int nhalf;      // -1: all BN columns; 0 / 1: first / second half of them
+};
+
+// Walks the units of one cluster: its share of the whole tiles, then at most
+// one piece of a split tile.  Producer, MMA and epilogue roles each run their
+// own copy and see the same sequence.
+struct UnitIter {
+    int next_dp;   // next whole tile
+    int stride;
+    int cluster;
+    bool split_done;
+
+    __host__ __device__ UnitIter(int cluster_id, int num_clusters)
+        : next_dp(cluster_id), stride(num_clusters), cluster(cluster_id), split_done(false) {}
+
+    __host__ __device__ bool next(const GemmParams& p, WorkUnit& u) {
+        if (next_dp < p.tiles_dp) {
+            u.tile = next_dp;
+            u.kb0 = 0;
+            u.kb1 = p.num_kb;
+            u.piece = 0;
+            u.slot = -1;
+            u.nhalf = -1;
+            next_dp += stride;
+            return true;
+        }
+        if (!split_done) {
+            split_done = true;
+            const int units = p.tiles_split * p.splits;
+            if (cluster < units) {
+                const int s = cluster / p.splits;
+                u.piece = cluster - s * p.splits;
+                u.tile = p.tiles_dp + s;
+                if (p.split_n) {
+                    u.kb0 = 0;
+                    u.kb1 = p.num_kb;
+                    u.slot = -1;
+                    u.nhalf = u.piece;
+                } else {
+                    u.slot = p.splits > 1 ? s : -1;
+                    u.nhalf = -1;
+                    u.kb0 = static_cast<int>((static_cast<int64_t>(u.piece) * p.num_kb) / p.splits);
+                    u.kb1 = static_cast<int>((static_cast<int64_t>(u.piece + 1) * p.num_kb) / p.splits);
+                }
+                return true;
+            }
+        }
+        return false;
+    }
 };
 
 template <int CTA_GROUP, int BN, int STAGES>
@@ -130,6 +206,8 @@ struct GemmCfg {
     static constexpr uint32_t kBarOff = STAGES * (kABytes + kBBytes);
     static constexpr uint32_t kNumBars = 2 * STAGES + 4 + 1;
     static constexpr uint32_t kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
+    // Workspace bytes per split piece (both CTAs of a pair).
+    static constexpr uint64_t kSlotBytes = static_cast<uint64_t>(CTA_GROUP) * 128 * BN * 4;
     static_assert(kTmemCols <= 512, "TMEM has 512 columns");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "epilogue works in 32-column chunks");
     static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
@@ -153,14 +231,58 @@ __device__ __forceinline__ void store_out<__nv_bfloat16>(__nv_bfloat16* p, float
     *p = __float2bfloat16_rn(v);
 }
 
-template <int CTA_GROUP, int BN, int STAGES, typename OutT>
+// alpha*acc (+ beta*C) for the 32 columns [col0, col0+32) of one row; `acc`
+// holds fp32 bit patterns.  Columns at or beyond N are skipped.
+template <typename OutT>
+__device__ __forceinline__ void epilogue_store32(OutT* dst, int64_t ldc, int64_t col0, int64_t N,
+                                                 const uint32_t (&acc)[32], float alpha, float beta,
+                                                 const float (&cold)[32], bool has_beta) {
+    if (has_beta) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (col0 + j < N) store_out<OutT>(dst + j * ldc, fmaf(alpha, __uint_as_float(acc[j]), beta * cold[j]));
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (col0 + j < N) store_out<OutT>(dst + j * ldc, alpha * __uint_as_float(acc[j]));
+        }
+    }
+}
+
+// beta != 0: issue all 32 reads of C before the first write so they are in
+// flight together (a write may alias a later read, so the compiler would
+// otherwise serialise them).
+template <typename OutT>
+__device__ __forceinline__ void load_cold32(const OutT* dst, int64_t ldc, int64_t col0, int64_t N,
+                                            float (&cold)[32]) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) cold[j] = (col0 + j < N) ? load_out<OutT>(dst + j * ldc) : 0.0f;
+}
+
+constexpr uint32_t kEpiBarrier = 1;     // named barrier id for the 4 epilogue warps
+constexpr uint32_t kEpiThreads = 128;
+
+// MC = 1: no multicast.  MC = 4 (single-CTA MMAs only): a cluster of 4 CTAs
+// computes a 2 x 2 block of tiles; CTA (rm, rn) = (rank & 1, rank >> 1) owns
+// tile (2*TM + rm, 2*TN + rn).  The two CTAs of a tile row need the same A
+// rows, the two of a tile column the same B columns, so each CTA loads half of
+// its A tile and half of its B tile and multicasts each half to itself and to
+// its partner: a quarter less traffic from L2 per CTA than a CTA pair, half of
+// a lone CTA's.  (The work log's "内核 8：线程块集群" multicasts the shared B
+// tile to two vertically adjacent tiles; this is the same idea in both
+// directions.)
+// tmBh is the B tensor map with half the box height, for half-width units.
+template <int CTA_GROUP, int BN, int STAGES, int MC, typename OutT>
 __global__ void __launch_bounds__(192, 1)
     gemm_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const GemmParams p) {
+                        const __grid_constant__ CUtensorMap tmBh, const GemmParams p) {
     using Cfg = GemmCfg<CTA_GROUP, BN, STAGES>;
+    static_assert(MC == 1 || (MC == 4 && CTA_GROUP == 1), "multicast clusters use single-CTA MMAs");
+    constexpr int kCluster = CTA_GROUP * MC;
     extern __shared__ uint8_t smem_raw[];
 
-    // 1 KB-aligned carve-up: [A stages][B stages][barriers][tmem slot][abort]
+    // 1 KB-aligned carve-up: [A stages][B stages][barriers][tmem slot][abort][last flag]
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t base = (raw_u32 + 1023u) & ~1023u;
     uint8_t* smem = smem_raw + (base - raw_u32);
@@ -174,18 +296,28 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kBarOff + Cfg::kNumBars * 8);
     volatile uint32_t* abort_flag = tmem_slot + 1;
+    volatile uint32_t* last_flag = tmem_slot + 2;
 
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31u;
-    const uint32_t rank = (CTA_GROUP == 2) ? cluster_ctarank() : 0u;
-    const int cluster_id = blockIdx.x / CTA_GROUP;
-    const int num_clusters = gridDim.x / CTA_GROUP;
-    const int num_tiles = p.tiles_m * p.tiles_n;
+    const uint32_t crank = (kCluster > 1) ? cluster_ctarank() : 0u;
+    const uint32_t rank = (CTA_GROUP == 2) ? crank : 0u;  // position in the MMA pair
+    const uint32_t rm = (MC == 4) ? (crank & 1u) : 0u;    // position in the 2 x 2 block
+    const uint32_t rn = (MC == 4) ? (crank >> 1) : 0u;
+    const int cluster_id = blockIdx.x / kCluster;
+    const int num_clusters = gridDim.x / kCluster;
+    auto tile_of = [&](int unit_tile, int& tm, int& tn) {
+        grouped_tile(unit_tile, p.grid_m, p.grid_n, p.group_m, tm, tn);
+        if (MC == 4) {
+            tm = 2 * tm + static_cast<int>(rm);
+            tn = 2 * tn + static_cast<int>(rn);
+        }
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), MC == 4 ? 3 : 1);  // MC: self, row partner, column partner
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
@@ -193,11 +325,12 @@ __global__ void __launch_bounds__(192, 1)
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0u;
+        *last_flag = 0u;
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc<CTA_GROUP>(smem_u32(tmem_slot), Cfg::kTmemCols);
     tc_fence_before_sync();
-    if constexpr (CTA_GROUP == 1) {
+    if constexpr (kCluster == 1) {
         __syncthreads();
     } else {
         cluster_sync();
@@ -211,31 +344,48 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) {
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
+            if (p.split_n) tma_prefetch_desc(&tmBh);
             uint32_t stage = 0, phase = 0;
             uint64_t issued = 0;
             bool ok = true;
-            for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
+            UnitIter it(cluster_id, num_clusters);
+            WorkUnit u;
+            while (ok && it.next(p, u)) {
                 int tm, tn;
-                grouped_tile(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+                tile_of(u.tile, tm, tn);
+                const bool half = u.nhalf >= 0;
                 const int a_row = tm * Cfg::kBM + static_cast<int>(rank) * Cfg::kRowsA;
-                const int b_row = tn * BN + static_cast<int>(rank) * Cfg::kRowsB;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                const int b_row = half ? tn * BN + u.nhalf * (BN / 2) + static_cast<int>(rank) * (Cfg::kRowsB / 2)
+                                       : tn * BN + static_cast<int>(rank) * Cfg::kRowsB;
+                const CUtensorMap* mB = half ? &tmBh : &tmB;
+                const uint32_t stage_tx = half ? CTA_GROUP * (Cfg::kABytes + Cfg::kBBytes / 2) : Cfg::kStageTx;
+                for (int kb = u.kb0; kb < u.kb1; ++kb) {
                     if (!wait_phase<false>(empty_bar(stage), phase ^ 1u, wctx, kWhereProducer)) {
                         ok = false;
                         break;
                     }
                     const uint32_t sa = sA0 + stage * Cfg::kABytes;
                     const uint32_t sb = sB0 + stage * Cfg::kBBytes;
-                    if constexpr (CTA_GROUP == 1) {
+                    if constexpr (MC == 4) {
+                        // Own half of A -> this CTA and its row partner; own
+                        // half of B -> this CTA and its column partner.
+                        const uint16_t mask_a = static_cast<uint16_t>((1u << rm) | (1u << (rm + 2u)));
+                        const uint16_t mask_b = static_cast<uint16_t>(3u << (2u * rn));
                         mbar_arrive_expect_tx(full_bar(stage), Cfg::kStageTx);
+                        tma_load_2d_multicast(sa + rn * (Cfg::kABytes / 2), &tmA, full_bar(stage), kb * Cfg::kBK,
+                                              a_row + static_cast<int>(rn) * (Cfg::kRowsA / 2), mask_a);
+                        tma_load_2d_multicast(sb + rm * (Cfg::kBBytes / 2), &tmB, full_bar(stage), kb * Cfg::kBK,
+                                              b_row + static_cast<int>(rm) * (BN / 2), mask_b);
+                    } else if constexpr (CTA_GROUP == 1) {
+                        mbar_arrive_expect_tx(full_bar(stage), stage_tx);
                         tma_load_2d(sa, &tmA, full_bar(stage), kb * Cfg::kBK, a_row);
-                        tma_load_2d(sb, &tmB, full_bar(stage), kb * Cfg::kBK, b_row);
+                        tma_load_2d(sb, mB, full_bar(stage), kb * Cfg::kBK, b_row);
                     } else {
                         // Both CTAs' bytes land on the leader's barrier.
-                        if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), Cfg::kStageTx);
+                        if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), stage_tx);
                         const uint32_t fb = map_to_cta(full_bar(stage), 0);
                         tma_load_2d_pair(sa, &tmA, fb, kb * Cfg::kBK, a_row);
-                        tma_load_2d_pair(sb, &tmB, fb, kb * Cfg::kBK, b_row);
+                        tma_load_2d_pair(sb, mB, fb, kb * Cfg::kBK, b_row);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -262,14 +412,18 @@ __global__ void __launch_bounds__(192, 1)
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer --
         if (lane == 0 && (CTA_GROUP == 1 || rank == 0)) {
-            constexpr uint32_t kIdesc = idesc_bf16_f32(Cfg::kBM, BN);
+            constexpr uint32_t kIdescFull = idesc_bf16_f32(Cfg::kBM, BN);
+            constexpr uint32_t kIdescHalf = idesc_bf16_f32(Cfg::kBM, BN / 2);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
-            for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
+            UnitIter it(cluster_id, num_clusters);
+            WorkUnit u;
+            while (ok && it.next(p, u)) {
                 if (!wait_phase<CTA_GROUP == 2>(tempty_bar(acc), acc_phase ^ 1u, wctx, kWhereMma)) break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                const uint32_t idesc = u.nhalf >= 0 ? kIdescHalf : kIdescFull;
+                for (int kb = u.kb0; kb < u.kb1; ++kb) {
                     if (!wait_phase<false>(full_bar(stage), phase, wctx, kWhereMma)) {
                         ok = false;
                         break;
@@ -280,10 +434,17 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                     for (int k = 0; k < Cfg::kBK / Cfg::kUmmaK; ++k) {
                         // +32 bytes along K per step: (32 >> 4) = 2 in the address field.
-                        mma_bf16<CTA_GROUP>(d_tmem, ad + 2u * k, bd + 2u * k, kIdesc,
-                                            (kb | k) != 0 ? 1u : 0u);
+                        mma_bf16<CTA_GROUP>(d_tmem, ad + 2u * k, bd + 2u * k, idesc,
+                                            (kb != u.kb0 || k != 0) ? 1u : 0u);
                     }
-                    if constexpr (CTA_GROUP == 1) {
+                    if constexpr (MC == 4) {
+                        // The stage is free once this CTA and both partners
+                        // that multicast into it are done with it.
+                        const uint32_t row_partner = rm + 2u * (1u - rn);
+                        const uint32_t col_partner = (1u - rm) + 2u * rn;
+                        mma_commit_multicast(empty_bar(stage), static_cast<uint16_t>((1u << crank) | (1u << row_partner) |
+                                                                                     (1u << col_partner)));
+                    } else if constexpr (CTA_GROUP == 1) {
                         mma_commit(empty_bar(stage));
                     } else {
                         mma_commit_pair(empty_bar(stage), 0x3);
@@ -314,51 +475,113 @@ __global__ void __launch_bounds__(192, 1)
         // --------------------------------------------------- epilogue --
         // Warp w may only touch TMEM lanes 32*(w%4) .. 32*(w%4)+31.
         const uint32_t q = warp & 3u;
+        const uint32_t row_local = q * 32u + lane;  // 0..127 within this CTA's rows
         OutT* C = static_cast<OutT*>(p.C);
         const bool has_beta = p.beta != 0.0f;
         uint32_t acc = 0, acc_phase = 0;
-        for (int t = cluster_id; t < num_tiles; t += num_clusters) {
+        UnitIter it(cluster_id, num_clusters);
+        WorkUnit u;
+        while (it.next(p, u)) {
             int tm, tn;
-            grouped_tile(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+            tile_of(u.tile, tm, tn);
             uint32_t ok = 1;
             if (lane == 0) ok = wait_phase<false>(tfull_bar(acc), acc_phase, wctx, kWhereEpilogue) ? 1u : 0u;
             ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
+            // All four epilogue warps agree before going on, so none is left
+            // alone at a named barrier below if another one gave up.
+            if (!named_barrier_and(kEpiBarrier, kEpiThreads, ok != 0u)) break;
             tc_fence_after_sync();
-            const int64_t row = static_cast<int64_t>(tm) * Cfg::kBM + rank * 128 + q * 32 + lane;
+            const int64_t row = static_cast<int64_t>(tm) * Cfg::kBM + rank * 128 + row_local;
             const bool row_ok = row < p.M;
             const uint32_t tbase = tmem_base + ((q * 32u) << 16) + acc * BN;
+            // First column of the unit and its width (half-width units hold
+            // their BN/2 columns in the first BN/2 accumulator columns).
+            const int64_t colt = static_cast<int64_t>(tn) * BN + (u.nhalf > 0 ? BN / 2 : 0);
+            const int ncols = u.nhalf >= 0 ? BN / 2 : BN;
+
+            if (u.slot < 0) {
+                // Whole tile: TMEM -> alpha/beta -> C.
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
-                const int64_t col0 = static_cast<int64_t>(tn) * BN + c;
-                if (col0 >= p.N) break;
-                uint32_t r[32];
-                tmem_ld32(tbase + c, r);
-                tmem_ld_wait32(r);
-                if (row_ok) {
+                for (int c = 0; c < ncols; c += 32) {
+                    const int64_t col0 = colt + c;
+                    if (col0 >= p.N) break;
                     OutT* dst = C + col0 * p.ldc + row;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        if (col0 + j < p.N) {
-                            float v = __uint_as_float(r[j]);
-                            if (has_beta) {
-                                v = fmaf(p.alpha, v, p.beta * load_out<OutT>(dst));
-                            } else {
-                                v = p.alpha * v;
-                            }
-                            store_out<OutT>(dst, v);
-                        }
-                        dst += p.ldc;
+                    float cold[32];
+                    if (has_beta && row_ok) load_cold32<OutT>(dst, p.ldc, col0, p.N, cold);
+                    uint32_t r[32];
+                    tmem_ld32(tbase + c, r);
+                    tmem_ld_wait32(r);
+                    if (row_ok) epilogue_store32<OutT>(dst, p.ldc, col0, p.N, r, p.alpha, p.beta, cold, has_beta);
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (CTA_GROUP == 1) {
+                        mbar_arrive(tempty_bar(acc));
+                    } else {
+                        mbar_arrive_cluster(map_to_cta(tempty_bar(acc), 0));
                     }
                 }
-            }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-                if constexpr (CTA_GROUP == 1) {
-                    mbar_arrive(tempty_bar(acc));
-                } else {
-                    mbar_arrive_cluster(map_to_cta(tempty_bar(acc), 0));
+            } else {
+                // Piece of a split tile: write the fp32 partial (every row and
+                // column of the tile, in or out of range) to this piece's slot.
+                float* mine = p.ws + ((static_cast<int64_t>(u.slot) * p.splits + u.piece) * CTA_GROUP + rank) *
+                                         (static_cast<int64_t>(BN) * 128);
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tbase + c, r);
+                    tmem_ld_wait32(r);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) __stcg(mine + (c + j) * 128 + row_local, __uint_as_float(r[j]));
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (CTA_GROUP == 1) {
+                        mbar_arrive(tempty_bar(acc));
+                    } else {
+                        mbar_arrive_cluster(map_to_cta(tempty_bar(acc), 0));
+                    }
+                }
+                // Publish, then count arrivals on this (tile, rank).
+                __threadfence();
+                named_barrier_sync(kEpiBarrier, kEpiThreads);
+                if (warp == 2 && lane == 0) {
+                    unsigned int* cnt = p.counters + u.slot * CTA_GROUP + rank;
+                    const unsigned int prev = atomicAdd(cnt, 1u);
+                    const bool last = prev == static_cast<unsigned int>(p.splits - 1);
+                    if (last) atomicExch(cnt, 0u);  // leave it zero for the next launch
+                    *last_flag = last ? 1u : 0u;
+                }
+                named_barrier_sync(kEpiBarrier, kEpiThreads);
+                const bool last = *last_flag != 0u;
+                named_barrier_sync(kEpiBarrier, kEpiThreads);  // flag read by all before it is reused
+                if (last) {
+                    __threadfence();
+                    const float* slot0 = p.ws + (static_cast<int64_t>(u.slot) * p.splits * CTA_GROUP + rank) *
+                                                    (static_cast<int64_t>(BN) * 128);
+                    const int64_t piece_stride = static_cast<int64_t>(CTA_GROUP) * BN * 128;
+#pragma unroll 1
+                    for (int c = 0; c < BN; c += 32) {
+                        const int64_t col0 = colt + c;
+                        if (col0 >= p.N) break;
+                        OutT* dst = C + col0 * p.ldc + row;
+                        float cold[32];
+                        if (has_beta && row_ok) load_cold32<OutT>(dst, p.ldc, col0, p.N, cold);
+                        float sum[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) sum[j] = 0.0f;
+                        for (int s = 0; s < p.splits; ++s) {
+                            const float* src = slot0 + s * piece_stride + c * 128 + row_local;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) sum[j] += __ldcg(src + j * 128);
+                        }
+                        uint32_t r[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(sum[j]);
+                        if (row_ok) epilogue_store32<OutT>(dst, p.ldc, col0, p.N, r, p.alpha, p.beta, cold, has_beta);
+                    }
                 }
             }
             acc ^= 1u;
@@ -369,7 +592,7 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------- teardown --
     __syncwarp();
     tc_fence_before_sync();
-    if constexpr (CTA_GROUP == 1) {
+    if constexpr (kCluster == 1) {
         __syncthreads();
     } else {
         cluster_sync();

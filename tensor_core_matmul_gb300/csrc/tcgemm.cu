@@ -10,7 +10,9 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "../../include/tcgemm.h"
 #include "gemm_kernel.cuh"
@@ -67,6 +69,7 @@ struct DeviceInfo {
     bool supported = false;
     int sms = 0;
     int max_pairs = 0;  // co-resident CTA pairs for the 2-CTA kernel
+    int max_quads = 0;  // co-resident 4-CTA clusters for the multicast kernel
 };
 
 std::mutex g_dev_mu;
@@ -77,29 +80,56 @@ DeviceInfo g_dev[kMaxDevices];
 struct Plan {
     int variant = 0;
     int cta_group = 1;
+    int mc = 1;            // 4: 2 x 2 multicast cluster of single-CTA tiles
+    int grid_m = 0, grid_n = 0;
     int bm = 128, bn = 256;
     int tiles_m = 0, tiles_n = 0, num_kb = 0;
     int grid = 0;
     int group_m = 1;
+    int tiles_dp = 0, tiles_split = 0, splits = 1, split_n = 0;
     uint32_t smem = 0;
+    uint64_t slot_bytes = 0;  // workspace bytes per split piece
+    uint64_t ws_bytes = 0;    // workspace this plan needs (0 without a split)
 };
 
-constexpr int kStages1 = 4;  // 1-CTA: 4 x (16 KB A + 32 KB B)
-constexpr int kStages2 = 6;  // 2-CTA: 6 x (16 KB A + 16 KB B) per CTA
+constexpr int kMinKbPerPiece = 4;   // a split piece covers at least 4 k-blocks (256 of K)
+constexpr int kMaxSplits = 16;
+constexpr uint64_t kCounterBytes = 4096;  // arrival counters precede the partials
+
+#ifndef TCGEMM_STAGES2
+#define TCGEMM_STAGES2 7
+#endif
+constexpr int kStages1 = 4;               // 1-CTA: 4 x (16 KB A + 32 KB B) per CTA
+constexpr int kStages2 = TCGEMM_STAGES2;  // 2-CTA: 7 x (16 KB A + 16 KB B) per CTA
+constexpr int kStagesN64 = 9;             // 1-CTA narrow: 9 x (16 KB A + 8 KB B)
 using Cfg1 = tcg::GemmCfg<1, 256, kStages1>;
 using Cfg2 = tcg::GemmCfg<2, 256, kStages2>;
+using CfgN64 = tcg::GemmCfg<1, 64, kStagesN64>;
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
+// TCGEMM_SPLIT=0 in the environment turns the tail split off (for A/B timing).
+bool split_enabled() {
+    static const bool on = [] {
+        const char* s = std::getenv("TCGEMM_SPLIT");
+        return !(s && s[0] == '0');
+    }();
+    return on;
+}
+
+// CTA pairs (M = 256 per MMA) halve the operand traffic per SM; they pay off
+// once there are more than 128 rows.  Up to 128 rows ("skinny" products, B
+// streamed from memory once) narrow 128 x 64 tiles give every SM its own
+// columns of B and a deep 9-stage pipeline without splitting K.
 int pick_variant(int64_t M, int64_t N, int64_t K, int sms) {
-    (void)M;
     (void)N;
     (void)K;
     (void)sms;
-    return TCGEMM_VARIANT_1CTA;
+    return M > 128 ? TCGEMM_VARIANT_2CTA : TCGEMM_VARIANT_1CTA_N64;
 }
 
-bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pairs, Plan& pl) {
+bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pairs, int max_quads, Plan& pl,
+               bool allow_split = true) {
     if (sms <= 0) return false;
     if (variant == TCGEMM_VARIANT_AUTO) variant = pick_variant(M, N, K, sms);
     pl.variant = variant;
@@ -113,21 +143,70 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pa
         pl.bm = Cfg2::kBM;
         pl.bn = 256;
         pl.smem = Cfg2::kSmemBytes;
+    } else if (variant == TCGEMM_VARIANT_1CTA_MC) {
+        pl.cta_group = 1;
+        pl.mc = 4;
+        pl.bm = Cfg1::kBM;
+        pl.bn = 256;
+        pl.smem = Cfg1::kSmemBytes;
+    } else if (variant == TCGEMM_VARIANT_1CTA_N64) {
+        pl.cta_group = 1;
+        pl.bm = CfgN64::kBM;
+        pl.bn = 64;
+        pl.smem = CfgN64::kSmemBytes;
     } else {
         return false;
     }
     pl.tiles_m = ceil_div(M, pl.bm);
     pl.tiles_n = ceil_div(N, pl.bn);
     pl.num_kb = ceil_div(K, 64);
-    const int64_t tiles = static_cast<int64_t>(pl.tiles_m) * pl.tiles_n;
-    const int64_t clusters = pl.cta_group == 1 ? sms : std::max(1, max_pairs > 0 ? max_pairs : sms / 2);
-    pl.grid = static_cast<int>(std::min<int64_t>(tiles, clusters)) * pl.cta_group;
+    pl.slot_bytes = static_cast<uint64_t>(pl.cta_group) * 128 * pl.bn * 4;
+    pl.grid_m = pl.mc == 4 ? (pl.tiles_m + 1) / 2 : pl.tiles_m;
+    pl.grid_n = pl.mc == 4 ? (pl.tiles_n + 1) / 2 : pl.tiles_n;
+    const int64_t tiles = static_cast<int64_t>(pl.grid_m) * pl.grid_n;  // units of the order
+    if (tiles > (int64_t{1} << 30)) return false;
+    int64_t clusters = sms;
+    if (pl.cta_group == 2) clusters = std::max(1, max_pairs > 0 ? max_pairs : sms / 2);
+    if (pl.mc == 4) {
+        clusters = std::max(1, max_quads > 0 ? max_quads : sms / 4);
+        allow_split = false;  // the 2 x 2 blocks are scheduled whole
+    }
+    const int csize = pl.cta_group * pl.mc;
+    // Whole tiles round-robin.  The tiles of a last, partial round are split
+    // so that more clusters share that round: along N into two half-width
+    // tiles when there are full rounds before it (or K is short), along K
+    // when the whole problem is less than one round and K is long.
+    pl.tiles_dp = static_cast<int>(tiles);
+    pl.tiles_split = 0;
+    pl.splits = 1;
+    pl.split_n = 0;
+    const int64_t rem = tiles % clusters;
+    if (rem != 0 && allow_split && split_enabled()) {
+        int64_t ksp = std::min<int64_t>(std::min<int64_t>(clusters / rem, pl.num_kb / kMinKbPerPiece), kMaxSplits);
+        const bool long_k = pl.num_kb >= 4 * kMinKbPerPiece;
+        if (tiles < clusters && long_k && ksp >= 2) {
+            pl.splits = static_cast<int>(ksp);
+        } else if (2 * rem <= clusters && pl.bn >= 64) {
+            pl.splits = 2;
+            pl.split_n = 1;
+        }
+        if (pl.splits > 1) {
+            pl.tiles_split = static_cast<int>(rem);
+            pl.tiles_dp = static_cast<int>(tiles - rem);
+        }
+    }
+    const int64_t units = std::max<int64_t>(std::min<int64_t>(pl.tiles_dp, clusters),
+                                            static_cast<int64_t>(pl.tiles_split) * pl.splits);
+    pl.grid = static_cast<int>(std::min<int64_t>(std::max<int64_t>(units, 1), clusters)) * csize;
+    pl.ws_bytes = (pl.tiles_split > 0 && !pl.split_n)
+                      ? kCounterBytes + static_cast<uint64_t>(pl.tiles_split) * pl.splits * pl.slot_bytes
+                      : 0;
     // Band height so that the tiles in flight at once cover a roughly square
     // patch of C: group_m^2 ~ concurrent tiles * (tile width / tile height).
-    const double ideal = std::sqrt(static_cast<double>(pl.grid / pl.cta_group) * pl.bn / pl.bm);
+    const double ideal = std::sqrt(static_cast<double>(pl.grid / csize) * pl.bn / pl.bm);
     int g = 1;
     while (g * 2 <= ideal) g *= 2;
-    pl.group_m = std::max(1, std::min(g, pl.tiles_m));
+    pl.group_m = std::max(1, std::min(g, pl.grid_m));
     return true;
 }
 
@@ -159,13 +238,13 @@ bool encode_kmajor(CUtensorMap* m, const void* ptr, int64_t k_extent, int64_t ro
 
 // The dynamic shared-memory opt-in is a per-kernel attribute; it is set once
 // per device for each kernel instantiation.
-template <int CG, int BN, int ST, typename OutT>
+template <int CG, int BN, int ST, int MC, typename OutT>
 bool ensure_smem_attr(int dev) {
     static std::mutex mu;
     static bool done[kMaxDevices] = {};
     std::lock_guard<std::mutex> lk(mu);
     if (done[dev]) return true;
-    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, OutT>;
+    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, MC, OutT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(tcg::GemmCfg<CG, BN, ST>::kSmemBytes));
     if (e != cudaSuccess) {
@@ -176,11 +255,11 @@ bool ensure_smem_attr(int dev) {
     return true;
 }
 
-template <int CG, int BN, int ST, typename OutT>
-int launch_gemm(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, const tcg::GemmParams& gp,
-                cudaStream_t stream, int dev) {
-    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, OutT>;
-    if (!ensure_smem_attr<CG, BN, ST, OutT>(dev)) return TCGEMM_ERR_CUDA;
+template <int CG, int BN, int ST, int MC, typename OutT>
+int launch_gemm(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbh,
+                const tcg::GemmParams& gp, cudaStream_t stream, int dev) {
+    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, MC, OutT>;
+    if (!ensure_smem_attr<CG, BN, ST, MC, OutT>(dev)) return TCGEMM_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(pl.grid), 1, 1);
     cfg.blockDim = dim3(tcg::GemmCfg<CG, BN, ST>::kThreads, 1, 1);
@@ -188,21 +267,40 @@ int launch_gemm(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, co
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     cfg.numAttrs = 0;
-    if (CG == 2) {
+    if (CG * MC > 1) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.x = CG * MC;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, gp);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tbh, gp);
     if (e != cudaSuccess) {
         set_error("kernel launch: %s", cudaGetErrorString(e));
         return TCGEMM_ERR_CUDA;
     }
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return TCGEMM_OK;
+}
+
+template <typename Kern>
+int max_active_clusters(Kern kern, int cluster, uint32_t smem, int sms) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(sms / cluster * cluster), 1, 1);
+    cfg.blockDim = dim3(192, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+    (void)cudaGetLastError();
+    return n;
 }
 
 int probe_device(int& dev_out, DeviceInfo& info) {
@@ -227,25 +325,19 @@ int probe_device(int& dev_out, DeviceInfo& info) {
         d.supported = (major == 10 && minor == 3);
         d.sms = sms;
         d.max_pairs = sms / 2;
+        d.max_quads = sms / 4;
         if (d.supported) {
-            // How many CTA pairs of the 2-CTA kernel can be resident at once
-            // (cluster placement may leave some SMs unpaired).
-            auto kern = tcg::gemm_bf16_tn_kernel<2, 256, kStages2, __nv_bfloat16>;
-            if (ensure_smem_attr<2, 256, kStages2, __nv_bfloat16>(dev)) {
-                cudaLaunchConfig_t cfg = {};
-                cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
-                cfg.blockDim = dim3(Cfg2::kThreads, 1, 1);
-                cfg.dynamicSmemBytes = Cfg2::kSmemBytes;
-                cudaLaunchAttribute attr[1];
-                attr[0].id = cudaLaunchAttributeClusterDimension;
-                attr[0].val.clusterDim.x = 2;
-                attr[0].val.clusterDim.y = 1;
-                attr[0].val.clusterDim.z = 1;
-                cfg.attrs = attr;
-                cfg.numAttrs = 1;
-                int n = 0;
-                if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) d.max_pairs = n;
-                (void)cudaGetLastError();
+            // How many clusters of each kind can be resident at once (cluster
+            // placement may leave some SMs of a GPC unused).
+            if (ensure_smem_attr<2, 256, kStages2, 1, __nv_bfloat16>(dev)) {
+                const int n = max_active_clusters(tcg::gemm_bf16_tn_kernel<2, 256, kStages2, 1, __nv_bfloat16>,
+                                                  2, Cfg2::kSmemBytes, sms);
+                if (n > 0) d.max_pairs = n;
+            }
+            if (ensure_smem_attr<1, 256, kStages1, 4, __nv_bfloat16>(dev)) {
+                const int n = max_active_clusters(tcg::gemm_bf16_tn_kernel<1, 256, kStages1, 4, __nv_bfloat16>,
+                                                  4, Cfg1::kSmemBytes, sms);
+                if (n > 0) d.max_quads = n;
             }
         }
         d.probed = true;
@@ -305,10 +397,54 @@ int validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     return TCGEMM_OK;
 }
 
+// Largest workspace any plan on a device with `sms` SMs can need: at most one
+// split piece per cluster, 128 rows x 256 columns of fp32 per CTA.
+uint64_t max_workspace_bytes(int sms) { return kCounterBytes + static_cast<uint64_t>(sms) * 128 * 256 * 4; }
+
+// Library-owned split workspace, one per (device, stream) so that calls on
+// different streams never share partials.  Allocated (and its counters
+// zeroed, in stream order) the first time a split plan runs on that stream.
+struct InternalWs {
+    void* ptr = nullptr;
+    uint64_t bytes = 0;
+};
+std::mutex g_ws_mu;
+std::map<std::pair<int, uintptr_t>, InternalWs> g_ws;
+
+int internal_workspace(int dev, int sms, cudaStream_t stream, uint64_t need, void** out) {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    InternalWs& w = g_ws[{dev, reinterpret_cast<uintptr_t>(stream)}];
+    if (w.bytes < need) {
+        const uint64_t bytes = std::max(need, max_workspace_bytes(sms));
+        void* p = nullptr;
+        cudaError_t e = cudaMalloc(&p, bytes);
+        if (e != cudaSuccess) {
+            set_error("workspace cudaMalloc(%llu): %s", static_cast<unsigned long long>(bytes), cudaGetErrorString(e));
+            return TCGEMM_ERR_CUDA;
+        }
+        e = cudaMemsetAsync(p, 0, kCounterBytes, stream);
+        if (e != cudaSuccess) {
+            cudaFree(p);
+            set_error("workspace memset: %s", cudaGetErrorString(e));
+            return TCGEMM_ERR_CUDA;
+        }
+        if (w.ptr) cudaFree(w.ptr);  // never reached in practice: the first block is the maximum
+        w.ptr = p;
+        w.bytes = bytes;
+    }
+    *out = w.ptr;
+    return TCGEMM_OK;
+}
+
+constexpr int kWsInternal = 0;
+constexpr int kWsCaller = 1;
+constexpr int kWsNone = 2;  // plan without any split
+
 int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
-             int64_t ldc, float alpha, float beta, int out_dtype, void* stream_v, int variant) {
+             int64_t ldc, float alpha, float beta, int out_dtype, void* stream_v, int variant,
+             int ws_mode = kWsInternal, void* ws = nullptr, int64_t ws_bytes = 0) {
     t_last_error[0] = '\0';
-    if (variant < TCGEMM_VARIANT_AUTO || variant > TCGEMM_VARIANT_2CTA) {
+    if (variant < TCGEMM_VARIANT_AUTO || variant > TCGEMM_VARIANT_1CTA_N64) {
         set_error("unknown variant %d", variant);
         return TCGEMM_ERR_INVALID_ARG;
     }
@@ -342,14 +478,37 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     }
 
     Plan pl;
-    if (!make_plan(M, N, K, variant, info.sms, info.max_pairs, pl)) {
+    if (!make_plan(M, N, K, variant, info.sms, info.max_pairs, info.max_quads, pl, ws_mode != kWsNone)) {
         set_error("no launch plan for this shape and variant");
         return TCGEMM_ERR_INVALID_ARG;
     }
-    const uint32_t b_box_rows = static_cast<uint32_t>(pl.bn / pl.cta_group);
-    CUtensorMap ta, tb;
-    if (!encode_kmajor(&ta, A, K, M, lda, 128u) || !encode_kmajor(&tb, B, K, N, ldb, b_box_rows)) {
+    void* wsp = nullptr;
+    if (pl.ws_bytes > 0) {
+        if (ws_mode == kWsCaller) {
+            if (ws == nullptr || ws_bytes < 0 || static_cast<uint64_t>(ws_bytes) < pl.ws_bytes ||
+                (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) {
+                set_error("workspace must be 256-byte aligned and hold %llu bytes",
+                          static_cast<unsigned long long>(pl.ws_bytes));
+                return TCGEMM_ERR_INVALID_ARG;
+            }
+            wsp = ws;
+        } else {
+            rc = internal_workspace(dev, info.sms, static_cast<cudaStream_t>(stream_v), pl.ws_bytes, &wsp);
+            if (rc != TCGEMM_OK) return rc;
+        }
+    }
+    // Box heights: a CTA pair loads half of the B tile per CTA; a multicast
+    // CTA loads half of its A tile and half of its B tile.
+    const uint32_t a_box_rows = pl.mc == 4 ? 64u : 128u;
+    const uint32_t b_box_rows = static_cast<uint32_t>(pl.bn / pl.cta_group / (pl.mc == 4 ? 2 : 1));
+    CUtensorMap ta, tb, tbh;
+    if (!encode_kmajor(&ta, A, K, M, lda, a_box_rows) || !encode_kmajor(&tb, B, K, N, ldb, b_box_rows)) {
         return TCGEMM_ERR_INVALID_ARG;
+    }
+    if (pl.split_n) {
+        if (!encode_kmajor(&tbh, B, K, N, ldb, b_box_rows / 2)) return TCGEMM_ERR_INVALID_ARG;
+    } else {
+        tbh = tb;
     }
     tcg::GemmParams gp;
     gp.M = static_cast<int>(M);
@@ -359,19 +518,35 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     gp.tiles_n = pl.tiles_n;
     gp.num_kb = pl.num_kb;
     gp.group_m = pl.group_m;
+    gp.grid_m = pl.grid_m;
+    gp.grid_n = pl.grid_n;
     gp.ldc = ldc;
     gp.C = C;
     gp.alpha = alpha;
     gp.beta = beta;
+    gp.tiles_dp = pl.tiles_dp;
+    gp.tiles_split = pl.tiles_split;
+    gp.splits = pl.splits;
+    gp.split_n = pl.split_n;
+    gp.counters = static_cast<unsigned int*>(wsp);
+    gp.ws = wsp ? reinterpret_cast<float*>(static_cast<char*>(wsp) + kCounterBytes) : nullptr;
     gp.timeout_ns = timeout_ns();
 
     const bool bf16 = out_dtype == TCGEMM_OUT_BF16;
-    if (pl.cta_group == 1) {
-        return bf16 ? launch_gemm<1, 256, kStages1, __nv_bfloat16>(pl, ta, tb, gp, stream, dev)
-                    : launch_gemm<1, 256, kStages1, float>(pl, ta, tb, gp, stream, dev);
+    if (pl.mc == 4) {
+        return bf16 ? launch_gemm<1, 256, kStages1, 4, __nv_bfloat16>(pl, ta, tb, tbh, gp, stream, dev)
+                    : launch_gemm<1, 256, kStages1, 4, float>(pl, ta, tb, tbh, gp, stream, dev);
     }
-    return bf16 ? launch_gemm<2, 256, kStages2, __nv_bfloat16>(pl, ta, tb, gp, stream, dev)
-                : launch_gemm<2, 256, kStages2, float>(pl, ta, tb, gp, stream, dev);
+    if (pl.bn == 64) {
+        return bf16 ? launch_gemm<1, 64, kStagesN64, 1, __nv_bfloat16>(pl, ta, tb, tbh, gp, stream, dev)
+                    : launch_gemm<1, 64, kStagesN64, 1, float>(pl, ta, tb, tbh, gp, stream, dev);
+    }
+    if (pl.cta_group == 1) {
+        return bf16 ? launch_gemm<1, 256, kStages1, 1, __nv_bfloat16>(pl, ta, tb, tbh, gp, stream, dev)
+                    : launch_gemm<1, 256, kStages1, 1, float>(pl, ta, tb, tbh, gp, stream, dev);
+    }
+    return bf16 ? launch_gemm<2, 256, kStages2, 1, __nv_bfloat16>(pl, ta, tb, tbh, gp, stream, dev)
+                : launch_gemm<2, 256, kStages2, 1, float>(pl, ta, tb, tbh, gp, stream, dev);
 }
 
 }  // namespace
@@ -388,20 +563,44 @@ int gemm_bf16_variant(int64_t M, int64_t N, int64_t K, const void* A, int64_t ld
     return run_gemm(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, stream, variant);
 }
 
+int gemm_bf16_ws(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                 int64_t ldc, float alpha, float beta, int out_dtype, void* stream, int variant, void* workspace,
+                 int64_t workspace_bytes) {
+    return run_gemm(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, stream, variant, kWsCaller, workspace,
+                    workspace_bytes);
+}
+
+int64_t tcgemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int variant, int num_sms) {
+    if (M <= 0 || N <= 0 || K <= 0 || num_sms <= 0) return 0;
+    Plan pl;
+    if (!make_plan(M, N, K, variant, num_sms, num_sms / 2, num_sms / 4, pl)) return -1;
+    return static_cast<int64_t>(pl.ws_bytes);
+}
+
 int tcgemm_pick_variant(int64_t M, int64_t N, int64_t K, int num_sms) { return pick_variant(M, N, K, num_sms); }
 
 int tcgemm_plan(int64_t M, int64_t N, int64_t K, int variant, int num_sms, int64_t* out) {
     if (out == nullptr || M <= 0 || N <= 0 || K <= 0 || num_sms <= 0) return TCGEMM_ERR_INVALID_ARG;
     Plan pl;
-    if (!make_plan(M, N, K, variant, num_sms, num_sms / 2, pl)) return TCGEMM_ERR_INVALID_ARG;
+    if (!make_plan(M, N, K, variant, num_sms, num_sms / 2, num_sms / 4, pl)) return TCGEMM_ERR_INVALID_ARG;
     out[0] = pl.grid;
-    out[1] = pl.cta_group;
+    out[1] = pl.cta_group * pl.mc;
     out[2] = pl.tiles_m;
     out[3] = pl.tiles_n;
     out[4] = pl.bm;
     out[5] = pl.bn;
     out[6] = pl.num_kb;
     out[7] = pl.smem;
+    out[8] = pl.tiles_dp;
+    out[9] = pl.tiles_split;
+    out[10] = pl.splits;
+    out[11] = static_cast<int64_t>(pl.ws_bytes);
+    out[12] = pl.group_m;
+    out[13] = pl.variant;
+    out[14] = pl.cta_group;
+    out[15] = pl.grid_m;
+    out[16] = pl.grid_n;
+    out[17] = pl.split_n;
     return TCGEMM_OK;
 }
 

@@ -21,8 +21,9 @@ pytestmark = pytest.mark.gpu
 
 import os
 
-# 1-CTA and 2-CTA kernels; TCGEMM_TEST_VARIANTS="1" narrows a run to one of them.
-VARIANTS = [int(v) for v in os.environ.get("TCGEMM_TEST_VARIANTS", "1,2").split(",") if v]
+# 1-CTA, 2-CTA, 2x2-multicast and narrow 128x64 kernels; TCGEMM_TEST_VARIANTS="1"
+# narrows a run to one of them.
+VARIANTS = [int(v) for v in os.environ.get("TCGEMM_TEST_VARIANTS", "1,2,3,4").split(",") if v]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -161,3 +162,78 @@ def test_hang_guard_selftest():
     assert tc.check_device_status()[0] == 0  # status word was cleared
     case = gi.make_case("after", 128, 256, 64, out_dtype=gi.OUT_F32, seed=2, kind="integer")
     H.run_case(case)
+
+
+def _split_case():
+    # 2-CTA: 4 x 5 = 20 tiles on 76 pairs -> every tile split 3 ways along K.
+    return gi.make_case("split", 1024, 1280, 2048, alpha=0.5, beta=0.25, out_dtype=gi.OUT_F32, seed=31)
+
+
+def test_split_tiles_repeat_deterministic(oracle_lib):
+    """Tiles split along K: correct, and bit-identical over repeated calls
+    (partials are added in piece order, whatever order the pieces finish)."""
+    import tensor_core_matmul_gb300 as tc
+    case = _split_case()
+    p = tc.plan(case.M, case.N, case.K, 0, torch.cuda.get_device_properties(0).multi_processor_count)
+    assert p["tiles_split"] > 0 and p["splits"] >= 2, p
+    first = None
+    for _ in range(3):
+        g = H.run_case(case, 0)
+        got = g.result_np()
+        H.compare_full(oracle_lib, case, got, what="split")
+        if first is None:
+            first = got
+        else:
+            assert np.array_equal(got.view(np.uint32), first.view(np.uint32))
+
+
+def test_caller_workspace_matches_internal(oracle_lib):
+    import tensor_core_matmul_gb300 as tc
+    case = _split_case()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    need = tc.workspace_bytes(case.M, case.N, case.K, 0, sms)
+    assert need > 0
+    ws = torch.zeros(need + 256, dtype=torch.uint8, device="cuda")
+    A, B = case.A.cuda(), case.B.cuda()
+    g = H.GuardedC(case)
+    s = torch.cuda.current_stream().cuda_stream
+    st = tc.gemm_bf16_ws_raw(case.M, case.N, case.K, A.data_ptr(), case.lda, B.data_ptr(), case.ldb,
+                             g.C.data_ptr(), case.ldc, case.alpha, case.beta, case.out_dtype, s, 0,
+                             ws.data_ptr(), need)
+    assert st == 0, tc.binding.last_error()
+    torch.cuda.synchronize()
+    g.check_guards()
+    ref = H.run_case(case, 0).result_np()
+    assert np.array_equal(g.result_np().view(np.uint32), ref.view(np.uint32))
+    assert not ws[:4096].any(), "arrival counters must be left at zero"
+    st = tc.gemm_bf16_ws_raw(case.M, case.N, case.K, A.data_ptr(), case.lda, B.data_ptr(), case.ldb,
+                             g.C.data_ptr(), case.ldc, case.alpha, case.beta, case.out_dtype, s, 0,
+                             ws.data_ptr(), need - 1)
+    assert st == 1
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_split_small_k_pieces(oracle_lib, variant):
+    """Few tiles and a long K: maximal splitting, with pieces of uneven length."""
+    case = gi.make_case("longk", 200, 300, 64 * 37 + 24, alpha=1.0, beta=0.0, out_dtype=gi.OUT_BF16, seed=33)
+    g = H.run_case(case, variant)
+    H.compare_full(oracle_lib, case, g.result_np(), what=f"long K v{variant}")
+
+
+@pytest.mark.parametrize("variant", [1, 2, 4])
+def test_half_width_tail_tiles(oracle_lib, variant):
+    """More tiles than one round with a short last round: the tail tiles run as
+    two half-width tiles each (bit-exact on integer inputs, both halves of
+    every tail tile written, nothing else)."""
+    import tensor_core_matmul_gb300 as tc
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    bm = {1: 128, 2: 256, 4: 128}[variant]
+    bn = {1: 256, 2: 256, 4: 64}[variant]
+    clusters = sms // (2 if variant == 2 else 1)
+    tiles_n = (clusters + 3) // 4 + 1
+    M, N = bm * 4 + 40, bn * tiles_n - 24     # ragged edges on both sides
+    p = tc.plan(M, N, 320, variant, sms)
+    assert p["split_n"] == 1 and p["tiles_split"] > 0, p
+    case = gi.make_case("half", M, N, 320, alpha=1.0, beta=0.5, out_dtype=gi.OUT_F32, seed=51, kind="integer")
+    g = H.run_case(case, variant)
+    H.compare_full(oracle_lib, case, g.result_np(), exact=True, what=f"half-width v{variant}")
