@@ -109,6 +109,30 @@ int gemm_bf16_ws(int64_t M, int64_t N, int64_t K,
                  float alpha, float beta, int out_dtype, void* stream, int variant,
                  void* workspace, int64_t workspace_bytes);
 
+/* Same operation for callers that cannot allocate device memory once they are
+ * running (a fixed memory budget, an allocator that owns all device memory, or
+ * code that must not stall on cudaMalloc's implicit device synchronisation).
+ * Nothing is allocated: shapes whose tiles are split along K keep their
+ * partial tiles in a fixed scratch array compiled into this library
+ * (tcgemm_noalloc_scratch_bytes(), 16 MiB per GPU that loads the library, held
+ * until the process exits).  A shape that would need more scratch than that
+ * is rejected with TCGEMM_ERR_INVALID_ARG and tcgemm_last_error() says how
+ * much it needs.  The first call on a device looks up the array's device
+ * address (once per device, with that device current); make that first call
+ * before any stream capture.  Every call shares the one array and each call
+ * clears its counters on `stream` before use, so calls that overlap on the GPU
+ * (other streams, other host threads) race on it and must be serialised by the
+ * caller.  The pages this library follows have no counterpart of this entry
+ * point.  Other rules and errors as gemm_bf16_variant. */
+int gemm_bf16_noalloc(int64_t M, int64_t N, int64_t K,
+                      const void* A, int64_t lda,
+                      const void* B, int64_t ldb,
+                      void* C, int64_t ldc,
+                      float alpha, float beta, int out_dtype, void* stream, int variant);
+
+/* Size in bytes of gemm_bf16_noalloc's fixed scratch array.  Host only. */
+int64_t tcgemm_noalloc_scratch_bytes(void);
+
 /* Workspace bytes the launch for this shape and variant needs on a device
  * with `num_sms` SMs (0: none).  Host only. */
 int64_t tcgemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int variant, int num_sms);

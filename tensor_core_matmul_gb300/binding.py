@@ -57,6 +57,10 @@ def lib() -> ctypes.CDLL:
     L.gemm_bf16_variant.restype = i32
     L.gemm_bf16_ws.argtypes = gemm_args + [i32, p, i64]
     L.gemm_bf16_ws.restype = i32
+    L.gemm_bf16_noalloc.argtypes = gemm_args + [i32]
+    L.gemm_bf16_noalloc.restype = i32
+    L.tcgemm_noalloc_scratch_bytes.argtypes = []
+    L.tcgemm_noalloc_scratch_bytes.restype = i64
     L.tcgemm_workspace_bytes.argtypes = [i64, i64, i64, i32, i32]
     L.tcgemm_workspace_bytes.restype = i64
     L.tcgemm_pick_variant.argtypes = [i64, i64, i64, i32]
@@ -163,6 +167,17 @@ def plan(M: int, N: int, K: int, variant: int = 0, num_sms: int = 152) -> dict:
             "tiles_split", "splits", "ws_bytes", "group_m", "variant", "cta_group", "grid_m", "grid_n",
             "split_n"]
     return dict(zip(keys, [int(v) for v in out]))
+
+
+def gemm_bf16_noalloc_raw(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int, C: int, ldc: int,
+                          alpha: float, beta: float, out_dtype: int, stream: int, variant: int = 0) -> int:
+    """Pointer-level call of the allocation-free entry point (fixed scratch
+    array inside the library); returns the status."""
+    return lib().gemm_bf16_noalloc(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, stream, variant)
+
+
+def noalloc_scratch_bytes() -> int:
+    return int(lib().tcgemm_noalloc_scratch_bytes())
 
 
 def workspace_bytes(M: int, N: int, K: int, variant: int = 0, num_sms: int = 152) -> int:

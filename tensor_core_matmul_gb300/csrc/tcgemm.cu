@@ -436,9 +436,38 @@ int internal_workspace(int dev, int sms, cudaStream_t stream, uint64_t need, voi
     return TCGEMM_OK;
 }
 
+// ---------------------------------------------- fixed scratch, no allocation --
+//
+// Scratch for gemm_bf16_noalloc: a file-scope device array of fixed size, so
+// that entry point never allocates.  Every GPU that loads this library holds
+// these 16 MiB until the process exits.  In host code the array's name is only
+// a stand-in: its device address comes from cudaGetSymbolAddress, taken once
+// per device (with that device current) on the first call there.
+constexpr uint64_t kNoAllocScratchBytes = uint64_t{16} << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+int noalloc_scratch(int dev, void** out) {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr) {
+            set_error("cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+            return TCGEMM_ERR_CUDA;
+        }
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return TCGEMM_OK;
+}
+
 constexpr int kWsInternal = 0;
 constexpr int kWsCaller = 1;
-constexpr int kWsNone = 2;  // plan without any split
+constexpr int kWsNone = 2;     // plan without any split
+constexpr int kWsNoAlloc = 3;  // the fixed scratch array above
 
 int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
              int64_t ldc, float alpha, float beta, int out_dtype, void* stream_v, int variant,
@@ -492,6 +521,22 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
                 return TCGEMM_ERR_INVALID_ARG;
             }
             wsp = ws;
+        } else if (ws_mode == kWsNoAlloc) {
+            if (pl.ws_bytes > kNoAllocScratchBytes) {
+                set_error("this shape needs %llu bytes of scratch, more than the fixed %llu of gemm_bf16_noalloc",
+                          static_cast<unsigned long long>(pl.ws_bytes),
+                          static_cast<unsigned long long>(kNoAllocScratchBytes));
+                return TCGEMM_ERR_INVALID_ARG;
+            }
+            rc = noalloc_scratch(dev, &wsp);
+            if (rc != TCGEMM_OK) return rc;
+            // The array keeps the last call's contents: the arrival counters
+            // must start at zero, so clear them in stream order first.
+            cudaError_t e = cudaMemsetAsync(wsp, 0, kCounterBytes, static_cast<cudaStream_t>(stream_v));
+            if (e != cudaSuccess) {
+                set_error("clearing the scratch counters: %s", cudaGetErrorString(e));
+                return TCGEMM_ERR_CUDA;
+            }
         } else {
             rc = internal_workspace(dev, info.sms, static_cast<cudaStream_t>(stream_v), pl.ws_bytes, &wsp);
             if (rc != TCGEMM_OK) return rc;
@@ -569,6 +614,13 @@ int gemm_bf16_ws(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, co
     return run_gemm(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, stream, variant, kWsCaller, workspace,
                     workspace_bytes);
 }
+
+int gemm_bf16_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                      void* C, int64_t ldc, float alpha, float beta, int out_dtype, void* stream, int variant) {
+    return run_gemm(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, stream, variant, kWsNoAlloc);
+}
+
+int64_t tcgemm_noalloc_scratch_bytes(void) { return static_cast<int64_t>(kNoAllocScratchBytes); }
 
 int64_t tcgemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int variant, int num_sms) {
     if (M <= 0 || N <= 0 || K <= 0 || num_sms <= 0) return 0;
