@@ -203,8 +203,13 @@ struct GemmCfg {
     static constexpr uint32_t kStageTx = CTA_GROUP * (kABytes + kBBytes);  // bytes landing per stage
     static constexpr uint32_t kTmemCols = 2 * BN;         // two accumulators
     static constexpr int kThreads = 192;                  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
-    static constexpr uint32_t kBarOff = STAGES * (kABytes + kBBytes);
-    static constexpr uint32_t kNumBars = 2 * STAGES + 4 + 1;
+    // Epilogue staging shared by the four epilogue warps: two buffers of one
+    // 128-row x 32-column chunk of C (sized for fp32 output).
+    static constexpr uint32_t kEpiBufBytes = 128 * 32 * 4;
+    static constexpr uint32_t kEpiOff = STAGES * (kABytes + kBBytes);
+    static constexpr uint32_t kEpiBytes = 2 * kEpiBufBytes;
+    static constexpr uint32_t kBarOff = kEpiOff + kEpiBytes;
+    static constexpr uint32_t kNumBars = 2 * STAGES + 4 + 1 + 2;
     static constexpr uint32_t kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
     // Workspace bytes per split piece (both CTAs of a pair).
     static constexpr uint64_t kSlotBytes = static_cast<uint64_t>(CTA_GROUP) * 128 * BN * 4;
@@ -272,11 +277,14 @@ constexpr uint32_t kEpiThreads = 128;
 // a lone CTA's.  (The work log's "内核 8：线程块集群" multicasts the shared B
 // tile to two vertically adjacent tiles; this is the same idea in both
 // directions.)
-// tmBh is the B tensor map with half the box height, for half-width units.
+// tmBh is the B tensor map with half the box height, for half-width units;
+// tmC maps C (column-major M x N) in 32-row x 32-column boxes for the
+// epilogue's TMA stores and its L2 prefetch of the beta*C operand.
 template <int CTA_GROUP, int BN, int STAGES, int MC, typename OutT>
 __global__ void __launch_bounds__(192, 1)
     gemm_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmBh, const GemmParams p) {
+                        const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmC,
+                        const GemmParams p) {
     using Cfg = GemmCfg<CTA_GROUP, BN, STAGES>;
     static_assert(MC == 1 || (MC == 4 && CTA_GROUP == 1), "multicast clusters use single-CTA MMAs");
     constexpr int kCluster = CTA_GROUP * MC;
@@ -294,6 +302,7 @@ __global__ void __launch_bounds__(192, 1)
     auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
     const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+    auto cold_bar = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 5 + b); };  // C chunk loads
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kBarOff + Cfg::kNumBars * 8);
     volatile uint32_t* abort_flag = tmem_slot + 1;
     volatile uint32_t* last_flag = tmem_slot + 2;
@@ -324,6 +333,8 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(tempty_bar(a), 4 * CTA_GROUP);  // one arrive per epilogue warp of each CTA
         }
         mbar_init(drain_bar, 1);
+        mbar_init(cold_bar(0), 1);
+        mbar_init(cold_bar(1), 1);
         *abort_flag = 0u;
         *last_flag = 0u;
         fence_barrier_init();
@@ -478,12 +489,34 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t row_local = q * 32u + lane;  // 0..127 within this CTA's rows
         OutT* C = static_cast<OutT*>(p.C);
         const bool has_beta = p.beta != 0.0f;
+        // Two staging buffers shared by the four epilogue warps, each one
+        // 128-row x 32-column chunk of C with rows fastest (the layout of the
+        // TMA box).  One thread (warp 2, lane 0) issues the TMA copies.
+        const bool leader = (warp == 2 && lane == 0);
+        OutT* stage_ptr0 = reinterpret_cast<OutT*>(smem + Cfg::kEpiOff);
+        constexpr uint32_t kBufElems = Cfg::kEpiBufBytes / sizeof(OutT);
+        constexpr uint32_t kChunkBytes = 128 * 32 * sizeof(OutT);
+        uint32_t nchunk = 0;      // chunks staged so far; chunk i uses buffer i & 1
+        uint32_t cold_phase = 0;  // bit b: parity of the next completion of cold_bar(b)
+        bool aborted = false;
+        if (leader) tma_prefetch_desc(&tmC);
         uint32_t acc = 0, acc_phase = 0;
         UnitIter it(cluster_id, num_clusters);
         WorkUnit u;
-        while (it.next(p, u)) {
+        while (!aborted && it.next(p, u)) {
             int tm, tn;
             tile_of(u.tile, tm, tn);
+            const int row_blk = tm * Cfg::kBM + static_cast<int>(rank) * 128;  // this CTA's 128 rows
+            // First column of the unit and its width (half-width units hold
+            // their BN/2 columns in the first BN/2 accumulator columns).
+            const int64_t colt = static_cast<int64_t>(tn) * BN + (u.nhalf > 0 ? BN / 2 : 0);
+            const int ncols = u.nhalf >= 0 ? BN / 2 : BN;
+            // beta*C: start pulling the C tile into L2 now; the tile's mainloop
+            // hides the memory latency.
+            if (has_beta && leader && row_blk < p.M) {
+                for (int c = 0; c < ncols && colt + c < p.N; c += 32)
+                    tma_prefetch_l2_2d(&tmC, row_blk, static_cast<int32_t>(colt + c));
+            }
             uint32_t ok = 1;
             if (lane == 0) ok = wait_phase<false>(tfull_bar(acc), acc_phase, wctx, kWhereEpilogue) ? 1u : 0u;
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -491,16 +524,16 @@ __global__ void __launch_bounds__(192, 1)
             // alone at a named barrier below if another one gave up.
             if (!named_barrier_and(kEpiBarrier, kEpiThreads, ok != 0u)) break;
             tc_fence_after_sync();
-            const int64_t row = static_cast<int64_t>(tm) * Cfg::kBM + rank * 128 + row_local;
+            const int64_t row = static_cast<int64_t>(row_blk) + row_local;
             const bool row_ok = row < p.M;
             const uint32_t tbase = tmem_base + ((q * 32u) << 16) + acc * BN;
-            // First column of the unit and its width (half-width units hold
-            // their BN/2 columns in the first BN/2 accumulator columns).
-            const int64_t colt = static_cast<int64_t>(tn) * BN + (u.nhalf > 0 ? BN / 2 : 0);
-            const int ncols = u.nhalf >= 0 ? BN / 2 : BN;
 
-            if (u.slot < 0) {
-                // Whole tile: TMEM -> alpha/beta -> C.
+            // The TMA store clips at 16-byte granules along the contiguous
+            // (row) dimension, so a 128-row block that ends inside such a
+            // granule at row M would also write rows M.. of the ldc padding:
+            // that block is stored with masked plain stores instead.
+            const bool tma_rows = row_blk + 128 <= p.M || ((static_cast<int64_t>(p.M) * sizeof(OutT)) % 16) == 0;
+            if (u.slot < 0 && !tma_rows) {
 #pragma unroll 1
                 for (int c = 0; c < ncols; c += 32) {
                     const int64_t col0 = colt + c;
@@ -513,6 +546,78 @@ __global__ void __launch_bounds__(192, 1)
                     tmem_ld_wait32(r);
                     if (row_ok) epilogue_store32<OutT>(dst, p.ldc, col0, p.N, r, p.alpha, p.beta, cold, has_beta);
                 }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (CTA_GROUP == 1) {
+                        mbar_arrive(tempty_bar(acc));
+                    } else {
+                        mbar_arrive_cluster(map_to_cta(tempty_bar(acc), 0));
+                    }
+                }
+            } else if (u.slot < 0) {
+                // Whole tile, chunk by chunk: (TMA load of C ->) TMEM ->
+                // alpha*acc (+ beta*C) in place in the staging buffer -> TMA
+                // store of the 128 x 32 chunk (it clips columns >= N).
+                const int64_t width = (p.N - colt) < ncols ? (p.N - colt) : ncols;
+                const int nch = static_cast<int>((width + 31) / 32);
+                const bool rows_in = row_blk < p.M;  // same for the whole CTA
+                const bool load_c = has_beta && rows_in;
+                if (load_c && leader) {
+                    tma_store_wait_read<0>();  // no older store still reads a buffer
+                    const uint32_t b = nchunk & 1u;
+                    mbar_arrive_expect_tx(cold_bar(b), kChunkBytes);
+                    tma_load_2d(base + Cfg::kEpiOff + b * Cfg::kEpiBufBytes, &tmC, cold_bar(b), row_blk,
+                                static_cast<int32_t>(colt));
+                }
+#pragma unroll 1
+                for (int i = 0; i < nch; ++i) {
+                    const int64_t col0 = colt + 32 * i;
+                    const uint32_t b = nchunk & 1u;
+                    OutT* sp = stage_ptr0 + b * kBufElems;
+                    uint32_t r[32];
+                    tmem_ld32(tbase + 32 * i, r);
+                    if (load_c) {
+                        if (leader && i + 1 < nch) {
+                            // The other buffer's last store must be done reading it.
+                            tma_store_wait_read<0>();
+                            mbar_arrive_expect_tx(cold_bar(b ^ 1u), kChunkBytes);
+                            tma_load_2d(base + Cfg::kEpiOff + (b ^ 1u) * Cfg::kEpiBufBytes, &tmC, cold_bar(b ^ 1u),
+                                        row_blk, static_cast<int32_t>(col0 + 32));
+                        }
+                        uint32_t okc = 1;
+                        if (lane == 0) okc = wait_phase<false>(cold_bar(b), (cold_phase >> b) & 1u, wctx,
+                                                               kWhereEpilogue) ? 1u : 0u;
+                        okc = __shfl_sync(0xffffffffu, okc, 0);
+                        cold_phase ^= 1u << b;
+                        if (!named_barrier_and(kEpiBarrier, kEpiThreads, okc != 0u)) {
+                            aborted = true;
+                            break;
+                        }
+                    } else {
+                        // The buffer's previous store (two chunks ago) must be
+                        // done reading it before it is overwritten.
+                        if (leader && nchunk >= 2) tma_store_wait_read<1>();
+                        named_barrier_sync(kEpiBarrier, kEpiThreads);
+                    }
+                    tmem_ld_wait32(r);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        OutT* e = sp + j * 128 + row_local;
+                        float v = p.alpha * __uint_as_float(r[j]);
+                        if (load_c) v = fmaf(p.alpha, __uint_as_float(r[j]), p.beta * load_out<OutT>(e));
+                        store_out<OutT>(e, v);
+                    }
+                    fence_proxy_async_smem();
+                    named_barrier_sync(kEpiBarrier, kEpiThreads);
+                    if (leader && rows_in) {
+                        tma_store_2d(&tmC, base + Cfg::kEpiOff + b * Cfg::kEpiBufBytes, row_blk,
+                                     static_cast<int32_t>(col0));
+                        tma_store_commit();
+                    }
+                    ++nchunk;
+                }
+                if (aborted) break;
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) {
@@ -587,6 +692,9 @@ __global__ void __launch_bounds__(192, 1)
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
+        // Every TMA store has completed before the CTA exits.
+        if (leader) tma_store_wait_all();
+        __syncwarp();
     }
 
     // ------------------------------------------------------- teardown --

@@ -96,12 +96,11 @@ constexpr int kMinKbPerPiece = 4;   // a split piece covers at least 4 k-blocks 
 constexpr int kMaxSplits = 16;
 constexpr uint64_t kCounterBytes = 4096;  // arrival counters precede the partials
 
-#ifndef TCGEMM_STAGES2
-#define TCGEMM_STAGES2 7
-#endif
-constexpr int kStages1 = 4;               // 1-CTA: 4 x (16 KB A + 32 KB B) per CTA
-constexpr int kStages2 = TCGEMM_STAGES2;  // 2-CTA: 7 x (16 KB A + 16 KB B) per CTA
-constexpr int kStagesN64 = 9;             // 1-CTA narrow: 9 x (16 KB A + 8 KB B)
+// Pipeline depths: what fits in 227 KB of shared memory next to the 32 KB of
+// epilogue staging.
+constexpr int kStages1 = 4;    // 1-CTA: 4 x (16 KB A + 32 KB B) per CTA
+constexpr int kStages2 = 6;    // 2-CTA: 6 x (16 KB A + 16 KB B) per CTA
+constexpr int kStagesN64 = 8;  // 1-CTA narrow: 8 x (16 KB A + 8 KB B)
 using Cfg1 = tcg::GemmCfg<1, 256, kStages1>;
 using Cfg2 = tcg::GemmCfg<2, 256, kStages2>;
 using CfgN64 = tcg::GemmCfg<1, 64, kStagesN64>;
@@ -212,6 +211,30 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pa
 
 // --------------------------------------------------------- tensor maps --
 
+// C (column-major M x N, fp32 or bf16) in 128-row x 32-column boxes, for the
+// epilogue's TMA loads, stores and L2 prefetches.
+bool encode_c(CUtensorMap* m, void* ptr, int64_t M, int64_t N, int64_t ldc, bool bf16) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) {
+        set_error("cuTensorMapEncodeTiled is not available from the driver");
+        return false;
+    }
+    const uint64_t esz = bf16 ? 2 : 4;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(N)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc) * esz};
+    cuuint32_t box[2] = {128u, 32u};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled failed (%d) for C %lld x %lld, ldc %lld", static_cast<int>(r),
+                  static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(ldc));
+        return false;
+    }
+    return true;
+}
+
 bool encode_kmajor(CUtensorMap* m, const void* ptr, int64_t k_extent, int64_t rows, int64_t ld,
                    uint32_t box_rows) {
     EncodeTiledFn fn = encode_fn();
@@ -257,7 +280,7 @@ bool ensure_smem_attr(int dev) {
 
 template <int CG, int BN, int ST, int MC, typename OutT>
 int launch_gemm(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbh,
-                const tcg::GemmParams& gp, cudaStream_t stream, int dev) {
+                const CUtensorMap& tcm, const tcg::GemmParams& gp, cudaStream_t stream, int dev) {
     auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, MC, OutT>;
     if (!ensure_smem_attr<CG, BN, ST, MC, OutT>(dev)) return TCGEMM_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -275,7 +298,7 @@ int launch_gemm(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, co
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tbh, gp);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tbh, tcm, gp);
     if (e != cudaSuccess) {
         set_error("kernel launch: %s", cudaGetErrorString(e));
         return TCGEMM_ERR_CUDA;
@@ -555,6 +578,8 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     } else {
         tbh = tb;
     }
+    CUtensorMap tcm;
+    if (!encode_c(&tcm, C, M, N, ldc, out_dtype == TCGEMM_OUT_BF16)) return TCGEMM_ERR_INVALID_ARG;
     tcg::GemmParams gp;
     gp.M = static_cast<int>(M);
     gp.N = static_cast<int>(N);
@@ -579,19 +604,19 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
 
     const bool bf16 = out_dtype == TCGEMM_OUT_BF16;
     if (pl.mc == 4) {
-        return bf16 ? launch_gemm<1, 256, kStages1, 4, __nv_bfloat16>(pl, ta, tb, tbh, gp, stream, dev)
-                    : launch_gemm<1, 256, kStages1, 4, float>(pl, ta, tb, tbh, gp, stream, dev);
+        return bf16 ? launch_gemm<1, 256, kStages1, 4, __nv_bfloat16>(pl, ta, tb, tbh, tcm, gp, stream, dev)
+                    : launch_gemm<1, 256, kStages1, 4, float>(pl, ta, tb, tbh, tcm, gp, stream, dev);
     }
     if (pl.bn == 64) {
-        return bf16 ? launch_gemm<1, 64, kStagesN64, 1, __nv_bfloat16>(pl, ta, tb, tbh, gp, stream, dev)
-                    : launch_gemm<1, 64, kStagesN64, 1, float>(pl, ta, tb, tbh, gp, stream, dev);
+        return bf16 ? launch_gemm<1, 64, kStagesN64, 1, __nv_bfloat16>(pl, ta, tb, tbh, tcm, gp, stream, dev)
+                    : launch_gemm<1, 64, kStagesN64, 1, float>(pl, ta, tb, tbh, tcm, gp, stream, dev);
     }
     if (pl.cta_group == 1) {
-        return bf16 ? launch_gemm<1, 256, kStages1, 1, __nv_bfloat16>(pl, ta, tb, tbh, gp, stream, dev)
-                    : launch_gemm<1, 256, kStages1, 1, float>(pl, ta, tb, tbh, gp, stream, dev);
+        return bf16 ? launch_gemm<1, 256, kStages1, 1, __nv_bfloat16>(pl, ta, tb, tbh, tcm, gp, stream, dev)
+                    : launch_gemm<1, 256, kStages1, 1, float>(pl, ta, tb, tbh, tcm, gp, stream, dev);
     }
-    return bf16 ? launch_gemm<2, 256, kStages2, 1, __nv_bfloat16>(pl, ta, tb, tbh, gp, stream, dev)
-                : launch_gemm<2, 256, kStages2, 1, float>(pl, ta, tb, tbh, gp, stream, dev);
+    return bf16 ? launch_gemm<2, 256, kStages2, 1, __nv_bfloat16>(pl, ta, tb, tbh, tcm, gp, stream, dev)
+                : launch_gemm<2, 256, kStages2, 1, float>(pl, ta, tb, tbh, tcm, gp, stream, dev);
 }
 
 }  // namespace
