@@ -65,12 +65,15 @@ typedef enum {
 typedef enum {
     TCGEMM_VARIANT_AUTO = 0,
     TCGEMM_VARIANT_1CTA = 1,  /* one CTA per SM, 128 x 256 tiles, cta_group::1 MMA   */
-    TCGEMM_VARIANT_2CTA = 2,  /* CTA pairs, 256 x 256 tiles, cta_group::2 MMA (M=256) */
+    TCGEMM_VARIANT_2CTA = 2,  /* CTA pairs, cta_group::2 MMA (M=256), tiles 256 x 256 or 256 x 224,
+                                 whichever finishes the persistent rounds sooner */
     TCGEMM_VARIANT_1CTA_MC = 3, /* 4-CTA clusters on 2 x 2 blocks of 128 x 256 tiles; each CTA
                                   loads half of its A and B tiles and multicasts them to the
                                   CTA sharing its tile row / tile column */
-    TCGEMM_VARIANT_1CTA_N64 = 4 /* one CTA per SM, narrow 128 x 64 tiles, 9-stage pipeline: the
-                                  choice for M <= 128, where B is streamed from memory once */
+    TCGEMM_VARIANT_1CTA_N64 = 4, /* one CTA per SM, narrow 128 x 64 tiles, 8-stage pipeline (12
+                                   stages and 64-row A tiles when M <= 64): the choice for
+                                   M <= 128, where B is streamed from memory once */
+    TCGEMM_VARIANT_2CTA_W256 = 5 /* as TCGEMM_VARIANT_2CTA with the tile width fixed at 256 */
 } tcgemm_variant_t;
 
 /* C = alpha*A*B + beta*C as described above.  Returns TCGEMM_OK once the work
@@ -91,16 +94,16 @@ int gemm_bf16_variant(int64_t M, int64_t N, int64_t K,
                       float alpha, float beta, int out_dtype, void* stream, int variant);
 
 /* Same operation with a caller-supplied workspace instead of the library's
- * own.  Some shapes split the tiles of the last, partial round of work along
- * K (see tcgemm_workspace_bytes); their fp32 partial tiles and arrival
- * counters live in the workspace.  `workspace` is device memory of at least
- * tcgemm_workspace_bytes(M, N, K, variant, SMs) bytes, 256-byte aligned, whose
- * first 4096 bytes are zero before its first use; the library leaves them
- * zero after every completed call.  Calls that overlap on the GPU must not
- * share a workspace.  With a plan that needs none, `workspace` may be NULL.
+ * own.  When the tiles do not fill the last round of the persistent CTAs, the
+ * k-blocks of that round's tiles are shared out evenly ("stream-K"); the fp32
+ * partial tiles this needs live in the workspace (see
+ * tcgemm_workspace_bytes), and a second kernel on the same stream adds them up.  `workspace` is device memory of at least
+ * tcgemm_workspace_bytes(M, N, K, variant, SMs) bytes, 256-byte aligned (no
+ * initialisation needed).  Calls that overlap on the GPU must not share a
+ * workspace.  With a plan that needs none, `workspace` may be NULL.
  * Too small, misaligned or NULL when needed -> TCGEMM_ERR_INVALID_ARG.
  * (gemm_bf16 and gemm_bf16_variant use a library-owned workspace per device
- * and stream instead: about 19.5 MiB, allocated on the first call that needs
+ * and stream instead: about 38 MiB, allocated on the first call that needs
  * one on that stream, so make that first call before any stream capture.) */
 int gemm_bf16_ws(int64_t M, int64_t N, int64_t K,
                  const void* A, int64_t lda,
@@ -112,17 +115,17 @@ int gemm_bf16_ws(int64_t M, int64_t N, int64_t K,
 /* Same operation for callers that cannot allocate device memory once they are
  * running (a fixed memory budget, an allocator that owns all device memory, or
  * code that must not stall on cudaMalloc's implicit device synchronisation).
- * Nothing is allocated: shapes whose tiles are split along K keep their
- * partial tiles in a fixed scratch array compiled into this library
- * (tcgemm_noalloc_scratch_bytes(), 16 MiB per GPU that loads the library, held
+ * Nothing is allocated: shapes that share out their last round of work keep
+ * their partial tiles in a fixed scratch array compiled into this library
+ * (tcgemm_noalloc_scratch_bytes(), 40 MiB per GPU that loads the library, held
  * until the process exits).  A shape that would need more scratch than that
  * is rejected with TCGEMM_ERR_INVALID_ARG and tcgemm_last_error() says how
  * much it needs.  The first call on a device looks up the array's device
  * address (once per device, with that device current); make that first call
- * before any stream capture.  Every call shares the one array and each call
- * clears its counters on `stream` before use, so calls that overlap on the GPU
- * (other streams, other host threads) race on it and must be serialised by the
- * caller.  The pages this library follows have no counterpart of this entry
+ * before any stream capture.  Every call shares the one array (which keeps
+ * the previous call's partial tiles; nothing in it needs to start at zero), so
+ * calls that overlap on the GPU (other streams, other host threads) race on
+ * it and must be serialised by the caller.  The pages this library follows have no counterpart of this entry
  * point.  Other rules and errors as gemm_bf16_variant. */
 int gemm_bf16_noalloc(int64_t M, int64_t N, int64_t K,
                       const void* A, int64_t lda,
@@ -145,15 +148,35 @@ int tcgemm_pick_variant(int64_t M, int64_t N, int64_t K, int num_sms);
  * and tools: out[0] = grid size (CTAs), out[1] = CTAs per cluster, out[2] =
  * tile rows (tiles_m), out[3] = tile columns (tiles_n), out[4] = tile height,
  * out[5] = tile width, out[6] = k-blocks per tile, out[7] = dynamic shared
- * memory bytes, out[8] = tiles computed whole, out[9] = tiles split along K,
- * out[10] = pieces per split tile, out[11] = workspace bytes, out[12] = tile
+ * memory bytes, out[8] = tiles computed whole, out[9] = tiles of the last
+ * round shared out by stream-K, out[10] = their k-blocks in total, out[11] =
+ * workspace bytes, out[12] = tile
  * band height of the visiting order, out[13] = variant, out[14] = CTAs per
  * MMA (cta_group), out[15], out[16] = rows and columns of the unit grid the
  * visiting order walks (tiles, or 2 x 2 tile blocks for variant 3), out[17] =
- * 1 when the split tiles are split along N into two half-width tiles (0: along
- * K).  `out` must hold 18 values.  Returns TCGEMM_OK or TCGEMM_ERR_INVALID_ARG.  Needs no
+ * 1 when stream-K is used, out[18] = rows of A loaded per CTA (64 for M <= 64
+ * with variant 4, else 128).  `out` must hold 19 values.  Returns TCGEMM_OK or TCGEMM_ERR_INVALID_ARG.  Needs no
  * GPU. */
 int tcgemm_plan(int64_t M, int64_t N, int64_t K, int variant, int num_sms, int64_t* out);
+
+/* The same description for the current device, using its actual number of
+ * SMs and of clusters that can be resident at once (what gemm_bf16_variant
+ * itself uses).  Needs a supported GPU. */
+int tcgemm_plan_device(int64_t M, int64_t N, int64_t K, int variant, int64_t* out);
+
+/* Current device: out[0] = SMs, out[1] = CTA pairs and out[2] = 4-CTA clusters
+ * that can be resident at once with this library's kernels, out[3] = device
+ * ordinal.  `out` must hold 4 values.  Needs a supported GPU. */
+int tcgemm_device_info(int64_t* out);
+
+/* The work units cluster `cluster` runs under the host plan of tcgemm_plan
+ * (host copy of the device iterator): for unit i, out[7i..7i+6] = unit index
+ * in visiting order, first and one-past-last k-block, workspace slot (-1 for
+ * a whole tile), stream-K tile index (-1 for round-robin tiles), piece index
+ * and number of pieces of that tile.  Writes at most max_units units and
+ * returns how many there are (-1 on bad arguments).  Needs no GPU. */
+int tcgemm_units(int64_t M, int64_t N, int64_t K, int variant, int num_sms, int cluster, int max_units,
+                 int32_t* out);
 
 /* Tile visiting order used by the persistent kernels (host copy of the device
  * function): writes the tile row and column of order index t = 0..count-1

@@ -19,7 +19,7 @@ from . import _build
 
 OUT_F32 = 0
 OUT_BF16 = 1
-VARIANT_AUTO, VARIANT_1CTA, VARIANT_2CTA, VARIANT_1CTA_MC, VARIANT_1CTA_N64 = 0, 1, 2, 3, 4
+VARIANT_AUTO, VARIANT_1CTA, VARIANT_2CTA, VARIANT_1CTA_MC, VARIANT_1CTA_N64, VARIANT_2CTA_W256 = 0, 1, 2, 3, 4, 5
 
 STATUS = {0: "TCGEMM_OK", 1: "TCGEMM_ERR_INVALID_ARG", 2: "TCGEMM_ERR_ALIGNMENT",
           3: "TCGEMM_ERR_UNSUPPORTED_DEVICE", 4: "TCGEMM_ERR_CUDA", 5: "TCGEMM_ERR_TIMEOUT"}
@@ -67,6 +67,12 @@ def lib() -> ctypes.CDLL:
     L.tcgemm_pick_variant.restype = i32
     L.tcgemm_plan.argtypes = [i64, i64, i64, i32, i32, ctypes.POINTER(ctypes.c_int64)]
     L.tcgemm_plan.restype = i32
+    L.tcgemm_plan_device.argtypes = [i64, i64, i64, i32, ctypes.POINTER(ctypes.c_int64)]
+    L.tcgemm_plan_device.restype = i32
+    L.tcgemm_device_info.argtypes = [ctypes.POINTER(ctypes.c_int64)]
+    L.tcgemm_device_info.restype = i32
+    L.tcgemm_units.argtypes = [i64, i64, i64, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int32)]
+    L.tcgemm_units.restype = i32
     L.tcgemm_tile_order.argtypes = [i32, i32, i32, i64, ctypes.POINTER(ctypes.c_int32),
                                     ctypes.POINTER(ctypes.c_int32)]
     L.tcgemm_tile_order.restype = i32
@@ -160,13 +166,30 @@ def pick_variant(M: int, N: int, K: int, num_sms: int) -> int:
     return int(lib().tcgemm_pick_variant(M, N, K, num_sms))
 
 
+PLAN_KEYS = ["grid", "cluster", "tiles_m", "tiles_n", "bm", "bn", "num_kb", "smem", "tiles_dp",
+             "sk_tiles", "sk_iters", "ws_bytes", "group_m", "variant", "cta_group", "grid_m", "grid_n",
+             "stream_k", "arows"]
+
+
 def plan(M: int, N: int, K: int, variant: int = 0, num_sms: int = 152) -> dict:
-    out = (ctypes.c_int64 * 18)()
+    """Launch plan for a device with `num_sms` SMs (host only; assumes every
+    pair / 4-cluster of SMs can be resident)."""
+    out = (ctypes.c_int64 * len(PLAN_KEYS))()
     _check(lib().tcgemm_plan(M, N, K, variant, num_sms, out))
-    keys = ["grid", "cluster", "tiles_m", "tiles_n", "bm", "bn", "num_kb", "smem", "tiles_dp",
-            "tiles_split", "splits", "ws_bytes", "group_m", "variant", "cta_group", "grid_m", "grid_n",
-            "split_n"]
-    return dict(zip(keys, [int(v) for v in out]))
+    return dict(zip(PLAN_KEYS, [int(v) for v in out]))
+
+
+def plan_device(M: int, N: int, K: int, variant: int = 0) -> dict:
+    """The plan gemm_bf16 uses on the current device."""
+    out = (ctypes.c_int64 * len(PLAN_KEYS))()
+    _check(lib().tcgemm_plan_device(M, N, K, variant, out))
+    return dict(zip(PLAN_KEYS, [int(v) for v in out]))
+
+
+def device_info() -> dict:
+    out = (ctypes.c_int64 * 4)()
+    _check(lib().tcgemm_device_info(out))
+    return {"sms": int(out[0]), "max_pairs": int(out[1]), "max_quads": int(out[2]), "device": int(out[3])}
 
 
 def gemm_bf16_noalloc_raw(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int, C: int, ldc: int,
@@ -190,6 +213,20 @@ def gemm_bf16_ws_raw(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int,
     """Pointer-level call with a caller-owned workspace; returns the status."""
     return lib().gemm_bf16_ws(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, stream, variant,
                               workspace, workspace_bytes)
+
+
+UNIT_KEYS = ["tile", "kb0", "kb1", "slot", "sk_tile", "piece", "npieces"]
+
+
+def units(M: int, N: int, K: int, variant: int, num_sms: int, cluster: int) -> list:
+    """The work units of one cluster under the host plan (the kernel's own
+    iterator, run on the host)."""
+    n = int(lib().tcgemm_units(M, N, K, variant, num_sms, cluster, 0, (ctypes.c_int32 * 1)()))
+    if n < 0:
+        raise ValueError("bad arguments")
+    buf = (ctypes.c_int32 * max(1, 7 * n))()
+    lib().tcgemm_units(M, N, K, variant, num_sms, cluster, n, buf)
+    return [dict(zip(UNIT_KEYS, buf[7 * i:7 * i + 7])) for i in range(n)]
 
 
 def tile_order(tiles_m: int, tiles_n: int, group_m: int, count: Optional[int] = None):

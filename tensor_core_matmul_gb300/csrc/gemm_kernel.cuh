@@ -27,17 +27,15 @@
 //    out-of-range A/B elements with zeros, so they add nothing; the epilogue
 //    masks out-of-range rows and columns of C.
 //
-// Tail splits (not on the pages; the work log's conclusion attributes its
-// remaining per-size gaps to tuning).  When the tile count is not a multiple
-// of the number of persistent CTAs (pairs), the tiles of the last, partial
-// round are split so that more CTAs share that round:
-//  * along N into two half-width tiles (MMA N = BN/2): no workspace, and the
-//    same arithmetic as a whole tile;
-//  * along K into S pieces (problems with fewer tiles than CTAs and a long K):
-//    each piece writes its fp32 partial tile to a workspace slot and bumps a
-//    per-tile counter; the piece that arrives last adds the S partials in
-//    piece order (the result does not depend on arrival order) and runs the
-//    epilogue.  No CTA ever waits for another.
+// Stream-K (not on the pages; the work log's conclusion attributes its
+// remaining per-size gaps to tuning).  When there are too few tiles to keep
+// the persistent clusters busy (the host decides; see use_stream_k), the tiles
+// of the last, partial round are not handed out whole: their k-blocks, taken
+// in order, are cut into one contiguous range per cluster, so every cluster
+// does the same amount of that work.  A range that covers only part of a tile produces an fp32 partial
+// tile, written through TMA to the cluster's workspace slot; a second, small
+// kernel (sk_reduce_kernel) then adds each shared tile's partials in K order
+// and runs its epilogue.  No CTA ever waits for another.
 //
 // Every wait on a barrier is bounded by %globaltimer.  On expiry the waiting
 // thread records TCGEMM_ERR_TIMEOUT in the device status word, raises the
@@ -122,79 +120,110 @@ struct GemmParams {
     int M, N, K;
     int tiles_m, tiles_n, num_kb, group_m;
     int grid_m, grid_n;  // grid the unit order walks: tiles, or 2 x 2 tile blocks of a multicast cluster
-    int tiles_dp;      // tiles computed whole, round-robin over the clusters
-    int tiles_split;   // trailing tiles split ...
-    int splits;        // ... into this many pieces (1 = no split) ...
-    int split_n;       // ... along N (1, then splits == 2) or along K (0)
+    int tiles_dp;        // tiles computed whole, round-robin over the clusters
+    int sk_tiles;        // trailing tiles whose k-blocks are shared out by stream-K (0: none)
+    int64_t sk_iters;    // sk_tiles * num_kb
     int64_t ldc;
     void* C;
     float alpha, beta;
-    float* ws;               // split partials: [slot][cta rank][BN cols][128 rows] fp32
-    unsigned int* counters;  // one arrival counter per (split tile, cta rank), zero between launches
     uint64_t timeout_ns;
 };
 
-// One unit of work for a cluster: a whole tile, or one K-piece of a split tile.
+// First stream-K iteration of cluster c: the ranges are [lo(c), lo(c+1)).
+__host__ __device__ __forceinline__ int64_t sk_lo(int64_t c, int64_t iters, int64_t clusters) {
+    return (c * iters) / clusters;
+}
+
+// The cluster whose range holds iteration `it` (the largest c with lo(c) <= it).
+__host__ __device__ __forceinline__ int sk_owner(int64_t it, int64_t iters, int64_t clusters) {
+    return static_cast<int>(((it + 1) * clusters - 1) / iters);
+}
+
+// Workspace slot of cluster c's piece of the stream-K tile starting at
+// iteration t_begin: a cluster has at most two partial pieces, the first and
+// the last segment of its range.
+__host__ __device__ __forceinline__ int sk_slot(int c, int64_t t_begin, int64_t iters, int64_t clusters) {
+    return 2 * c + (sk_lo(c, iters, clusters) >= t_begin ? 0 : 1);
+}
+
+// One unit of work for a cluster: a whole tile, or one piece of a stream-K tile.
 struct WorkUnit {
-    int tile;       // index in grouped order
-    int kb0, kb1;   // k-block range [kb0, kb1)
-    int piece;      // piece index (0 for whole tiles)
-    int slot;       // K-split tile index among the split tiles (-1: no partials)
-    int nhalf;      // -1: all BN columns; 0 / 1: first / second half of them
+    int tile;          // unit index in grouped order
+    int kb0, kb1;      // k-block range [kb0, kb1)
+    int slot;          // -1: a whole tile; else this piece's workspace slot
+    int sk_tile;       // index among the stream-K tiles (-1 for round-robin tiles)
+    int piece, npieces;  // place of this piece among the tile's pieces (K order)
 };
 
-// Walks the units of one cluster: its share of the whole tiles, then at most
-// one piece of a split tile.  Producer, MMA and epilogue roles each run their
-// own copy and see the same sequence.
+// Walks the units of one cluster: first the segments of its stream-K range,
+// then its share of the whole tiles.  Doing the shared tiles first lets the
+// piece that finishes a shared tile last add up the partials in its epilogue
+// warps while its MMA thread already works on whole tiles.  Producer, MMA and
+// epilogue roles each run their own copy and see the same sequence.
 struct UnitIter {
     int next_dp;   // next whole tile
-    int stride;
+    int stride;    // number of clusters
     int cluster;
-    bool split_done;
+    int64_t sk_it, sk_end;
 
     __host__ __device__ UnitIter(int cluster_id, int num_clusters)
-        : next_dp(cluster_id), stride(num_clusters), cluster(cluster_id), split_done(false) {}
+        : next_dp(cluster_id), stride(num_clusters), cluster(cluster_id), sk_it(0), sk_end(0) {}
+
+    // Must be called once with the launch parameters before next().
+    __host__ __device__ void start(const GemmParams& p) {
+        if (p.sk_tiles > 0) {
+            sk_it = sk_lo(cluster, p.sk_iters, stride);
+            sk_end = sk_lo(cluster + 1, p.sk_iters, stride);
+        }
+    }
 
     __host__ __device__ bool next(const GemmParams& p, WorkUnit& u) {
+        if (sk_it < sk_end) {
+            const int t = static_cast<int>(sk_it / p.num_kb);
+            const int64_t t_begin = static_cast<int64_t>(t) * p.num_kb;
+            const int64_t t_end = t_begin + p.num_kb;
+            const int64_t seg_end = sk_end < t_end ? sk_end : t_end;
+            u.tile = p.tiles_dp + t;
+            u.sk_tile = t;
+            u.kb0 = static_cast<int>(sk_it - t_begin);
+            u.kb1 = static_cast<int>(seg_end - t_begin);
+            if (u.kb0 == 0 && u.kb1 == p.num_kb) {
+                u.slot = -1;
+                u.piece = 0;
+                u.npieces = 1;
+            } else {
+                const int first = sk_owner(t_begin, p.sk_iters, stride);
+                const int last = sk_owner(t_end - 1, p.sk_iters, stride);
+                u.piece = cluster - first;
+                u.npieces = last - first + 1;
+                u.slot = sk_slot(cluster, t_begin, p.sk_iters, stride);
+            }
+            sk_it = seg_end;
+            return true;
+        }
         if (next_dp < p.tiles_dp) {
             u.tile = next_dp;
             u.kb0 = 0;
             u.kb1 = p.num_kb;
-            u.piece = 0;
             u.slot = -1;
-            u.nhalf = -1;
+            u.sk_tile = -1;
+            u.piece = 0;
+            u.npieces = 1;
             next_dp += stride;
             return true;
-        }
-        if (!split_done) {
-            split_done = true;
-            const int units = p.tiles_split * p.splits;
-            if (cluster < units) {
-                const int s = cluster / p.splits;
-                u.piece = cluster - s * p.splits;
-                u.tile = p.tiles_dp + s;
-                if (p.split_n) {
-                    u.kb0 = 0;
-                    u.kb1 = p.num_kb;
-                    u.slot = -1;
-                    u.nhalf = u.piece;
-                } else {
-                    u.slot = p.splits > 1 ? s : -1;
-                    u.nhalf = -1;
-                    u.kb0 = static_cast<int>((static_cast<int64_t>(u.piece) * p.num_kb) / p.splits);
-                    u.kb1 = static_cast<int>((static_cast<int64_t>(u.piece + 1) * p.num_kb) / p.splits);
-                }
-                return true;
-            }
         }
         return false;
     }
 };
 
-template <int CTA_GROUP, int BN, int STAGES>
+// AROWS = 64 (single CTA, M <= 64 only): only the 64 real rows of A are
+// loaded; the MMA still computes 128 rows and reads rows 64..127 from the
+// shared memory that follows the A stage.  Those accumulator rows are never
+// stored, so whatever they hold does not matter, and A's traffic halves.
+template <int CTA_GROUP, int BN, int STAGES, int AROWS = 128>
 struct GemmCfg {
     static constexpr int kBK = 64;                        // 64 bf16 = one 128-byte swizzle row
-    static constexpr int kRowsA = 128;                    // A rows per CTA
+    static constexpr int kRowsA = AROWS;                  // A rows loaded per CTA
     static constexpr int kBM = 128 * CTA_GROUP;           // MMA M (pair tile height)
     static constexpr int kRowsB = BN / CTA_GROUP;         // B rows (tile columns) per CTA
     static constexpr int kUmmaK = 16;
@@ -202,6 +231,8 @@ struct GemmCfg {
     static constexpr uint32_t kBBytes = kRowsB * kBK * 2;
     static constexpr uint32_t kStageTx = CTA_GROUP * (kABytes + kBBytes);  // bytes landing per stage
     static constexpr uint32_t kTmemCols = 2 * BN;         // two accumulators
+    static constexpr uint32_t kTmemAlloc = kTmemCols <= 32 ? 32 : kTmemCols <= 64 ? 64 : kTmemCols <= 128 ? 128
+                                         : kTmemCols <= 256 ? 256 : 512;  // allocations are powers of two
     static constexpr int kThreads = 192;                  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
     // Epilogue staging shared by the four epilogue warps: two buffers of one
     // 128-row x 32-column chunk of C (sized for fp32 output).
@@ -214,6 +245,7 @@ struct GemmCfg {
     // Workspace bytes per split piece (both CTAs of a pair).
     static constexpr uint64_t kSlotBytes = static_cast<uint64_t>(CTA_GROUP) * 128 * BN * 4;
     static_assert(kTmemCols <= 512, "TMEM has 512 columns");
+    static_assert(AROWS == 128 || (AROWS == 64 && CTA_GROUP == 1), "half-height A tiles are single-CTA only");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "epilogue works in 32-column chunks");
     static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
 };
@@ -277,16 +309,16 @@ constexpr uint32_t kEpiThreads = 128;
 // a lone CTA's.  (The work log's "内核 8：线程块集群" multicasts the shared B
 // tile to two vertically adjacent tiles; this is the same idea in both
 // directions.)
-// tmBh is the B tensor map with half the box height, for half-width units;
-// tmC maps C (column-major M x N) in 32-row x 32-column boxes for the
-// epilogue's TMA stores and its L2 prefetch of the beta*C operand.
-template <int CTA_GROUP, int BN, int STAGES, int MC, typename OutT>
+// tmC maps C (column-major M x N) in 128-row x 32-column boxes for the
+// epilogue's TMA loads / stores and L2 prefetches; tmW maps the stream-K
+// workspace (fp32, 128 rows x [slot][CTA of pair][BN] columns) the same way.
+template <int CTA_GROUP, int BN, int STAGES, int MC, int AROWS, typename OutT>
 __global__ void __launch_bounds__(192, 1)
     gemm_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmC,
+                        const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
                         const GemmParams p) {
-    using Cfg = GemmCfg<CTA_GROUP, BN, STAGES>;
-    static_assert(MC == 1 || (MC == 4 && CTA_GROUP == 1), "multicast clusters use single-CTA MMAs");
+    using Cfg = GemmCfg<CTA_GROUP, BN, STAGES, AROWS>;
+    static_assert(MC == 1 || (MC == 4 && CTA_GROUP == 1 && AROWS == 128), "multicast clusters use single-CTA MMAs");
     constexpr int kCluster = CTA_GROUP * MC;
     extern __shared__ uint8_t smem_raw[];
 
@@ -305,7 +337,6 @@ __global__ void __launch_bounds__(192, 1)
     auto cold_bar = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 5 + b); };  // C chunk loads
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kBarOff + Cfg::kNumBars * 8);
     volatile uint32_t* abort_flag = tmem_slot + 1;
-    volatile uint32_t* last_flag = tmem_slot + 2;
 
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31u;
@@ -336,10 +367,9 @@ __global__ void __launch_bounds__(192, 1)
         mbar_init(cold_bar(0), 1);
         mbar_init(cold_bar(1), 1);
         *abort_flag = 0u;
-        *last_flag = 0u;
         fence_barrier_init();
     }
-    if (warp == 1) tmem_alloc<CTA_GROUP>(smem_u32(tmem_slot), Cfg::kTmemCols);
+    if (warp == 1) tmem_alloc<CTA_GROUP>(smem_u32(tmem_slot), Cfg::kTmemAlloc);
     tc_fence_before_sync();
     if constexpr (kCluster == 1) {
         __syncthreads();
@@ -355,21 +385,19 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) {
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
-            if (p.split_n) tma_prefetch_desc(&tmBh);
             uint32_t stage = 0, phase = 0;
             uint64_t issued = 0;
             bool ok = true;
             UnitIter it(cluster_id, num_clusters);
+            it.start(p);
             WorkUnit u;
             while (ok && it.next(p, u)) {
                 int tm, tn;
                 tile_of(u.tile, tm, tn);
-                const bool half = u.nhalf >= 0;
                 const int a_row = tm * Cfg::kBM + static_cast<int>(rank) * Cfg::kRowsA;
-                const int b_row = half ? tn * BN + u.nhalf * (BN / 2) + static_cast<int>(rank) * (Cfg::kRowsB / 2)
-                                       : tn * BN + static_cast<int>(rank) * Cfg::kRowsB;
-                const CUtensorMap* mB = half ? &tmBh : &tmB;
-                const uint32_t stage_tx = half ? CTA_GROUP * (Cfg::kABytes + Cfg::kBBytes / 2) : Cfg::kStageTx;
+                const int b_row = tn * BN + static_cast<int>(rank) * Cfg::kRowsB;
+                const CUtensorMap* mB = &tmB;
+                const uint32_t stage_tx = Cfg::kStageTx;
                 for (int kb = u.kb0; kb < u.kb1; ++kb) {
                     if (!wait_phase<false>(empty_bar(stage), phase ^ 1u, wctx, kWhereProducer)) {
                         ok = false;
@@ -423,17 +451,17 @@ __global__ void __launch_bounds__(192, 1)
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer --
         if (lane == 0 && (CTA_GROUP == 1 || rank == 0)) {
-            constexpr uint32_t kIdescFull = idesc_bf16_f32(Cfg::kBM, BN);
-            constexpr uint32_t kIdescHalf = idesc_bf16_f32(Cfg::kBM, BN / 2);
+            constexpr uint32_t kIdesc = idesc_bf16_f32(Cfg::kBM, BN);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             UnitIter it(cluster_id, num_clusters);
+            it.start(p);
             WorkUnit u;
             while (ok && it.next(p, u)) {
                 if (!wait_phase<CTA_GROUP == 2>(tempty_bar(acc), acc_phase ^ 1u, wctx, kWhereMma)) break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                const uint32_t idesc = u.nhalf >= 0 ? kIdescHalf : kIdescFull;
+                const uint32_t idesc = kIdesc;
                 for (int kb = u.kb0; kb < u.kb1; ++kb) {
                     if (!wait_phase<false>(full_bar(stage), phase, wctx, kWhereMma)) {
                         ok = false;
@@ -502,15 +530,14 @@ __global__ void __launch_bounds__(192, 1)
         if (leader) tma_prefetch_desc(&tmC);
         uint32_t acc = 0, acc_phase = 0;
         UnitIter it(cluster_id, num_clusters);
+            it.start(p);
         WorkUnit u;
         while (!aborted && it.next(p, u)) {
             int tm, tn;
             tile_of(u.tile, tm, tn);
             const int row_blk = tm * Cfg::kBM + static_cast<int>(rank) * 128;  // this CTA's 128 rows
-            // First column of the unit and its width (half-width units hold
-            // their BN/2 columns in the first BN/2 accumulator columns).
-            const int64_t colt = static_cast<int64_t>(tn) * BN + (u.nhalf > 0 ? BN / 2 : 0);
-            const int ncols = u.nhalf >= 0 ? BN / 2 : BN;
+            const int64_t colt = static_cast<int64_t>(tn) * BN;  // first column of the tile
+            const int ncols = BN;
             // beta*C: start pulling the C tile into L2 now; the tile's mainloop
             // hides the memory latency.
             if (has_beta && leader && row_blk < p.M) {
@@ -628,17 +655,29 @@ __global__ void __launch_bounds__(192, 1)
                     }
                 }
             } else {
-                // Piece of a split tile: write the fp32 partial (every row and
-                // column of the tile, in or out of range) to this piece's slot.
-                float* mine = p.ws + ((static_cast<int64_t>(u.slot) * p.splits + u.piece) * CTA_GROUP + rank) *
-                                         (static_cast<int64_t>(BN) * 128);
+                // Stream-K piece: stage the fp32 partial tile (all 128 rows,
+                // all BN columns) and TMA-store it to this piece's slot.
+                float* fsp0 = reinterpret_cast<float*>(smem + Cfg::kEpiOff);
+                constexpr uint32_t kFBufElems = Cfg::kEpiBufBytes / 4;
+                const int ws_col0 = (u.slot * CTA_GROUP + static_cast<int>(rank)) * BN;
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
+                for (int i = 0; i < BN / 32; ++i) {
+                    const uint32_t b = nchunk & 1u;
+                    float* sp = fsp0 + b * kFBufElems;
                     uint32_t r[32];
-                    tmem_ld32(tbase + c, r);
+                    tmem_ld32(tbase + 32 * i, r);
+                    if (leader && nchunk >= 2) tma_store_wait_read<1>();
+                    named_barrier_sync(kEpiBarrier, kEpiThreads);
                     tmem_ld_wait32(r);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) __stcg(mine + (c + j) * 128 + row_local, __uint_as_float(r[j]));
+                    for (int j = 0; j < 32; ++j) sp[j * 128 + row_local] = __uint_as_float(r[j]);
+                    fence_proxy_async_smem();
+                    named_barrier_sync(kEpiBarrier, kEpiThreads);
+                    if (leader) {
+                        tma_store_2d(&tmW, base + Cfg::kEpiOff + b * Cfg::kEpiBufBytes, 0, ws_col0 + 32 * i);
+                        tma_store_commit();
+                    }
+                    ++nchunk;
                 }
                 tc_fence_before_sync();
                 __syncwarp();
@@ -647,45 +686,6 @@ __global__ void __launch_bounds__(192, 1)
                         mbar_arrive(tempty_bar(acc));
                     } else {
                         mbar_arrive_cluster(map_to_cta(tempty_bar(acc), 0));
-                    }
-                }
-                // Publish, then count arrivals on this (tile, rank).
-                __threadfence();
-                named_barrier_sync(kEpiBarrier, kEpiThreads);
-                if (warp == 2 && lane == 0) {
-                    unsigned int* cnt = p.counters + u.slot * CTA_GROUP + rank;
-                    const unsigned int prev = atomicAdd(cnt, 1u);
-                    const bool last = prev == static_cast<unsigned int>(p.splits - 1);
-                    if (last) atomicExch(cnt, 0u);  // leave it zero for the next launch
-                    *last_flag = last ? 1u : 0u;
-                }
-                named_barrier_sync(kEpiBarrier, kEpiThreads);
-                const bool last = *last_flag != 0u;
-                named_barrier_sync(kEpiBarrier, kEpiThreads);  // flag read by all before it is reused
-                if (last) {
-                    __threadfence();
-                    const float* slot0 = p.ws + (static_cast<int64_t>(u.slot) * p.splits * CTA_GROUP + rank) *
-                                                    (static_cast<int64_t>(BN) * 128);
-                    const int64_t piece_stride = static_cast<int64_t>(CTA_GROUP) * BN * 128;
-#pragma unroll 1
-                    for (int c = 0; c < BN; c += 32) {
-                        const int64_t col0 = colt + c;
-                        if (col0 >= p.N) break;
-                        OutT* dst = C + col0 * p.ldc + row;
-                        float cold[32];
-                        if (has_beta && row_ok) load_cold32<OutT>(dst, p.ldc, col0, p.N, cold);
-                        float sum[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) sum[j] = 0.0f;
-                        for (int s = 0; s < p.splits; ++s) {
-                            const float* src = slot0 + s * piece_stride + c * 128 + row_local;
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) sum[j] += __ldcg(src + j * 128);
-                        }
-                        uint32_t r[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(sum[j]);
-                        if (row_ok) epilogue_store32<OutT>(dst, p.ldc, col0, p.N, r, p.alpha, p.beta, cold, has_beta);
                     }
                 }
             }
@@ -707,8 +707,53 @@ __global__ void __launch_bounds__(192, 1)
     }
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc<CTA_GROUP>(tmem_base, Cfg::kTmemCols);
+        tmem_dealloc<CTA_GROUP>(tmem_base, Cfg::kTmemAlloc);
     }
+}
+
+// Stream-K reduction: one block per (shared tile, CTA of pair, 32-column
+// chunk), one thread per row.  Adds the tile's pieces in K order (the same
+// order whatever order they were computed in), then alpha/beta, the output
+// cast and masked, coalesced stores (a warp writes 32 consecutive rows of a
+// column).  Partials: fp32, 128 rows x [slot][CTA of pair][BN] columns.
+template <int CTA_GROUP, int BN, typename OutT>
+__global__ void __launch_bounds__(128)
+    sk_reduce_kernel(const float* __restrict__ ws, const GemmParams p, int num_clusters) {
+    const int chunks = BN / 32;
+    const int blk = blockIdx.x;
+    const int c = blk % chunks;
+    const int rank = (blk / chunks) % CTA_GROUP;
+    const int t = blk / (chunks * CTA_GROUP);
+    const int row_local = threadIdx.x;
+    int tm, tn;
+    grouped_tile(p.tiles_dp + t, p.grid_m, p.grid_n, p.group_m, tm, tn);
+    const int64_t row = static_cast<int64_t>(tm) * (128 * CTA_GROUP) + rank * 128 + row_local;
+    const int64_t col0 = static_cast<int64_t>(tn) * BN + 32 * c;
+    if (col0 >= p.N) return;
+    const int64_t t_begin = static_cast<int64_t>(t) * p.num_kb;
+    const int first = sk_owner(t_begin, p.sk_iters, num_clusters);
+    const int last = sk_owner(t_begin + p.num_kb - 1, p.sk_iters, num_clusters);
+    float sum[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) sum[j] = 0.0f;
+    for (int cl = first; cl <= last; ++cl) {
+        const int slot = sk_slot(cl, t_begin, p.sk_iters, num_clusters);
+        const float* src = ws + (static_cast<int64_t>(slot * CTA_GROUP + rank) * BN + 32 * c) * 128 + row_local;
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __ldcg(src + j * 128);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sum[j] += v[j];
+    }
+    if (row >= p.M) return;
+    OutT* dst = static_cast<OutT*>(p.C) + col0 * p.ldc + row;
+    const bool has_beta = p.beta != 0.0f;
+    float cold[32];
+    if (has_beta) load_cold32<OutT>(dst, p.ldc, col0, p.N, cold);
+    uint32_t r[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(sum[j]);
+    epilogue_store32<OutT>(dst, p.ldc, col0, p.N, r, p.alpha, p.beta, cold, has_beta);
 }
 
 // C = beta * C (or 0 when beta == 0): the K == 0 case, where the product is

@@ -81,29 +81,33 @@ struct Plan {
     int variant = 0;
     int cta_group = 1;
     int mc = 1;            // 4: 2 x 2 multicast cluster of single-CTA tiles
+    int arows = 128;       // A rows loaded per CTA (64: M <= 64, narrow kernel)
     int grid_m = 0, grid_n = 0;
     int bm = 128, bn = 256;
     int tiles_m = 0, tiles_n = 0, num_kb = 0;
     int grid = 0;
     int group_m = 1;
-    int tiles_dp = 0, tiles_split = 0, splits = 1, split_n = 0;
+    int tiles_dp = 0, sk_tiles = 0;
+    int64_t sk_iters = 0;
     uint32_t smem = 0;
-    uint64_t slot_bytes = 0;  // workspace bytes per split piece
-    uint64_t ws_bytes = 0;    // workspace this plan needs (0 without a split)
+    uint64_t slot_bytes = 0;  // workspace bytes per stream-K partial piece
+    uint64_t ws_bytes = 0;    // workspace this plan needs (0 without stream-K)
+    void* ws_ptr = nullptr;   // the workspace of this launch
 };
 
-constexpr int kMinKbPerPiece = 4;   // a split piece covers at least 4 k-blocks (256 of K)
-constexpr int kMaxSplits = 16;
-constexpr uint64_t kCounterBytes = 4096;  // arrival counters precede the partials
 
 // Pipeline depths: what fits in 227 KB of shared memory next to the 32 KB of
 // epilogue staging.
-constexpr int kStages1 = 4;    // 1-CTA: 4 x (16 KB A + 32 KB B) per CTA
-constexpr int kStages2 = 6;    // 2-CTA: 6 x (16 KB A + 16 KB B) per CTA
-constexpr int kStagesN64 = 8;  // 1-CTA narrow: 8 x (16 KB A + 8 KB B)
+constexpr int kStages1 = 4;     // 1-CTA: 4 x (16 KB A + 32 KB B) per CTA
+constexpr int kStages2 = 6;     // 2-CTA: 6 x (16 KB A + 16 KB B) per CTA
+constexpr int kStages2n = 6;    // 2-CTA, 224 wide: 6 x (16 KB A + 14 KB B) per CTA
+constexpr int kStagesN64 = 8;   // 1-CTA narrow: 8 x (16 KB A + 8 KB B)
+constexpr int kStagesN64h = 12; // 1-CTA narrow, M <= 64: 12 x (8 KB A + 8 KB B)
 using Cfg1 = tcg::GemmCfg<1, 256, kStages1>;
 using Cfg2 = tcg::GemmCfg<2, 256, kStages2>;
+using Cfg2n = tcg::GemmCfg<2, 224, kStages2n>;
 using CfgN64 = tcg::GemmCfg<1, 64, kStagesN64>;
+using CfgN64h = tcg::GemmCfg<1, 64, kStagesN64h, 64>;
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
@@ -127,21 +131,46 @@ int pick_variant(int64_t M, int64_t N, int64_t K, int sms) {
     return M > 128 ? TCGEMM_VARIANT_2CTA : TCGEMM_VARIANT_1CTA_N64;
 }
 
+// Stream-K sharing: a piece pays the same fixed costs as a whole tile
+// (pipeline fill, epilogue) and needs a reduction pass, so it only pays off
+// when whole tiles would leave most clusters idle for a long mainloop: all
+// tiles fit in half a round, K is at least 4096 (64 k-blocks), and every
+// cluster still gets at least 4 k-blocks.  (Measured on GB300: 512x512x16384
+// 80 -> 35 us, 256x2048x8192 46 -> 31 us; 1024x1280x2048 is faster without.)
+bool use_stream_k(int64_t tiles, int64_t clusters, int64_t num_kb) {
+    return 2 * tiles <= clusters && num_kb >= 64 && tiles * num_kb >= 4 * clusters;
+}
+
 bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pairs, int max_quads, Plan& pl,
                bool allow_split = true) {
     if (sms <= 0) return false;
     if (variant == TCGEMM_VARIANT_AUTO) variant = pick_variant(M, N, K, sms);
     pl.variant = variant;
+    allow_split = allow_split && split_enabled();
+    const int64_t num_kb = (K + 63) / 64;
     if (variant == TCGEMM_VARIANT_1CTA) {
         pl.cta_group = 1;
         pl.bm = Cfg1::kBM;
         pl.bn = 256;
         pl.smem = Cfg1::kSmemBytes;
-    } else if (variant == TCGEMM_VARIANT_2CTA) {
+    } else if (variant == TCGEMM_VARIANT_2CTA || variant == TCGEMM_VARIANT_2CTA_W256) {
         pl.cta_group = 2;
         pl.bm = Cfg2::kBM;
-        pl.bn = 256;
-        pl.smem = Cfg2::kSmemBytes;
+        // Tile width 256 or 224, whichever is estimated to finish sooner.
+        // Time per k-block ~ width + 32 (the shared-memory bytes a unit moves:
+        // its A tile whatever the width, plus the B tile); k-blocks per cluster
+        // = a balanced share with stream-K, else whole rounds of tiles.
+        const int64_t pairs = std::max(1, max_pairs > 0 ? max_pairs : sms / 2);
+        const int64_t tm = (M + 255) / 256;
+        auto cost = [&](int64_t bn) {
+            const int64_t t = tm * ((N + bn - 1) / bn);
+            const double kbs = (allow_split && use_stream_k(t, pairs, num_kb))
+                                   ? static_cast<double>(t * num_kb) / static_cast<double>(pairs)
+                                   : static_cast<double>((t + pairs - 1) / pairs * num_kb);
+            return kbs * static_cast<double>(bn + 32);
+        };
+        pl.bn = (variant == TCGEMM_VARIANT_2CTA && cost(224) < cost(256) * 0.97) ? 224 : 256;
+        pl.smem = pl.bn == 224 ? Cfg2n::kSmemBytes : Cfg2::kSmemBytes;
     } else if (variant == TCGEMM_VARIANT_1CTA_MC) {
         pl.cta_group = 1;
         pl.mc = 4;
@@ -152,13 +181,14 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pa
         pl.cta_group = 1;
         pl.bm = CfgN64::kBM;
         pl.bn = 64;
-        pl.smem = CfgN64::kSmemBytes;
+        pl.arows = M <= 64 ? 64 : 128;
+        pl.smem = pl.arows == 64 ? CfgN64h::kSmemBytes : CfgN64::kSmemBytes;
     } else {
         return false;
     }
     pl.tiles_m = ceil_div(M, pl.bm);
     pl.tiles_n = ceil_div(N, pl.bn);
-    pl.num_kb = ceil_div(K, 64);
+    pl.num_kb = static_cast<int>(num_kb);
     pl.slot_bytes = static_cast<uint64_t>(pl.cta_group) * 128 * pl.bn * 4;
     pl.grid_m = pl.mc == 4 ? (pl.tiles_m + 1) / 2 : pl.tiles_m;
     pl.grid_n = pl.mc == 4 ? (pl.tiles_n + 1) / 2 : pl.tiles_n;
@@ -171,35 +201,21 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pa
         allow_split = false;  // the 2 x 2 blocks are scheduled whole
     }
     const int csize = pl.cta_group * pl.mc;
-    // Whole tiles round-robin.  The tiles of a last, partial round are split
-    // so that more clusters share that round: along N into two half-width
-    // tiles when there are full rounds before it (or K is short), along K
-    // when the whole problem is less than one round and K is long.
     pl.tiles_dp = static_cast<int>(tiles);
-    pl.tiles_split = 0;
-    pl.splits = 1;
-    pl.split_n = 0;
-    const int64_t rem = tiles % clusters;
-    if (rem != 0 && allow_split && split_enabled()) {
-        int64_t ksp = std::min<int64_t>(std::min<int64_t>(clusters / rem, pl.num_kb / kMinKbPerPiece), kMaxSplits);
-        const bool long_k = pl.num_kb >= 4 * kMinKbPerPiece;
-        if (tiles < clusters && long_k && ksp >= 2) {
-            pl.splits = static_cast<int>(ksp);
-        } else if (2 * rem <= clusters && pl.bn >= 64) {
-            pl.splits = 2;
-            pl.split_n = 1;
-        }
-        if (pl.splits > 1) {
-            pl.tiles_split = static_cast<int>(rem);
-            pl.tiles_dp = static_cast<int>(tiles - rem);
-        }
+    pl.sk_tiles = 0;
+    pl.sk_iters = 0;
+    if (allow_split && use_stream_k(tiles, clusters, num_kb)) {
+        const int64_t rem = tiles % clusters;
+        pl.sk_tiles = static_cast<int>(rem);
+        pl.sk_iters = rem * num_kb;
+        pl.tiles_dp = static_cast<int>(tiles - rem);
+        pl.grid = static_cast<int>(clusters) * csize;
+        // Two partial slots per cluster (the first and last segment of its range).
+        pl.ws_bytes = 2 * static_cast<uint64_t>(clusters) * pl.slot_bytes;
+    } else {
+        pl.grid = static_cast<int>(std::min<int64_t>(tiles, clusters)) * csize;
+        pl.ws_bytes = 0;
     }
-    const int64_t units = std::max<int64_t>(std::min<int64_t>(pl.tiles_dp, clusters),
-                                            static_cast<int64_t>(pl.tiles_split) * pl.splits);
-    pl.grid = static_cast<int>(std::min<int64_t>(std::max<int64_t>(units, 1), clusters)) * csize;
-    pl.ws_bytes = (pl.tiles_split > 0 && !pl.split_n)
-                      ? kCounterBytes + static_cast<uint64_t>(pl.tiles_split) * pl.splits * pl.slot_bytes
-                      : 0;
     // Band height so that the tiles in flight at once cover a roughly square
     // patch of C: group_m^2 ~ concurrent tiles * (tile width / tile height).
     const double ideal = std::sqrt(static_cast<double>(pl.grid / csize) * pl.bn / pl.bm);
@@ -212,7 +228,8 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pa
 // --------------------------------------------------------- tensor maps --
 
 // C (column-major M x N, fp32 or bf16) in 128-row x 32-column boxes, for the
-// epilogue's TMA loads, stores and L2 prefetches.
+// epilogue's TMA loads, stores and L2 prefetches.  The stream-K workspace is
+// mapped the same way (fp32, 128 rows, ldc = 128).
 bool encode_c(CUtensorMap* m, void* ptr, int64_t M, int64_t N, int64_t ldc, bool bf16) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) {
@@ -261,15 +278,15 @@ bool encode_kmajor(CUtensorMap* m, const void* ptr, int64_t k_extent, int64_t ro
 
 // The dynamic shared-memory opt-in is a per-kernel attribute; it is set once
 // per device for each kernel instantiation.
-template <int CG, int BN, int ST, int MC, typename OutT>
+template <int CG, int BN, int ST, int MC, int AR, typename OutT>
 bool ensure_smem_attr(int dev) {
     static std::mutex mu;
     static bool done[kMaxDevices] = {};
     std::lock_guard<std::mutex> lk(mu);
     if (done[dev]) return true;
-    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, MC, OutT>;
+    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, MC, AR, OutT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(tcg::GemmCfg<CG, BN, ST>::kSmemBytes));
+                                         static_cast<int>(tcg::GemmCfg<CG, BN, ST, AR>::kSmemBytes));
     if (e != cudaSuccess) {
         set_error("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         return false;
@@ -278,14 +295,14 @@ bool ensure_smem_attr(int dev) {
     return true;
 }
 
-template <int CG, int BN, int ST, int MC, typename OutT>
-int launch_gemm(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbh,
-                const CUtensorMap& tcm, const tcg::GemmParams& gp, cudaStream_t stream, int dev) {
-    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, MC, OutT>;
-    if (!ensure_smem_attr<CG, BN, ST, MC, OutT>(dev)) return TCGEMM_ERR_CUDA;
+template <int CG, int BN, int ST, int MC, int AR, typename OutT>
+int launch_gemm(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tcm,
+                const CUtensorMap& twm, const tcg::GemmParams& gp, cudaStream_t stream, int dev) {
+    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, MC, AR, OutT>;
+    if (!ensure_smem_attr<CG, BN, ST, MC, AR, OutT>(dev)) return TCGEMM_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(pl.grid), 1, 1);
-    cfg.blockDim = dim3(tcg::GemmCfg<CG, BN, ST>::kThreads, 1, 1);
+    cfg.blockDim = dim3(tcg::GemmCfg<CG, BN, ST, AR>::kThreads, 1, 1);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -298,12 +315,25 @@ int launch_gemm(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, co
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tbh, tcm, gp);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tcm, twm, gp);
     if (e != cudaSuccess) {
         set_error("kernel launch: %s", cudaGetErrorString(e));
         return TCGEMM_ERR_CUDA;
     }
     g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (pl.sk_tiles > 0) {
+        // Add up the shared tiles' partials (same stream, so after the GEMM).
+        const unsigned blocks = static_cast<unsigned>(pl.sk_tiles * CG * (BN / 32));
+        tcg::sk_reduce_kernel<CG, BN, OutT><<<blocks, 128, 0, stream>>>(
+            static_cast<const float*>(pl.ws_ptr), gp,
+            pl.grid / (CG * MC));
+        e = cudaGetLastError();
+        if (e != cudaSuccess) {
+            set_error("reduction kernel launch: %s", cudaGetErrorString(e));
+            return TCGEMM_ERR_CUDA;
+        }
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+    }
     return TCGEMM_OK;
 }
 
@@ -352,13 +382,13 @@ int probe_device(int& dev_out, DeviceInfo& info) {
         if (d.supported) {
             // How many clusters of each kind can be resident at once (cluster
             // placement may leave some SMs of a GPC unused).
-            if (ensure_smem_attr<2, 256, kStages2, 1, __nv_bfloat16>(dev)) {
-                const int n = max_active_clusters(tcg::gemm_bf16_tn_kernel<2, 256, kStages2, 1, __nv_bfloat16>,
+            if (ensure_smem_attr<2, 256, kStages2, 1, 128, __nv_bfloat16>(dev)) {
+                const int n = max_active_clusters(tcg::gemm_bf16_tn_kernel<2, 256, kStages2, 1, 128, __nv_bfloat16>,
                                                   2, Cfg2::kSmemBytes, sms);
                 if (n > 0) d.max_pairs = n;
             }
-            if (ensure_smem_attr<1, 256, kStages1, 4, __nv_bfloat16>(dev)) {
-                const int n = max_active_clusters(tcg::gemm_bf16_tn_kernel<1, 256, kStages1, 4, __nv_bfloat16>,
+            if (ensure_smem_attr<1, 256, kStages1, 4, 128, __nv_bfloat16>(dev)) {
+                const int n = max_active_clusters(tcg::gemm_bf16_tn_kernel<1, 256, kStages1, 4, 128, __nv_bfloat16>,
                                                   4, Cfg1::kSmemBytes, sms);
                 if (n > 0) d.max_quads = n;
             }
@@ -420,13 +450,13 @@ int validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     return TCGEMM_OK;
 }
 
-// Largest workspace any plan on a device with `sms` SMs can need: at most one
-// split piece per cluster, 128 rows x 256 columns of fp32 per CTA.
-uint64_t max_workspace_bytes(int sms) { return kCounterBytes + static_cast<uint64_t>(sms) * 128 * 256 * 4; }
+// Largest workspace any plan on a device with `sms` SMs can need: two partial
+// slots per cluster, 128 rows x 256 columns of fp32 per CTA.
+uint64_t max_workspace_bytes(int sms) { return 2 * static_cast<uint64_t>(sms) * 128 * 256 * 4; }
 
 // Library-owned split workspace, one per (device, stream) so that calls on
-// different streams never share partials.  Allocated (and its counters
-// zeroed, in stream order) the first time a split plan runs on that stream.
+// different streams never share partials.  Allocated the first time a
+// stream-K plan runs on that stream.
 struct InternalWs {
     void* ptr = nullptr;
     uint64_t bytes = 0;
@@ -445,12 +475,6 @@ int internal_workspace(int dev, int sms, cudaStream_t stream, uint64_t need, voi
             set_error("workspace cudaMalloc(%llu): %s", static_cast<unsigned long long>(bytes), cudaGetErrorString(e));
             return TCGEMM_ERR_CUDA;
         }
-        e = cudaMemsetAsync(p, 0, kCounterBytes, stream);
-        if (e != cudaSuccess) {
-            cudaFree(p);
-            set_error("workspace memset: %s", cudaGetErrorString(e));
-            return TCGEMM_ERR_CUDA;
-        }
         if (w.ptr) cudaFree(w.ptr);  // never reached in practice: the first block is the maximum
         w.ptr = p;
         w.bytes = bytes;
@@ -463,10 +487,10 @@ int internal_workspace(int dev, int sms, cudaStream_t stream, uint64_t need, voi
 //
 // Scratch for gemm_bf16_noalloc: a file-scope device array of fixed size, so
 // that entry point never allocates.  Every GPU that loads this library holds
-// these 16 MiB until the process exits.  In host code the array's name is only
+// these 40 MiB until the process exits.  In host code the array's name is only
 // a stand-in: its device address comes from cudaGetSymbolAddress, taken once
 // per device (with that device current) on the first call there.
-constexpr uint64_t kNoAllocScratchBytes = uint64_t{16} << 20;
+constexpr uint64_t kNoAllocScratchBytes = uint64_t{40} << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_noalloc_mu;
@@ -487,6 +511,28 @@ int noalloc_scratch(int dev, void** out) {
     return TCGEMM_OK;
 }
 
+void fill_plan_out(const Plan& pl, int64_t* out) {
+    out[0] = pl.grid;
+    out[1] = pl.cta_group * pl.mc;
+    out[2] = pl.tiles_m;
+    out[3] = pl.tiles_n;
+    out[4] = pl.bm;
+    out[5] = pl.bn;
+    out[6] = pl.num_kb;
+    out[7] = pl.smem;
+    out[8] = pl.tiles_dp;
+    out[9] = pl.sk_tiles;
+    out[10] = pl.sk_iters;
+    out[11] = static_cast<int64_t>(pl.ws_bytes);
+    out[12] = pl.group_m;
+    out[13] = pl.variant;
+    out[14] = pl.cta_group;
+    out[15] = pl.grid_m;
+    out[16] = pl.grid_n;
+    out[17] = pl.sk_tiles > 0 ? 1 : 0;
+    out[18] = pl.arows;
+}
+
 constexpr int kWsInternal = 0;
 constexpr int kWsCaller = 1;
 constexpr int kWsNone = 2;     // plan without any split
@@ -496,7 +542,7 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
              int64_t ldc, float alpha, float beta, int out_dtype, void* stream_v, int variant,
              int ws_mode = kWsInternal, void* ws = nullptr, int64_t ws_bytes = 0) {
     t_last_error[0] = '\0';
-    if (variant < TCGEMM_VARIANT_AUTO || variant > TCGEMM_VARIANT_1CTA_N64) {
+    if (variant < TCGEMM_VARIANT_AUTO || variant > TCGEMM_VARIANT_2CTA_W256) {
         set_error("unknown variant %d", variant);
         return TCGEMM_ERR_INVALID_ARG;
     }
@@ -551,15 +597,10 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
                           static_cast<unsigned long long>(kNoAllocScratchBytes));
                 return TCGEMM_ERR_INVALID_ARG;
             }
+            // The array keeps the last call's contents; every partial is
+            // written before it is read, so nothing needs clearing.
             rc = noalloc_scratch(dev, &wsp);
             if (rc != TCGEMM_OK) return rc;
-            // The array keeps the last call's contents: the arrival counters
-            // must start at zero, so clear them in stream order first.
-            cudaError_t e = cudaMemsetAsync(wsp, 0, kCounterBytes, static_cast<cudaStream_t>(stream_v));
-            if (e != cudaSuccess) {
-                set_error("clearing the scratch counters: %s", cudaGetErrorString(e));
-                return TCGEMM_ERR_CUDA;
-            }
         } else {
             rc = internal_workspace(dev, info.sms, static_cast<cudaStream_t>(stream_v), pl.ws_bytes, &wsp);
             if (rc != TCGEMM_OK) return rc;
@@ -567,19 +608,22 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     }
     // Box heights: a CTA pair loads half of the B tile per CTA; a multicast
     // CTA loads half of its A tile and half of its B tile.
-    const uint32_t a_box_rows = pl.mc == 4 ? 64u : 128u;
+    const uint32_t a_box_rows = (pl.mc == 4 || pl.arows == 64) ? 64u : 128u;
     const uint32_t b_box_rows = static_cast<uint32_t>(pl.bn / pl.cta_group / (pl.mc == 4 ? 2 : 1));
-    CUtensorMap ta, tb, tbh;
+    CUtensorMap ta, tb;
     if (!encode_kmajor(&ta, A, K, M, lda, a_box_rows) || !encode_kmajor(&tb, B, K, N, ldb, b_box_rows)) {
         return TCGEMM_ERR_INVALID_ARG;
     }
-    if (pl.split_n) {
-        if (!encode_kmajor(&tbh, B, K, N, ldb, b_box_rows / 2)) return TCGEMM_ERR_INVALID_ARG;
-    } else {
-        tbh = tb;
-    }
-    CUtensorMap tcm;
+    pl.ws_ptr = wsp;
+    CUtensorMap tcm, twm;
     if (!encode_c(&tcm, C, M, N, ldc, out_dtype == TCGEMM_OUT_BF16)) return TCGEMM_ERR_INVALID_ARG;
+    if (pl.sk_tiles > 0) {
+        const int64_t wcols = 2 * static_cast<int64_t>(pl.grid / pl.cta_group) * pl.cta_group * pl.bn;
+        if (!encode_c(&twm, wsp, 128, wcols, 128, false))
+            return TCGEMM_ERR_INVALID_ARG;
+    } else {
+        twm = tcm;
+    }
     tcg::GemmParams gp;
     gp.M = static_cast<int>(M);
     gp.N = static_cast<int>(N);
@@ -595,28 +639,21 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     gp.alpha = alpha;
     gp.beta = beta;
     gp.tiles_dp = pl.tiles_dp;
-    gp.tiles_split = pl.tiles_split;
-    gp.splits = pl.splits;
-    gp.split_n = pl.split_n;
-    gp.counters = static_cast<unsigned int*>(wsp);
-    gp.ws = wsp ? reinterpret_cast<float*>(static_cast<char*>(wsp) + kCounterBytes) : nullptr;
+    gp.sk_tiles = pl.sk_tiles;
+    gp.sk_iters = pl.sk_iters;
     gp.timeout_ns = timeout_ns();
 
     const bool bf16 = out_dtype == TCGEMM_OUT_BF16;
-    if (pl.mc == 4) {
-        return bf16 ? launch_gemm<1, 256, kStages1, 4, __nv_bfloat16>(pl, ta, tb, tbh, tcm, gp, stream, dev)
-                    : launch_gemm<1, 256, kStages1, 4, float>(pl, ta, tb, tbh, tcm, gp, stream, dev);
-    }
-    if (pl.bn == 64) {
-        return bf16 ? launch_gemm<1, 64, kStagesN64, 1, __nv_bfloat16>(pl, ta, tb, tbh, tcm, gp, stream, dev)
-                    : launch_gemm<1, 64, kStagesN64, 1, float>(pl, ta, tb, tbh, tcm, gp, stream, dev);
-    }
-    if (pl.cta_group == 1) {
-        return bf16 ? launch_gemm<1, 256, kStages1, 1, __nv_bfloat16>(pl, ta, tb, tbh, tcm, gp, stream, dev)
-                    : launch_gemm<1, 256, kStages1, 1, float>(pl, ta, tb, tbh, tcm, gp, stream, dev);
-    }
-    return bf16 ? launch_gemm<2, 256, kStages2, 1, __nv_bfloat16>(pl, ta, tb, tbh, tcm, gp, stream, dev)
-                : launch_gemm<2, 256, kStages2, 1, float>(pl, ta, tb, tbh, tcm, gp, stream, dev);
+#define TCGEMM_LAUNCH(CG, BN, ST, MC, AR)                                                              \
+    return bf16 ? launch_gemm<CG, BN, ST, MC, AR, __nv_bfloat16>(pl, ta, tb, tcm, twm, gp, stream, dev) \
+                : launch_gemm<CG, BN, ST, MC, AR, float>(pl, ta, tb, tcm, twm, gp, stream, dev)
+    if (pl.mc == 4) TCGEMM_LAUNCH(1, 256, kStages1, 4, 128);
+    if (pl.bn == 64 && pl.arows == 64) TCGEMM_LAUNCH(1, 64, kStagesN64h, 1, 64);
+    if (pl.bn == 64) TCGEMM_LAUNCH(1, 64, kStagesN64, 1, 128);
+    if (pl.cta_group == 1) TCGEMM_LAUNCH(1, 256, kStages1, 1, 128);
+    if (pl.bn == 224) TCGEMM_LAUNCH(2, 224, kStages2n, 1, 128);
+    TCGEMM_LAUNCH(2, 256, kStages2, 1, 128);
+#undef TCGEMM_LAUNCH
 }
 
 }  // namespace
@@ -660,25 +697,65 @@ int tcgemm_plan(int64_t M, int64_t N, int64_t K, int variant, int num_sms, int64
     if (out == nullptr || M <= 0 || N <= 0 || K <= 0 || num_sms <= 0) return TCGEMM_ERR_INVALID_ARG;
     Plan pl;
     if (!make_plan(M, N, K, variant, num_sms, num_sms / 2, num_sms / 4, pl)) return TCGEMM_ERR_INVALID_ARG;
-    out[0] = pl.grid;
-    out[1] = pl.cta_group * pl.mc;
-    out[2] = pl.tiles_m;
-    out[3] = pl.tiles_n;
-    out[4] = pl.bm;
-    out[5] = pl.bn;
-    out[6] = pl.num_kb;
-    out[7] = pl.smem;
-    out[8] = pl.tiles_dp;
-    out[9] = pl.tiles_split;
-    out[10] = pl.splits;
-    out[11] = static_cast<int64_t>(pl.ws_bytes);
-    out[12] = pl.group_m;
-    out[13] = pl.variant;
-    out[14] = pl.cta_group;
-    out[15] = pl.grid_m;
-    out[16] = pl.grid_n;
-    out[17] = pl.split_n;
+    fill_plan_out(pl, out);
     return TCGEMM_OK;
+}
+
+int tcgemm_device_info(int64_t* out) {
+    if (out == nullptr) return TCGEMM_ERR_INVALID_ARG;
+    int dev = 0;
+    DeviceInfo info;
+    const int rc = probe_device(dev, info);
+    if (rc != TCGEMM_OK) return rc;
+    out[0] = info.sms;
+    out[1] = info.max_pairs;
+    out[2] = info.max_quads;
+    out[3] = dev;
+    return TCGEMM_OK;
+}
+
+int tcgemm_plan_device(int64_t M, int64_t N, int64_t K, int variant, int64_t* out) {
+    int64_t d[4];
+    const int rc = tcgemm_device_info(d);
+    if (rc != TCGEMM_OK) return rc;
+    if (out == nullptr || M <= 0 || N <= 0 || K <= 0) return TCGEMM_ERR_INVALID_ARG;
+    Plan pl;
+    if (!make_plan(M, N, K, variant, static_cast<int>(d[0]), static_cast<int>(d[1]), static_cast<int>(d[2]), pl))
+        return TCGEMM_ERR_INVALID_ARG;
+    fill_plan_out(pl, out);
+    return TCGEMM_OK;
+}
+
+int tcgemm_units(int64_t M, int64_t N, int64_t K, int variant, int num_sms, int cluster, int max_units,
+                 int32_t* out) {
+    if (out == nullptr || M <= 0 || N <= 0 || K <= 0 || num_sms <= 0 || max_units < 0) return -1;
+    Plan pl;
+    if (!make_plan(M, N, K, variant, num_sms, num_sms / 2, num_sms / 4, pl)) return -1;
+    const int clusters = pl.grid / (pl.cta_group * pl.mc);
+    if (cluster < 0 || cluster >= clusters) return -1;
+    tcg::GemmParams gp = {};
+    gp.num_kb = pl.num_kb;
+    gp.tiles_dp = pl.tiles_dp;
+    gp.sk_tiles = pl.sk_tiles;
+    gp.sk_iters = pl.sk_iters;
+    tcg::UnitIter it(cluster, clusters);
+    it.start(gp);
+    tcg::WorkUnit u;
+    int n = 0;
+    while (it.next(gp, u)) {
+        if (n < max_units) {
+            int32_t* o = out + 7 * n;
+            o[0] = u.tile;
+            o[1] = u.kb0;
+            o[2] = u.kb1;
+            o[3] = u.slot;
+            o[4] = u.sk_tile;
+            o[5] = u.piece;
+            o[6] = u.npieces;
+        }
+        ++n;
+    }
+    return n;
 }
 
 int tcgemm_tile_order(int tiles_m, int tiles_n, int group_m, int64_t count, int32_t* tm, int32_t* tn) {

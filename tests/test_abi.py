@@ -93,74 +93,84 @@ def test_tile_order_groups_for_l2(tc):
 
 @pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (8192, 8192, 8192), (4000, 4100, 4104),
                                    (64, 8192, 8192), (256, 256, 256), (1, 1, 1)])
-@pytest.mark.parametrize("variant", [1, 2, 3, 4])
+@pytest.mark.parametrize("variant", [1, 2, 3, 4, 5])
 def test_plans(tc, M, N, K, variant):
     p = tc.plan(M, N, K, variant, 152)
     assert p["tiles_m"] * p["bm"] >= M and (p["tiles_m"] - 1) * p["bm"] < M
     assert p["tiles_n"] * p["bn"] >= N and (p["tiles_n"] - 1) * p["bn"] < N
     assert p["num_kb"] * 64 >= K
     assert p["grid"] % p["cluster"] == 0 and 0 < p["grid"] <= 152
-    assert p["grid"] // p["cluster"] <= p["grid_m"] * p["grid_n"] * p["splits"]
+    assert p["grid"] // p["cluster"] <= p["grid_m"] * p["grid_n"] or p["stream_k"]
     assert p["smem"] <= 227 * 1024
 
 
-@pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (8192, 8192, 8192), (4000, 4100, 4104), (64, 8192, 8192),
-                                   (1024, 1280, 2048), (513, 200, 1000), (200, 300, 2392), (1, 1, 1),
-                                   (129, 257, 65), (100000, 128, 64)])
-@pytest.mark.parametrize("variant", [1, 2, 3, 4])
+SK_SHAPES = [(4096, 4096, 4096), (8192, 8192, 8192), (4000, 4100, 4104), (64, 8192, 8192), (512, 512, 16384),
+             (513, 200, 1000), (200, 300, 2392), (1, 1, 1), (129, 257, 65), (100000, 128, 64), (3000, 5000, 777)]
+
+
+@pytest.mark.parametrize("M,N,K", SK_SHAPES)
+@pytest.mark.parametrize("variant", [1, 2, 3, 4, 5])
 @pytest.mark.parametrize("sms", [152, 148, 20])
-def test_split_plan_invariants(tc, M, N, K, variant, sms):
+def test_stream_k_plan_invariants(tc, M, N, K, variant, sms):
     p = tc.plan(M, N, K, variant, sms)
-    tiles = p["grid_m"] * p["grid_n"]
-    clusters = sms // p["cluster"]
-    assert p["tiles_dp"] + p["tiles_split"] == tiles
-    assert p["tiles_dp"] % clusters == 0 or p["tiles_split"] == 0
-    if p["tiles_split"] and p["split_n"]:
-        assert p["splits"] == 2 and p["tiles_split"] * 2 <= clusters and p["ws_bytes"] == 0
-    elif p["tiles_split"]:
-        assert p["splits"] >= 2 and p["tiles_split"] * p["splits"] <= clusters
-        assert p["splits"] * 4 <= p["num_kb"]
-        assert p["ws_bytes"] == 4096 + p["tiles_split"] * p["splits"] * p["cta_group"] * 128 * p["bn"] * 4
-        assert p["ws_bytes"] <= 4096 + sms * 128 * 256 * 4
+    units = p["grid_m"] * p["grid_n"]
+    clusters = p["grid"] // p["cluster"]
+    assert p["tiles_dp"] + p["sk_tiles"] == units
+    if p["stream_k"]:
+        full = (sms // p["cluster"]) if p["cluster"] > 1 else sms
+        assert clusters == min(full, sms // p["cluster"]) and p["tiles_dp"] % clusters == 0
+        assert 0 < p["sk_tiles"] < clusters and 2 * p["sk_tiles"] <= clusters and p["tiles_dp"] == 0
+        assert p["sk_iters"] == p["sk_tiles"] * p["num_kb"] >= 4 * clusters
+        assert p["ws_bytes"] == 2 * clusters * p["cta_group"] * 128 * p["bn"] * 4
+        assert p["ws_bytes"] <= 2 * sms * 128 * 256 * 4
     else:
-        assert p["splits"] == 1 and p["ws_bytes"] == 0
+        assert p["sk_tiles"] == 0 and p["ws_bytes"] == 0
     assert tc.workspace_bytes(M, N, K, variant, sms) == p["ws_bytes"]
 
 
-def test_unit_schedule_covers_every_k_block_once(tc):
-    """Simulates the kernel's unit walk on the host for a few plans: every
-    (tile, column half, k-block) triple is produced by exactly one cluster."""
-    cases = [(4096, 4096, 4096, 2), (8192, 8192, 8192, 2), (1024, 1280, 2048, 2), (64, 8192, 8192, 1),
-             (513, 200, 1000, 1), (4000, 4100, 4104, 3), (129, 257, 65, 3), (64, 8192, 8192, 4),
-             (4096, 4096, 4096, 1)]
-    for (M, N, K, v) in cases:
-        p = tc.plan(M, N, K, v, 152)
-        G = p["grid"] // p["cluster"]
-        seen = {}
+def _sk_slot(c, t_begin, iters, clusters):
+    # the fixup's formula, restated: a cluster's first segment uses slot 2c
+    return 2 * c + (0 if (c * iters) // clusters >= t_begin else 1)
 
-        def add(t, half, kb):
-            for h in ((0, 1) if half < 0 else (half,)):
-                seen[(t, h, kb)] = seen.get((t, h, kb), 0) + 1
 
-        for c in range(G):
-            t = c
-            while t < p["tiles_dp"]:
-                for kb in range(p["num_kb"]):
-                    add(t, -1, kb)
-                t += G
-            if c < p["tiles_split"] * p["splits"]:
-                s, piece = divmod(c, p["splits"])
-                if p["split_n"]:
-                    for kb in range(p["num_kb"]):
-                        add(p["tiles_dp"] + s, piece, kb)
-                else:
-                    kb0 = piece * p["num_kb"] // p["splits"]
-                    kb1 = (piece + 1) * p["num_kb"] // p["splits"]
-                    assert kb1 > kb0
-                    for kb in range(kb0, kb1):
-                        add(p["tiles_dp"] + s, -1, kb)
-        tiles = p["grid_m"] * p["grid_n"]
-        assert len(seen) == tiles * 2 * p["num_kb"] and set(seen.values()) == {1}, (M, N, K, v)
+@pytest.mark.parametrize("M,N,K,v", [(4096, 4096, 4096, 2), (8192, 8192, 8192, 2), (512, 512, 16384, 2),
+                                     (256, 2048, 8192, 1), (600, 700, 8192, 5), (1024, 1280, 2048, 2),
+                                     (64, 8192, 8192, 1), (513, 200, 1000, 1), (4000, 4100, 4104, 3),
+                                     (129, 257, 65, 3), (64, 8192, 8192, 4), (4096, 4096, 4096, 1),
+                                     (4096, 4096, 4096, 5), (8192, 8192, 8192, 5), (4000, 4100, 4104, 2),
+                                     (200, 300, 2392, 2), (3000, 5000, 777, 2)])
+def test_unit_schedule_covers_every_k_block_once(tc, M, N, K, v):
+    """Runs the kernel's own unit iterator (host copy) for every cluster:
+    every (tile, k-block) is produced exactly once; the pieces of each
+    stream-K tile are numbered 0..n-1 in K order, agree on n, use distinct
+    workspace slots, and the slot the fixup computes for piece i is the slot
+    that piece writes."""
+    p = tc.plan(M, N, K, v, 152)
+    G = p["grid"] // p["cluster"]
+    seen = {}
+    pieces = {}
+    for c in range(G):
+        for u in tc.binding.units(M, N, K, v, 152, c):
+            assert 0 <= u["kb0"] < u["kb1"] <= p["num_kb"]
+            for kb in range(u["kb0"], u["kb1"]):
+                seen[(u["tile"], kb)] = seen.get((u["tile"], kb), 0) + 1
+            if u["slot"] >= 0:
+                pieces.setdefault(u["sk_tile"], []).append((u["kb0"], u["piece"], u["npieces"], u["slot"], c))
+            else:
+                assert u["kb0"] == 0 and u["kb1"] == p["num_kb"]
+    assert len(seen) == p["grid_m"] * p["grid_n"] * p["num_kb"] and set(seen.values()) == {1}
+    slots = set()
+    for t, ps in pieces.items():
+        ps.sort()
+        n = ps[0][2]
+        assert [x[1] for x in ps] == list(range(n)) and all(x[2] == n for x in ps) and n >= 2
+        first = ps[0][4]
+        for i, (_, _, _, slot, c) in enumerate(ps):
+            assert c == first + i
+            assert slot == _sk_slot(c, t * p["num_kb"], p["sk_iters"], G)
+            assert slot not in slots
+            slots.add(slot)
+    assert all(0 <= sl < 2 * G for sl in slots)
 
 
 @pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (4000, 4100, 4104), (129, 257, 65), (1, 1, 1)])
@@ -169,7 +179,22 @@ def test_multicast_plan_blocks(tc, M, N, K):
     p = tc.plan(M, N, K, 3, 152)
     assert p["cluster"] == 4 and p["cta_group"] == 1 and p["bm"] == 128 and p["bn"] == 256
     assert p["grid_m"] == (p["tiles_m"] + 1) // 2 and p["grid_n"] == (p["tiles_n"] + 1) // 2
-    assert p["tiles_split"] == 0 and p["ws_bytes"] == 0
+    assert p["sk_tiles"] == 0 and p["ws_bytes"] == 0
+
+
+def test_width_choice(tc):
+    """The pair kernel takes 224-wide tiles where whole rounds of them finish
+    sooner (4096^2: 304 tiles = 4 rounds instead of 256 tiles = 3.4 rounds);
+    variant 5 always uses 256; skinny shapes load 64-row A tiles; stream-K only
+    for problems with at most half a round of tiles and a long K."""
+    assert tc.plan(4096, 4096, 4096, 2, 152)["bn"] == 224    # 304 tiles = 4 full rounds of 76 pairs
+    assert tc.plan(8192, 8192, 8192, 2, 152)["bn"] == 256
+    assert tc.plan(4096, 4096, 4096, 5, 152)["bn"] == 256
+    assert tc.plan(64, 8192, 8192, 4, 152)["arows"] == 64
+    assert tc.plan(128, 8192, 8192, 4, 152)["arows"] == 128
+    assert tc.plan(4096, 4096, 4096, 2, 152)["stream_k"] == 0
+    assert tc.plan(1024, 1280, 2048, 2, 152)["stream_k"] == 0   # K too short to pay for it
+    assert tc.plan(512, 512, 16384, 2, 152)["stream_k"] == 1    # 4 tiles, long K
 
 
 def test_auto_variant_choice(tc):

@@ -21,9 +21,9 @@ pytestmark = pytest.mark.gpu
 
 import os
 
-# 1-CTA, 2-CTA, 2x2-multicast and narrow 128x64 kernels; TCGEMM_TEST_VARIANTS="1"
-# narrows a run to one of them.
-VARIANTS = [int(v) for v in os.environ.get("TCGEMM_TEST_VARIANTS", "1,2,3,4").split(",") if v]
+# 1-CTA, 2-CTA (auto width), 2x2-multicast, narrow 128x64 and 2-CTA 256-wide
+# kernels; TCGEMM_TEST_VARIANTS="1" narrows a run to one of them.
+VARIANTS = [int(v) for v in os.environ.get("TCGEMM_TEST_VARIANTS", "1,2,3,4,5").split(",") if v]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -165,17 +165,18 @@ def test_hang_guard_selftest():
 
 
 def _split_case():
-    # 2-CTA: 4 x 5 = 20 tiles on 76 pairs -> every tile split 3 ways along K.
-    return gi.make_case("split", 1024, 1280, 2048, alpha=0.5, beta=0.25, out_dtype=gi.OUT_F32, seed=31)
+    # A handful of pair tiles and K = 8192: stream-K shares their k-blocks out
+    # over all the pairs.
+    return gi.make_case("split", 600, 700, 8192, alpha=0.5, beta=0.25, out_dtype=gi.OUT_F32, seed=31)
 
 
 def test_split_tiles_repeat_deterministic(oracle_lib):
-    """Tiles split along K: correct, and bit-identical over repeated calls
-    (partials are added in piece order, whatever order the pieces finish)."""
+    """Stream-K tiles: correct, and bit-identical over repeated calls
+    (partials are added in K order, whatever order the pieces finish)."""
     import tensor_core_matmul_gb300 as tc
     case = _split_case()
-    p = tc.plan(case.M, case.N, case.K, 0, torch.cuda.get_device_properties(0).multi_processor_count)
-    assert p["tiles_split"] > 0 and p["splits"] >= 2, p
+    p = tc.binding.plan_device(case.M, case.N, case.K, 0)
+    assert p["stream_k"] == 1 and p["sk_tiles"] > 0, p
     first = None
     for _ in range(3):
         g = H.run_case(case, 0)
@@ -193,7 +194,7 @@ def test_caller_workspace_matches_internal(oracle_lib):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     need = tc.workspace_bytes(case.M, case.N, case.K, 0, sms)
     assert need > 0
-    ws = torch.zeros(need + 256, dtype=torch.uint8, device="cuda")
+    ws = torch.full((need + 256,), 0x7F, dtype=torch.uint8, device="cuda")  # no zeroing needed
     A, B = case.A.cuda(), case.B.cuda()
     g = H.GuardedC(case)
     s = torch.cuda.current_stream().cuda_stream
@@ -205,7 +206,6 @@ def test_caller_workspace_matches_internal(oracle_lib):
     g.check_guards()
     ref = H.run_case(case, 0).result_np()
     assert np.array_equal(g.result_np().view(np.uint32), ref.view(np.uint32))
-    assert not ws[:4096].any(), "arrival counters must be left at zero"
     st = tc.gemm_bf16_ws_raw(case.M, case.N, case.K, A.data_ptr(), case.lda, B.data_ptr(), case.ldb,
                              g.C.data_ptr(), case.ldc, case.alpha, case.beta, case.out_dtype, s, 0,
                              ws.data_ptr(), need - 1)
@@ -220,20 +220,30 @@ def test_split_small_k_pieces(oracle_lib, variant):
     H.compare_full(oracle_lib, case, g.result_np(), what=f"long K v{variant}")
 
 
-@pytest.mark.parametrize("variant", [1, 2, 4])
-def test_half_width_tail_tiles(oracle_lib, variant):
-    """More tiles than one round with a short last round: the tail tiles run as
-    two half-width tiles each (bit-exact on integer inputs, both halves of
-    every tail tile written, nothing else)."""
+@pytest.mark.parametrize("variant", [1, 2, 4, 5])
+@pytest.mark.parametrize("kind", ["integer", "normal"])
+def test_stream_k_small_problems(oracle_lib, variant, kind):
+    """Few tiles and a long K, so stream-K shares every k-block out over all
+    clusters (ragged edges, K not a multiple of 64): integer inputs bit-exact,
+    N(0,1) inputs within tolerance, beta = 0.5 over C."""
     import tensor_core_matmul_gb300 as tc
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    bm = {1: 128, 2: 256, 4: 128}[variant]
-    bn = {1: 256, 2: 256, 4: 64}[variant]
-    clusters = sms // (2 if variant == 2 else 1)
-    tiles_n = (clusters + 3) // 4 + 1
-    M, N = bm * 4 + 40, bn * tiles_n - 24     # ragged edges on both sides
-    p = tc.plan(M, N, 320, variant, sms)
-    assert p["split_n"] == 1 and p["tiles_split"] > 0, p
-    case = gi.make_case("half", M, N, 320, alpha=1.0, beta=0.5, out_dtype=gi.OUT_F32, seed=51, kind="integer")
-    g = H.run_case(case, variant)
-    H.compare_full(oracle_lib, case, g.result_np(), exact=True, what=f"half-width v{variant}")
+    bm = {1: 128, 2: 256, 4: 128, 5: 256}[variant]
+    bn = {1: 256, 2: 256, 4: 64, 5: 256}[variant]
+    shapes = [(bm * 2 - 40, bn * 3 - 24, 8000), (bm - 7, bn * 5 - 100, 12000)]
+    for n, (M, N, K) in enumerate(shapes):
+        p = tc.binding.plan_device(M, N, K, variant)
+        assert p["stream_k"] == 1, (M, N, K, p)
+        case = gi.make_case("sk", M, N, K, alpha=1.0, beta=0.5, out_dtype=gi.OUT_F32 if n == 0 else gi.OUT_BF16,
+                            seed=70 + n, kind=kind)
+        g = H.run_case(case, variant)
+        H.compare_full(oracle_lib, case, g.result_np(), exact=(kind == "integer"), what=f"stream-K v{variant} {M}x{N}x{K}")
+
+
+def test_device_plan_and_width_choice():
+    import tensor_core_matmul_gb300 as tc
+    info = tc.binding.device_info()
+    assert info["sms"] >= 100 and 0 < info["max_pairs"] <= info["sms"] // 2
+    p = tc.binding.plan_device(4096, 4096, 4096, 0)
+    assert p["cta_group"] == 2 and p["bn"] in (224, 256)
+    assert p["grid"] == 2 * min(info["max_pairs"], p["tiles_m"] * p["tiles_n"])
+    assert tc.binding.plan_device(64, 8192, 8192, 0)["arows"] == 64

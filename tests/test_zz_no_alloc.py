@@ -53,12 +53,13 @@ def _run(tc, case, noalloc: bool):
 
 
 def test_noalloc_matches_regular_entry_point_twice(tc):
-    """Two different problems in a row whose tiles are split along K, so both
-    use the scratch array; each result matches gemm_bf16 within the fp32
-    tolerance of the parity tests (and, same plan, bit for bit)."""
+    """Two different problems in a row that share out their k-blocks
+    (stream-K), so both use the scratch array; each result matches gemm_bf16
+    within the fp32 tolerance of the parity tests (and, same plan, bit for
+    bit)."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     for seed in (61, 62):
-        case = gi.make_case(f"noalloc{seed}", 1024, 1280, 2048, alpha=0.75, beta=0.5, out_dtype=gi.OUT_F32,
+        case = gi.make_case(f"noalloc{seed}", 600, 700, 8192, alpha=0.75, beta=0.5, out_dtype=gi.OUT_F32,
                             seed=seed)
         need = tc.workspace_bytes(case.M, case.N, case.K, 0, sms)
         assert 0 < need <= tc.binding.noalloc_scratch_bytes()
@@ -76,8 +77,9 @@ def test_noalloc_without_split_and_bf16(tc):
 
 
 def test_noalloc_refuses_shapes_beyond_its_scratch(tc):
-    """1-CTA tiles, 70 tiles split two ways: 140 partial tiles of 128 KiB
-    exceed the fixed 16 MiB; the call fails before launching anything."""
+    """A shape whose plan needs more scratch than the fixed array is refused
+    before anything is launched.  (On a 152-SM GB300 every plan fits the
+    40 MiB array, and the test says so by skipping.)"""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     M, N, K = 896, 2560, 4096
     if tc.workspace_bytes(M, N, K, 1, sms) <= tc.binding.noalloc_scratch_bytes():
