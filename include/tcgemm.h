@@ -73,7 +73,9 @@ typedef enum {
     TCGEMM_VARIANT_1CTA_N64 = 4, /* one CTA per SM, narrow 128 x 64 tiles, 8-stage pipeline (12
                                    stages and 64-row A tiles when M <= 64): the choice for
                                    M <= 128, where B is streamed from memory once */
-    TCGEMM_VARIANT_2CTA_W256 = 5 /* as TCGEMM_VARIANT_2CTA with the tile width fixed at 256 */
+    TCGEMM_VARIANT_2CTA_W256 = 5, /* as TCGEMM_VARIANT_2CTA with the tile width fixed at 256 */
+    TCGEMM_VARIANT_SWAP_N64 = 6   /* the transposed product C^T = B^T A^T on 128 x 64 tiles (128
+                                    columns of C by up to 64 rows): the choice for M <= 64 */
 } tcgemm_variant_t;
 
 /* C = alpha*A*B + beta*C as described above.  Returns TCGEMM_OK once the work
@@ -155,7 +157,9 @@ int tcgemm_pick_variant(int64_t M, int64_t N, int64_t K, int num_sms);
  * MMA (cta_group), out[15], out[16] = rows and columns of the unit grid the
  * visiting order walks (tiles, or 2 x 2 tile blocks for variant 3), out[17] =
  * 1 when stream-K is used, out[18] = rows of A loaded per CTA (64 for M <= 64
- * with variant 4, else 128).  `out` must hold 19 values.  Returns TCGEMM_OK or TCGEMM_ERR_INVALID_ARG.  Needs no
+ * with variant 4, else 128), out[19] = 1 when the launch computes the
+ * transposed product (variant 6; then out[2..] describe C^T).  `out` must
+ * hold 20 values.  Returns TCGEMM_OK or TCGEMM_ERR_INVALID_ARG.  Needs no
  * GPU. */
 int tcgemm_plan(int64_t M, int64_t N, int64_t K, int variant, int num_sms, int64_t* out);
 

@@ -19,7 +19,8 @@ from . import _build
 
 OUT_F32 = 0
 OUT_BF16 = 1
-VARIANT_AUTO, VARIANT_1CTA, VARIANT_2CTA, VARIANT_1CTA_MC, VARIANT_1CTA_N64, VARIANT_2CTA_W256 = 0, 1, 2, 3, 4, 5
+(VARIANT_AUTO, VARIANT_1CTA, VARIANT_2CTA, VARIANT_1CTA_MC, VARIANT_1CTA_N64, VARIANT_2CTA_W256,
+ VARIANT_SWAP_N64) = range(7)
 
 STATUS = {0: "TCGEMM_OK", 1: "TCGEMM_ERR_INVALID_ARG", 2: "TCGEMM_ERR_ALIGNMENT",
           3: "TCGEMM_ERR_UNSUPPORTED_DEVICE", 4: "TCGEMM_ERR_CUDA", 5: "TCGEMM_ERR_TIMEOUT"}
@@ -168,7 +169,7 @@ def pick_variant(M: int, N: int, K: int, num_sms: int) -> int:
 
 PLAN_KEYS = ["grid", "cluster", "tiles_m", "tiles_n", "bm", "bn", "num_kb", "smem", "tiles_dp",
              "sk_tiles", "sk_iters", "ws_bytes", "group_m", "variant", "cta_group", "grid_m", "grid_n",
-             "stream_k", "arows"]
+             "stream_k", "arows", "swap"]
 
 
 def plan(M: int, N: int, K: int, variant: int = 0, num_sms: int = 152) -> dict:

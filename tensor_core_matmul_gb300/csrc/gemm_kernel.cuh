@@ -297,6 +297,71 @@ __device__ __forceinline__ void load_cold32(const OutT* dst, int64_t ldc, int64_
     for (int j = 0; j < 32; ++j) cold[j] = (col0 + j < N) ? load_out<OutT>(dst + j * ldc) : 0.0f;
 }
 
+// Swapped product (C^T = B^T A^T): one thread holds 32 consecutive rows of
+// one column of C, contiguous in memory.  alpha*acc (+ beta*C) for the first
+// `valid` of them, with 16-byte vector accesses when all 32 are in range (the
+// run starts 64- or 128-byte aligned: C is 16-byte aligned, ldc*sizeof(T) is a
+// multiple of 16 and the run starts at a multiple of 32 rows).
+template <typename OutT>
+__device__ __forceinline__ void store_run32(OutT* dst, int64_t valid, const uint32_t (&acc)[32], float alpha,
+                                            float beta, bool has_beta) {
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = alpha * __uint_as_float(acc[j]);
+    if (valid >= 32) {
+        if constexpr (sizeof(OutT) == 4) {
+            float4* d4 = reinterpret_cast<float4*>(dst);
+            if (has_beta) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 o = d4[q];
+                    v[4 * q + 0] = fmaf(alpha, __uint_as_float(acc[4 * q + 0]), beta * o.x);
+                    v[4 * q + 1] = fmaf(alpha, __uint_as_float(acc[4 * q + 1]), beta * o.y);
+                    v[4 * q + 2] = fmaf(alpha, __uint_as_float(acc[4 * q + 2]), beta * o.z);
+                    v[4 * q + 3] = fmaf(alpha, __uint_as_float(acc[4 * q + 3]), beta * o.w);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else {
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+            if (has_beta) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 o = d4[q];
+                    const uint32_t w[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[h]);
+                        v[8 * q + 2 * h] = fmaf(alpha, __uint_as_float(acc[8 * q + 2 * h]), beta * __low2float(b2));
+                        v[8 * q + 2 * h + 1] =
+                            fmaf(alpha, __uint_as_float(acc[8 * q + 2 * h + 1]), beta * __high2float(b2));
+                    }
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t w[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * q + 2 * h], v[8 * q + 2 * h + 1]);
+                    w[h] = *reinterpret_cast<const uint32_t*>(&b2);
+                }
+                d4[q] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (j < valid) {
+                float x = v[j];
+                if (has_beta) x = fmaf(alpha, __uint_as_float(acc[j]), beta * load_out<OutT>(dst + j));
+                store_out<OutT>(dst + j, x);
+            }
+        }
+    }
+}
+
 constexpr uint32_t kEpiBarrier = 1;     // named barrier id for the 4 epilogue warps
 constexpr uint32_t kEpiThreads = 128;
 
@@ -312,13 +377,17 @@ constexpr uint32_t kEpiThreads = 128;
 // tmC maps C (column-major M x N) in 128-row x 32-column boxes for the
 // epilogue's TMA loads / stores and L2 prefetches; tmW maps the stream-K
 // workspace (fp32, 128 rows x [slot][CTA of pair][BN] columns) the same way.
-template <int CTA_GROUP, int BN, int STAGES, int MC, int AROWS, typename OutT>
+// SWAP: the launch computes D = C^T (the host swapped A with B and M with N);
+// D's rows are C's columns, so the epilogue writes each TMEM row as a
+// contiguous run of one column of C (D row-major with leading dimension ldc).
+template <int CTA_GROUP, int BN, int STAGES, int MC, int AROWS, bool SWAP, typename OutT>
 __global__ void __launch_bounds__(192, 1)
     gemm_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
                         const GemmParams p) {
     using Cfg = GemmCfg<CTA_GROUP, BN, STAGES, AROWS>;
     static_assert(MC == 1 || (MC == 4 && CTA_GROUP == 1 && AROWS == 128), "multicast clusters use single-CTA MMAs");
+    static_assert(!SWAP || (CTA_GROUP == 1 && MC == 1), "the swapped product runs on single-CTA tiles");
     constexpr int kCluster = CTA_GROUP * MC;
     extern __shared__ uint8_t smem_raw[];
 
@@ -540,7 +609,7 @@ __global__ void __launch_bounds__(192, 1)
             const int ncols = BN;
             // beta*C: start pulling the C tile into L2 now; the tile's mainloop
             // hides the memory latency.
-            if (has_beta && leader && row_blk < p.M) {
+            if (!SWAP && has_beta && leader && row_blk < p.M) {
                 for (int c = 0; c < ncols && colt + c < p.N; c += 32)
                     tma_prefetch_l2_2d(&tmC, row_blk, static_cast<int32_t>(colt + c));
             }
@@ -560,7 +629,24 @@ __global__ void __launch_bounds__(192, 1)
             // granule at row M would also write rows M.. of the ldc padding:
             // that block is stored with masked plain stores instead.
             const bool tma_rows = row_blk + 128 <= p.M || ((static_cast<int64_t>(p.M) * sizeof(OutT)) % 16) == 0;
-            if (u.slot < 0 && !tma_rows) {
+            if (SWAP && u.slot < 0) {
+                // D row `row` = column `row` of C; D columns = rows of C.
+#pragma unroll 1
+                for (int c = 0; c < ncols; c += 32) {
+                    const int64_t col0 = colt + c;
+                    if (col0 >= p.N) break;
+                    uint32_t r[32];
+                    tmem_ld32(tbase + c, r);
+                    tmem_ld_wait32(r);
+                    if (row_ok) {
+                        OutT* dst = C + row * p.ldc + col0;
+                        store_run32<OutT>(dst, p.N - col0, r, p.alpha, p.beta, has_beta);
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(acc));
+            } else if (u.slot < 0 && !tma_rows) {
 #pragma unroll 1
                 for (int c = 0; c < ncols; c += 32) {
                     const int64_t col0 = colt + c;
@@ -716,7 +802,7 @@ __global__ void __launch_bounds__(192, 1)
 // order whatever order they were computed in), then alpha/beta, the output
 // cast and masked, coalesced stores (a warp writes 32 consecutive rows of a
 // column).  Partials: fp32, 128 rows x [slot][CTA of pair][BN] columns.
-template <int CTA_GROUP, int BN, typename OutT>
+template <int CTA_GROUP, int BN, bool SWAP, typename OutT>
 __global__ void __launch_bounds__(128)
     sk_reduce_kernel(const float* __restrict__ ws, const GemmParams p, int num_clusters) {
     const int chunks = BN / 32;
@@ -746,14 +832,18 @@ __global__ void __launch_bounds__(128)
         for (int j = 0; j < 32; ++j) sum[j] += v[j];
     }
     if (row >= p.M) return;
-    OutT* dst = static_cast<OutT*>(p.C) + col0 * p.ldc + row;
     const bool has_beta = p.beta != 0.0f;
-    float cold[32];
-    if (has_beta) load_cold32<OutT>(dst, p.ldc, col0, p.N, cold);
     uint32_t r[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(sum[j]);
-    epilogue_store32<OutT>(dst, p.ldc, col0, p.N, r, p.alpha, p.beta, cold, has_beta);
+    if constexpr (SWAP) {
+        store_run32<OutT>(static_cast<OutT*>(p.C) + row * p.ldc + col0, p.N - col0, r, p.alpha, p.beta, has_beta);
+    } else {
+        OutT* dst = static_cast<OutT*>(p.C) + col0 * p.ldc + row;
+        float cold[32];
+        if (has_beta) load_cold32<OutT>(dst, p.ldc, col0, p.N, cold);
+        epilogue_store32<OutT>(dst, p.ldc, col0, p.N, r, p.alpha, p.beta, cold, has_beta);
+    }
 }
 
 // C = beta * C (or 0 when beta == 0): the K == 0 case, where the product is

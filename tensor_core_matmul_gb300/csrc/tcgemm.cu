@@ -82,6 +82,7 @@ struct Plan {
     int cta_group = 1;
     int mc = 1;            // 4: 2 x 2 multicast cluster of single-CTA tiles
     int arows = 128;       // A rows loaded per CTA (64: M <= 64, narrow kernel)
+    int swap = 0;          // 1: the launch computes C^T = B^T A^T (M and N, A and B exchanged)
     int grid_m = 0, grid_n = 0;
     int bm = 128, bn = 256;
     int tiles_m = 0, tiles_n = 0, num_kb = 0;
@@ -123,12 +124,15 @@ bool split_enabled() {
 // CTA pairs (M = 256 per MMA) halve the operand traffic per SM; they pay off
 // once there are more than 128 rows.  Up to 128 rows ("skinny" products, B
 // streamed from memory once) narrow 128 x 64 tiles give every SM its own
-// columns of B and a deep 9-stage pipeline without splitting K.
+// columns of B and a deep pipeline; up to 64 rows the product is computed
+// transposed (C^T = B^T A^T), so that B's columns fill all 128 MMA rows and
+// the 64 rows of A become the MMA's N.
 int pick_variant(int64_t M, int64_t N, int64_t K, int sms) {
-    (void)N;
     (void)K;
     (void)sms;
-    return M > 128 ? TCGEMM_VARIANT_2CTA : TCGEMM_VARIANT_1CTA_N64;
+    if (M > 128) return TCGEMM_VARIANT_2CTA;
+    if (M <= 64 && N >= 256) return TCGEMM_VARIANT_SWAP_N64;
+    return TCGEMM_VARIANT_1CTA_N64;
 }
 
 // Stream-K sharing: a piece pays the same fixed costs as a whole tile
@@ -147,6 +151,11 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pa
     if (variant == TCGEMM_VARIANT_AUTO) variant = pick_variant(M, N, K, sms);
     pl.variant = variant;
     allow_split = allow_split && split_enabled();
+    if (variant == TCGEMM_VARIANT_SWAP_N64) {
+        // The transposed product: its M is N, its N is M.
+        pl.swap = 1;
+        std::swap(M, N);
+    }
     const int64_t num_kb = (K + 63) / 64;
     if (variant == TCGEMM_VARIANT_1CTA) {
         pl.cta_group = 1;
@@ -177,11 +186,11 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pa
         pl.bm = Cfg1::kBM;
         pl.bn = 256;
         pl.smem = Cfg1::kSmemBytes;
-    } else if (variant == TCGEMM_VARIANT_1CTA_N64) {
+    } else if (variant == TCGEMM_VARIANT_1CTA_N64 || variant == TCGEMM_VARIANT_SWAP_N64) {
         pl.cta_group = 1;
         pl.bm = CfgN64::kBM;
         pl.bn = 64;
-        pl.arows = M <= 64 ? 64 : 128;
+        pl.arows = (!pl.swap && M <= 64) ? 64 : 128;
         pl.smem = pl.arows == 64 ? CfgN64h::kSmemBytes : CfgN64::kSmemBytes;
     } else {
         return false;
@@ -278,13 +287,13 @@ bool encode_kmajor(CUtensorMap* m, const void* ptr, int64_t k_extent, int64_t ro
 
 // The dynamic shared-memory opt-in is a per-kernel attribute; it is set once
 // per device for each kernel instantiation.
-template <int CG, int BN, int ST, int MC, int AR, typename OutT>
+template <int CG, int BN, int ST, int MC, int AR, bool SW, typename OutT>
 bool ensure_smem_attr(int dev) {
     static std::mutex mu;
     static bool done[kMaxDevices] = {};
     std::lock_guard<std::mutex> lk(mu);
     if (done[dev]) return true;
-    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, MC, AR, OutT>;
+    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, MC, AR, SW, OutT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(tcg::GemmCfg<CG, BN, ST, AR>::kSmemBytes));
     if (e != cudaSuccess) {
@@ -295,11 +304,11 @@ bool ensure_smem_attr(int dev) {
     return true;
 }
 
-template <int CG, int BN, int ST, int MC, int AR, typename OutT>
+template <int CG, int BN, int ST, int MC, int AR, bool SW, typename OutT>
 int launch_gemm(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tcm,
                 const CUtensorMap& twm, const tcg::GemmParams& gp, cudaStream_t stream, int dev) {
-    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, MC, AR, OutT>;
-    if (!ensure_smem_attr<CG, BN, ST, MC, AR, OutT>(dev)) return TCGEMM_ERR_CUDA;
+    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, MC, AR, SW, OutT>;
+    if (!ensure_smem_attr<CG, BN, ST, MC, AR, SW, OutT>(dev)) return TCGEMM_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(pl.grid), 1, 1);
     cfg.blockDim = dim3(tcg::GemmCfg<CG, BN, ST, AR>::kThreads, 1, 1);
@@ -324,7 +333,7 @@ int launch_gemm(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, co
     if (pl.sk_tiles > 0) {
         // Add up the shared tiles' partials (same stream, so after the GEMM).
         const unsigned blocks = static_cast<unsigned>(pl.sk_tiles * CG * (BN / 32));
-        tcg::sk_reduce_kernel<CG, BN, OutT><<<blocks, 128, 0, stream>>>(
+        tcg::sk_reduce_kernel<CG, BN, SW, OutT><<<blocks, 128, 0, stream>>>(
             static_cast<const float*>(pl.ws_ptr), gp,
             pl.grid / (CG * MC));
         e = cudaGetLastError();
@@ -382,13 +391,13 @@ int probe_device(int& dev_out, DeviceInfo& info) {
         if (d.supported) {
             // How many clusters of each kind can be resident at once (cluster
             // placement may leave some SMs of a GPC unused).
-            if (ensure_smem_attr<2, 256, kStages2, 1, 128, __nv_bfloat16>(dev)) {
-                const int n = max_active_clusters(tcg::gemm_bf16_tn_kernel<2, 256, kStages2, 1, 128, __nv_bfloat16>,
+            if (ensure_smem_attr<2, 256, kStages2, 1, 128, false, __nv_bfloat16>(dev)) {
+                const int n = max_active_clusters(tcg::gemm_bf16_tn_kernel<2, 256, kStages2, 1, 128, false, __nv_bfloat16>,
                                                   2, Cfg2::kSmemBytes, sms);
                 if (n > 0) d.max_pairs = n;
             }
-            if (ensure_smem_attr<1, 256, kStages1, 4, 128, __nv_bfloat16>(dev)) {
-                const int n = max_active_clusters(tcg::gemm_bf16_tn_kernel<1, 256, kStages1, 4, 128, __nv_bfloat16>,
+            if (ensure_smem_attr<1, 256, kStages1, 4, 128, false, __nv_bfloat16>(dev)) {
+                const int n = max_active_clusters(tcg::gemm_bf16_tn_kernel<1, 256, kStages1, 4, 128, false, __nv_bfloat16>,
                                                   4, Cfg1::kSmemBytes, sms);
                 if (n > 0) d.max_quads = n;
             }
@@ -531,6 +540,7 @@ void fill_plan_out(const Plan& pl, int64_t* out) {
     out[16] = pl.grid_n;
     out[17] = pl.sk_tiles > 0 ? 1 : 0;
     out[18] = pl.arows;
+    out[19] = pl.swap;
 }
 
 constexpr int kWsInternal = 0;
@@ -542,7 +552,7 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
              int64_t ldc, float alpha, float beta, int out_dtype, void* stream_v, int variant,
              int ws_mode = kWsInternal, void* ws = nullptr, int64_t ws_bytes = 0) {
     t_last_error[0] = '\0';
-    if (variant < TCGEMM_VARIANT_AUTO || variant > TCGEMM_VARIANT_2CTA_W256) {
+    if (variant < TCGEMM_VARIANT_AUTO || variant > TCGEMM_VARIANT_SWAP_N64) {
         set_error("unknown variant %d", variant);
         return TCGEMM_ERR_INVALID_ARG;
     }
@@ -610,8 +620,14 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     // CTA loads half of its A tile and half of its B tile.
     const uint32_t a_box_rows = (pl.mc == 4 || pl.arows == 64) ? 64u : 128u;
     const uint32_t b_box_rows = static_cast<uint32_t>(pl.bn / pl.cta_group / (pl.mc == 4 ? 2 : 1));
+    // The transposed product multiplies B^T (N x K, rows of B contiguous in
+    // k) by A^T: the operands trade places.
+    const void* opA = pl.swap ? B : A;
+    const void* opB = pl.swap ? A : B;
+    const int64_t rowsA = pl.swap ? N : M, rowsB = pl.swap ? M : N;
+    const int64_t ldA = pl.swap ? ldb : lda, ldB = pl.swap ? lda : ldb;
     CUtensorMap ta, tb;
-    if (!encode_kmajor(&ta, A, K, M, lda, a_box_rows) || !encode_kmajor(&tb, B, K, N, ldb, b_box_rows)) {
+    if (!encode_kmajor(&ta, opA, K, rowsA, ldA, a_box_rows) || !encode_kmajor(&tb, opB, K, rowsB, ldB, b_box_rows)) {
         return TCGEMM_ERR_INVALID_ARG;
     }
     pl.ws_ptr = wsp;
@@ -625,8 +641,8 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
         twm = tcm;
     }
     tcg::GemmParams gp;
-    gp.M = static_cast<int>(M);
-    gp.N = static_cast<int>(N);
+    gp.M = static_cast<int>(pl.swap ? N : M);
+    gp.N = static_cast<int>(pl.swap ? M : N);
     gp.K = static_cast<int>(K);
     gp.tiles_m = pl.tiles_m;
     gp.tiles_n = pl.tiles_n;
@@ -644,15 +660,16 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     gp.timeout_ns = timeout_ns();
 
     const bool bf16 = out_dtype == TCGEMM_OUT_BF16;
-#define TCGEMM_LAUNCH(CG, BN, ST, MC, AR)                                                              \
-    return bf16 ? launch_gemm<CG, BN, ST, MC, AR, __nv_bfloat16>(pl, ta, tb, tcm, twm, gp, stream, dev) \
-                : launch_gemm<CG, BN, ST, MC, AR, float>(pl, ta, tb, tcm, twm, gp, stream, dev)
-    if (pl.mc == 4) TCGEMM_LAUNCH(1, 256, kStages1, 4, 128);
-    if (pl.bn == 64 && pl.arows == 64) TCGEMM_LAUNCH(1, 64, kStagesN64h, 1, 64);
-    if (pl.bn == 64) TCGEMM_LAUNCH(1, 64, kStagesN64, 1, 128);
-    if (pl.cta_group == 1) TCGEMM_LAUNCH(1, 256, kStages1, 1, 128);
-    if (pl.bn == 224) TCGEMM_LAUNCH(2, 224, kStages2n, 1, 128);
-    TCGEMM_LAUNCH(2, 256, kStages2, 1, 128);
+#define TCGEMM_LAUNCH(CG, BN, ST, MC, AR, SW)                                                               \
+    return bf16 ? launch_gemm<CG, BN, ST, MC, AR, SW, __nv_bfloat16>(pl, ta, tb, tcm, twm, gp, stream, dev) \
+                : launch_gemm<CG, BN, ST, MC, AR, SW, float>(pl, ta, tb, tcm, twm, gp, stream, dev)
+    if (pl.mc == 4) TCGEMM_LAUNCH(1, 256, kStages1, 4, 128, false);
+    if (pl.swap) TCGEMM_LAUNCH(1, 64, kStagesN64, 1, 128, true);
+    if (pl.bn == 64 && pl.arows == 64) TCGEMM_LAUNCH(1, 64, kStagesN64h, 1, 64, false);
+    if (pl.bn == 64) TCGEMM_LAUNCH(1, 64, kStagesN64, 1, 128, false);
+    if (pl.cta_group == 1) TCGEMM_LAUNCH(1, 256, kStages1, 1, 128, false);
+    if (pl.bn == 224) TCGEMM_LAUNCH(2, 224, kStages2n, 1, 128, false);
+    TCGEMM_LAUNCH(2, 256, kStages2, 1, 128, false);
 #undef TCGEMM_LAUNCH
 }
 

@@ -93,9 +93,11 @@ def test_tile_order_groups_for_l2(tc):
 
 @pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (8192, 8192, 8192), (4000, 4100, 4104),
                                    (64, 8192, 8192), (256, 256, 256), (1, 1, 1)])
-@pytest.mark.parametrize("variant", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("variant", [1, 2, 3, 4, 5, 6])
 def test_plans(tc, M, N, K, variant):
     p = tc.plan(M, N, K, variant, 152)
+    if p["swap"]:
+        M, N = N, M          # the launch describes C^T
     assert p["tiles_m"] * p["bm"] >= M and (p["tiles_m"] - 1) * p["bm"] < M
     assert p["tiles_n"] * p["bn"] >= N and (p["tiles_n"] - 1) * p["bn"] < N
     assert p["num_kb"] * 64 >= K
@@ -109,7 +111,7 @@ SK_SHAPES = [(4096, 4096, 4096), (8192, 8192, 8192), (4000, 4100, 4104), (64, 81
 
 
 @pytest.mark.parametrize("M,N,K", SK_SHAPES)
-@pytest.mark.parametrize("variant", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("variant", [1, 2, 3, 4, 5, 6])
 @pytest.mark.parametrize("sms", [152, 148, 20])
 def test_stream_k_plan_invariants(tc, M, N, K, variant, sms):
     p = tc.plan(M, N, K, variant, sms)
@@ -138,7 +140,8 @@ def _sk_slot(c, t_begin, iters, clusters):
                                      (64, 8192, 8192, 1), (513, 200, 1000, 1), (4000, 4100, 4104, 3),
                                      (129, 257, 65, 3), (64, 8192, 8192, 4), (4096, 4096, 4096, 1),
                                      (4096, 4096, 4096, 5), (8192, 8192, 8192, 5), (4000, 4100, 4104, 2),
-                                     (200, 300, 2392, 2), (3000, 5000, 777, 2)])
+                                     (200, 300, 2392, 2), (3000, 5000, 777, 2), (64, 8192, 8192, 6),
+                                     (50, 3000, 5000, 6)])
 def test_unit_schedule_covers_every_k_block_once(tc, M, N, K, v):
     """Runs the kernel's own unit iterator (host copy) for every cluster:
     every (tile, k-block) is produced exactly once; the pieces of each
@@ -192,13 +195,15 @@ def test_width_choice(tc):
     assert tc.plan(4096, 4096, 4096, 5, 152)["bn"] == 256
     assert tc.plan(64, 8192, 8192, 4, 152)["arows"] == 64
     assert tc.plan(128, 8192, 8192, 4, 152)["arows"] == 128
+    assert tc.plan(64, 8192, 8192, 0, 152)["swap"] == 1
     assert tc.plan(4096, 4096, 4096, 2, 152)["stream_k"] == 0
     assert tc.plan(1024, 1280, 2048, 2, 152)["stream_k"] == 0   # K too short to pay for it
     assert tc.plan(512, 512, 16384, 2, 152)["stream_k"] == 1    # 4 tiles, long K
 
 
 def test_auto_variant_choice(tc):
-    assert tc.pick_variant(64, 8192, 8192, 152) == 4
+    assert tc.pick_variant(64, 8192, 8192, 152) == 6
     assert tc.pick_variant(128, 4096, 4096, 152) == 4
+    assert tc.pick_variant(64, 128, 4096, 152) == 4
     assert tc.pick_variant(129, 4096, 4096, 152) == 2
     assert tc.pick_variant(4096, 4096, 4096, 152) == 2

@@ -21,9 +21,9 @@ pytestmark = pytest.mark.gpu
 
 import os
 
-# 1-CTA, 2-CTA (auto width), 2x2-multicast, narrow 128x64 and 2-CTA 256-wide
-# kernels; TCGEMM_TEST_VARIANTS="1" narrows a run to one of them.
-VARIANTS = [int(v) for v in os.environ.get("TCGEMM_TEST_VARIANTS", "1,2,3,4,5").split(",") if v]
+# 1-CTA, 2-CTA (auto width), 2x2-multicast, narrow 128x64, 2-CTA 256-wide and
+# transposed-product kernels; TCGEMM_TEST_VARIANTS="1" narrows a run to one.
+VARIANTS = [int(v) for v in os.environ.get("TCGEMM_TEST_VARIANTS", "1,2,3,4,5,6").split(",") if v]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -220,15 +220,15 @@ def test_split_small_k_pieces(oracle_lib, variant):
     H.compare_full(oracle_lib, case, g.result_np(), what=f"long K v{variant}")
 
 
-@pytest.mark.parametrize("variant", [1, 2, 4, 5])
+@pytest.mark.parametrize("variant", [1, 2, 4, 5, 6])
 @pytest.mark.parametrize("kind", ["integer", "normal"])
 def test_stream_k_small_problems(oracle_lib, variant, kind):
     """Few tiles and a long K, so stream-K shares every k-block out over all
     clusters (ragged edges, K not a multiple of 64): integer inputs bit-exact,
     N(0,1) inputs within tolerance, beta = 0.5 over C."""
     import tensor_core_matmul_gb300 as tc
-    bm = {1: 128, 2: 256, 4: 128, 5: 256}[variant]
-    bn = {1: 256, 2: 256, 4: 64, 5: 256}[variant]
+    bm = {1: 128, 2: 256, 4: 128, 5: 256, 6: 64}[variant]
+    bn = {1: 256, 2: 256, 4: 64, 5: 256, 6: 128}[variant]
     shapes = [(bm * 2 - 40, bn * 3 - 24, 8000), (bm - 7, bn * 5 - 100, 12000)]
     for n, (M, N, K) in enumerate(shapes):
         p = tc.binding.plan_device(M, N, K, variant)
@@ -246,4 +246,5 @@ def test_device_plan_and_width_choice():
     p = tc.binding.plan_device(4096, 4096, 4096, 0)
     assert p["cta_group"] == 2 and p["bn"] in (224, 256)
     assert p["grid"] == 2 * min(info["max_pairs"], p["tiles_m"] * p["tiles_n"])
-    assert tc.binding.plan_device(64, 8192, 8192, 0)["arows"] == 64
+    assert tc.binding.plan_device(64, 8192, 8192, 0)["swap"] == 1
+    assert tc.binding.plan_device(100, 8192, 8192, 0)["arows"] == 128
