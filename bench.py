@@ -137,6 +137,26 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(x: float) -> float:
+    """The largest x over all ranks (identity without a process group).  Every
+    rank times its own independent problem; the job takes as long as the
+    slowest rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_step: float, steps: int, world: int, max_seconds: float) -> float:
+    """Whole-job TFLOP/s: every rank ran `steps` steps of `flops_per_step`
+    (weak scaling), and the job lasted as long as the slowest rank."""
+    return world * flops_per_step * steps / max_seconds / 1e12
+
+
 def run_ours(args) -> None:
     import torch
 
@@ -198,13 +218,9 @@ def run_ours(args) -> None:
         raise RuntimeError(f"device status {st} in the timed region (role {where})")
 
     times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_s = sum(times_ms) / 1e3
-    if pg:
-        t = torch.tensor([total_s], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_s = float(t.item())
+    total_s = max_over_ranks(sum(times_ms) / 1e3)
     flops = case.flops
-    value = world * flops * args.steps / total_s / 1e12
+    value = job_throughput(flops, args.steps, world, total_s)
     ms_per_step = total_s / args.steps * 1e3
 
     peaks, peak_src = load_peaks()

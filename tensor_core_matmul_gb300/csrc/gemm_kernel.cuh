@@ -502,6 +502,10 @@ __global__ void __launch_bounds__(192, 1)
                     }
                 }
             }
+            // Every load is issued: a dependent kernel (the stream-K
+            // reduction) may begin launching; it waits for this grid to
+            // complete before it reads anything.
+            grid_launch_dependents();
             // Drain: every load this thread issued has landed before the CTA
             // may exit.  The leader (or a lone CTA) sees that on its full
             // barriers; a pair's second CTA sees it when the leader's MMA
@@ -784,6 +788,7 @@ __global__ void __launch_bounds__(192, 1)
     }
 
     // ------------------------------------------------------- teardown --
+    grid_launch_dependents();
     __syncwarp();
     tc_fence_before_sync();
     if constexpr (kCluster == 1) {
@@ -802,34 +807,56 @@ __global__ void __launch_bounds__(192, 1)
 // order whatever order they were computed in), then alpha/beta, the output
 // cast and masked, coalesced stores (a warp writes 32 consecutive rows of a
 // column).  Partials: fp32, 128 rows x [slot][CTA of pair][BN] columns.
+// Launched as a programmatic dependent of the GEMM, so that its launch
+// overlaps the GEMM's last units; it waits for the whole GEMM grid, and for
+// its memory operations, before it reads a partial.
+constexpr int kSkReduceCols = 32;   // columns per reduction block
+
+template <int CTA_GROUP, int BN>
+__host__ __device__ constexpr int sk_reduce_blocks_per_tile() { return CTA_GROUP * (BN / kSkReduceCols); }
+
 template <int CTA_GROUP, int BN, bool SWAP, typename OutT>
 __global__ void __launch_bounds__(128)
     sk_reduce_kernel(const float* __restrict__ ws, const GemmParams p, int num_clusters) {
-    const int chunks = BN / 32;
+    static_assert(BN % kSkReduceCols == 0, "tile width must be a whole number of reduction chunks");
+    const int chunks = BN / kSkReduceCols;
     const int blk = blockIdx.x;
     const int c = blk % chunks;
     const int rank = (blk / chunks) % CTA_GROUP;
     const int t = blk / (chunks * CTA_GROUP);
+    if (t >= p.sk_tiles) return;
     const int row_local = threadIdx.x;
     int tm, tn;
     grouped_tile(p.tiles_dp + t, p.grid_m, p.grid_n, p.group_m, tm, tn);
     const int64_t row = static_cast<int64_t>(tm) * (128 * CTA_GROUP) + rank * 128 + row_local;
-    const int64_t col0 = static_cast<int64_t>(tn) * BN + 32 * c;
+    const int64_t col0 = static_cast<int64_t>(tn) * BN + kSkReduceCols * c;
+    grid_dependency_wait();
     if (col0 >= p.N) return;
     const int64_t t_begin = static_cast<int64_t>(t) * p.num_kb;
     const int first = sk_owner(t_begin, p.sk_iters, num_clusters);
     const int last = sk_owner(t_begin + p.num_kb - 1, p.sk_iters, num_clusters);
+    const int64_t piece_stride = static_cast<int64_t>(BN) * 128;
+    const int64_t base = static_cast<int64_t>(rank * BN + kSkReduceCols * c) * 128 + row_local;
     float sum[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) sum[j] = 0.0f;
-    for (int cl = first; cl <= last; ++cl) {
-        const int slot = sk_slot(cl, t_begin, p.sk_iters, num_clusters);
-        const float* src = ws + (static_cast<int64_t>(slot * CTA_GROUP + rank) * BN + 32 * c) * 128 + row_local;
-        float v[32];
+    // Two pieces' loads in flight at a time; the additions stay in K order.
+    int cl = first;
+    for (; cl + 1 <= last; cl += 2) {
+        const float* s0 = ws + sk_slot(cl, t_begin, p.sk_iters, num_clusters) * CTA_GROUP * piece_stride + base;
+        const float* s1 = ws + sk_slot(cl + 1, t_begin, p.sk_iters, num_clusters) * CTA_GROUP * piece_stride + base;
+        float v0[32], v1[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __ldcg(src + j * 128);
+        for (int j = 0; j < 32; ++j) v0[j] = __ldcg(s0 + j * 128);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) sum[j] += v[j];
+        for (int j = 0; j < 32; ++j) v1[j] = __ldcg(s1 + j * 128);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sum[j] = (sum[j] + v0[j]) + v1[j];
+    }
+    if (cl <= last) {
+        const float* s0 = ws + sk_slot(cl, t_begin, p.sk_iters, num_clusters) * CTA_GROUP * piece_stride + base;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sum[j] += __ldcg(s0 + j * 128);
     }
     if (row >= p.M) return;
     const bool has_beta = p.beta != 0.0f;

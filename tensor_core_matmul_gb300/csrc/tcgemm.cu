@@ -332,11 +332,18 @@ int launch_gemm(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, co
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (pl.sk_tiles > 0) {
         // Add up the shared tiles' partials (same stream, so after the GEMM).
-        const unsigned blocks = static_cast<unsigned>(pl.sk_tiles * CG * (BN / 32));
-        tcg::sk_reduce_kernel<CG, BN, SW, OutT><<<blocks, 128, 0, stream>>>(
-            static_cast<const float*>(pl.ws_ptr), gp,
-            pl.grid / (CG * MC));
-        e = cudaGetLastError();
+        const unsigned blocks = static_cast<unsigned>(pl.sk_tiles * tcg::sk_reduce_blocks_per_tile<CG, BN>());
+        cudaLaunchConfig_t rcfg = {};
+        rcfg.gridDim = dim3(blocks, 1, 1);
+        rcfg.blockDim = dim3(128, 1, 1);
+        rcfg.stream = stream;
+        cudaLaunchAttribute rattr[1];
+        rattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        rattr[0].val.programmaticStreamSerializationAllowed = 1;
+        rcfg.attrs = rattr;
+        rcfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&rcfg, tcg::sk_reduce_kernel<CG, BN, SW, OutT>, static_cast<const float*>(pl.ws_ptr),
+                               gp, pl.grid / (CG * MC));
         if (e != cudaSuccess) {
             set_error("reduction kernel launch: %s", cudaGetErrorString(e));
             return TCGEMM_ERR_CUDA;
