@@ -9,7 +9,9 @@ and this file only marshals numpy arrays into it.
 Every function cites the passage it follows in ``gemm_oracle.c``'s header:
 the product and layouts from the H100 work log "在 H100 上超越 cuBLAS：一份工作日志"
 (sections "Simon 博客的快速回顾" and "实验设置"), and the alpha/beta update
-from the "DeepGEMM" article, section 1.1.
+from the "DeepGEMM" article, section 1.1; the fused bias + activation
+epilogue from the same article, section 6.1 (the readings taken where it is
+silent are listed in ``gemm_oracle.c``'s header).
 
 Parity pins for this oracle live in ``tests/test_oracle_pins.py``.  The fp32
 accumulation order of the GPU is a hardware choice; it is covered only by the
@@ -29,6 +31,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gemm_oracle.c")
 _BUILD = os.path.join(_HERE, "_build")
 _lock = threading.Lock()
+
+# Activation codes of gemm_oracle.c (its own numbering; callers use the names).
+ACTIVATIONS = {"none": 0, "relu": 1, "gelu": 2, "gelu_tanh": 3}
 
 
 def lib_path(mutant: int = 0, build_dir: Optional[str] = None) -> str:
@@ -67,6 +72,15 @@ class Oracle:
         L.oracle_gemm_sampled_f64.argtypes = [i64, i64, i64, p, i64, p, i64, p, i64, ctypes.c_int,
                                               ctypes.c_float, ctypes.c_float, i64, p, p, p]
         L.oracle_gemm_sampled_f64.restype = ctypes.c_int
+        L.oracle_gemm_epi_f64.argtypes = [i64, i64, i64, p, i64, p, i64, p, i64, ctypes.c_int,
+                                          ctypes.c_float, ctypes.c_float, p, ctypes.c_int, ctypes.c_int,
+                                          p, ctypes.c_int]
+        L.oracle_gemm_epi_f64.restype = ctypes.c_int
+        L.oracle_gemm_epi_sampled_f64.argtypes = [i64, i64, i64, p, i64, p, i64, p, i64, ctypes.c_int,
+                                                  ctypes.c_float, ctypes.c_float, p, ctypes.c_int, ctypes.c_int,
+                                                  i64, p, p, p]
+        L.oracle_gemm_epi_sampled_f64.restype = ctypes.c_int
+        L.oracle_activation_array.argtypes = [p, p, i64, ctypes.c_int]
         L.oracle_absdot_sampled_f64.argtypes = [i64, i64, i64, p, i64, p, i64, i64, p, p, p]
         L.oracle_absdot_sampled_f64.restype = ctypes.c_int
         L.oracle_round_bf16.argtypes = [ctypes.c_double]
@@ -98,6 +112,23 @@ class Oracle:
             return C_in, C_in.shape[1], 0
         raise TypeError("C_in must be float32 or bf16 bits (uint16)")
 
+    @staticmethod
+    def _bias(bias):
+        """bias: None, float32 array (kind 1) or uint16 bf16 bits (kind 2), one
+        value per column j of C."""
+        if bias is None:
+            return None, 0
+        bias = np.ascontiguousarray(bias)
+        if bias.dtype == np.float32:
+            return bias, 1
+        if bias.dtype == np.uint16:
+            return bias, 2
+        raise TypeError("bias must be float32 or bf16 bits (uint16)")
+
+    @staticmethod
+    def _act(act) -> int:
+        return ACTIVATIONS[act] if isinstance(act, str) else int(act)
+
     @property
     def mutant(self) -> int:
         return self._L.oracle_mutant_id()
@@ -128,6 +159,54 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_gemm_f64: bad arguments")
         return D
+
+    def gemm_epi_f64(self, M: int, N: int, K: int, A: np.ndarray, B: np.ndarray,
+                     C_in: Optional[np.ndarray] = None, alpha: float = 1.0, beta: float = 0.0,
+                     bias: Optional[np.ndarray] = None, act="none", threads: int = 0) -> np.ndarray:
+        """E = act(alpha*A*B + beta*C_in + bias[j]) in fp64, as an (N, M) array
+        (the fused epilogue; see gemm_f64 for the layouts)."""
+        A = np.ascontiguousarray(A, dtype=np.uint16)
+        B = np.ascontiguousarray(B, dtype=np.uint16)
+        assert A.shape[0] == M and B.shape[0] == N
+        lda = A.shape[1] if A.ndim == 2 else K
+        ldb = B.shape[1] if B.ndim == 2 else K
+        cin, ldc, cin_bf16 = self._cin(C_in, beta)
+        b, kind = self._bias(bias)
+        assert b is None or b.shape[0] >= N
+        D = np.empty((N, M), dtype=np.float64)
+        rc = self._L.oracle_gemm_epi_f64(M, N, K, self._ptr(A), lda, self._ptr(B), ldb,
+                                         self._ptr(cin), max(ldc, M), cin_bf16, float(alpha), float(beta),
+                                         self._ptr(b), kind, self._act(act), self._ptr(D), int(threads))
+        if rc != 0:
+            raise ValueError("oracle_gemm_epi_f64: bad arguments")
+        return D
+
+    def gemm_epi_sampled_f64(self, M: int, N: int, K: int, A: np.ndarray, B: np.ndarray,
+                             rows: np.ndarray, cols: np.ndarray,
+                             C_in: Optional[np.ndarray] = None, alpha: float = 1.0, beta: float = 0.0,
+                             bias: Optional[np.ndarray] = None, act="none") -> np.ndarray:
+        A = np.ascontiguousarray(A, dtype=np.uint16)
+        B = np.ascontiguousarray(B, dtype=np.uint16)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        cols = np.ascontiguousarray(cols, dtype=np.int64)
+        cin, ldc, cin_bf16 = self._cin(C_in, beta)
+        b, kind = self._bias(bias)
+        out = np.empty(rows.shape[0], dtype=np.float64)
+        rc = self._L.oracle_gemm_epi_sampled_f64(M, N, K, self._ptr(A), A.shape[1], self._ptr(B), B.shape[1],
+                                                 self._ptr(cin), max(ldc, M), cin_bf16, float(alpha),
+                                                 float(beta), self._ptr(b), kind, self._act(act),
+                                                 rows.shape[0], self._ptr(rows), self._ptr(cols),
+                                                 self._ptr(out))
+        if rc != 0:
+            raise ValueError("oracle_gemm_epi_sampled_f64: bad arguments")
+        return out
+
+    def activation(self, x: np.ndarray, act) -> np.ndarray:
+        """The oracle's activation function applied to fp64 values."""
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        out = np.empty(x.shape, dtype=np.float64)
+        self._L.oracle_activation_array(self._ptr(x), self._ptr(out), x.size, self._act(act))
+        return out
 
     def gemm_sampled_f64(self, M: int, N: int, K: int, A: np.ndarray, B: np.ndarray,
                          rows: np.ndarray, cols: np.ndarray,

@@ -34,6 +34,32 @@
  * round_out: fp32 output rounds the double to nearest-even binary32; bf16
  * output rounds the double directly (once) to nearest-even bf16.
  *
+ * Fused epilogue (the "DeepGEMM" article, section 6.1: after a fully
+ * connected layer a bias is added and then ReLU or GELU applied, fused into
+ * the end of the GEMM kernel).  The article fixes the order -- bias first,
+ * then the activation, then the output -- but not where alpha and beta enter,
+ * which axis the bias runs along, nor which GELU.  Readings taken:
+ *
+ *   E[i,j]     = act( D[i,j] + bias[j] )                    (fp64)
+ *   C_out[i,j] = round_out(E[i,j])
+ *
+ * bias[j] is one value per output column j (per output feature of the layer
+ * whose weights are B), fp32 or bf16, decoded exactly to double.  act is one
+ * of
+ *   none       act(x) = x
+ *   relu       act(x) = max(x, 0); NaN stays NaN and -0 becomes +0
+ *   gelu       act(x) = x * Phi(x), Phi the standard normal distribution
+ *              function, Phi(x) = erfc(-x / sqrt(2)) / 2 (the definition of
+ *              Hendrycks and Gimpel, "Gaussian Error Linear Units", 2016);
+ *              written with erfc rather than 1 + erf so that negative x does
+ *              not cancel
+ *   gelu_tanh  the same paper's approximation
+ *              x/2 * (1 + tanh( sqrt(2/pi) * (x + 0.044715 x^3) )),
+ *              evaluated through the identity (1 + tanh z)/2 = 1/(1 + e^-2z)
+ *              so that negative x does not cancel
+ * Both sides of every identity above are equal in exact arithmetic; the
+ * formulas produce NaN for x = -inf (0 * inf), and so does the oracle.
+ *
  * Planted mistakes: when compiled with -DORACLE_MUTANT=n (n > 0) one
  * deliberate error is switched on.  The test suite builds these variants to
  * prove that its pins catch every such error; the normal build has n = 0.
@@ -111,7 +137,51 @@ typedef struct {
     const void* Cin; int64_t ldc; int cin_bf16; /* C_in dtype: 0 fp32, 1 bf16 */
     double alpha, beta;
     int absolute;       /* 1: sum |A[i,k]*B[k,j]| instead (error model, no alpha/beta) */
+    const void* bias; int bias_kind;  /* 0 none, 1 fp32, 2 bf16 bits; one value per column j */
+    int act;            /* 0 none, 1 relu, 2 gelu, 3 gelu_tanh */
 } problem_t;
+
+/* ---- activations (see the header) ------------------------------------- */
+
+static double activation(double x, int act) {
+    switch (act) {
+    case 1:
+        return (x > 0.0 || isnan(x)) ? x : 0.0;
+    case 2:
+#if ORACLE_MUTANT == 13
+        return 0.5 * x * erfc(-x);                      /* planted: 1/sqrt(2) dropped */
+#else
+        return 0.5 * x * erfc(-x / sqrt(2.0));
+#endif
+    case 3: {
+        const double c = sqrt(2.0 / acos(-1.0));        /* sqrt(2/pi) */
+#if ORACLE_MUTANT == 14
+        const double z = c * x;                         /* planted: cubic term dropped */
+#else
+        const double z = c * (x + 0.044715 * x * x * x);
+#endif
+        return x / (1.0 + exp(-2.0 * z));
+    }
+    default:
+        return x;
+    }
+}
+
+void oracle_activation_array(const double* x, double* out, int64_t n, int act) {
+    for (int64_t i = 0; i < n; ++i) out[i] = activation(x[i], act);
+}
+
+static double bias_at(const problem_t* p, int64_t i, int64_t j) {
+#if ORACLE_MUTANT == 11
+    const int64_t idx = i;                              /* planted: bias along rows */
+#else
+    const int64_t idx = j;
+    (void)i;
+#endif
+    if (p->bias_kind == 1) return (double)((const float*)p->bias)[idx];
+    if (p->bias_kind == 2) return bf16_to_double(((const uint16_t*)p->bias)[idx]);
+    return 0.0;
+}
 
 static double c_in_at(const problem_t* p, int64_t i, int64_t j) {
 #if ORACLE_MUTANT == 8
@@ -159,14 +229,37 @@ static double element(const problem_t* p, int64_t i, int64_t j) {
 #elif ORACLE_MUTANT == 9
     double d = p->alpha * (double)s;                    /* planted: reads C even when beta == 0 */
     if (p->Cin != NULL) d += p->beta * c_in_at(p, i, j);
+#elif ORACLE_MUTANT == 15
+    double d = (double)s;                               /* planted: bias added before alpha */
+    if (p->bias_kind != 0) d += bias_at(p, i, j);
+    d *= p->alpha;
+    if (p->beta != 0.0) d += p->beta * c_in_at(p, i, j);
+    return activation(d, p->act);
 #else
     double d = p->alpha * (double)s;
     if (p->beta != 0.0) d += p->beta * c_in_at(p, i, j);
 #endif
-    return d;
+    if (p->bias_kind == 0 && p->act == 0) return d;
+#if ORACLE_MUTANT == 12
+    return activation(d, p->act) + bias_at(p, i, j);    /* planted: activation before bias */
+#else
+    return activation(d + bias_at(p, i, j), p->act);
+#endif
 }
 
 /* ---- full matrix, threaded over columns ------------------------------- */
+
+int oracle_gemm_epi_f64(int64_t M, int64_t N, int64_t K,
+                        const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                        const void* Cin, int64_t ldc, int cin_bf16,
+                        float alpha, float beta, const void* bias, int bias_kind, int act,
+                        double* D, int nthreads);
+int oracle_gemm_epi_sampled_f64(int64_t M, int64_t N, int64_t K,
+                                const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                                const void* Cin, int64_t ldc, int cin_bf16,
+                                float alpha, float beta, const void* bias, int bias_kind, int act,
+                                int64_t count, const int64_t* rows, const int64_t* cols,
+                                double* out);
 
 typedef struct {
     const problem_t* p;
@@ -197,14 +290,35 @@ int oracle_threads(int nthreads) { return pick_threads(nthreads, 1 << 30); }
 
 /* D (column-major M x N, leading dimension M) = alpha*A*B + beta*C_in in fp64.
  * Returns 0 on success, -1 on a bad argument. */
+static int run_full(const problem_t* pp, double* D, int nthreads);
+
 int oracle_gemm_f64(int64_t M, int64_t N, int64_t K,
                     const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
                     const void* Cin, int64_t ldc, int cin_bf16,
                     float alpha, float beta, double* D, int nthreads) {
+    return oracle_gemm_epi_f64(M, N, K, A, lda, B, ldb, Cin, ldc, cin_bf16, alpha, beta, NULL, 0, 0, D,
+                               nthreads);
+}
+
+/* E = act(alpha*A*B + beta*C_in + bias) in fp64 (the fused epilogue, see the
+ * header); bias_kind 0 and act 0 give D itself. */
+int oracle_gemm_epi_f64(int64_t M, int64_t N, int64_t K,
+                        const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                        const void* Cin, int64_t ldc, int cin_bf16,
+                        float alpha, float beta, const void* bias, int bias_kind, int act,
+                        double* D, int nthreads) {
     if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || ldc < M) return -1;
     if (beta != 0.0f && Cin == NULL) return -1;
-    problem_t p = {M, N, K, A, lda, B, ldb, Cin, ldc, cin_bf16, (double)alpha, (double)beta, 0};
-    if (M == 0 || N == 0) return 0;
+    if (bias_kind < 0 || bias_kind > 2 || (bias_kind != 0 && bias == NULL) || act < 0 || act > 3) return -1;
+    problem_t p = {M, N, K, A, lda, B, ldb, Cin, ldc, cin_bf16, (double)alpha, (double)beta, 0,
+                   bias, bias_kind, act};
+    return run_full(&p, D, nthreads);
+}
+
+static int run_full(const problem_t* pp, double* D, int nthreads) {
+    const problem_t p = *pp;
+    const int64_t N = p.N;
+    if (p.M == 0 || N == 0) return 0;
     int nt = pick_threads(nthreads, N);
     pthread_t tid[256];
     int spawned[256];
@@ -233,9 +347,21 @@ int oracle_gemm_sampled_f64(int64_t M, int64_t N, int64_t K,
                             float alpha, float beta,
                             int64_t count, const int64_t* rows, const int64_t* cols,
                             double* out) {
+    return oracle_gemm_epi_sampled_f64(M, N, K, A, lda, B, ldb, Cin, ldc, cin_bf16, alpha, beta, NULL, 0, 0,
+                                       count, rows, cols, out);
+}
+
+int oracle_gemm_epi_sampled_f64(int64_t M, int64_t N, int64_t K,
+                                const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                                const void* Cin, int64_t ldc, int cin_bf16,
+                                float alpha, float beta, const void* bias, int bias_kind, int act,
+                                int64_t count, const int64_t* rows, const int64_t* cols,
+                                double* out) {
     if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || ldc < M) return -1;
     if (beta != 0.0f && Cin == NULL) return -1;
-    problem_t p = {M, N, K, A, lda, B, ldb, Cin, ldc, cin_bf16, (double)alpha, (double)beta, 0};
+    if (bias_kind < 0 || bias_kind > 2 || (bias_kind != 0 && bias == NULL) || act < 0 || act > 3) return -1;
+    problem_t p = {M, N, K, A, lda, B, ldb, Cin, ldc, cin_bf16, (double)alpha, (double)beta, 0,
+                   bias, bias_kind, act};
     for (int64_t s = 0; s < count; ++s) {
         if (rows[s] < 0 || rows[s] >= M || cols[s] < 0 || cols[s] >= N) return -1;
         out[s] = element(&p, rows[s], cols[s]);
@@ -252,7 +378,7 @@ int oracle_absdot_sampled_f64(int64_t M, int64_t N, int64_t K,
                               int64_t count, const int64_t* rows, const int64_t* cols,
                               double* out) {
     if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K) return -1;
-    problem_t p = {M, N, K, A, lda, B, ldb, NULL, M, 0, 1.0, 0.0, 1};
+    problem_t p = {M, N, K, A, lda, B, ldb, NULL, M, 0, 1.0, 0.0, 1, NULL, 0, 0};
     for (int64_t s = 0; s < count; ++s) {
         if (rows[s] < 0 || rows[s] >= M || cols[s] < 0 || cols[s] >= N) return -1;
         out[s] = element(&p, rows[s], cols[s]);

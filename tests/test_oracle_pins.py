@@ -9,7 +9,12 @@ The pages print no worked numerical example, so the pins are:
     hand from the bf16 format, plus torch's fp32 -> bf16 conversion where the
     value is exactly a float,
   * beta == 0 never reading C, K == 0, and the N(0, K) statistics of the
-    product of N(0,1) matrices.
+    product of N(0,1) matrices,
+  * for the fused bias + activation epilogue: exact brute force with
+    integer inputs and biases through ReLU, the activations against
+    independent library routines (torch.relu, scipy's normal distribution
+    function for GELU, torch's tanh-approximated GELU), and the identity
+    act(x) - act(-x) = x that ReLU and both GELUs satisfy.
 
 Each pin is a plain function of an ``Oracle`` so that ``test_planted_mistakes``
 can run the same pins against oracle builds with one deliberate error each
@@ -212,9 +217,88 @@ def pin_sampled_matches_full(o):
     assert np.array_equal(s, D[cols, rows])
 
 
+def pin_epilogue_integer_bruteforce(o):
+    """Integer inputs and an integer bias: D + bias[j] is an exact integer
+    (or half-integer), so act none / relu must give exactly
+    max(alpha*S + beta*C + bias[j], 0) computed with rationals.  Shapes are
+    not square and the bias array is longer than N (its extra entries must
+    never be read), so a bias indexed by row would show."""
+    shapes = [(5, 3, 9, 2.0, 0.0, "f32"), (3, 6, 17, -1.0, 0.5, "bf16"), (7, 4, 5, 1.0, -2.0, "f32"),
+              (2, 9, 12, 0.5, 1.0, "bf16")]
+    rng = np.random.default_rng(5)
+    for n, (M, N, K, alpha, beta, bkind) in enumerate(shapes):
+        case = gi.make_case(f"eint{n}", M, N, K, alpha=alpha, beta=beta, out_dtype=gi.OUT_F32,
+                            seed=300 + n, kind="integer", lda=K + 1, ldb=K + 2, ldc=M + 1)
+        vals = rng.integers(-40, 41, size=M + N + 3).astype(np.float32)
+        bias = vals if bkind == "f32" else _u16(torch.from_numpy(vals).to(torch.bfloat16))
+        A = _as_int(_u16(case.A)[:, :K])
+        B = _as_int(_u16(case.B)[:, :K])
+        Cin = None if case.C_in is None else case.C_in.numpy()
+        for act in ("none", "relu"):
+            E = o.gemm_epi_f64(M, N, K, _u16(case.A), _u16(case.B), _cin_np(case), alpha, beta,
+                               bias=bias, act=act)
+            for i in range(M):
+                for j in range(N):
+                    s = sum((A[i, k] * B[j, k] for k in range(K)), Fraction(0))
+                    want = Fraction(alpha) * s + Fraction(int(vals[j]))
+                    if beta != 0.0:
+                        want += Fraction(beta) * Fraction(float(Cin[j, i]))
+                    if act == "relu":
+                        want = max(want, Fraction(0))
+                    assert E[j, i] == float(want), (n, act, i, j, E[j, i], want)
+        rows, cols = gi.sample_indices(M, N, 12, 3)
+        smp = o.gemm_epi_sampled_f64(M, N, K, _u16(case.A), _u16(case.B), rows, cols, _cin_np(case),
+                                     alpha, beta, bias=bias, act="relu")
+        assert np.array_equal(smp, E[cols, rows])
+
+
+def _act_grid():
+    x = np.concatenate([np.linspace(-9.0, 9.0, 3601), [0.0, -0.0, 1e-30, -1e-30, 1e-8, -1e-8, 30.0, -30.0]])
+    return x
+
+
+def pin_activations_library(o):
+    """The activations against independent library routines in float64:
+    torch.relu; x * Phi(x) with Phi from scipy.special.ndtr (the normal
+    distribution function, computed there without cancellation); torch's
+    GELU with approximate='tanh' where its own 1 + tanh form does not cancel
+    (x >= -3), and within its absolute rounding error below that."""
+    from scipy.special import ndtr
+    x = _act_grid()
+    xt = torch.from_numpy(x)
+    relu = o.activation(x, "relu")
+    assert np.array_equal(relu, torch.relu(xt).numpy())
+    gelu = o.activation(x, "gelu")
+    ref = x * ndtr(x)
+    assert np.allclose(gelu, ref, rtol=1e-12, atol=0.0), np.max(np.abs(gelu - ref) / np.maximum(np.abs(ref), 1e-300))
+    gt = o.activation(x, "gelu_tanh")
+    reft = torch.nn.functional.gelu(xt, approximate="tanh").numpy()
+    hi = x >= -3.0
+    assert np.allclose(gt[hi], reft[hi], rtol=1e-12, atol=1e-15)
+    assert np.all(np.abs(gt[~hi] - reft[~hi]) <= 1e-14 * np.abs(x[~hi]))
+    # The approximation stays close to the exact GELU (a published property
+    # of the tanh form: the two differ by well under 1e-3 everywhere).
+    assert np.max(np.abs(gt - ref)) < 1e-3
+
+
+def pin_activation_odd_identity(o):
+    """act(x) - act(-x) = x for ReLU (exactly) and for both GELUs (x*Phi(x)
+    + x*Phi(-x) = x; the tanh form's (1 + tanh z)/2 + (1 - tanh z)/2 = 1), to
+    within fp64 rounding.  Also act(0) = 0 and act(x) -> x for large x."""
+    x = _act_grid()
+    x = x[np.isfinite(x)]
+    for act in ("relu", "gelu", "gelu_tanh"):
+        d = o.activation(x, act) - o.activation(-x, act)
+        tol = 0.0 if act == "relu" else 4e-16 * np.abs(x) + 1e-300
+        assert np.all(np.abs(d - x) <= tol), act
+        assert o.activation(np.array([0.0]), act)[0] == 0.0
+        assert abs(o.activation(np.array([30.0]), act)[0] - 30.0) < 1e-12
+
+
 PINS = [pin_integer_bruteforce, pin_numpy_f64, pin_identity_and_permutation, pin_closed_forms,
         pin_bf16_rounding, pin_beta_zero_ignores_c, pin_k_zero, pin_statistics,
-        pin_sampled_matches_full]
+        pin_sampled_matches_full, pin_epilogue_integer_bruteforce, pin_activations_library,
+        pin_activation_odd_identity]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -233,6 +317,11 @@ MUTANTS = {
     8: "C_in read as row-major",
     9: "C_in read when beta == 0",
     10: "fp32 accumulation",
+    11: "bias indexed by row",
+    12: "activation applied before the bias",
+    13: "GELU without the 1/sqrt(2) scaling",
+    14: "tanh GELU without its cubic term",
+    15: "bias added before alpha",
 }
 
 
