@@ -157,6 +157,19 @@ def job_throughput(flops_per_step: float, steps: int, world: int, max_seconds: f
     return world * flops_per_step * steps / max_seconds / 1e12
 
 
+EPILOGUES = {"none": (False, "none"), "bias": (True, "none"), "bias_relu": (True, "relu"),
+             "bias_gelu": (True, "gelu"), "bias_gelu_tanh": (True, "gelu_tanh")}
+
+
+def make_bias(args, N: int):
+    """The fused epilogue's bias: N(0,1) fp32, one value per column of C
+    (fixed seed), or None."""
+    import torch
+    if not EPILOGUES[args.epilogue][0]:
+        return None
+    return torch.randn(N, generator=torch.Generator().manual_seed(9001), dtype=torch.float32)
+
+
 def run_ours(args) -> None:
     import torch
 
@@ -180,9 +193,16 @@ def run_ours(args) -> None:
          else torch.zeros((N, case.ldc), dtype=case.out_torch_dtype(), device=dev))
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    bias_cpu = make_bias(args, N)
+    act = EPILOGUES[args.epilogue][1]
+    bias = None if bias_cpu is None else bias_cpu.to(dev)
 
     def gemm():
-        tc.gemm_bf16(A, B, C, case.alpha, case.beta, M=M, N=N, K=K, stream=stream, variant=args.variant)
+        if args.epilogue == "none":
+            tc.gemm_bf16(A, B, C, case.alpha, case.beta, M=M, N=N, K=K, stream=stream, variant=args.variant)
+        else:
+            tc.gemm_bf16_bias_act(A, B, C, case.alpha, case.beta, bias=bias, activation=act, M=M, N=N, K=K,
+                                  stream=stream, variant=args.variant)
 
     for _ in range(args.warmup):
         flush.fill_(1)
@@ -224,17 +244,18 @@ def run_ours(args) -> None:
     ms_per_step = total_s / args.steps * 1e3
 
     peaks, peak_src = load_peaks()
-    traffic = profile_traffic(f"gemm_{args.config}_full")
+    tag = f"gemm_{args.config}_full" + ("" if args.epilogue == "none" else f"_{args.epilogue}")
+    traffic = profile_traffic(tag)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     variant = args.variant or tc.pick_variant(M, N, K, sms)
     plan = tc.plan(M, N, K, variant, sms)
 
     e2e = None
     if not args.no_e2e:
-        e2e = measure_e2e(args, case, dev, stream)
+        e2e = measure_e2e(args, case, dev, stream, bias_cpu, act)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(case, target_s=args.cpu_seconds)
+        cpu = cpu_baseline(case, target_s=args.cpu_seconds, bias=bias_cpu, act=act)
 
     if rank == 0:
         out = {
@@ -253,14 +274,18 @@ def run_ours(args) -> None:
             "config": {
                 "workload": f"gemm {args.config}: M={M} N={N} K={K}, bf16 A row-major x B col-major, "
                             f"fp32 accumulate, {'bf16' if case.out_dtype else 'fp32'} C col-major, "
-                            f"alpha={case.alpha} beta={case.beta}, N(0,1) inputs",
+                            f"alpha={case.alpha} beta={case.beta}, N(0,1) inputs"
+                            + ("" if args.epilogue == "none" else
+                               f", fused epilogue C = {act}(alpha*A*B + beta*C + bias[j]), fp32 N(0,1) bias"),
                 "M": M, "N": N, "K": K,
+                "epilogue": args.epilogue,
                 "l2": f"flushed between timed steps ({FLUSH_BYTES >> 20} MiB write, untimed)",
                 "kernel": {"variant": {1: "1cta", 2: "2cta"}.get(variant, str(variant)), **plan},
                 "parallelism": f"independent problem per GPU x{world}",
                 "wall_s_timed_loop": round(wall, 3),
             },
-            "roofline": roofline(case, total_s / args.steps, peaks, peak_src, traffic),
+            "roofline": roofline(case, total_s / args.steps, peaks, peak_src, traffic,
+                                 extra_bytes=0 if bias_cpu is None else 4 * N),
             "clocks": clocks,
             "e2e": e2e,
             "gpu_launches": int(launches),
@@ -279,12 +304,13 @@ def algorithmic_bytes(case) -> int:
     return 2 * case.M * case.K + 2 * case.N * case.K + c + (c if case.beta != 0.0 else 0)
 
 
-def roofline(case, t_launch: float, peaks: dict, peak_src: str, traffic) -> dict:
+def roofline(case, t_launch: float, peaks: dict, peak_src: str, traffic, extra_bytes: int = 0) -> dict:
     """Dominant kernel (the GEMM itself) against its bound: the tensor cores
     for the square / edge shapes, HBM for the skinny shape (intensity
-    2MNK / bytes far below the ridge point)."""
+    2MNK / bytes far below the ridge point).  extra_bytes: the fused
+    epilogue's bias vector."""
     flops = case.flops
-    nbytes = algorithmic_bytes(case)
+    nbytes = algorithmic_bytes(case) + extra_bytes
     peak_flops = float(peaks["bf16_tflops"])
     ridge = peak_flops * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
     src = "measured" if peak_src == "measured" else "fallback"
@@ -302,7 +328,7 @@ def roofline(case, t_launch: float, peaks: dict, peak_src: str, traffic) -> dict
             "nominal_dense_bf16_tflops": 2250.0, "frac_of_nominal": round(achieved / 2250.0, 4)}
 
 
-def measure_e2e(args, case, dev, stream) -> dict:
+def measure_e2e(args, case, dev, stream, bias_cpu=None, act="none") -> dict:
     """Same metric through the public API with host buffers: every step copies
     A and B from pinned host memory to the device, runs the GEMM and copies C
     back to pinned host memory.  Steps alternate between two streams with their
@@ -321,6 +347,8 @@ def measure_e2e(args, case, dev, stream) -> dict:
     hB = [case.B.pin_memory() for _ in range(nbuf)]
     hC_in = [C0.pin_memory() for _ in range(nbuf)]
     hC = [torch.empty_like(C0).pin_memory() for _ in range(nbuf)]
+    hbias = [None if bias_cpu is None else bias_cpu.pin_memory() for _ in range(nbuf)]
+    dbias = [None if bias_cpu is None else torch.empty_like(bias_cpu, device=dev) for _ in range(nbuf)]
     dA = [torch.empty_like(case.A, device=dev) for _ in range(nbuf)]
     dB = [torch.empty_like(case.B, device=dev) for _ in range(nbuf)]
     dC = [torch.empty_like(C0, device=dev) for _ in range(nbuf)]
@@ -334,8 +362,14 @@ def measure_e2e(args, case, dev, stream) -> dict:
             dB[b].copy_(hB[b], non_blocking=True)
             if has_beta:
                 dC[b].copy_(hC_in[b], non_blocking=True)
-            tc.gemm_bf16(dA[b], dB[b], dC[b], case.alpha, case.beta, M=case.M, N=case.N, K=case.K, stream=s,
-                         variant=args.variant)
+            if bias_cpu is None and act == "none":
+                tc.gemm_bf16(dA[b], dB[b], dC[b], case.alpha, case.beta, M=case.M, N=case.N, K=case.K, stream=s,
+                             variant=args.variant)
+            else:
+                if bias_cpu is not None:
+                    dbias[b].copy_(hbias[b], non_blocking=True)
+                tc.gemm_bf16_bias_act(dA[b], dB[b], dC[b], case.alpha, case.beta, bias=dbias[b], activation=act,
+                                      M=case.M, N=case.N, K=case.K, stream=s, variant=args.variant)
             hC[b].copy_(dC[b], non_blocking=True)
 
     for i in range(4):
@@ -354,6 +388,7 @@ def measure_e2e(args, case, dev, stream) -> dict:
     torch.cuda.synchronize(dev)
     t = start.elapsed_time(end) / 1e3
     h2d = case.A.numel() * 2 + case.B.numel() * 2 + (C0.numel() * C0.element_size() if has_beta else 0)
+    h2d += 0 if bias_cpu is None else bias_cpu.numel() * 4
     d2h = C0.numel() * C0.element_size()
     return {"value": round(case.flops * steps / t / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
@@ -361,8 +396,9 @@ def measure_e2e(args, case, dev, stream) -> dict:
             "link_gbs": round((h2d + d2h) * steps / t / 1e9, 1)}
 
 
-def oracle_slab(case, ncols: int, threads: int = 0) -> float:
-    """Seconds for the oracle to compute columns [0, ncols) of C."""
+def oracle_slab(case, ncols: int, threads: int = 0, bias=None, act: str = "none") -> float:
+    """Seconds for the oracle to compute columns [0, ncols) of C (with the
+    fused epilogue when a bias or an activation is given)."""
     import numpy as np
 
     import gemm_inputs as gi
@@ -374,20 +410,25 @@ def oracle_slab(case, ncols: int, threads: int = 0) -> float:
     if case.C_in is not None:
         cin = case.C_in[:ncols]
         cin = gi.as_u16(cin) if cin.dtype.is_floating_point and cin.element_size() == 2 else cin.numpy()
+    b = None if bias is None else bias[:ncols].numpy()
     t0 = time.perf_counter()
-    o.gemm_f64(case.M, ncols, case.K, A, np.ascontiguousarray(B), cin, case.alpha, case.beta, threads=threads)
+    if b is None and act == "none":
+        o.gemm_f64(case.M, ncols, case.K, A, np.ascontiguousarray(B), cin, case.alpha, case.beta, threads=threads)
+    else:
+        o.gemm_epi_f64(case.M, ncols, case.K, A, np.ascontiguousarray(B), cin, case.alpha, case.beta, bias=b,
+                       act=act, threads=threads)
     return time.perf_counter() - t0
 
 
-def cpu_baseline(case, target_s: float) -> dict:
+def cpu_baseline(case, target_s: float, bias=None, act: str = "none") -> dict:
     import oracle
     cores = oracle.get().threads(0)
     ncal = max(1, min(case.N, cores))
-    t = oracle_slab(case, ncal)
+    t = oracle_slab(case, ncal, bias=bias, act=act)
     per_col = t / ncal
     ncols = int(max(1, min(case.N, round(target_s / max(per_col, 1e-9)))))
     ncols = max(ncols, min(case.N, cores))
-    t = oracle_slab(case, ncols)
+    t = oracle_slab(case, ncols, bias=bias, act=act)
     flops = 2 * case.M * ncols * case.K
     return {"value": round(flops / t / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"columns 0..{ncols - 1} of C ({case.M}x{ncols}x{case.K}, {flops / 1e9:.1f} GFLOP), "
@@ -402,17 +443,19 @@ def run_reference(args) -> None:
 
     import gemm_inputs as gi
     case = gi.config_case(args.config)
+    bias = make_bias(args, case.N)
+    act = EPILOGUES[args.epilogue][1]
     cores = oracle.get().threads(0)
     # Size each step's column slab so the whole run takes about args.ref_seconds.
     ncal = max(1, min(case.N, cores))
-    per_col = oracle_slab(case, ncal) / ncal
+    per_col = oracle_slab(case, ncal, bias=bias, act=act) / ncal
     total_steps = args.steps + args.warmup
     ncols = int(max(1, min(case.N, round(args.ref_seconds / total_steps / max(per_col, 1e-9)))))
     for _ in range(args.warmup):
-        oracle_slab(case, ncols)
+        oracle_slab(case, ncols, bias=bias, act=act)
     t = 0.0
     for _ in range(args.steps):
-        t += oracle_slab(case, ncols)
+        t += oracle_slab(case, ncols, bias=bias, act=act)
     flops = 2 * case.M * ncols * case.K
     value = flops * args.steps / t / 1e12
     out = {
@@ -430,8 +473,9 @@ def run_reference(args) -> None:
         "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": f"gemm {args.config}: M={case.M} N={case.N} K={case.K}; each step computes "
-                               f"columns 0..{ncols - 1} of C with the CPU oracle",
-                   "M": case.M, "N": case.N, "K": case.K},
+                               f"columns 0..{ncols - 1} of C with the CPU oracle"
+                               + ("" if args.epilogue == "none" else f", fused epilogue {args.epilogue}"),
+                   "M": case.M, "N": case.N, "K": case.K, "epilogue": args.epilogue},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"{ncols} columns of C per step ({case.M}x{ncols}x{case.K})"},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -447,6 +491,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="s4k", choices=["s256", "s4k", "s8k", "edge", "skinny"])
     ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 one-CTA, 2 CTA-pair kernel")
+    ap.add_argument("--epilogue", default="none", choices=sorted(EPILOGUES),
+                    help="fused epilogue: bias and/or activation (gemm_bf16_bias_act)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")

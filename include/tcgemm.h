@@ -135,6 +135,58 @@ int gemm_bf16_noalloc(int64_t M, int64_t N, int64_t K,
                       void* C, int64_t ldc,
                       float alpha, float beta, int out_dtype, void* stream, int variant);
 
+/* Fused epilogue activations (gemm_bf16_bias_act). */
+typedef enum {
+    TCGEMM_ACT_NONE = 0,
+    TCGEMM_ACT_RELU = 1,      /* max(x, 0); NaN stays NaN                                  */
+    TCGEMM_ACT_GELU = 2,      /* x * Phi(x), Phi the standard normal distribution function  */
+    TCGEMM_ACT_GELU_TANH = 3  /* x/2 * (1 + tanh(sqrt(2/pi) * (x + 0.044715 x^3)))          */
+} tcgemm_activation_t;
+
+/* Element type of the fused epilogue's bias vector. */
+typedef enum {
+    TCGEMM_BIAS_NONE = 0,
+    TCGEMM_BIAS_F32 = 1,
+    TCGEMM_BIAS_BF16 = 2
+} tcgemm_bias_t;
+
+/* GEMM with the fused epilogue of the "DeepGEMM" article, section 6.1 (after
+ * a fully connected layer the output gets a bias and then ReLU or GELU, done
+ * at the end of the GEMM kernel instead of in a second pass over C):
+ *
+ *   C[i,j] = act( alpha * sum_k A[i,k] B[k,j] + beta * C[i,j] + bias[j] )
+ *
+ * computed in fp32 from the fp32 accumulator and rounded once to out_dtype.
+ * The article fixes the order (bias, then activation); where alpha and beta
+ * enter, the bias axis and the GELU form are this library's readings: bias[j]
+ * is one value per column j of C (per output feature when B holds a layer's
+ * weights), and TCGEMM_ACT_GELU is the exact definition (Hendrycks and Gimpel,
+ * "Gaussian Error Linear Units", 2016; evaluated as x * erfc(-x/sqrt 2) / 2),
+ * TCGEMM_ACT_GELU_TANH that paper's tanh approximation (evaluated as
+ * x * sigmoid(2z)).  The GPU evaluates erfc as t * exp(-z^2 + P(t)),
+ * t = 1/(1 + z/2) (the form of "Numerical Recipes", section 6.2) with a
+ * fitted degree-9 P, and exp with CUDA's __expf: the activations are within a
+ * relative 4e-5 of their exact values (tested on a dense grid).
+ *
+ * bias:       device pointer to N values of bias_dtype (fp32 or bf16), aligned
+ *             to the element size, not overlapping C; NULL exactly when
+ *             bias_dtype is TCGEMM_BIAS_NONE.  Read only; the caller owns it.
+ * bias_dtype: tcgemm_bias_t.
+ * activation: tcgemm_activation_t.
+ * variant:    as gemm_bf16_variant (0 = chosen by shape).
+ * With TCGEMM_BIAS_NONE and TCGEMM_ACT_NONE this is gemm_bf16_variant.  K == 0
+ * gives act(beta * C + bias[j]).  Errors: an unknown activation or bias dtype,
+ * a bias pointer that is NULL when needed (or given with TCGEMM_BIAS_NONE), or
+ * a bias overlapping C -> TCGEMM_ERR_INVALID_ARG; a misaligned bias ->
+ * TCGEMM_ERR_ALIGNMENT; all other rules and errors as gemm_bf16_variant. */
+int gemm_bf16_bias_act(int64_t M, int64_t N, int64_t K,
+                       const void* A, int64_t lda,
+                       const void* B, int64_t ldb,
+                       void* C, int64_t ldc,
+                       float alpha, float beta, int out_dtype,
+                       const void* bias, int bias_dtype, int activation,
+                       void* stream, int variant);
+
 /* Size in bytes of gemm_bf16_noalloc's fixed scratch array.  Host only. */
 int64_t tcgemm_noalloc_scratch_bytes(void);
 

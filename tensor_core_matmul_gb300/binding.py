@@ -22,6 +22,10 @@ OUT_BF16 = 1
 (VARIANT_AUTO, VARIANT_1CTA, VARIANT_2CTA, VARIANT_1CTA_MC, VARIANT_1CTA_N64, VARIANT_2CTA_W256,
  VARIANT_SWAP_N64) = range(7)
 
+ACT_NONE, ACT_RELU, ACT_GELU, ACT_GELU_TANH = range(4)
+ACTIVATIONS = {"none": ACT_NONE, "relu": ACT_RELU, "gelu": ACT_GELU, "gelu_tanh": ACT_GELU_TANH}
+BIAS_NONE, BIAS_F32, BIAS_BF16 = range(3)
+
 STATUS = {0: "TCGEMM_OK", 1: "TCGEMM_ERR_INVALID_ARG", 2: "TCGEMM_ERR_ALIGNMENT",
           3: "TCGEMM_ERR_UNSUPPORTED_DEVICE", 4: "TCGEMM_ERR_CUDA", 5: "TCGEMM_ERR_TIMEOUT"}
 
@@ -58,6 +62,8 @@ def lib() -> ctypes.CDLL:
     L.gemm_bf16_variant.restype = i32
     L.gemm_bf16_ws.argtypes = gemm_args + [i32, p, i64]
     L.gemm_bf16_ws.restype = i32
+    L.gemm_bf16_bias_act.argtypes = gemm_args[:-1] + [p, i32, i32, p, i32]
+    L.gemm_bf16_bias_act.restype = i32
     L.gemm_bf16_noalloc.argtypes = gemm_args + [i32]
     L.gemm_bf16_noalloc.restype = i32
     L.tcgemm_noalloc_scratch_bytes.argtypes = []
@@ -141,10 +147,60 @@ def gemm_bf16(A, B, C, alpha: float = 1.0, beta: float = 0.0, *, M: Optional[int
     M = C.shape[1] if M is None else M
     N = C.shape[0] if N is None else N
     K = A.shape[1] if K is None else K
-    if A.shape[0] < M or B.shape[0] < N or C.shape[0] < N:
-        raise ValueError("tensor shapes smaller than M/N")
+    if C.shape[0] < N or (K > 0 and (A.shape[0] < M or B.shape[0] < N)):
+        raise ValueError("tensor shapes smaller than M/N")  # A and B are not read when K == 0
     st = gemm_bf16_raw(M, N, K, A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0), C.data_ptr(),
                        C.stride(0), float(alpha), float(beta), out, _stream_ptr(stream), variant)
+    _check(st)
+    return C
+
+
+def gemm_bf16_bias_act_raw(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int, C: int, ldc: int,
+                           alpha: float, beta: float, out_dtype: int, bias: Optional[int], bias_dtype: int,
+                           activation: int, stream: int, variant: int = 0) -> int:
+    """Pointer-level call of the fused-epilogue entry point; returns the status."""
+    return lib().gemm_bf16_bias_act(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, bias, bias_dtype,
+                                    activation, stream, variant)
+
+
+def gemm_bf16_bias_act(A, B, C, alpha: float = 1.0, beta: float = 0.0, *, bias=None, activation="none",
+                       M: Optional[int] = None, N: Optional[int] = None, K: Optional[int] = None, stream=None,
+                       variant: int = 0):
+    """C = act(alpha * A * B + beta * C + bias[j]) on the GPU (the fused
+    epilogue), tensors as in gemm_bf16; ``bias`` a 1-D fp32 or bf16 CUDA
+    tensor of at least N values (or None); ``activation`` one of ACTIVATIONS."""
+    import torch
+    if not (A.is_cuda and B.is_cuda and C.is_cuda):
+        raise ValueError("A, B and C must be CUDA tensors")
+    if C.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("C must be float32 or bfloat16")
+    out = OUT_F32 if C.dtype == torch.float32 else OUT_BF16
+    M = C.shape[1] if M is None else M
+    N = C.shape[0] if N is None else N
+    K = A.shape[1] if K is None else K
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise ValueError("A and B must be bfloat16")
+    for t in (A, B, C):
+        if t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError("A, B, C must be 2-D with unit inner stride")
+    if C.shape[0] < N or (K > 0 and (A.shape[0] < M or B.shape[0] < N)):
+        raise ValueError("tensor shapes smaller than M/N")  # A and B are not read when K == 0
+    if bias is None:
+        bptr, bkind = None, BIAS_NONE
+    else:
+        if not bias.is_cuda or bias.dim() != 1 or bias.stride(0) != 1 or bias.shape[0] < N:
+            raise ValueError("bias must be a contiguous 1-D CUDA tensor of at least N values")
+        if bias.dtype == torch.float32:
+            bkind = BIAS_F32
+        elif bias.dtype == torch.bfloat16:
+            bkind = BIAS_BF16
+        else:
+            raise ValueError("bias must be float32 or bfloat16")
+        bptr = bias.data_ptr()
+    act = ACTIVATIONS[activation] if isinstance(activation, str) else int(activation)
+    st = gemm_bf16_bias_act_raw(M, N, K, A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0), C.data_ptr(),
+                                C.stride(0), float(alpha), float(beta), out, bptr, bkind, act, _stream_ptr(stream),
+                                variant)
     _check(st)
     return C
 

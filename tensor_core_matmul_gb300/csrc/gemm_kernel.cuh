@@ -126,8 +126,97 @@ struct GemmParams {
     int64_t ldc;
     void* C;
     float alpha, beta;
+    // Fused epilogue: out = act(alpha*acc + beta*C + bias[column of C]).
+    const void* bias;    // one value per column of C (per row of D in the transposed product), or null
+    int bias_kind;       // 0 none, 1 fp32, 2 bf16
+    int act;             // kAct*
     uint64_t timeout_ns;
 };
+
+// ------------------------------------------------------ fused epilogue --
+// The "DeepGEMM" article (section 6.1) fuses the bias add and the ReLU/GELU
+// that follow a fully connected layer into the GEMM's epilogue; the order is
+// bias, then activation, then the store.  Both run in fp32 on the value
+// alpha*acc (+ beta*C); the activation is chosen per call (a warp-uniform
+// branch) rather than per compiled kernel.
+//
+// The epilogue warps share the SM sub-partitions' issue slots with the TMA
+// and MMA warps of the next tile's mainloop, so the activations are written
+// to issue few instructions: no data-dependent branches, and pairs of values
+// through Blackwell's packed fp32x2 operations (__ffma2_rn and friends,
+// IEEE-rounded per lane, so a pair gives the same bits as two scalar calls).
+enum : int { kActNone = 0, kActRelu = 1, kActGelu = 2, kActGeluTanh = 3 };
+
+// P(t) of erfc(z) = t * exp(-z^2 + P(t)), t = 1/(1 + z/2), z >= 0: the form of
+// Press et al., "Numerical Recipes" (2nd ed., section 6.2); coefficients (of
+// t^0 .. t^9) from the least-squares Chebyshev fit in fit_erfc.py beside this
+// file (relative error of erfc below 1.1e-7 on [0, 30] in exact arithmetic).
+__device__ constexpr float kErfcP[10] = {-1.2655122f, 1.0000237f, 0.37409195f, 0.09678419f, -0.18628806f,
+                                         0.27886808f, -1.135204f, 1.4885159f, -0.82215226f, 0.17087278f};
+constexpr float kRsqrt2 = 0.70710678118654752f;        // 1/sqrt(2)
+constexpr float kSqrt2OverPi = 0.79788456080286536f;   // sqrt(2/pi)
+constexpr float kGeluCubic = 0.044715f;                 // the tanh approximation's cubic coefficient
+
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
+
+// GELU(x) = x * Phi(x), Phi(x) = erfc(-x/sqrt 2)/2, which is h = erfc(|x|/sqrt 2)/2
+// for x < 0 and 1 - h for x >= 0 (no cancellation on either side).
+__device__ __forceinline__ float2 gelu_erf2(float2 x) {
+    const float2 w = __fmul2_rn(make_float2(fabsf(x.x), fabsf(x.y)), f2(kRsqrt2));
+    const float2 d = __ffma2_rn(f2(0.5f), w, f2(1.0f));
+    const float2 t = make_float2(__fdividef(1.0f, d.x), __fdividef(1.0f, d.y));
+    float2 q = f2(kErfcP[9]);
+#pragma unroll
+    for (int k = 8; k >= 0; --k) q = __ffma2_rn(q, t, f2(kErfcP[k]));
+    const float2 a = __ffma2_rn(make_float2(-w.x, -w.y), w, q);
+    const float2 h = __fmul2_rn(__fmul2_rn(f2(0.5f), t), make_float2(__expf(a.x), __expf(a.y)));
+    return __fmul2_rn(x, make_float2(x.x >= 0.0f ? 1.0f - h.x : h.x, x.y >= 0.0f ? 1.0f - h.y : h.y));
+}
+
+// x/2 (1 + tanh z) = x * sigmoid(2z), z = sqrt(2/pi) (x + 0.044715 x^3); with
+// u = exp(-2|z|) <= 1, sigmoid(2z) = 1/(1+u) for z >= 0 and u/(1+u) below, so
+// nothing overflows.
+__device__ __forceinline__ float2 gelu_tanh2(float2 x) {
+    const float2 k = __fmul2_rn(__fmul2_rn(x, x), f2(kGeluCubic));
+    const float2 z = __fmul2_rn(__ffma2_rn(k, x, x), f2(kSqrt2OverPi));
+    const float2 u = make_float2(__expf(-2.0f * fabsf(z.x)), __expf(-2.0f * fabsf(z.y)));
+    const float2 den = __fadd2_rn(u, f2(1.0f));
+    const float2 num = make_float2(z.x >= 0.0f ? 1.0f : u.x, z.y >= 0.0f ? 1.0f : u.y);
+    return __fmul2_rn(x, make_float2(__fdividef(num.x, den.x), __fdividef(num.y, den.y)));
+}
+
+__device__ __forceinline__ float relu(float x) { return (x > 0.0f || x != x) ? x : 0.0f; }
+
+__device__ __forceinline__ float2 activation2(float2 v, int act) {
+    if (act == kActRelu) return make_float2(relu(v.x), relu(v.y));
+    if (act == kActGelu) return gelu_erf2(v);
+    if (act == kActGeluTanh) return gelu_tanh2(v);
+    return v;
+}
+
+// One value: the same operations (a pair with a duplicate), so every path
+// gives the same bits for the same input.
+__device__ __forceinline__ float activation(float x, int act) { return activation2(f2(x), act).x; }
+
+// In place on an even number of values held in registers.
+template <int W>
+__device__ __forceinline__ void activation_n(float (&v)[W], int act) {
+    static_assert(W % 2 == 0, "pairs");
+#pragma unroll
+    for (int j = 0; j < W; j += 2) {
+        const float2 r = activation2(make_float2(v[j], v[j + 1]), act);
+        v[j] = r.x;
+        v[j + 1] = r.y;
+    }
+}
+
+__device__ __forceinline__ float bias_at(const GemmParams& p, int64_t i) {
+    if (p.bias_kind == 1) return __ldg(static_cast<const float*>(p.bias) + i);
+    if (p.bias_kind == 2) return __bfloat162float(__ldg(static_cast<const __nv_bfloat16*>(p.bias) + i));
+    return 0.0f;
+}
+
+__device__ __forceinline__ bool has_epilogue(const GemmParams& p) { return p.bias_kind != 0 || p.act != kActNone; }
 
 // First stream-K iteration of cluster c: the ranges are [lo(c), lo(c+1)).
 __host__ __device__ __forceinline__ int64_t sk_lo(int64_t c, int64_t iters, int64_t clusters) {
@@ -241,7 +330,10 @@ struct GemmCfg {
     static constexpr uint32_t kEpiBytes = 2 * kEpiBufBytes;
     static constexpr uint32_t kBarOff = kEpiOff + kEpiBytes;
     static constexpr uint32_t kNumBars = 2 * STAGES + 4 + 1 + 2;
-    static constexpr uint32_t kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
+    // The fused epilogue's bias values for the current tile's BN columns
+    // (fp32), staged once per tile.
+    static constexpr uint32_t kBiasOff = (kBarOff + kNumBars * 8 + 16 + 15) / 16 * 16;
+    static constexpr uint32_t kSmemBytes = kBiasOff + BN * 4 + 1024;  // + alignment slack
     // Workspace bytes per split piece (both CTAs of a pair).
     static constexpr uint64_t kSlotBytes = static_cast<uint64_t>(CTA_GROUP) * 128 * BN * 4;
     static_assert(kTmemCols <= 512, "TMEM has 512 columns");
@@ -287,6 +379,31 @@ __device__ __forceinline__ void epilogue_store32(OutT* dst, int64_t ldc, int64_t
     }
 }
 
+// The same with the fused epilogue: + bias[column] (the 32 columns' values,
+// already in registers so no load waits behind a store), then the activation.
+template <typename OutT>
+__device__ __forceinline__ void epilogue_store32_fused(OutT* dst, int64_t ldc, int64_t col0, const GemmParams& p,
+                                                       const uint32_t (&acc)[32], const float (&cold)[32],
+                                                       bool has_beta, const float (&bias)[32]) {
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        v[j] = (has_beta ? fmaf(p.alpha, __uint_as_float(acc[j]), p.beta * cold[j])
+                         : p.alpha * __uint_as_float(acc[j])) + bias[j];
+    }
+    activation_n(v, p.act);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        if (col0 + j < p.N) store_out<OutT>(dst + j * ldc, v[j]);
+    }
+}
+
+// The 32 bias values of columns [col0, col0 + 32), 0 beyond N.
+__device__ __forceinline__ void load_bias32(const GemmParams& p, int64_t col0, float (&bias)[32]) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) bias[j] = (col0 + j < p.N) ? bias_at(p, col0 + j) : 0.0f;
+}
+
 // beta != 0: issue all 32 reads of C before the first write so they are in
 // flight together (a write may alias a later read, so the compiler would
 // otherwise serialise them).
@@ -302,9 +419,11 @@ __device__ __forceinline__ void load_cold32(const OutT* dst, int64_t ldc, int64_
 // `valid` of them, with 16-byte vector accesses when all 32 are in range (the
 // run starts 64- or 128-byte aligned: C is 16-byte aligned, ldc*sizeof(T) is a
 // multiple of 16 and the run starts at a multiple of 32 rows).
-template <typename OutT>
+// With FUSED, every value then gets + bias (the one bias value of this row
+// of D, a column of C) and the activation before it is stored.
+template <typename OutT, bool FUSED = false>
 __device__ __forceinline__ void store_run32(OutT* dst, int64_t valid, const uint32_t (&acc)[32], float alpha,
-                                            float beta, bool has_beta) {
+                                            float beta, bool has_beta, float bias_v = 0.0f, int act = kActNone) {
     float v[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = alpha * __uint_as_float(acc[j]);
@@ -320,6 +439,11 @@ __device__ __forceinline__ void store_run32(OutT* dst, int64_t valid, const uint
                     v[4 * q + 2] = fmaf(alpha, __uint_as_float(acc[4 * q + 2]), beta * o.z);
                     v[4 * q + 3] = fmaf(alpha, __uint_as_float(acc[4 * q + 3]), beta * o.w);
                 }
+            }
+            if constexpr (FUSED) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] += bias_v;
+                activation_n(v, act);
             }
 #pragma unroll
             for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
@@ -339,6 +463,11 @@ __device__ __forceinline__ void store_run32(OutT* dst, int64_t valid, const uint
                     }
                 }
             }
+            if constexpr (FUSED) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] += bias_v;
+                activation_n(v, act);
+            }
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 uint32_t w[4];
@@ -356,6 +485,7 @@ __device__ __forceinline__ void store_run32(OutT* dst, int64_t valid, const uint
             if (j < valid) {
                 float x = v[j];
                 if (has_beta) x = fmaf(alpha, __uint_as_float(acc[j]), beta * load_out<OutT>(dst + j));
+                if constexpr (FUSED) x = activation(x + bias_v, act);
                 store_out<OutT>(dst + j, x);
             }
         }
@@ -590,6 +720,8 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t row_local = q * 32u + lane;  // 0..127 within this CTA's rows
         OutT* C = static_cast<OutT*>(p.C);
         const bool has_beta = p.beta != 0.0f;
+        const bool fused = has_epilogue(p);
+        float* bias_s = reinterpret_cast<float*>(smem + Cfg::kBiasOff);
         // Two staging buffers shared by the four epilogue warps, each one
         // 128-row x 32-column chunk of C with rows fastest (the layout of the
         // TMA box).  One thread (warp 2, lane 0) issues the TMA copies.
@@ -617,6 +749,22 @@ __global__ void __launch_bounds__(192, 1)
                 for (int c = 0; c < ncols && colt + c < p.N; c += 32)
                     tma_prefetch_l2_2d(&tmC, row_blk, static_cast<int32_t>(colt + c));
             }
+            const int64_t row = static_cast<int64_t>(row_blk) + row_local;
+            const bool row_ok = row < p.M;
+            // Fused epilogue: fetch the tile's bias now, while the mainloop
+            // runs.  Plain product: the tile's BN column values go to shared
+            // memory (every reader of the previous tile's values has passed a
+            // barrier of that tile since its last read); transposed product:
+            // this thread's row has one value.
+            float bias_v = 0.0f;
+            if (fused && u.slot < 0) {
+                if constexpr (SWAP) {
+                    if (row_ok) bias_v = bias_at(p, row);
+                } else {
+                    for (int c = static_cast<int>(row_local); c < BN; c += 128)
+                        bias_s[c] = (colt + c < p.N) ? bias_at(p, colt + c) : 0.0f;
+                }
+            }
             uint32_t ok = 1;
             if (lane == 0) ok = wait_phase<false>(tfull_bar(acc), acc_phase, wctx, kWhereEpilogue) ? 1u : 0u;
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -624,8 +772,6 @@ __global__ void __launch_bounds__(192, 1)
             // alone at a named barrier below if another one gave up.
             if (!named_barrier_and(kEpiBarrier, kEpiThreads, ok != 0u)) break;
             tc_fence_after_sync();
-            const int64_t row = static_cast<int64_t>(row_blk) + row_local;
-            const bool row_ok = row < p.M;
             const uint32_t tbase = tmem_base + ((q * 32u) << 16) + acc * BN;
 
             // The TMA store clips at 16-byte granules along the contiguous
@@ -644,7 +790,11 @@ __global__ void __launch_bounds__(192, 1)
                     tmem_ld_wait32(r);
                     if (row_ok) {
                         OutT* dst = C + row * p.ldc + col0;
-                        store_run32<OutT>(dst, p.N - col0, r, p.alpha, p.beta, has_beta);
+                        if (fused) {
+                            store_run32<OutT, true>(dst, p.N - col0, r, p.alpha, p.beta, has_beta, bias_v, p.act);
+                        } else {
+                            store_run32<OutT>(dst, p.N - col0, r, p.alpha, p.beta, has_beta);
+                        }
                     }
                 }
                 tc_fence_before_sync();
@@ -661,8 +811,19 @@ __global__ void __launch_bounds__(192, 1)
                     uint32_t r[32];
                     tmem_ld32(tbase + c, r);
                     tmem_ld_wait32(r);
-                    if (row_ok) epilogue_store32<OutT>(dst, p.ldc, col0, p.N, r, p.alpha, p.beta, cold, has_beta);
+                    if (row_ok) {
+                        if (fused) {
+                            float bj[32];
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) bj[j] = bias_s[c + j];
+                            epilogue_store32_fused<OutT>(dst, p.ldc, col0, p, r, cold, has_beta, bj);
+                        } else {
+                            epilogue_store32<OutT>(dst, p.ldc, col0, p.N, r, p.alpha, p.beta, cold, has_beta);
+                        }
+                    }
                 }
+                // The next tile overwrites the staged bias: all reads first.
+                if (fused) named_barrier_sync(kEpiBarrier, kEpiThreads);
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) {
@@ -718,12 +879,38 @@ __global__ void __launch_bounds__(192, 1)
                         named_barrier_sync(kEpiBarrier, kEpiThreads);
                     }
                     tmem_ld_wait32(r);
+                    if (fused) {
+                        // + bias[column] (staged; 0 beyond N, where the store
+                        // clips anyway), activation.  The 32 values are read
+                        // into registers before the first store.
+                        float bj[32];
+                        const float4* b4 = reinterpret_cast<const float4*>(bias_s + 32 * i);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        OutT* e = sp + j * 128 + row_local;
-                        float v = p.alpha * __uint_as_float(r[j]);
-                        if (load_c) v = fmaf(p.alpha, __uint_as_float(r[j]), p.beta * load_out<OutT>(e));
-                        store_out<OutT>(e, v);
+                        for (int q = 0; q < 8; ++q) {
+                            const float4 t4 = b4[q];
+                            bj[4 * q] = t4.x;
+                            bj[4 * q + 1] = t4.y;
+                            bj[4 * q + 2] = t4.z;
+                            bj[4 * q + 3] = t4.w;
+                        }
+                        float vv[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            float v = p.alpha * __uint_as_float(r[j]);
+                            if (load_c) v = fmaf(p.alpha, __uint_as_float(r[j]), p.beta * load_out<OutT>(sp + j * 128 + row_local));
+                            vv[j] = v + bj[j];
+                        }
+                        activation_n(vv, p.act);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) store_out<OutT>(sp + j * 128 + row_local, vv[j]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            OutT* e = sp + j * 128 + row_local;
+                            float v = p.alpha * __uint_as_float(r[j]);
+                            if (load_c) v = fmaf(p.alpha, __uint_as_float(r[j]), p.beta * load_out<OutT>(e));
+                            store_out<OutT>(e, v);
+                        }
                     }
                     fence_proxy_async_smem();
                     named_barrier_sync(kEpiBarrier, kEpiThreads);
@@ -830,6 +1017,18 @@ __global__ void __launch_bounds__(128)
     grouped_tile(p.tiles_dp + t, p.grid_m, p.grid_n, p.group_m, tm, tn);
     const int64_t row = static_cast<int64_t>(tm) * (128 * CTA_GROUP) + rank * 128 + row_local;
     const int64_t col0 = static_cast<int64_t>(tn) * BN + kSkReduceCols * c;
+    // The bias is an input, not written by the GEMM: fetch it before waiting.
+    const bool fused = has_epilogue(p);
+    float bj[32];
+    if (fused) {
+        if constexpr (SWAP) {
+            const float b = row < p.M ? bias_at(p, row) : 0.0f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) bj[j] = b;
+        } else {
+            load_bias32(p, col0, bj);
+        }
+    }
     grid_dependency_wait();
     if (col0 >= p.N) return;
     const int64_t t_begin = static_cast<int64_t>(t) * p.num_kb;
@@ -864,25 +1063,40 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
     for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(sum[j]);
     if constexpr (SWAP) {
-        store_run32<OutT>(static_cast<OutT*>(p.C) + row * p.ldc + col0, p.N - col0, r, p.alpha, p.beta, has_beta);
+        OutT* dst = static_cast<OutT*>(p.C) + row * p.ldc + col0;
+        if (fused) {
+            store_run32<OutT, true>(dst, p.N - col0, r, p.alpha, p.beta, has_beta, bj[0], p.act);
+        } else {
+            store_run32<OutT>(dst, p.N - col0, r, p.alpha, p.beta, has_beta);
+        }
     } else {
         OutT* dst = static_cast<OutT*>(p.C) + col0 * p.ldc + row;
         float cold[32];
         if (has_beta) load_cold32<OutT>(dst, p.ldc, col0, p.N, cold);
-        epilogue_store32<OutT>(dst, p.ldc, col0, p.N, r, p.alpha, p.beta, cold, has_beta);
+        if (fused) {
+            epilogue_store32_fused<OutT>(dst, p.ldc, col0, p, r, cold, has_beta, bj);
+        } else {
+            epilogue_store32<OutT>(dst, p.ldc, col0, p.N, r, p.alpha, p.beta, cold, has_beta);
+        }
     }
 }
 
 // C = beta * C (or 0 when beta == 0): the K == 0 case, where the product is
-// an empty sum.
+// an empty sum; with the fused epilogue, act(beta * C + bias[j]).  Only
+// p.M, p.N, p.ldc, p.C, p.beta and the epilogue fields are used.
 template <typename OutT>
-__global__ void scale_c_kernel(OutT* C, int64_t M, int64_t N, int64_t ldc, float beta) {
+__global__ void scale_c_kernel(const GemmParams p) {
+    const int64_t M = p.M, N = p.N;
     const int64_t total = M * N;
+    OutT* C = static_cast<OutT*>(p.C);
+    const bool fused = has_epilogue(p);
     for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
          idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t j = idx / M, i = idx - j * M;
-        OutT* dst = C + j * ldc + i;
-        store_out<OutT>(dst, beta == 0.0f ? 0.0f : beta * load_out<OutT>(dst));
+        OutT* dst = C + j * p.ldc + i;
+        float v = p.beta == 0.0f ? 0.0f : p.beta * load_out<OutT>(dst);
+        if (fused) v = activation(v + bias_at(p, j), p.act);
+        store_out<OutT>(dst, v);
     }
 }
 

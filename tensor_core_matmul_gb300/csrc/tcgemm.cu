@@ -555,15 +555,52 @@ constexpr int kWsCaller = 1;
 constexpr int kWsNone = 2;     // plan without any split
 constexpr int kWsNoAlloc = 3;  // the fixed scratch array above
 
+// The fused epilogue of one call: bias (one value per column of C) and
+// activation; the default is none of either.
+struct Epilogue {
+    const void* bias = nullptr;
+    int bias_kind = TCGEMM_BIAS_NONE;
+    int act = TCGEMM_ACT_NONE;
+};
+
+int validate_epilogue(const Epilogue& ep, int64_t M, int64_t N, const void* C, int64_t ldc, int out_dtype) {
+    if (ep.act < TCGEMM_ACT_NONE || ep.act > TCGEMM_ACT_GELU_TANH) {
+        set_error("unknown activation %d", ep.act);
+        return TCGEMM_ERR_INVALID_ARG;
+    }
+    if (ep.bias_kind < TCGEMM_BIAS_NONE || ep.bias_kind > TCGEMM_BIAS_BF16) {
+        set_error("unknown bias dtype %d", ep.bias_kind);
+        return TCGEMM_ERR_INVALID_ARG;
+    }
+    if ((ep.bias_kind == TCGEMM_BIAS_NONE) != (ep.bias == nullptr)) {
+        set_error("bias must be NULL exactly when bias_dtype is TCGEMM_BIAS_NONE");
+        return TCGEMM_ERR_INVALID_ARG;
+    }
+    if (ep.bias_kind == TCGEMM_BIAS_NONE || M == 0 || N == 0) return TCGEMM_OK;
+    const int64_t besz = ep.bias_kind == TCGEMM_BIAS_F32 ? 4 : 2;
+    if ((reinterpret_cast<uintptr_t>(ep.bias) & static_cast<uintptr_t>(besz - 1)) != 0) {
+        set_error("bias must be aligned to its element size (%lld bytes)", static_cast<long long>(besz));
+        return TCGEMM_ERR_ALIGNMENT;
+    }
+    const int64_t esz = out_dtype == TCGEMM_OUT_F32 ? 4 : 2;
+    if (overlaps(C, ((N - 1) * ldc + M) * esz, ep.bias, N * besz)) {
+        set_error("bias overlaps C");
+        return TCGEMM_ERR_INVALID_ARG;
+    }
+    return TCGEMM_OK;
+}
+
 int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
              int64_t ldc, float alpha, float beta, int out_dtype, void* stream_v, int variant,
-             int ws_mode = kWsInternal, void* ws = nullptr, int64_t ws_bytes = 0) {
+             int ws_mode = kWsInternal, void* ws = nullptr, int64_t ws_bytes = 0, const Epilogue& ep = Epilogue()) {
     t_last_error[0] = '\0';
     if (variant < TCGEMM_VARIANT_AUTO || variant > TCGEMM_VARIANT_SWAP_N64) {
         set_error("unknown variant %d", variant);
         return TCGEMM_ERR_INVALID_ARG;
     }
     int rc = validate(M, N, K, A, lda, B, ldb, C, ldc, out_dtype);
+    if (rc != TCGEMM_OK) return rc;
+    rc = validate_epilogue(ep, M, N, C, ldc, out_dtype);
     if (rc != TCGEMM_OK) return rc;
     if (M == 0 || N == 0) return TCGEMM_OK;
     int dev = 0;
@@ -576,12 +613,20 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
         const int64_t total = M * N;
         const int threads = 256;
         const int64_t blocks = std::min<int64_t>((total + threads - 1) / threads, int64_t{info.sms} * 8);
+        tcg::GemmParams sp{};
+        sp.M = static_cast<int>(M);
+        sp.N = static_cast<int>(N);
+        sp.ldc = ldc;
+        sp.C = C;
+        sp.alpha = alpha;
+        sp.beta = beta;
+        sp.bias = ep.bias;
+        sp.bias_kind = ep.bias_kind;
+        sp.act = ep.act;
         if (out_dtype == TCGEMM_OUT_F32) {
-            tcg::scale_c_kernel<float><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-                static_cast<float*>(C), M, N, ldc, beta);
+            tcg::scale_c_kernel<float><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(sp);
         } else {
-            tcg::scale_c_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-                static_cast<__nv_bfloat16*>(C), M, N, ldc, beta);
+            tcg::scale_c_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(sp);
         }
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) {
@@ -647,7 +692,7 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     } else {
         twm = tcm;
     }
-    tcg::GemmParams gp;
+    tcg::GemmParams gp{};
     gp.M = static_cast<int>(pl.swap ? N : M);
     gp.N = static_cast<int>(pl.swap ? M : N);
     gp.K = static_cast<int>(K);
@@ -661,6 +706,9 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     gp.C = C;
     gp.alpha = alpha;
     gp.beta = beta;
+    gp.bias = ep.bias;
+    gp.bias_kind = ep.bias_kind;
+    gp.act = ep.act;
     gp.tiles_dp = pl.tiles_dp;
     gp.sk_tiles = pl.sk_tiles;
     gp.sk_iters = pl.sk_iters;
@@ -704,6 +752,17 @@ int gemm_bf16_ws(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, co
 int gemm_bf16_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
                       void* C, int64_t ldc, float alpha, float beta, int out_dtype, void* stream, int variant) {
     return run_gemm(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, stream, variant, kWsNoAlloc);
+}
+
+int gemm_bf16_bias_act(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                       void* C, int64_t ldc, float alpha, float beta, int out_dtype, const void* bias, int bias_dtype,
+                       int activation, void* stream, int variant) {
+    Epilogue ep;
+    ep.bias = bias;
+    ep.bias_kind = bias_dtype;
+    ep.act = activation;
+    return run_gemm(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, stream, variant, kWsInternal, nullptr, 0,
+                    ep);
 }
 
 int64_t tcgemm_noalloc_scratch_bytes(void) { return static_cast<int64_t>(kNoAllocScratchBytes); }

@@ -11,6 +11,16 @@
   order, plus the output rounding.  At most 0.5% (+2) of the elements may
   need this second clause, so a real bug cannot hide behind it.
 * Integer-valued inputs: bit-exact.
+* Fused epilogue E = act(D + bias): the activations are Lipschitz with
+  constant L (1 for ReLU and none; 1.129 for both GELUs, the largest slope of
+  x*Phi(x) and of its tanh form), so an error e in the value before the
+  activation becomes at most L*e after it.  fp32 output:
+      |C - E| <= L * 1e-3 * sqrt(K) * max(1, |D + bias|)  (+ 2^-20 |E| for the
+      fp32 activation function's own error);
+  bf16 output: within 1 ulp, or (second clause, same 0.5% (+2) cap)
+      |C - E| <= ulp_bf16(E) + L * (|alpha| K 2^-24 G + 2^-22 (|alpha S| +
+      |beta C| + |bias|)) + 2^-20 |E|,
+  the accumulation bound plus the fp32 epilogue's few roundings.
 
 C_ref is the oracle's fp64 value D (for fp32 output) or its bf16 rounding.
 """
@@ -85,6 +95,57 @@ def check_bf16(got_bits: np.ndarray, ref_bits: np.ndarray, what: str = "", max_u
             D, G, K = fallback(flat)
             got = bf16_to_f64(got_bits.reshape(-1)[flat])
             ok = np.abs(got - D) <= bf16_ulp(D) + K * ACC_UNIT * G
+            bad.reshape(-1)[flat[ok]] = False
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError(f"{what}: {int(bad.sum())} of {got_bits.size} bf16 outputs more than "
+                             f"{max_ulp} ulp away; first {idx.tolist()} got "
+                             f"{[hex(x) for x in got_bits[bad][:5]]} ref {[hex(x) for x in ref_bits[bad][:5]]}")
+
+
+LIPSCHITZ = {"none": 1.0, "relu": 1.0, "gelu": 1.13, "gelu_tanh": 1.13}
+ACT_FN_REL = 2.0 ** -20  # allowance for the fp32 activation function's error (erfcf, expf: a few ulp)
+
+
+def check_f32_epilogue(got: np.ndarray, E: np.ndarray, pre: np.ndarray, K: int, act: str, what: str = "") -> None:
+    """fp32 output of the fused epilogue: E the oracle's act(D + bias), pre
+    its D + bias (the value the activation is applied to)."""
+    got = np.asarray(got, dtype=np.float64)
+    E = np.asarray(E, dtype=np.float64)
+    pre = np.asarray(pre, dtype=np.float64)
+    assert got.shape == E.shape == pre.shape
+    if got.size == 0:
+        return
+    tol = LIPSCHITZ[act] * f32_tolerance(pre, K) + ACT_FN_REL * np.abs(E)
+    err = np.abs(got - E)
+    bad = ~(err <= tol)
+    bad &= ~(np.isnan(got) & np.isnan(E))
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError(f"{what}: {int(bad.sum())} of {got.size} fp32 outputs out of tolerance; "
+                             f"first {idx.tolist()} got {got[bad][:5]} ref {E[bad][:5]}")
+
+
+def check_bf16_bound(got_bits: np.ndarray, ref_bits: np.ndarray, bound_fn, what: str = "",
+                     max_ulp: int = 1) -> None:
+    """As check_bf16, the second clause given as ``bound_fn(flat) -> (E,
+    bound)``: an element is also accepted if |C - E| <= ulp_bf16(E) + bound."""
+    got_bits = np.asarray(got_bits, dtype=np.uint16)
+    ref_bits = np.asarray(ref_bits, dtype=np.uint16)
+    assert got_bits.shape == ref_bits.shape
+    if got_bits.size == 0:
+        return
+    bad = bf16_ulp_distance(got_bits, ref_bits) > max_ulp
+    nan_got = (got_bits & 0x7FFF) > 0x7F80
+    nan_ref = (ref_bits & 0x7FFF) > 0x7F80
+    bad |= nan_got != nan_ref
+    bad &= ~(nan_got & nan_ref)
+    if bad.any():
+        flat = np.flatnonzero(bad)
+        if flat.size <= int(0.005 * got_bits.size) + 2:
+            E, bound = bound_fn(flat)
+            got = bf16_to_f64(got_bits.reshape(-1)[flat])
+            ok = np.abs(got - E) <= bf16_ulp(E) + bound
             bad.reshape(-1)[flat[ok]] = False
     if bad.any():
         idx = np.argwhere(bad)[:5]

@@ -64,6 +64,29 @@ def test_bad_dtype_and_variant(tc):
     assert tc.gemm_bf16_raw(8, 8, 8, FAKE, 8, FAKE * 2, 8, FAKE * 4, 8, 1.0, 0.0, 0, 0, 9) == 1
 
 
+@pytest.mark.parametrize("bias,bias_dtype,act,status", [
+    (None, 0, 4, 1),               # unknown activation
+    (None, 0, -1, 1),              # unknown activation
+    (FAKE * 8, 3, 0, 1),           # unknown bias dtype
+    (None, 1, 0, 1),               # bias dtype given, pointer NULL
+    (FAKE * 8, 0, 0, 1),           # pointer given with TCGEMM_BIAS_NONE
+    (FAKE * 8 + 2, 1, 1, 2),       # fp32 bias not 4-byte aligned
+    (FAKE * 8 + 1, 2, 2, 2),       # bf16 bias not 2-byte aligned
+    (FAKE * 4 + 8, 1, 0, 1),       # bias overlaps C
+])
+def test_epilogue_argument_errors(tc, bias, bias_dtype, act, status):
+    """The fused-epilogue entry point checks its extra arguments on the host,
+    before anything is launched (C is at FAKE*4, 8 x 8 fp32)."""
+    st = tc.binding.gemm_bf16_bias_act_raw(8, 8, 8, FAKE, 8, FAKE * 2, 8, FAKE * 4, 8, 1.0, 0.0, 0, bias,
+                                           bias_dtype, act, 0, 0)
+    assert st == status, (st, tc.binding.last_error())
+    assert tc.binding.last_error()
+
+
+def test_epilogue_empty_problem_is_noop(tc):
+    assert tc.binding.gemm_bf16_bias_act_raw(0, 8, 8, 0, 8, 0, 8, 0, 8, 1.0, 0.0, 0, FAKE, 1, 2, 0, 0) == 0
+
+
 def test_empty_problems_are_noops(tc):
     assert tc.gemm_bf16_raw(0, 8, 8, 0, 8, 0, 8, 0, 8, 1.0, 0.0, 0, 0) == 0
     assert tc.gemm_bf16_raw(8, 0, 8, 0, 8, 0, 8, 0, 8, 1.0, 0.0, 0, 0) == 0
