@@ -23,6 +23,10 @@ Memory layout convention (every tensor here lives on the host):
 
 Padding columns beyond K (or M for C) are filled with a fixed sentinel so a
 kernel that reads them would produce a visibly wrong answer.
+
+FP8 inputs (E4M3 or E5M2, the OCP 8-bit formats) are drawn the same way and
+rounded with torch's conversion to ``float8_e4m3fn`` / ``float8_e5m2``
+(round to nearest even); their padding holds the code 0x7F, a NaN in both.
 """
 from __future__ import annotations
 
@@ -39,6 +43,9 @@ PAD_BF16_BITS = 0x7FC0
 OUT_F32 = 0
 OUT_BF16 = 1
 
+FP8_DTYPES = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+PAD_FP8_BITS = 0x7F  # NaN in E4M3 and in E5M2
+
 
 @dataclasses.dataclass
 class GemmCase:
@@ -54,9 +61,10 @@ class GemmCase:
     alpha: float
     beta: float
     out_dtype: int  # OUT_F32 or OUT_BF16
-    A: torch.Tensor  # (M, lda) bf16, host
-    B: torch.Tensor  # (N, ldb) bf16, host
+    A: torch.Tensor  # (M, lda) bf16 or FP8, host
+    B: torch.Tensor  # (N, ldb) bf16 or FP8, host
     C_in: Optional[torch.Tensor]  # (N, ldc) out dtype, host; None when beta == 0
+    in_format: str = "bf16"  # "bf16", "e4m3" or "e5m2" (A and B)
 
     @property
     def flops(self) -> int:
@@ -114,6 +122,39 @@ def integer_out(rows: int, cols: int, seed: int, out_dtype: int, lo: int = -8, h
     return out
 
 
+def _fp8(vals: torch.Tensor, rows: int, cols: int, fmt: str, ld: int) -> torch.Tensor:
+    out = torch.empty((rows, ld), dtype=FP8_DTYPES[fmt])
+    if ld > cols:
+        out.view(torch.uint8)[:, cols:] = PAD_FP8_BITS
+    out[:, :cols] = vals.to(FP8_DTYPES[fmt])
+    return out
+
+
+def normal_fp8(rows: int, cols: int, seed: int, fmt: str, ld: Optional[int] = None) -> torch.Tensor:
+    """(rows, ld) FP8 tensor: N(0,1) rounded to the format, NaN padding."""
+    ld = cols if ld is None else ld
+    return _fp8(torch.randn((rows, cols), generator=_gen(seed), dtype=torch.float32), rows, cols, fmt, ld)
+
+
+def integer_fp8(rows: int, cols: int, seed: int, fmt: str, lo: int = -4, hi: int = 4,
+                ld: Optional[int] = None) -> torch.Tensor:
+    """Small integers from [lo, hi], exact in both FP8 formats for |x| <= 4."""
+    ld = cols if ld is None else ld
+    vals = torch.randint(lo, hi + 1, (rows, cols), generator=_gen(seed), dtype=torch.int32)
+    return _fp8(vals.to(torch.float32), rows, cols, fmt, ld)
+
+
+def as_u8(t: torch.Tensor) -> np.ndarray:
+    """FP8 torch tensor -> numpy uint8 view of the same bytes."""
+    assert t.element_size() == 1
+    return t.contiguous().view(torch.uint8).numpy()
+
+
+def as_bits(t: torch.Tensor) -> np.ndarray:
+    """Operand bytes for the oracle: uint16 bf16 bits or uint8 FP8 codes."""
+    return as_u8(t) if t.element_size() == 1 else as_u16(t)
+
+
 def round_up(x: int, m: int) -> int:
     return (x + m - 1) // m * m
 
@@ -121,15 +162,25 @@ def round_up(x: int, m: int) -> int:
 def make_case(name: str, M: int, N: int, K: int, *, alpha: float = 1.0, beta: float = 0.0,
               out_dtype: int = OUT_BF16, seed: int = 0, kind: str = "normal",
               lda: Optional[int] = None, ldb: Optional[int] = None,
-              ldc: Optional[int] = None) -> GemmCase:
+              ldc: Optional[int] = None, in_format: str = "bf16") -> GemmCase:
     """Build a case.  Leading dimensions default to the smallest value the
-    16-byte stride rule allows (K rounded up to 8 elements for A/B, M rounded
-    up to 16 bytes for C)."""
-    lda = round_up(max(K, 1), 8) if lda is None else lda
-    ldb = round_up(max(K, 1), 8) if ldb is None else ldb
+    16-byte stride rule allows (K rounded up to 8 bf16 or 16 FP8 elements for
+    A/B, M rounded up to 16 bytes for C)."""
+    per16 = 8 if in_format == "bf16" else 16
+    lda = round_up(max(K, 1), per16) if lda is None else lda
+    ldb = round_up(max(K, 1), per16) if ldb is None else ldb
     esz = 4 if out_dtype == OUT_F32 else 2
     ldc = round_up(max(M, 1), 16 // esz) if ldc is None else ldc
-    if kind == "normal":
+    if in_format != "bf16":
+        if kind == "normal":
+            A = normal_fp8(M, K, seed * 1000 + 1, in_format, lda)
+            B = normal_fp8(N, K, seed * 1000 + 2, in_format, ldb)
+        elif kind == "integer":
+            A = integer_fp8(M, K, seed * 1000 + 1, in_format, ld=lda)
+            B = integer_fp8(N, K, seed * 1000 + 2, in_format, ld=ldb)
+        else:
+            raise ValueError(kind)
+    elif kind == "normal":
         A = normal_bf16(M, K, seed * 1000 + 1, lda)
         B = normal_bf16(N, K, seed * 1000 + 2, ldb)
     elif kind == "integer":
@@ -146,7 +197,7 @@ def make_case(name: str, M: int, N: int, K: int, *, alpha: float = 1.0, beta: fl
         else:
             C_in = normal_bf16(N, M, seed * 1000 + 3, ldc)
     return GemmCase(name, M, N, K, lda, ldb, ldc, float(alpha), float(beta), out_dtype,
-                    A, B, C_in)
+                    A, B, C_in, in_format)
 
 
 # The five workloads: square 256 (fp32 out), the square 4096 headline shape,

@@ -10,8 +10,9 @@ Every function cites the passage it follows in ``gemm_oracle.c``'s header:
 the product and layouts from the H100 work log "在 H100 上超越 cuBLAS：一份工作日志"
 (sections "Simon 博客的快速回顾" and "实验设置"), and the alpha/beta update
 from the "DeepGEMM" article, section 1.1; the fused bias + activation
-epilogue from the same article, section 6.1 (the readings taken where it is
-silent are listed in ``gemm_oracle.c``'s header).
+epilogue from the same article, section 6.1; FP8 inputs (section 6.3) in the
+OCP E4M3 / E5M2 formats (the readings taken where the article is silent are
+listed in ``gemm_oracle.c``'s header).
 
 Parity pins for this oracle live in ``tests/test_oracle_pins.py``.  The fp32
 accumulation order of the GPU is a hardware choice; it is covered only by the
@@ -34,6 +35,8 @@ _lock = threading.Lock()
 
 # Activation codes of gemm_oracle.c (its own numbering; callers use the names).
 ACTIVATIONS = {"none": 0, "relu": 1, "gelu": 2, "gelu_tanh": 3}
+# Input kinds of gemm_oracle.c: bf16 (uint16 bit arrays) or an FP8 format (uint8 arrays).
+FP8_KINDS = {"e4m3": 1, "e5m2": 2}
 
 
 def lib_path(mutant: int = 0, build_dir: Optional[str] = None) -> str:
@@ -72,13 +75,17 @@ class Oracle:
         L.oracle_gemm_sampled_f64.argtypes = [i64, i64, i64, p, i64, p, i64, p, i64, ctypes.c_int,
                                               ctypes.c_float, ctypes.c_float, i64, p, p, p]
         L.oracle_gemm_sampled_f64.restype = ctypes.c_int
-        L.oracle_gemm_epi_f64.argtypes = [i64, i64, i64, p, i64, p, i64, p, i64, ctypes.c_int,
+        L.oracle_gemm_epi_f64.argtypes = [i64, i64, i64, p, i64, p, i64, ctypes.c_int, p, i64, ctypes.c_int,
                                           ctypes.c_float, ctypes.c_float, p, ctypes.c_int, ctypes.c_int,
                                           p, ctypes.c_int]
         L.oracle_gemm_epi_f64.restype = ctypes.c_int
-        L.oracle_gemm_epi_sampled_f64.argtypes = [i64, i64, i64, p, i64, p, i64, p, i64, ctypes.c_int,
-                                                  ctypes.c_float, ctypes.c_float, p, ctypes.c_int, ctypes.c_int,
-                                                  i64, p, p, p]
+        L.oracle_gemm_epi_sampled_f64.argtypes = [i64, i64, i64, p, i64, p, i64, ctypes.c_int, p, i64,
+                                                  ctypes.c_int, ctypes.c_float, ctypes.c_float, p, ctypes.c_int,
+                                                  ctypes.c_int, i64, p, p, p]
+        L.oracle_absdot_kind_sampled_f64.argtypes = [i64, i64, i64, p, i64, p, i64, ctypes.c_int, i64, p, p, p]
+        L.oracle_absdot_kind_sampled_f64.restype = ctypes.c_int
+        L.oracle_fp8_to_double.argtypes = [ctypes.c_uint8, ctypes.c_int]
+        L.oracle_fp8_to_double.restype = ctypes.c_double
         L.oracle_gemm_epi_sampled_f64.restype = ctypes.c_int
         L.oracle_activation_array.argtypes = [p, p, i64, ctypes.c_int]
         L.oracle_absdot_sampled_f64.argtypes = [i64, i64, i64, p, i64, p, i64, i64, p, p, p]
@@ -126,6 +133,20 @@ class Oracle:
         raise TypeError("bias must be float32 or bf16 bits (uint16)")
 
     @staticmethod
+    def _operands(A, B, in_format):
+        """A, B as contiguous arrays plus the C code's input kind: uint16 arrays
+        hold bf16 bits; uint8 arrays hold FP8 codes of ``in_format``."""
+        A = np.ascontiguousarray(A)
+        B = np.ascontiguousarray(B)
+        if A.dtype == np.uint8 and B.dtype == np.uint8:
+            if in_format not in FP8_KINDS:
+                raise ValueError("uint8 operands need in_format 'e4m3' or 'e5m2'")
+            return A, B, FP8_KINDS[in_format]
+        if in_format not in (None, "bf16"):
+            raise ValueError("in_format given for bf16 operands")
+        return np.ascontiguousarray(A, dtype=np.uint16), np.ascontiguousarray(B, dtype=np.uint16), 0
+
+    @staticmethod
     def _act(act) -> int:
         return ACTIVATIONS[act] if isinstance(act, str) else int(act)
 
@@ -139,44 +160,49 @@ class Oracle:
     # -- the definition --------------------------------------------------------
     def gemm_f64(self, M: int, N: int, K: int, A: np.ndarray, B: np.ndarray,
                  C_in: Optional[np.ndarray] = None, alpha: float = 1.0, beta: float = 0.0,
-                 threads: int = 0) -> np.ndarray:
+                 threads: int = 0, in_format: Optional[str] = None) -> np.ndarray:
         """D = alpha*A*B + beta*C_in in fp64.
 
         A: uint16 bf16 bits, shape (M, lda).  B: uint16, shape (N, ldb) (column
         j of B is row j).  C_in: (N, ldc) float32 or uint16 bf16 bits.
-        Returns D as an (N, M) float64 array: D_arr[j, i] = D[i, j].
+        Returns D as an (N, M) float64 array: D_arr[j, i] = D[i, j].  With
+        uint8 operands (FP8 codes) ``in_format`` names their format.
         """
-        A = np.ascontiguousarray(A, dtype=np.uint16)
-        B = np.ascontiguousarray(B, dtype=np.uint16)
+        A, B, kind = self._operands(A, B, in_format)
         assert A.shape[0] == M and B.shape[0] == N
         lda = A.shape[1] if A.ndim == 2 else K
         ldb = B.shape[1] if B.ndim == 2 else K
         cin, ldc, cin_bf16 = self._cin(C_in, beta)
         D = np.empty((N, M), dtype=np.float64)
-        rc = self._L.oracle_gemm_f64(M, N, K, self._ptr(A), lda, self._ptr(B), ldb,
-                                     self._ptr(cin), max(ldc, M), cin_bf16,
-                                     float(alpha), float(beta), self._ptr(D), int(threads))
+        if kind == 0:
+            rc = self._L.oracle_gemm_f64(M, N, K, self._ptr(A), lda, self._ptr(B), ldb,
+                                         self._ptr(cin), max(ldc, M), cin_bf16,
+                                         float(alpha), float(beta), self._ptr(D), int(threads))
+        else:
+            rc = self._L.oracle_gemm_epi_f64(M, N, K, self._ptr(A), lda, self._ptr(B), ldb, kind,
+                                             self._ptr(cin), max(ldc, M), cin_bf16, float(alpha), float(beta),
+                                             None, 0, 0, self._ptr(D), int(threads))
         if rc != 0:
             raise ValueError("oracle_gemm_f64: bad arguments")
         return D
 
     def gemm_epi_f64(self, M: int, N: int, K: int, A: np.ndarray, B: np.ndarray,
                      C_in: Optional[np.ndarray] = None, alpha: float = 1.0, beta: float = 0.0,
-                     bias: Optional[np.ndarray] = None, act="none", threads: int = 0) -> np.ndarray:
+                     bias: Optional[np.ndarray] = None, act="none", threads: int = 0,
+                     in_format: Optional[str] = None) -> np.ndarray:
         """E = act(alpha*A*B + beta*C_in + bias[j]) in fp64, as an (N, M) array
         (the fused epilogue; see gemm_f64 for the layouts)."""
-        A = np.ascontiguousarray(A, dtype=np.uint16)
-        B = np.ascontiguousarray(B, dtype=np.uint16)
+        A, B, kind = self._operands(A, B, in_format)
         assert A.shape[0] == M and B.shape[0] == N
         lda = A.shape[1] if A.ndim == 2 else K
         ldb = B.shape[1] if B.ndim == 2 else K
         cin, ldc, cin_bf16 = self._cin(C_in, beta)
-        b, kind = self._bias(bias)
+        b, bkind = self._bias(bias)
         assert b is None or b.shape[0] >= N
         D = np.empty((N, M), dtype=np.float64)
-        rc = self._L.oracle_gemm_epi_f64(M, N, K, self._ptr(A), lda, self._ptr(B), ldb,
+        rc = self._L.oracle_gemm_epi_f64(M, N, K, self._ptr(A), lda, self._ptr(B), ldb, kind,
                                          self._ptr(cin), max(ldc, M), cin_bf16, float(alpha), float(beta),
-                                         self._ptr(b), kind, self._act(act), self._ptr(D), int(threads))
+                                         self._ptr(b), bkind, self._act(act), self._ptr(D), int(threads))
         if rc != 0:
             raise ValueError("oracle_gemm_epi_f64: bad arguments")
         return D
@@ -184,17 +210,17 @@ class Oracle:
     def gemm_epi_sampled_f64(self, M: int, N: int, K: int, A: np.ndarray, B: np.ndarray,
                              rows: np.ndarray, cols: np.ndarray,
                              C_in: Optional[np.ndarray] = None, alpha: float = 1.0, beta: float = 0.0,
-                             bias: Optional[np.ndarray] = None, act="none") -> np.ndarray:
-        A = np.ascontiguousarray(A, dtype=np.uint16)
-        B = np.ascontiguousarray(B, dtype=np.uint16)
+                             bias: Optional[np.ndarray] = None, act="none",
+                             in_format: Optional[str] = None) -> np.ndarray:
+        A, B, kind = self._operands(A, B, in_format)
         rows = np.ascontiguousarray(rows, dtype=np.int64)
         cols = np.ascontiguousarray(cols, dtype=np.int64)
         cin, ldc, cin_bf16 = self._cin(C_in, beta)
-        b, kind = self._bias(bias)
+        b, bkind = self._bias(bias)
         out = np.empty(rows.shape[0], dtype=np.float64)
         rc = self._L.oracle_gemm_epi_sampled_f64(M, N, K, self._ptr(A), A.shape[1], self._ptr(B), B.shape[1],
-                                                 self._ptr(cin), max(ldc, M), cin_bf16, float(alpha),
-                                                 float(beta), self._ptr(b), kind, self._act(act),
+                                                 kind, self._ptr(cin), max(ldc, M), cin_bf16, float(alpha),
+                                                 float(beta), self._ptr(b), bkind, self._act(act),
                                                  rows.shape[0], self._ptr(rows), self._ptr(cols),
                                                  self._ptr(out))
         if rc != 0:
@@ -211,7 +237,9 @@ class Oracle:
     def gemm_sampled_f64(self, M: int, N: int, K: int, A: np.ndarray, B: np.ndarray,
                          rows: np.ndarray, cols: np.ndarray,
                          C_in: Optional[np.ndarray] = None, alpha: float = 1.0,
-                         beta: float = 0.0) -> np.ndarray:
+                         beta: float = 0.0, in_format: Optional[str] = None) -> np.ndarray:
+        if in_format not in (None, "bf16"):
+            return self.gemm_epi_sampled_f64(M, N, K, A, B, rows, cols, C_in, alpha, beta, in_format=in_format)
         A = np.ascontiguousarray(A, dtype=np.uint16)
         B = np.ascontiguousarray(B, dtype=np.uint16)
         rows = np.ascontiguousarray(rows, dtype=np.int64)
@@ -227,16 +255,16 @@ class Oracle:
         return out
 
     def absdot_sampled_f64(self, M: int, N: int, K: int, A: np.ndarray, B: np.ndarray,
-                           rows: np.ndarray, cols: np.ndarray) -> np.ndarray:
+                           rows: np.ndarray, cols: np.ndarray, in_format: Optional[str] = None) -> np.ndarray:
         """G[i,j] = sum_k |A[i,k] * B[k,j]| at the given positions (fp64), the
         scale of the fp32-accumulation error bound."""
-        A = np.ascontiguousarray(A, dtype=np.uint16)
-        B = np.ascontiguousarray(B, dtype=np.uint16)
+        A, B, kind = self._operands(A, B, in_format)
         rows = np.ascontiguousarray(rows, dtype=np.int64)
         cols = np.ascontiguousarray(cols, dtype=np.int64)
         out = np.empty(rows.shape[0], dtype=np.float64)
-        rc = self._L.oracle_absdot_sampled_f64(M, N, K, self._ptr(A), A.shape[1], self._ptr(B), B.shape[1],
-                                               rows.shape[0], self._ptr(rows), self._ptr(cols), self._ptr(out))
+        rc = self._L.oracle_absdot_kind_sampled_f64(M, N, K, self._ptr(A), A.shape[1], self._ptr(B), B.shape[1],
+                                                    kind, rows.shape[0], self._ptr(rows), self._ptr(cols),
+                                                    self._ptr(out))
         if rc != 0:
             raise ValueError("oracle_absdot_sampled_f64: bad arguments")
         return out
@@ -259,6 +287,10 @@ class Oracle:
 
     def bf16_to_double(self, bits: int) -> float:
         return self._L.oracle_bf16_to_double(bits)
+
+    def fp8_to_double(self, code: int, in_format: str) -> float:
+        """The value of one FP8 code ('e4m3' or 'e5m2')."""
+        return self._L.oracle_fp8_to_double(code, FP8_KINDS[in_format] - 1)
 
 
 _default: Optional[Oracle] = None

@@ -60,6 +60,16 @@
  * Both sides of every identity above are equal in exact arithmetic; the
  * formulas produce NaN for x = -inf (0 * inf), and so does the oracle.
  *
+ * FP8 inputs (the "DeepGEMM" article, section 6.3, names an FP8 input path as
+ * the next step; it gives no format or scaling rules).  Readings taken: A and
+ * B hold 8-bit floats in one of the two formats of the OCP 8-bit floating
+ * point specification (Micikevicius et al., "FP8 Formats for Deep Learning",
+ * 2022): E4M3 (bias 7, no infinities, S.1111.111 is NaN, largest 448) or E5M2
+ * (bias 15, IEEE-style infinities and NaNs, largest 57344); both operands in
+ * the same format; same layouts and definition as above, with per-tensor
+ * scale factors folded into alpha.  Every FP8 value decodes exactly to double
+ * and every product of two is exact in double.
+ *
  * Planted mistakes: when compiled with -DORACLE_MUTANT=n (n > 0) one
  * deliberate error is switched on.  The test suite builds these variants to
  * prove that its pins catch every such error; the normal build has n = 0.
@@ -132,8 +142,9 @@ void oracle_round_f32_array(const double* x, float* out, int64_t n) {
 
 typedef struct {
     int64_t M, N, K;
-    const uint16_t* A; int64_t lda;
-    const uint16_t* B; int64_t ldb;
+    const void* A; int64_t lda;
+    const void* B; int64_t ldb;
+    int in_kind;        /* 0 bf16, 1 FP8 E4M3, 2 FP8 E5M2 (both operands) */
     const void* Cin; int64_t ldc; int cin_bf16; /* C_in dtype: 0 fp32, 1 bf16 */
     double alpha, beta;
     int absolute;       /* 1: sum |A[i,k]*B[k,j]| instead (error model, no alpha/beta) */
@@ -183,6 +194,55 @@ static double bias_at(const problem_t* p, int64_t i, int64_t j) {
     return 0.0;
 }
 
+/* ---- FP8 formats ------------------------------------------------------ */
+
+/* E4M3: sign, 4 exponent bits (bias 7), 3 fraction bits.  Exponent field 0
+ * holds subnormals m/8 * 2^-6; the pattern S.1111.111 is NaN and there are no
+ * infinities. */
+static double e4m3_to_double(uint8_t v) {
+    const int s = v >> 7, e = (v >> 3) & 0xF, m = v & 0x7;
+    double x;
+    if (e == 0xF && m == 0x7) return NAN;
+#if ORACLE_MUTANT == 16
+    if (e == 0) x = ldexp((double)m, -10);             /* planted: subnormal scale off by two */
+#else
+    if (e == 0) x = ldexp((double)m, -9);              /* (m/8) * 2^(1-7) */
+#endif
+    else x = ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -x : x;
+}
+
+/* E5M2: sign, 5 exponent bits (bias 15), 2 fraction bits; exponent field 31
+ * holds infinity (fraction 0) and NaN; field 0 holds subnormals m/4 * 2^-14. */
+static double e5m2_to_double(uint8_t v) {
+    const int s = v >> 7, e = (v >> 2) & 0x1F, m = v & 0x3;
+    double x;
+    if (e == 0x1F) x = m ? NAN : INFINITY;
+    else if (e == 0) x = ldexp((double)m, -16);         /* (m/4) * 2^(1-15) */
+#if ORACLE_MUTANT == 17
+    else x = ldexp(1.0 + m / 4.0, e - 7);               /* planted: E4M3's bias used */
+#else
+    else x = ldexp(1.0 + m / 4.0, e - 15);
+#endif
+    return s ? -x : x;
+}
+
+double oracle_fp8_to_double(uint8_t v, int format) {
+    return format == 0 ? e4m3_to_double(v) : e5m2_to_double(v);
+}
+
+static double a_at(const problem_t* p, int64_t idx) {
+    if (p->in_kind == 1) return e4m3_to_double(((const uint8_t*)p->A)[idx]);
+    if (p->in_kind == 2) return e5m2_to_double(((const uint8_t*)p->A)[idx]);
+    return bf16_to_double(((const uint16_t*)p->A)[idx]);
+}
+
+static double b_at(const problem_t* p, int64_t idx) {
+    if (p->in_kind == 1) return e4m3_to_double(((const uint8_t*)p->B)[idx]);
+    if (p->in_kind == 2) return e5m2_to_double(((const uint8_t*)p->B)[idx]);
+    return bf16_to_double(((const uint16_t*)p->B)[idx]);
+}
+
 static double c_in_at(const problem_t* p, int64_t i, int64_t j) {
 #if ORACLE_MUTANT == 8
     int64_t idx = i * p->N + j;     /* planted: C_in read row-major */
@@ -206,14 +266,14 @@ static double element(const problem_t* p, int64_t i, int64_t j) {
 #endif
     for (int64_t k = 0; k < kend; ++k) {
 #if ORACLE_MUTANT == 1
-        double a = bf16_to_double(p->A[k * p->M + i]);   /* planted: A as column-major */
+        double a = a_at(p, k * p->M + i);                /* planted: A as column-major */
 #else
-        double a = bf16_to_double(p->A[i * p->lda + k]);
+        double a = a_at(p, i * p->lda + k);
 #endif
 #if ORACLE_MUTANT == 2
-        double b = bf16_to_double(p->B[k * p->N + j]);   /* planted: B as row-major */
+        double b = b_at(p, k * p->N + j);                /* planted: B as row-major */
 #else
-        double b = bf16_to_double(p->B[j * p->ldb + k]);
+        double b = b_at(p, j * p->ldb + k);
 #endif
         s += p->absolute ? fabs(a * b) : a * b;
     }
@@ -250,12 +310,12 @@ static double element(const problem_t* p, int64_t i, int64_t j) {
 /* ---- full matrix, threaded over columns ------------------------------- */
 
 int oracle_gemm_epi_f64(int64_t M, int64_t N, int64_t K,
-                        const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                        const void* A, int64_t lda, const void* B, int64_t ldb, int in_kind,
                         const void* Cin, int64_t ldc, int cin_bf16,
                         float alpha, float beta, const void* bias, int bias_kind, int act,
                         double* D, int nthreads);
 int oracle_gemm_epi_sampled_f64(int64_t M, int64_t N, int64_t K,
-                                const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                                const void* A, int64_t lda, const void* B, int64_t ldb, int in_kind,
                                 const void* Cin, int64_t ldc, int cin_bf16,
                                 float alpha, float beta, const void* bias, int bias_kind, int act,
                                 int64_t count, const int64_t* rows, const int64_t* cols,
@@ -296,21 +356,22 @@ int oracle_gemm_f64(int64_t M, int64_t N, int64_t K,
                     const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
                     const void* Cin, int64_t ldc, int cin_bf16,
                     float alpha, float beta, double* D, int nthreads) {
-    return oracle_gemm_epi_f64(M, N, K, A, lda, B, ldb, Cin, ldc, cin_bf16, alpha, beta, NULL, 0, 0, D,
+    return oracle_gemm_epi_f64(M, N, K, A, lda, B, ldb, 0, Cin, ldc, cin_bf16, alpha, beta, NULL, 0, 0, D,
                                nthreads);
 }
 
 /* E = act(alpha*A*B + beta*C_in + bias) in fp64 (the fused epilogue, see the
  * header); bias_kind 0 and act 0 give D itself. */
 int oracle_gemm_epi_f64(int64_t M, int64_t N, int64_t K,
-                        const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                        const void* A, int64_t lda, const void* B, int64_t ldb, int in_kind,
                         const void* Cin, int64_t ldc, int cin_bf16,
                         float alpha, float beta, const void* bias, int bias_kind, int act,
                         double* D, int nthreads) {
     if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || ldc < M) return -1;
     if (beta != 0.0f && Cin == NULL) return -1;
     if (bias_kind < 0 || bias_kind > 2 || (bias_kind != 0 && bias == NULL) || act < 0 || act > 3) return -1;
-    problem_t p = {M, N, K, A, lda, B, ldb, Cin, ldc, cin_bf16, (double)alpha, (double)beta, 0,
+    if (in_kind < 0 || in_kind > 2) return -1;
+    problem_t p = {M, N, K, A, lda, B, ldb, in_kind, Cin, ldc, cin_bf16, (double)alpha, (double)beta, 0,
                    bias, bias_kind, act};
     return run_full(&p, D, nthreads);
 }
@@ -347,12 +408,12 @@ int oracle_gemm_sampled_f64(int64_t M, int64_t N, int64_t K,
                             float alpha, float beta,
                             int64_t count, const int64_t* rows, const int64_t* cols,
                             double* out) {
-    return oracle_gemm_epi_sampled_f64(M, N, K, A, lda, B, ldb, Cin, ldc, cin_bf16, alpha, beta, NULL, 0, 0,
+    return oracle_gemm_epi_sampled_f64(M, N, K, A, lda, B, ldb, 0, Cin, ldc, cin_bf16, alpha, beta, NULL, 0, 0,
                                        count, rows, cols, out);
 }
 
 int oracle_gemm_epi_sampled_f64(int64_t M, int64_t N, int64_t K,
-                                const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                                const void* A, int64_t lda, const void* B, int64_t ldb, int in_kind,
                                 const void* Cin, int64_t ldc, int cin_bf16,
                                 float alpha, float beta, const void* bias, int bias_kind, int act,
                                 int64_t count, const int64_t* rows, const int64_t* cols,
@@ -360,7 +421,8 @@ int oracle_gemm_epi_sampled_f64(int64_t M, int64_t N, int64_t K,
     if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || ldc < M) return -1;
     if (beta != 0.0f && Cin == NULL) return -1;
     if (bias_kind < 0 || bias_kind > 2 || (bias_kind != 0 && bias == NULL) || act < 0 || act > 3) return -1;
-    problem_t p = {M, N, K, A, lda, B, ldb, Cin, ldc, cin_bf16, (double)alpha, (double)beta, 0,
+    if (in_kind < 0 || in_kind > 2) return -1;
+    problem_t p = {M, N, K, A, lda, B, ldb, in_kind, Cin, ldc, cin_bf16, (double)alpha, (double)beta, 0,
                    bias, bias_kind, act};
     for (int64_t s = 0; s < count; ++s) {
         if (rows[s] < 0 || rows[s] >= M || cols[s] < 0 || cols[s] >= N) return -1;
@@ -373,17 +435,24 @@ int oracle_gemm_epi_sampled_f64(int64_t M, int64_t N, int64_t K,
  * in fp64, at selected positions.  A recursive fp32 sum of these K products,
  * in any order, differs from the exact sum by at most about
  * K * 2^-24 * G[i,j] (the classical bound for floating-point summation). */
-int oracle_absdot_sampled_f64(int64_t M, int64_t N, int64_t K,
-                              const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
-                              int64_t count, const int64_t* rows, const int64_t* cols,
-                              double* out) {
-    if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K) return -1;
-    problem_t p = {M, N, K, A, lda, B, ldb, NULL, M, 0, 1.0, 0.0, 1, NULL, 0, 0};
+int oracle_absdot_kind_sampled_f64(int64_t M, int64_t N, int64_t K,
+                                   const void* A, int64_t lda, const void* B, int64_t ldb, int in_kind,
+                                   int64_t count, const int64_t* rows, const int64_t* cols,
+                                   double* out) {
+    if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || in_kind < 0 || in_kind > 2) return -1;
+    problem_t p = {M, N, K, A, lda, B, ldb, in_kind, NULL, M, 0, 1.0, 0.0, 1, NULL, 0, 0};
     for (int64_t s = 0; s < count; ++s) {
         if (rows[s] < 0 || rows[s] >= M || cols[s] < 0 || cols[s] >= N) return -1;
         out[s] = element(&p, rows[s], cols[s]);
     }
     return 0;
+}
+
+int oracle_absdot_sampled_f64(int64_t M, int64_t N, int64_t K,
+                              const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                              int64_t count, const int64_t* rows, const int64_t* cols,
+                              double* out) {
+    return oracle_absdot_kind_sampled_f64(M, N, K, A, lda, B, ldb, 0, count, rows, cols, out);
 }
 
 int oracle_mutant_id(void) { return ORACLE_MUTANT; }

@@ -14,7 +14,11 @@ The pages print no worked numerical example, so the pins are:
     integer inputs and biases through ReLU, the activations against
     independent library routines (torch.relu, scipy's normal distribution
     function for GELU, torch's tanh-approximated GELU), and the identity
-    act(x) - act(-x) = x that ReLU and both GELUs satisfy.
+    act(x) - act(-x) = x that ReLU and both GELUs satisfy,
+  * for FP8 inputs: the hand-derived code table in
+    tests/golden/fp8_encodings.txt, every one of the 256 codes of each format
+    against torch's float8 -> float32 conversion, exact integer brute force and
+    numpy's float64 matmul on the decoded values.
 
 Each pin is a plain function of an ``Oracle`` so that ``test_planted_mistakes``
 can run the same pins against oracle builds with one deliberate error each
@@ -295,10 +299,80 @@ def pin_activation_odd_identity(o):
         assert abs(o.activation(np.array([30.0]), act)[0] - 30.0) < 1e-12
 
 
+def _fp8_values(codes: np.ndarray, fmt: str) -> np.ndarray:
+    """Decode FP8 codes with torch's conversion (a library routine)."""
+    t = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(gi.FP8_DTYPES[fmt])
+    return t.to(torch.float32).numpy().astype(np.float64)
+
+
+def pin_fp8_codes(o):
+    """The FP8 decoder against the hand-derived table and, for all 256 codes
+    of each format, against torch's float8 conversion."""
+    for line in open(os.path.join(GOLDEN, "fp8_encodings.txt")):
+        line = line.split("#")[0].split()
+        if not line:
+            continue
+        fmt, code, val = line[0], int(line[1], 16), line[2]
+        got = o.fp8_to_double(code, fmt)
+        if val == "nan":
+            assert np.isnan(got), (fmt, hex(code), got)
+        else:
+            want = float(val)
+            assert got == want and np.signbit(got) == np.signbit(want), (fmt, hex(code), got, want)
+    codes = np.arange(256, dtype=np.uint8)
+    for fmt in ("e4m3", "e5m2"):
+        got = np.array([o.fp8_to_double(int(c), fmt) for c in codes])
+        want = _fp8_values(codes, fmt)
+        same = (got == want) | (np.isnan(got) & np.isnan(want))
+        assert same.all(), (fmt, codes[~same][:5], got[~same][:5], want[~same][:5])
+
+
+def pin_fp8_integer_bruteforce(o):
+    """Integer-valued FP8 inputs (exact in both formats): D must equal the
+    exact rational alpha*sum + beta*C, with padded leading dimensions."""
+    for n, (M, N, K, alpha, beta, fmt) in enumerate([(5, 7, 9, 1.0, 0.0, "e4m3"), (4, 3, 33, -2.0, 0.5, "e5m2"),
+                                                      (3, 6, 17, 0.5, 1.0, "e4m3")]):
+        case = gi.make_case(f"f8int{n}", M, N, K, alpha=alpha, beta=beta, out_dtype=gi.OUT_F32, seed=700 + n,
+                            kind="integer", lda=K + 16 - K % 16 + 16, ldb=K + 16 - K % 16, ldc=M + 3,
+                            in_format=fmt)
+        A8, B8 = gi.as_u8(case.A), gi.as_u8(case.B)
+        D = o.gemm_f64(M, N, K, A8, B8, _cin_np(case), alpha, beta, in_format=fmt)
+        A = _fp8_values(A8[:, :K], fmt)
+        B = _fp8_values(B8[:, :K], fmt)
+        Cin = None if case.C_in is None else case.C_in.numpy()
+        for i in range(M):
+            for j in range(N):
+                s = sum((Fraction(int(A[i, k])) * Fraction(int(B[j, k])) for k in range(K)), Fraction(0))
+                want = Fraction(alpha) * s
+                if beta != 0.0:
+                    want += Fraction(beta) * Fraction(float(Cin[j, i]))
+                assert D[j, i] == float(want), (n, i, j, D[j, i], want)
+        rows, cols = gi.sample_indices(M, N, 10, 5)
+        smp = o.gemm_sampled_f64(M, N, K, A8, B8, rows, cols, _cin_np(case), alpha, beta, in_format=fmt)
+        assert np.array_equal(smp, D[cols, rows])
+
+
+def pin_fp8_numpy_f64(o):
+    """N(0,1) FP8 inputs: numpy's float64 matmul of the torch-decoded values
+    agrees within the fp64 summation bound."""
+    for fmt in ("e4m3", "e5m2"):
+        M, N, K = 23, 31, 200
+        case = gi.make_case("f8np", M, N, K, alpha=0.75, beta=0.0, out_dtype=gi.OUT_F32, seed=710, in_format=fmt)
+        A8, B8 = gi.as_u8(case.A), gi.as_u8(case.B)
+        D = o.gemm_f64(M, N, K, A8, B8, None, 0.75, 0.0, in_format=fmt)
+        A = _fp8_values(A8[:, :K], fmt)
+        B = _fp8_values(B8[:, :K], fmt)
+        ref = 0.75 * (B @ A.T)
+        G = np.abs(B) @ np.abs(A).T
+        assert np.all(np.abs(D - ref) <= K * 2.0 ** -52 * G + 1e-300), fmt
+        absd = o.absdot_sampled_f64(M, N, K, A8, B8, np.array([0, M - 1]), np.array([N - 1, 0]), in_format=fmt)
+        assert np.allclose(absd, [G[N - 1, 0], G[0, M - 1]], rtol=1e-12)
+
+
 PINS = [pin_integer_bruteforce, pin_numpy_f64, pin_identity_and_permutation, pin_closed_forms,
         pin_bf16_rounding, pin_beta_zero_ignores_c, pin_k_zero, pin_statistics,
         pin_sampled_matches_full, pin_epilogue_integer_bruteforce, pin_activations_library,
-        pin_activation_odd_identity]
+        pin_activation_odd_identity, pin_fp8_codes, pin_fp8_integer_bruteforce, pin_fp8_numpy_f64]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -322,6 +396,8 @@ MUTANTS = {
     13: "GELU without the 1/sqrt(2) scaling",
     14: "tanh GELU without its cubic term",
     15: "bias added before alpha",
+    16: "E4M3 subnormals scaled by 2^-10",
+    17: "E5M2 decoded with E4M3's exponent bias",
 }
 
 
