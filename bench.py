@@ -185,7 +185,7 @@ def run_ours(args) -> None:
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
 
-    case = gi.config_case(args.config)
+    case = bench_case(args)
     M, N, K = case.M, case.N, case.K
     A = case.A.to(dev)
     B = case.B.to(dev)
@@ -197,8 +197,13 @@ def run_ours(args) -> None:
     act = EPILOGUES[args.epilogue][1]
     bias = None if bias_cpu is None else bias_cpu.to(dev)
 
+    if args.in_format != "bf16" and args.epilogue != "none":
+        raise SystemExit("--epilogue is built for bf16 operands only")
+
     def gemm():
-        if args.epilogue == "none":
+        if args.in_format != "bf16":
+            tc.gemm_fp8(A, B, C, case.alpha, case.beta, M=M, N=N, K=K, stream=stream, variant=args.variant)
+        elif args.epilogue == "none":
             tc.gemm_bf16(A, B, C, case.alpha, case.beta, M=M, N=N, K=K, stream=stream, variant=args.variant)
         else:
             tc.gemm_bf16_bias_act(A, B, C, case.alpha, case.beta, bias=bias, activation=act, M=M, N=N, K=K,
@@ -244,11 +249,12 @@ def run_ours(args) -> None:
     ms_per_step = total_s / args.steps * 1e3
 
     peaks, peak_src = load_peaks()
-    tag = f"gemm_{args.config}_full" + ("" if args.epilogue == "none" else f"_{args.epilogue}")
+    tag = (f"gemm_{args.config}_full" + ("" if args.epilogue == "none" else f"_{args.epilogue}")
+           + ("" if args.in_format == "bf16" else f"_{args.in_format}"))
     traffic = profile_traffic(tag)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     variant = args.variant or tc.pick_variant(M, N, K, sms)
-    plan = tc.plan(M, N, K, variant, sms)
+    plan = tc.plan(M, N, K, variant, sms, in_kind=0 if args.in_format == "bf16" else 1)
 
     e2e = None
     if not args.no_e2e:
@@ -269,16 +275,17 @@ def run_ours(args) -> None:
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "bf16",
+            "dtype": "bf16" if args.in_format == "bf16" else f"fp8_{args.in_format}",
             "data": "synthetic",
             "config": {
-                "workload": f"gemm {args.config}: M={M} N={N} K={K}, bf16 A row-major x B col-major, "
+                "workload": f"gemm {args.config}: M={M} N={N} K={K}, {args.in_format} A row-major x B col-major, "
                             f"fp32 accumulate, {'bf16' if case.out_dtype else 'fp32'} C col-major, "
                             f"alpha={case.alpha} beta={case.beta}, N(0,1) inputs"
                             + ("" if args.epilogue == "none" else
                                f", fused epilogue C = {act}(alpha*A*B + beta*C + bias[j]), fp32 N(0,1) bias"),
                 "M": M, "N": N, "K": K,
                 "epilogue": args.epilogue,
+                "in_format": args.in_format,
                 "l2": f"flushed between timed steps ({FLUSH_BYTES >> 20} MiB write, untimed)",
                 "kernel": {"variant": {1: "1cta", 2: "2cta"}.get(variant, str(variant)), **plan},
                 "parallelism": f"independent problem per GPU x{world}",
@@ -296,12 +303,22 @@ def run_ours(args) -> None:
         pg.destroy_process_group()
 
 
+def bench_case(args):
+    """The workload: BASELINE's configuration, with 8-bit operands when
+    --in-format asks for them (same shapes, seeds and distribution)."""
+    import gemm_inputs as gi
+    c = gi.CONFIGS[args.config]
+    return gi.make_case(args.config, c["M"], c["N"], c["K"], alpha=c["alpha"], beta=c["beta"],
+                        out_dtype=c["out_dtype"], seed=c["seed"], in_format=args.in_format)
+
+
 def algorithmic_bytes(case) -> int:
     """Bytes a GEMM must move at least once: A and B read, C written, and C
     read too when beta != 0."""
     esz = 4 if case.out_dtype == 0 else 2
+    isz = 2 if case.in_format == "bf16" else 1
     c = case.M * case.N * esz
-    return 2 * case.M * case.K + 2 * case.N * case.K + c + (c if case.beta != 0.0 else 0)
+    return isz * case.M * case.K + isz * case.N * case.K + c + (c if case.beta != 0.0 else 0)
 
 
 def roofline(case, t_launch: float, peaks: dict, peak_src: str, traffic, extra_bytes: int = 0) -> dict:
@@ -312,6 +329,11 @@ def roofline(case, t_launch: float, peaks: dict, peak_src: str, traffic, extra_b
     flops = case.flops
     nbytes = algorithmic_bytes(case) + extra_bytes
     peak_flops = float(peaks["bf16_tflops"])
+    fp8 = case.in_format != "bf16"
+    if fp8:
+        # No measured FP8 peak: the measured bf16 peak times the nominal
+        # dense FP8 / BF16 ratio (4.5 / 2.25 PFLOP/s).
+        peak_flops *= 2.0
     ridge = peak_flops * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
     src = "measured" if peak_src == "measured" else "fallback"
     if flops / nbytes < ridge:
@@ -322,10 +344,12 @@ def roofline(case, t_launch: float, peaks: dict, peak_src: str, traffic, extra_b
                 "algorithmic_bytes": nbytes, "tflops": round(flops / t_launch / 1e12, 2),
                 "peak_source": f"{src} hbm_gbs (copy bandwidth)"}
     achieved = flops / t_launch / 1e12
+    nominal = 4500.0 if fp8 else 2250.0
     return {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_flops, "unit": "TFLOP/s",
             "frac": round(achieved / peak_flops, 4), "traffic": traffic, "algorithmic_bytes": nbytes,
-            "peak_source": f"{src} bf16_tflops (cuBLAS bf16 8192^3 burst)",
-            "nominal_dense_bf16_tflops": 2250.0, "frac_of_nominal": round(achieved / 2250.0, 4)}
+            "peak_source": (f"{src} bf16_tflops (cuBLAS bf16 8192^3 burst)" if not fp8 else
+                            f"{src} bf16_tflops x 2 (nominal dense fp8/bf16 ratio 4.5/2.25)"),
+            "nominal_dense_tflops": nominal, "frac_of_nominal": round(achieved / nominal, 4)}
 
 
 def measure_e2e(args, case, dev, stream, bias_cpu=None, act="none") -> dict:
@@ -362,7 +386,10 @@ def measure_e2e(args, case, dev, stream, bias_cpu=None, act="none") -> dict:
             dB[b].copy_(hB[b], non_blocking=True)
             if has_beta:
                 dC[b].copy_(hC_in[b], non_blocking=True)
-            if bias_cpu is None and act == "none":
+            if case.in_format != "bf16":
+                tc.gemm_fp8(dA[b], dB[b], dC[b], case.alpha, case.beta, M=case.M, N=case.N, K=case.K, stream=s,
+                            variant=args.variant)
+            elif bias_cpu is None and act == "none":
                 tc.gemm_bf16(dA[b], dB[b], dC[b], case.alpha, case.beta, M=case.M, N=case.N, K=case.K, stream=s,
                              variant=args.variant)
             else:
@@ -387,7 +414,8 @@ def measure_e2e(args, case, dev, stream, bias_cpu=None, act="none") -> dict:
     end.record(streams[0])
     torch.cuda.synchronize(dev)
     t = start.elapsed_time(end) / 1e3
-    h2d = case.A.numel() * 2 + case.B.numel() * 2 + (C0.numel() * C0.element_size() if has_beta else 0)
+    h2d = (case.A.numel() * case.A.element_size() + case.B.numel() * case.B.element_size()
+           + (C0.numel() * C0.element_size() if has_beta else 0))
     h2d += 0 if bias_cpu is None else bias_cpu.numel() * 4
     d2h = C0.numel() * C0.element_size()
     return {"value": round(case.flops * steps / t / 1e12, 2), "unit": "TFLOP/s",
@@ -404,8 +432,9 @@ def oracle_slab(case, ncols: int, threads: int = 0, bias=None, act: str = "none"
     import gemm_inputs as gi
     import oracle
     o = oracle.get()
-    A = gi.as_u16(case.A)
-    B = gi.as_u16(case.B)[:ncols]
+    A = gi.as_bits(case.A)
+    B = gi.as_bits(case.B)[:ncols]
+    fmt = None if case.in_format == "bf16" else case.in_format
     cin = None
     if case.C_in is not None:
         cin = case.C_in[:ncols]
@@ -413,7 +442,8 @@ def oracle_slab(case, ncols: int, threads: int = 0, bias=None, act: str = "none"
     b = None if bias is None else bias[:ncols].numpy()
     t0 = time.perf_counter()
     if b is None and act == "none":
-        o.gemm_f64(case.M, ncols, case.K, A, np.ascontiguousarray(B), cin, case.alpha, case.beta, threads=threads)
+        o.gemm_f64(case.M, ncols, case.K, A, np.ascontiguousarray(B), cin, case.alpha, case.beta, threads=threads,
+                   in_format=fmt)
     else:
         o.gemm_epi_f64(case.M, ncols, case.K, A, np.ascontiguousarray(B), cin, case.alpha, case.beta, bias=b,
                        act=act, threads=threads)
@@ -441,8 +471,7 @@ def run_reference(args) -> None:
         return
     import oracle
 
-    import gemm_inputs as gi
-    case = gi.config_case(args.config)
+    case = bench_case(args)
     bias = make_bias(args, case.N)
     act = EPILOGUES[args.epilogue][1]
     cores = oracle.get().threads(0)
@@ -475,7 +504,8 @@ def run_reference(args) -> None:
         "config": {"workload": f"gemm {args.config}: M={case.M} N={case.N} K={case.K}; each step computes "
                                f"columns 0..{ncols - 1} of C with the CPU oracle"
                                + ("" if args.epilogue == "none" else f", fused epilogue {args.epilogue}"),
-                   "M": case.M, "N": case.N, "K": case.K, "epilogue": args.epilogue},
+                   "M": case.M, "N": case.N, "K": case.K, "epilogue": args.epilogue,
+                   "in_format": args.in_format},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"{ncols} columns of C per step ({case.M}x{ncols}x{case.K})"},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -491,6 +521,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="s4k", choices=["s256", "s4k", "s8k", "edge", "skinny"])
     ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 one-CTA, 2 CTA-pair kernel")
+    ap.add_argument("--in-format", default="bf16", choices=["bf16", "e4m3", "e5m2"],
+                    help="operand type: bf16 (gemm_bf16) or 8-bit floats (gemm_fp8)")
     ap.add_argument("--epilogue", default="none", choices=sorted(EPILOGUES),
                     help="fused epilogue: bias and/or activation (gemm_bf16_bias_act)")
     ap.add_argument("--no-e2e", action="store_true")

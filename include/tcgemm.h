@@ -187,6 +187,41 @@ int gemm_bf16_bias_act(int64_t M, int64_t N, int64_t K,
                        const void* bias, int bias_dtype, int activation,
                        void* stream, int variant);
 
+/* 8-bit float operand formats (gemm_fp8): the two formats of the OCP 8-bit
+ * floating point specification. */
+typedef enum {
+    TCGEMM_FP8_E4M3 = 0,  /* sign, 4 exponent bits (bias 7), 3 fraction bits; no infinities; max 448 */
+    TCGEMM_FP8_E5M2 = 1   /* sign, 5 exponent bits (bias 15), 2 fraction bits; IEEE-style inf/NaN  */
+} tcgemm_fp8_format_t;
+
+/* The same GEMM on 8-bit float operands, the input path the "DeepGEMM"
+ * article (section 6.3) names as its next step:
+ *
+ *   C[i,j] = alpha * sum_k A[i,k] B[k,j] + beta * C[i,j]
+ *
+ * with A and B both in `in_format` (tcgemm_fp8_format_t), one byte per
+ * element, in the layouts of gemm_bf16 (A row-major M x K, B column-major
+ * K x N; lda, ldb in elements, i.e. bytes, multiples of 16).  Products are
+ * exact and accumulate in fp32 on the tensor cores (tcgen05 kind::f8f6f4);
+ * per-tensor scale factors go into alpha.  C is fp32 or bf16 as in
+ * gemm_bf16.  The article gives no formats or scaling rules: the OCP formats
+ * and alpha as the scale are this library's readings.
+ * variant: 0 (chosen by shape), TCGEMM_VARIANT_2CTA, _2CTA_W256, _1CTA_N64 or
+ * _SWAP_N64; TCGEMM_VARIANT_1CTA and _1CTA_MC are not built for 8-bit
+ * operands -> TCGEMM_ERR_INVALID_ARG, as is an unknown in_format.  Other
+ * rules and errors as gemm_bf16_variant (16-byte rules in bytes). */
+int gemm_fp8(int64_t M, int64_t N, int64_t K,
+             const void* A, int64_t lda,
+             const void* B, int64_t ldb,
+             void* C, int64_t ldc,
+             float alpha, float beta, int out_dtype, int in_format,
+             void* stream, int variant);
+
+/* tcgemm_plan for bf16 (in_kind 0) or 8-bit (in_kind 1) operands: a k-block
+ * holds 64 bf16 or 128 8-bit values, which changes the plan's k-block count
+ * and stream-K choice.  Host only. */
+int tcgemm_plan_kind(int64_t M, int64_t N, int64_t K, int variant, int in_kind, int num_sms, int64_t* out);
+
 /* Size in bytes of gemm_bf16_noalloc's fixed scratch array.  Host only. */
 int64_t tcgemm_noalloc_scratch_bytes(void);
 

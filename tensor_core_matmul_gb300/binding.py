@@ -25,6 +25,8 @@ OUT_BF16 = 1
 ACT_NONE, ACT_RELU, ACT_GELU, ACT_GELU_TANH = range(4)
 ACTIVATIONS = {"none": ACT_NONE, "relu": ACT_RELU, "gelu": ACT_GELU, "gelu_tanh": ACT_GELU_TANH}
 BIAS_NONE, BIAS_F32, BIAS_BF16 = range(3)
+FP8_E4M3, FP8_E5M2 = range(2)
+FP8_FORMATS = {"e4m3": FP8_E4M3, "e5m2": FP8_E5M2}
 
 STATUS = {0: "TCGEMM_OK", 1: "TCGEMM_ERR_INVALID_ARG", 2: "TCGEMM_ERR_ALIGNMENT",
           3: "TCGEMM_ERR_UNSUPPORTED_DEVICE", 4: "TCGEMM_ERR_CUDA", 5: "TCGEMM_ERR_TIMEOUT"}
@@ -64,6 +66,10 @@ def lib() -> ctypes.CDLL:
     L.gemm_bf16_ws.restype = i32
     L.gemm_bf16_bias_act.argtypes = gemm_args[:-1] + [p, i32, i32, p, i32]
     L.gemm_bf16_bias_act.restype = i32
+    L.gemm_fp8.argtypes = gemm_args[:-1] + [i32, p, i32]
+    L.gemm_fp8.restype = i32
+    L.tcgemm_plan_kind.argtypes = [i64, i64, i64, i32, i32, i32, ctypes.POINTER(ctypes.c_int64)]
+    L.tcgemm_plan_kind.restype = i32
     L.gemm_bf16_noalloc.argtypes = gemm_args + [i32]
     L.gemm_bf16_noalloc.restype = i32
     L.tcgemm_noalloc_scratch_bytes.argtypes = []
@@ -205,6 +211,40 @@ def gemm_bf16_bias_act(A, B, C, alpha: float = 1.0, beta: float = 0.0, *, bias=N
     return C
 
 
+def gemm_fp8_raw(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int, C: int, ldc: int,
+                 alpha: float, beta: float, out_dtype: int, in_format: int, stream: int, variant: int = 0) -> int:
+    """Pointer-level call of the 8-bit-operand entry point; returns the status."""
+    return lib().gemm_fp8(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, in_format, stream, variant)
+
+
+def gemm_fp8(A, B, C, alpha: float = 1.0, beta: float = 0.0, *, M: Optional[int] = None, N: Optional[int] = None,
+             K: Optional[int] = None, stream=None, variant: int = 0):
+    """C = alpha * A * B + beta * C with A, B torch float8_e4m3fn or
+    float8_e5m2 CUDA tensors (both the same), in the storage convention of
+    gemm_bf16 (A (M, lda), B (N, ldb)); C float32 or bfloat16."""
+    import torch
+    fmts = {torch.float8_e4m3fn: FP8_E4M3, torch.float8_e5m2: FP8_E5M2}
+    if not (A.is_cuda and B.is_cuda and C.is_cuda):
+        raise ValueError("A, B and C must be CUDA tensors")
+    if A.dtype not in fmts or B.dtype != A.dtype:
+        raise ValueError("A and B must both be float8_e4m3fn or both float8_e5m2")
+    if C.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("C must be float32 or bfloat16")
+    for t in (A, B, C):
+        if t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError("A, B, C must be 2-D with unit inner stride")
+    M = C.shape[1] if M is None else M
+    N = C.shape[0] if N is None else N
+    K = A.shape[1] if K is None else K
+    if C.shape[0] < N or (K > 0 and (A.shape[0] < M or B.shape[0] < N)):
+        raise ValueError("tensor shapes smaller than M/N")
+    out = OUT_F32 if C.dtype == torch.float32 else OUT_BF16
+    st = gemm_fp8_raw(M, N, K, A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0), C.data_ptr(), C.stride(0),
+                      float(alpha), float(beta), out, fmts[A.dtype], _stream_ptr(stream), variant)
+    _check(st)
+    return C
+
+
 def check_device_status(stream=None) -> tuple[int, int]:
     where = ctypes.c_uint32(0)
     st = lib().tcgemm_check_device_status(_stream_ptr(stream), ctypes.byref(where))
@@ -228,11 +268,14 @@ PLAN_KEYS = ["grid", "cluster", "tiles_m", "tiles_n", "bm", "bn", "num_kb", "sme
              "stream_k", "arows", "swap"]
 
 
-def plan(M: int, N: int, K: int, variant: int = 0, num_sms: int = 152) -> dict:
+def plan(M: int, N: int, K: int, variant: int = 0, num_sms: int = 152, in_kind: int = 0) -> dict:
     """Launch plan for a device with `num_sms` SMs (host only; assumes every
-    pair / 4-cluster of SMs can be resident)."""
+    pair / 4-cluster of SMs can be resident).  in_kind 1: 8-bit operands."""
     out = (ctypes.c_int64 * len(PLAN_KEYS))()
-    _check(lib().tcgemm_plan(M, N, K, variant, num_sms, out))
+    if in_kind:
+        _check(lib().tcgemm_plan_kind(M, N, K, variant, in_kind, num_sms, out))
+    else:
+        _check(lib().tcgemm_plan(M, N, K, variant, num_sms, out))
     return dict(zip(PLAN_KEYS, [int(v) for v in out]))
 
 

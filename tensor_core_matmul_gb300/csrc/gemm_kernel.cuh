@@ -126,6 +126,7 @@ struct GemmParams {
     int64_t ldc;
     void* C;
     float alpha, beta;
+    int in_fmt;          // 8-bit operands: 0 = E4M3, 1 = E5M2 (unused for bf16)
     // Fused epilogue: out = act(alpha*acc + beta*C + bias[column of C]).
     const void* bias;    // one value per column of C (per row of D in the transposed product), or null
     int bias_kind;       // 0 none, 1 fp32, 2 bf16
@@ -309,15 +310,18 @@ struct UnitIter {
 // loaded; the MMA still computes 128 rows and reads rows 64..127 from the
 // shared memory that follows the A stage.  Those accumulator rows are never
 // stored, so whatever they hold does not matter, and A's traffic halves.
-template <int CTA_GROUP, int BN, int STAGES, int AROWS = 128>
+// IN = 0: bf16 operands; IN = 1: 8-bit float operands (E4M3 or E5M2).  A
+// k-block is one 128-byte swizzle row either way: 64 bf16 or 128 FP8 values.
+template <int CTA_GROUP, int BN, int STAGES, int AROWS = 128, int IN = 0>
 struct GemmCfg {
-    static constexpr int kBK = 64;                        // 64 bf16 = one 128-byte swizzle row
+    static constexpr int kInBytes = IN == 1 ? 1 : 2;       // bytes per operand element
+    static constexpr int kBK = 128 / kInBytes;             // elements per k-block (one 128-byte row)
     static constexpr int kRowsA = AROWS;                  // A rows loaded per CTA
     static constexpr int kBM = 128 * CTA_GROUP;           // MMA M (pair tile height)
     static constexpr int kRowsB = BN / CTA_GROUP;         // B rows (tile columns) per CTA
-    static constexpr int kUmmaK = 16;
-    static constexpr uint32_t kABytes = kRowsA * kBK * 2;
-    static constexpr uint32_t kBBytes = kRowsB * kBK * 2;
+    static constexpr int kUmmaK = 32 / kInBytes;           // K of one MMA instruction (32 bytes)
+    static constexpr uint32_t kABytes = kRowsA * 128;
+    static constexpr uint32_t kBBytes = kRowsB * 128;
     static constexpr uint32_t kStageTx = CTA_GROUP * (kABytes + kBBytes);  // bytes landing per stage
     static constexpr uint32_t kTmemCols = 2 * BN;         // two accumulators
     static constexpr uint32_t kTmemAlloc = kTmemCols <= 32 ? 32 : kTmemCols <= 64 ? 64 : kTmemCols <= 128 ? 128
@@ -510,12 +514,12 @@ constexpr uint32_t kEpiThreads = 128;
 // SWAP: the launch computes D = C^T (the host swapped A with B and M with N);
 // D's rows are C's columns, so the epilogue writes each TMEM row as a
 // contiguous run of one column of C (D row-major with leading dimension ldc).
-template <int CTA_GROUP, int BN, int STAGES, int MC, int AROWS, bool SWAP, typename OutT>
+template <int CTA_GROUP, int BN, int STAGES, int MC, int AROWS, bool SWAP, typename OutT, int IN = 0>
 __global__ void __launch_bounds__(192, 1)
     gemm_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
                         const GemmParams p) {
-    using Cfg = GemmCfg<CTA_GROUP, BN, STAGES, AROWS>;
+    using Cfg = GemmCfg<CTA_GROUP, BN, STAGES, AROWS, IN>;
     static_assert(MC == 1 || (MC == 4 && CTA_GROUP == 1 && AROWS == 128), "multicast clusters use single-CTA MMAs");
     static_assert(!SWAP || (CTA_GROUP == 1 && MC == 1), "the swapped product runs on single-CTA tiles");
     constexpr int kCluster = CTA_GROUP * MC;
@@ -654,7 +658,8 @@ __global__ void __launch_bounds__(192, 1)
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer --
         if (lane == 0 && (CTA_GROUP == 1 || rank == 0)) {
-            constexpr uint32_t kIdesc = idesc_bf16_f32(Cfg::kBM, BN);
+            const uint32_t kIdesc = IN == 1 ? idesc_f8_f32(Cfg::kBM, BN, static_cast<uint32_t>(p.in_fmt) & 1u)
+                                            : idesc_bf16_f32(Cfg::kBM, BN);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             UnitIter it(cluster_id, num_clusters);
@@ -676,8 +681,8 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                     for (int k = 0; k < Cfg::kBK / Cfg::kUmmaK; ++k) {
                         // +32 bytes along K per step: (32 >> 4) = 2 in the address field.
-                        mma_bf16<CTA_GROUP>(d_tmem, ad + 2u * k, bd + 2u * k, idesc,
-                                            (kb != u.kb0 || k != 0) ? 1u : 0u);
+                        mma_tc<CTA_GROUP, IN>(d_tmem, ad + 2u * k, bd + 2u * k, idesc,
+                                              (kb != u.kb0 || k != 0) ? 1u : 0u);
                     }
                     if constexpr (MC == 4) {
                         // The stage is free once this CTA and both partners

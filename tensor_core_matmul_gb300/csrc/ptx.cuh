@@ -281,7 +281,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
+// The same for kind::f8f6f4 with both operands in one 8-bit format: A and B
+// format fields 0 = E4M3, 1 = E5M2.
+__host__ __device__ constexpr uint32_t idesc_f8_f32(uint32_t M, uint32_t N, uint32_t fmt) {
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread (bf16 operands).
 template <int CTA_GROUP>
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t accumulate) {
@@ -301,6 +307,33 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
             : "memory");
     }
 }
+
+// D[tmem] (+)= A[smem] * B[smem]^T for either operand type.  IN = 0: bf16
+// operands (kind::f16, K = 16 per instruction); IN = 1: 8-bit float operands
+// (kind::f8f6f4, K = 32 per instruction).  Either way one instruction covers
+// 32 bytes of each operand row.
+template <int CTA_GROUP, int IN = 0>
+__device__ __forceinline__ void mma_tc(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    if constexpr (IN == 1 && CTA_GROUP == 1) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    } else if constexpr (IN == 1) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    } else {
+        mma_bf16<CTA_GROUP>(d_tmem, adesc, bdesc, idesc, accumulate);
+    }
+}
+
 
 // Arrive once on `bar` (this CTA) when all prior tcgen05 async ops of the
 // issuing thread have completed.

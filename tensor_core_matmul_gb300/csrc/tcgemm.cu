@@ -145,8 +145,9 @@ bool use_stream_k(int64_t tiles, int64_t clusters, int64_t num_kb) {
     return 2 * tiles <= clusters && num_kb >= 64 && tiles * num_kb >= 4 * clusters;
 }
 
+// in_kind 0: bf16 operands (64 per k-block); 1: 8-bit operands (128 per k-block).
 bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pairs, int max_quads, Plan& pl,
-               bool allow_split = true) {
+               bool allow_split = true, int in_kind = 0) {
     if (sms <= 0) return false;
     if (variant == TCGEMM_VARIANT_AUTO) variant = pick_variant(M, N, K, sms);
     pl.variant = variant;
@@ -156,7 +157,8 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pa
         pl.swap = 1;
         std::swap(M, N);
     }
-    const int64_t num_kb = (K + 63) / 64;
+    const int64_t bk = in_kind == 1 ? 128 : 64;
+    const int64_t num_kb = (K + bk - 1) / bk;
     if (variant == TCGEMM_VARIANT_1CTA) {
         pl.cta_group = 1;
         pl.bm = Cfg1::kBM;
@@ -262,17 +264,19 @@ bool encode_c(CUtensorMap* m, void* ptr, int64_t M, int64_t N, int64_t ldc, bool
 }
 
 bool encode_kmajor(CUtensorMap* m, const void* ptr, int64_t k_extent, int64_t rows, int64_t ld,
-                   uint32_t box_rows) {
+                   uint32_t box_rows, int elem_bytes = 2) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) {
         set_error("cuTensorMapEncodeTiled is not available from the driver");
         return false;
     }
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(k_extent), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
-    cuuint32_t box[2] = {64u, box_rows};
+    // One 128-byte row per box row: 64 bf16 or 128 8-bit values.
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * static_cast<cuuint64_t>(elem_bytes)};
+    cuuint32_t box[2] = {128u / static_cast<cuuint32_t>(elem_bytes), box_rows};
     cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+    CUresult r = fn(m, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void*>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
@@ -287,15 +291,15 @@ bool encode_kmajor(CUtensorMap* m, const void* ptr, int64_t k_extent, int64_t ro
 
 // The dynamic shared-memory opt-in is a per-kernel attribute; it is set once
 // per device for each kernel instantiation.
-template <int CG, int BN, int ST, int MC, int AR, bool SW, typename OutT>
+template <int CG, int BN, int ST, int MC, int AR, bool SW, typename OutT, int IN = 0>
 bool ensure_smem_attr(int dev) {
     static std::mutex mu;
     static bool done[kMaxDevices] = {};
     std::lock_guard<std::mutex> lk(mu);
     if (done[dev]) return true;
-    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, MC, AR, SW, OutT>;
+    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, MC, AR, SW, OutT, IN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(tcg::GemmCfg<CG, BN, ST, AR>::kSmemBytes));
+                                         static_cast<int>(tcg::GemmCfg<CG, BN, ST, AR, IN>::kSmemBytes));
     if (e != cudaSuccess) {
         set_error("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         return false;
@@ -304,11 +308,11 @@ bool ensure_smem_attr(int dev) {
     return true;
 }
 
-template <int CG, int BN, int ST, int MC, int AR, bool SW, typename OutT>
+template <int CG, int BN, int ST, int MC, int AR, bool SW, typename OutT, int IN = 0>
 int launch_gemm(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tcm,
                 const CUtensorMap& twm, const tcg::GemmParams& gp, cudaStream_t stream, int dev) {
-    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, MC, AR, SW, OutT>;
-    if (!ensure_smem_attr<CG, BN, ST, MC, AR, SW, OutT>(dev)) return TCGEMM_ERR_CUDA;
+    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, MC, AR, SW, OutT, IN>;
+    if (!ensure_smem_attr<CG, BN, ST, MC, AR, SW, OutT, IN>(dev)) return TCGEMM_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(pl.grid), 1, 1);
     cfg.blockDim = dim3(tcg::GemmCfg<CG, BN, ST, AR>::kThreads, 1, 1);
@@ -426,7 +430,7 @@ bool overlaps(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
 }
 
 int validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
-             const void* C, int64_t ldc, int out_dtype) {
+             const void* C, int64_t ldc, int out_dtype, int64_t in_bytes = 2) {
     const int64_t lim = (int64_t{1} << 31) - 1;
     if (M < 0 || N < 0 || K < 0 || M > lim || N > lim || K > lim) {
         set_error("sizes must satisfy 0 <= M, N, K < 2^31 (got %lld, %lld, %lld)", static_cast<long long>(M),
@@ -453,12 +457,14 @@ int validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     }
     if (K > 0) {
         if ((reinterpret_cast<uintptr_t>(A) & 15u) != 0 || (reinterpret_cast<uintptr_t>(B) & 15u) != 0 ||
-            ((lda * 2) & 15) != 0 || ((ldb * 2) & 15) != 0) {
-            set_error("A and B must be 16-byte aligned with lda*2 and ldb*2 multiples of 16 bytes");
+            ((lda * in_bytes) & 15) != 0 || ((ldb * in_bytes) & 15) != 0) {
+            set_error("A and B must be 16-byte aligned with lda and ldb multiples of 16 bytes (%lld-byte elements)",
+                      static_cast<long long>(in_bytes));
             return TCGEMM_ERR_ALIGNMENT;
         }
         const int64_t cbytes = ((N - 1) * ldc + M) * esz;
-        if (overlaps(C, cbytes, A, ((M - 1) * lda + K) * 2) || overlaps(C, cbytes, B, ((N - 1) * ldb + K) * 2)) {
+        if (overlaps(C, cbytes, A, ((M - 1) * lda + K) * in_bytes) ||
+            overlaps(C, cbytes, B, ((N - 1) * ldb + K) * in_bytes)) {
             set_error("C overlaps A or B");
             return TCGEMM_ERR_INVALID_ARG;
         }
@@ -592,13 +598,24 @@ int validate_epilogue(const Epilogue& ep, int64_t M, int64_t N, const void* C, i
 
 int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
              int64_t ldc, float alpha, float beta, int out_dtype, void* stream_v, int variant,
-             int ws_mode = kWsInternal, void* ws = nullptr, int64_t ws_bytes = 0, const Epilogue& ep = Epilogue()) {
+             int ws_mode = kWsInternal, void* ws = nullptr, int64_t ws_bytes = 0, const Epilogue& ep = Epilogue(),
+             int in_kind = 0, int in_fmt = 0) {
     t_last_error[0] = '\0';
     if (variant < TCGEMM_VARIANT_AUTO || variant > TCGEMM_VARIANT_SWAP_N64) {
         set_error("unknown variant %d", variant);
         return TCGEMM_ERR_INVALID_ARG;
     }
-    int rc = validate(M, N, K, A, lda, B, ldb, C, ldc, out_dtype);
+    if (in_kind == 1) {
+        if (in_fmt != TCGEMM_FP8_E4M3 && in_fmt != TCGEMM_FP8_E5M2) {
+            set_error("unknown FP8 format %d", in_fmt);
+            return TCGEMM_ERR_INVALID_ARG;
+        }
+        if (variant == TCGEMM_VARIANT_1CTA || variant == TCGEMM_VARIANT_1CTA_MC) {
+            set_error("variant %d is not built for FP8 operands", variant);
+            return TCGEMM_ERR_INVALID_ARG;
+        }
+    }
+    int rc = validate(M, N, K, A, lda, B, ldb, C, ldc, out_dtype, in_kind == 1 ? 1 : 2);
     if (rc != TCGEMM_OK) return rc;
     rc = validate_epilogue(ep, M, N, C, ldc, out_dtype);
     if (rc != TCGEMM_OK) return rc;
@@ -638,7 +655,7 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     }
 
     Plan pl;
-    if (!make_plan(M, N, K, variant, info.sms, info.max_pairs, info.max_quads, pl, ws_mode != kWsNone)) {
+    if (!make_plan(M, N, K, variant, info.sms, info.max_pairs, info.max_quads, pl, ws_mode != kWsNone, in_kind)) {
         set_error("no launch plan for this shape and variant");
         return TCGEMM_ERR_INVALID_ARG;
     }
@@ -679,7 +696,9 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     const int64_t rowsA = pl.swap ? N : M, rowsB = pl.swap ? M : N;
     const int64_t ldA = pl.swap ? ldb : lda, ldB = pl.swap ? lda : ldb;
     CUtensorMap ta, tb;
-    if (!encode_kmajor(&ta, opA, K, rowsA, ldA, a_box_rows) || !encode_kmajor(&tb, opB, K, rowsB, ldB, b_box_rows)) {
+    const int in_bytes = in_kind == 1 ? 1 : 2;
+    if (!encode_kmajor(&ta, opA, K, rowsA, ldA, a_box_rows, in_bytes) ||
+        !encode_kmajor(&tb, opB, K, rowsB, ldB, b_box_rows, in_bytes)) {
         return TCGEMM_ERR_INVALID_ARG;
     }
     pl.ws_ptr = wsp;
@@ -709,12 +728,28 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     gp.bias = ep.bias;
     gp.bias_kind = ep.bias_kind;
     gp.act = ep.act;
+    gp.in_fmt = in_fmt;
     gp.tiles_dp = pl.tiles_dp;
     gp.sk_tiles = pl.sk_tiles;
     gp.sk_iters = pl.sk_iters;
     gp.timeout_ns = timeout_ns();
 
     const bool bf16 = out_dtype == TCGEMM_OUT_BF16;
+    if (in_kind == 1) {
+        // 8-bit operands: the CTA-pair tiles, the narrow tiles and the
+        // transposed product.
+#define TCGEMM_LAUNCH8(CG, BN, ST, MC, AR, SW)                                                                  \
+    return bf16 ? launch_gemm<CG, BN, ST, MC, AR, SW, __nv_bfloat16, 1>(pl, ta, tb, tcm, twm, gp, stream, dev) \
+                : launch_gemm<CG, BN, ST, MC, AR, SW, float, 1>(pl, ta, tb, tcm, twm, gp, stream, dev)
+        if (pl.swap) TCGEMM_LAUNCH8(1, 64, kStagesN64, 1, 128, true);
+        if (pl.bn == 64 && pl.arows == 64) TCGEMM_LAUNCH8(1, 64, kStagesN64h, 1, 64, false);
+        if (pl.bn == 64) TCGEMM_LAUNCH8(1, 64, kStagesN64, 1, 128, false);
+        if (pl.cta_group == 2 && pl.bn == 224) TCGEMM_LAUNCH8(2, 224, kStages2n, 1, 128, false);
+        if (pl.cta_group == 2) TCGEMM_LAUNCH8(2, 256, kStages2, 1, 128, false);
+#undef TCGEMM_LAUNCH8
+        set_error("no FP8 kernel for this plan");
+        return TCGEMM_ERR_INVALID_ARG;
+    }
 #define TCGEMM_LAUNCH(CG, BN, ST, MC, AR, SW)                                                               \
     return bf16 ? launch_gemm<CG, BN, ST, MC, AR, SW, __nv_bfloat16>(pl, ta, tb, tcm, twm, gp, stream, dev) \
                 : launch_gemm<CG, BN, ST, MC, AR, SW, float>(pl, ta, tb, tcm, twm, gp, stream, dev)
@@ -765,6 +800,12 @@ int gemm_bf16_bias_act(int64_t M, int64_t N, int64_t K, const void* A, int64_t l
                     ep);
 }
 
+int gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+             int64_t ldc, float alpha, float beta, int out_dtype, int in_format, void* stream, int variant) {
+    return run_gemm(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, stream, variant, kWsInternal, nullptr, 0,
+                    Epilogue(), 1, in_format);
+}
+
 int64_t tcgemm_noalloc_scratch_bytes(void) { return static_cast<int64_t>(kNoAllocScratchBytes); }
 
 int64_t tcgemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int variant, int num_sms) {
@@ -780,6 +821,15 @@ int tcgemm_plan(int64_t M, int64_t N, int64_t K, int variant, int num_sms, int64
     if (out == nullptr || M <= 0 || N <= 0 || K <= 0 || num_sms <= 0) return TCGEMM_ERR_INVALID_ARG;
     Plan pl;
     if (!make_plan(M, N, K, variant, num_sms, num_sms / 2, num_sms / 4, pl)) return TCGEMM_ERR_INVALID_ARG;
+    fill_plan_out(pl, out);
+    return TCGEMM_OK;
+}
+
+int tcgemm_plan_kind(int64_t M, int64_t N, int64_t K, int variant, int in_kind, int num_sms, int64_t* out) {
+    if (out == nullptr || M <= 0 || N <= 0 || K <= 0 || num_sms <= 0 || in_kind < 0 || in_kind > 1)
+        return TCGEMM_ERR_INVALID_ARG;
+    Plan pl;
+    if (!make_plan(M, N, K, variant, num_sms, num_sms / 2, num_sms / 4, pl, true, in_kind)) return TCGEMM_ERR_INVALID_ARG;
     fill_plan_out(pl, out);
     return TCGEMM_OK;
 }

@@ -83,6 +83,26 @@ def test_epilogue_argument_errors(tc, bias, bias_dtype, act, status):
     assert tc.binding.last_error()
 
 
+@pytest.mark.parametrize("args,fmt,variant,status", [
+    ((8, 8, 16, FAKE, 16, FAKE * 2, 16, FAKE * 4, 8), 2, 0, 1),     # unknown FP8 format
+    ((8, 8, 16, FAKE, 16, FAKE * 2, 16, FAKE * 4, 8), 0, 1, 1),     # variant not built for FP8
+    ((8, 8, 16, FAKE, 16, FAKE * 2, 16, FAKE * 4, 8), 1, 3, 1),     # variant not built for FP8
+    ((8, 8, 8, FAKE, 8, FAKE * 2, 16, FAKE * 4, 8), 0, 0, 2),       # lda = 8 bytes: not a 16-byte multiple
+    ((8, 8, 16, FAKE + 8, 16, FAKE * 2, 16, FAKE * 4, 8), 1, 0, 2), # A misaligned
+])
+def test_fp8_argument_errors(tc, args, fmt, variant, status):
+    st = tc.binding.gemm_fp8_raw(*args, 1.0, 0.0, 0, fmt, 0, variant)
+    assert st == status, (st, tc.binding.last_error())
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (64, 8192, 8192), (600, 700, 8192), (600, 700, 4096)])
+def test_fp8_plans_count_128_value_k_blocks(tc, M, N, K):
+    p8 = tc.plan(M, N, K, 0, 152, in_kind=1)
+    p16 = tc.plan(M, N, K, 0, 152)
+    assert p8["num_kb"] == (K + 127) // 128 and p16["num_kb"] == (K + 63) // 64
+    assert p8["smem"] == p16["smem"] or p8["bn"] != p16["bn"]
+
+
 def test_epilogue_empty_problem_is_noop(tc):
     assert tc.binding.gemm_bf16_bias_act_raw(0, 8, 8, 0, 8, 0, 8, 0, 8, 1.0, 0.0, 0, FAKE, 1, 2, 0, 0) == 0
 

@@ -1,0 +1,128 @@
+"""GPU parity of the 8-bit-operand GEMM (gemm_fp8: E4M3 or E5M2 inputs, fp32
+accumulation on tcgen05 kind::f8f6f4) against the oracle, through the C ABI.
+Same rules as the bf16 path (tests/parity.py): fp32 output within
+1e-3*sqrt(K)*max(1,|D|); bf16 output within 1 ulp, or the fp32-accumulation
+bound where cancellation makes D tiny; integer inputs bit-exact."""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import gemm_inputs as gi
+from tests import gpu_harness as H
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+FP8_VARIANTS = [int(v) for v in os.environ.get("FP8_VARIANTS", "0,2,4,5,6").split(",")]
+FORMATS = ["e4m3", "e5m2"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import tensor_core_matmul_gb300 as tc
+    tc.lib()
+
+
+def run_fp8(case: gi.GemmCase, variant: int = 0) -> np.ndarray:
+    import tensor_core_matmul_gb300 as tc
+    g = H.GuardedC(case)
+    tc.gemm_fp8(case.A.cuda(), case.B.cuda(), g.C, case.alpha, case.beta, M=case.M, N=case.N, K=case.K,
+                variant=variant)
+    torch.cuda.synchronize()
+    st, where = tc.check_device_status()
+    assert st == 0, f"device status {st} (role {where})"
+    g.check_guards()
+    return g.result_np()
+
+
+def compare(o, case: gi.GemmCase, got: np.ndarray, rows=None, cols=None, exact: bool = False, what: str = ""):
+    A8, B8, fmt = gi.as_u8(case.A), gi.as_u8(case.B), case.in_format
+    if rows is None:
+        cols, rows = np.divmod(np.arange(case.M * case.N, dtype=np.int64), case.M)
+    D = o.gemm_sampled_f64(case.M, case.N, case.K, A8, B8, rows, cols, H.cin_np(case), case.alpha, case.beta,
+                           in_format=fmt)
+    g = got[cols, rows]
+    if case.out_dtype == gi.OUT_F32:
+        if exact:
+            parity.check_exact(g, o.round_f32(D), what)
+        else:
+            parity.check_f32(g, D, case.K, what)
+        return
+    ref = o.round_bf16(D)
+    if exact:
+        parity.check_exact(g, ref, what)
+        return
+
+    def fallback(flat):
+        G = o.absdot_sampled_f64(case.M, case.N, case.K, A8, B8, rows[flat], cols[flat], in_format=fmt)
+        return D[flat], abs(case.alpha) * G, case.K
+    parity.check_bf16(g, ref, what, fallback=fallback)
+
+
+@pytest.mark.parametrize("variant", FP8_VARIANTS)
+@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("out", [gi.OUT_F32, gi.OUT_BF16], ids=["f32", "bf16"])
+def test_fp8_small_shapes(oracle_lib, variant, fmt, out):
+    """Ragged shapes (several tiles, odd and even k-block counts, a K tail
+    inside the 128-value k-block), beta on and off."""
+    for n, (M, N, K, beta) in enumerate([(200, 300, 320, 0.0), (129, 520, 200, 0.5), (48, 260, 1000, 0.0),
+                                         (257, 65, 128, 0.25)]):
+        case = gi.make_case(f"f8_{n}", M, N, K, alpha=0.5, beta=beta, out_dtype=out, seed=800 + 10 * n + out,
+                            in_format=fmt)
+        got = run_fp8(case, variant)
+        compare(oracle_lib, case, got, what=f"v{variant} {fmt} {case.name}")
+
+
+@pytest.mark.parametrize("variant", FP8_VARIANTS)
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_fp8_integer_exact(oracle_lib, variant, fmt):
+    """Integer inputs: every product and partial sum is exact in fp32, so the
+    result is bit-exact (fp32 and bf16 output)."""
+    for out in (gi.OUT_F32, gi.OUT_BF16):
+        case = gi.make_case("f8_int", 300, 270, 700, alpha=1.0, beta=0.5, out_dtype=out, seed=810 + out,
+                            kind="integer", in_format=fmt)
+        got = run_fp8(case, variant)
+        compare(oracle_lib, case, got, exact=True, what=f"v{variant} {fmt} integer")
+
+
+def test_fp8_padded_leading_dimensions(oracle_lib):
+    case = gi.make_case("f8_pad", 131, 77, 300, alpha=1.0, beta=0.0, out_dtype=gi.OUT_F32, seed=820,
+                        lda=352, ldb=320, ldc=140, in_format="e4m3")
+    compare(oracle_lib, case, run_fp8(case), what="padded")
+
+
+def test_fp8_stream_k(oracle_lib):
+    """Shapes whose plan shares out k-blocks: plain and transposed, repeatable
+    bit for bit."""
+    import tensor_core_matmul_gb300 as tc
+    for n, (M, N, K) in enumerate([(600, 700, 8192), (40, 1000, 16384)]):
+        p = tc.plan(M, N, K, 0, torch.cuda.get_device_properties(0).multi_processor_count, in_kind=1)
+        assert p["stream_k"] == 1, p
+        case = gi.make_case(f"f8_sk{n}", M, N, K, alpha=0.25, beta=0.0, out_dtype=gi.OUT_BF16, seed=830 + n,
+                            in_format="e4m3")
+        got = run_fp8(case)
+        compare(oracle_lib, case, got, what=f"stream-K {case.name}")
+        assert np.array_equal(got, run_fp8(case)), "stream-K FP8 not repeatable"
+
+
+def test_fp8_k_zero(oracle_lib):
+    case = gi.make_case("f8_k0", 70, 90, 0, alpha=1.0, beta=0.75, out_dtype=gi.OUT_F32, seed=840, in_format="e5m2")
+    compare(oracle_lib, case, run_fp8(case), what="K=0")
+
+
+@pytest.mark.parametrize("config,fmt", [("s4k", "e4m3"), ("skinny", "e4m3"), ("edge", "e5m2"), ("s8k", "e4m3")])
+def test_fp8_full_size_sampled(oracle_lib, config, fmt):
+    """The benchmark's workloads with 8-bit operands, in its launch
+    configuration, checked at 2 positions in every 128 x 128 cell of C."""
+    c = gi.CONFIGS[config]
+    case = gi.make_case(config, c["M"], c["N"], c["K"], alpha=c["alpha"], beta=c["beta"], out_dtype=c["out_dtype"],
+                        seed=c["seed"], in_format=fmt)
+    got = run_fp8(case)
+    rows, cols = gi.cell_sample_indices(case.M, case.N, 128, 128, 2, seed=9)
+    compare(oracle_lib, case, got, rows=rows, cols=cols, what=f"{config} {fmt}")
