@@ -11,8 +11,9 @@ the product and layouts from the H100 work log "åœ¨ H100 ä¸Šè¶…è¶Š cuBLASï¼šä¸€ä
 (sections "Simon åšå®¢çš„å¿«é€Ÿå›žé¡¾" and "å®žéªŒè®¾ç½®"), and the alpha/beta update
 from the "DeepGEMM" article, section 1.1; the fused bias + activation
 epilogue from the same article, section 6.1; FP8 inputs (section 6.3) in the
-OCP E4M3 / E5M2 formats (the readings taken where the article is silent are
-listed in ``gemm_oracle.c``'s header).
+OCP E4M3 / E5M2 formats; the per-token int8 quantisation of section 6.2 (the
+readings taken where the article is silent are listed in ``gemm_oracle.c``'s
+header).
 
 Parity pins for this oracle live in ``tests/test_oracle_pins.py``.  The fp32
 accumulation order of the GPU is a hardware choice; it is covered only by the
@@ -84,6 +85,8 @@ class Oracle:
                                                   ctypes.c_int, i64, p, p, p]
         L.oracle_absdot_kind_sampled_f64.argtypes = [i64, i64, i64, p, i64, p, i64, ctypes.c_int, i64, p, p, p]
         L.oracle_absdot_kind_sampled_f64.restype = ctypes.c_int
+        L.oracle_quantize_i8.argtypes = [p, i64, i64, p, ctypes.c_int32, p]
+        L.oracle_quantize_i8_sampled.argtypes = [p, i64, p, p, ctypes.c_int32, p]
         L.oracle_fp8_to_double.argtypes = [ctypes.c_uint8, ctypes.c_int]
         L.oracle_fp8_to_double.restype = ctypes.c_double
         L.oracle_gemm_epi_sampled_f64.restype = ctypes.c_int
@@ -284,6 +287,27 @@ class Oracle:
     def round_out(self, d: np.ndarray, out_dtype: int) -> np.ndarray:
         """out_dtype 0 -> float32 array, 1 -> uint16 bf16 bits."""
         return self.round_f32(d) if out_dtype == 0 else self.round_bf16(d)
+
+    def quantize_i8(self, E: np.ndarray, row_scale: np.ndarray, zero_point: int) -> np.ndarray:
+        """int8 codes of the quantising epilogue from E, an (N, M) array of
+        epilogue values (the layout gemm_f64 returns); row_scale: M fp32."""
+        E = np.ascontiguousarray(E, dtype=np.float64)
+        N, M = E.shape
+        sc = np.ascontiguousarray(row_scale, dtype=np.float32)
+        assert sc.shape[0] >= M
+        Q = np.empty((N, M), dtype=np.int8)
+        self._L.oracle_quantize_i8(self._ptr(E), M, N, self._ptr(sc), int(zero_point), self._ptr(Q))
+        return Q
+
+    def quantize_i8_sampled(self, values: np.ndarray, rows: np.ndarray, row_scale: np.ndarray,
+                            zero_point: int) -> np.ndarray:
+        values = np.ascontiguousarray(values, dtype=np.float64)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        sc = np.ascontiguousarray(row_scale, dtype=np.float32)
+        out = np.empty(values.shape[0], dtype=np.int8)
+        self._L.oracle_quantize_i8_sampled(self._ptr(values), values.shape[0], self._ptr(rows), self._ptr(sc),
+                                           int(zero_point), self._ptr(out))
+        return out
 
     def bf16_to_double(self, bits: int) -> float:
         return self._L.oracle_bf16_to_double(bits)

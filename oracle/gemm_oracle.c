@@ -70,6 +70,17 @@
  * scale factors folded into alpha.  Every FP8 value decodes exactly to double
  * and every product of two is exact in double.
  *
+ * Quantising epilogue (the same article, section 6.2: y = round(x * scale +
+ * zero_point) with one scale per row -- per token -- fused after the GEMM).
+ * Readings taken: x is the epilogue's value E[i,j] above (with beta = 0: the
+ * int8 output is not read); scale[i] is an fp32 value per row i of C; the
+ * zero point is one integer; "round" is to nearest with ties to even; the
+ * result saturates to the int8 range [-128, 127]; NaN gives 0, +-inf
+ * saturate.  The code is an integer decided by floating point, so the oracle
+ * takes that decision in the kernel's precision: E rounded once to fp32, then
+ * q = rne(fmaf(E32, scale[i], zero_point)) with one fp32 rounding of the
+ * fused multiply-add (C99 fmaf), then saturation.
+ *
  * Planted mistakes: when compiled with -DORACLE_MUTANT=n (n > 0) one
  * deliberate error is switched on.  The test suite builds these variants to
  * prove that its pins catch every such error; the normal build has n = 0.
@@ -453,6 +464,47 @@ int oracle_absdot_sampled_f64(int64_t M, int64_t N, int64_t K,
                               int64_t count, const int64_t* rows, const int64_t* cols,
                               double* out) {
     return oracle_absdot_kind_sampled_f64(M, N, K, A, lda, B, ldb, 0, count, rows, cols, out);
+}
+
+/* ---- quantising epilogue (see the header) ----------------------------- */
+
+static int8_t quant_i8(double e, float scale, int32_t zero_point) {
+    const float e32 = (float)e;
+#if ORACLE_MUTANT == 20
+    const float v = fmaf(e32, scale, 0.0f);               /* planted: zero point added after rounding */
+#else
+    const float v = fmaf(e32, scale, (float)zero_point);
+#endif
+    if (isnan(v)) return 0;
+#if ORACLE_MUTANT == 18
+    double r = trunc((double)v);                          /* planted: truncation instead of rounding */
+#else
+    double r = nearbyint((double)v);                      /* ties to even in the default rounding mode */
+#endif
+#if ORACLE_MUTANT == 20
+    r += (double)zero_point;
+#endif
+#if ORACLE_MUTANT == 19
+    return (int8_t)(uint8_t)(int64_t)fmod(r, 256.0);      /* planted: wraps instead of saturating */
+#else
+    if (r > 127.0) r = 127.0;
+    if (r < -128.0) r = -128.0;
+    return (int8_t)r;
+#endif
+}
+
+/* Q (column-major M x N int8, leading dimension M) from E (same layout,
+ * fp64): q[i,j] = quant(E[i,j], row_scale[i], zero_point). */
+void oracle_quantize_i8(const double* E, int64_t M, int64_t N, const float* row_scale, int32_t zero_point,
+                        int8_t* Q) {
+    for (int64_t j = 0; j < N; ++j)
+        for (int64_t i = 0; i < M; ++i) Q[j * M + i] = quant_i8(E[j * M + i], row_scale[i], zero_point);
+}
+
+/* The same at sampled positions: values[s] is E at (rows[s], any column). */
+void oracle_quantize_i8_sampled(const double* values, int64_t count, const int64_t* rows, const float* row_scale,
+                                int32_t zero_point, int8_t* out) {
+    for (int64_t s = 0; s < count; ++s) out[s] = quant_i8(values[s], row_scale[rows[s]], zero_point);
 }
 
 int oracle_mutant_id(void) { return ORACLE_MUTANT; }

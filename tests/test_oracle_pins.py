@@ -18,7 +18,10 @@ The pages print no worked numerical example, so the pins are:
   * for FP8 inputs: the hand-derived code table in
     tests/golden/fp8_encodings.txt, every one of the 256 codes of each format
     against torch's float8 -> float32 conversion, exact integer brute force and
-    numpy's float64 matmul on the decoded values.
+    numpy's float64 matmul on the decoded values,
+  * for the int8 quantising epilogue: the hand-derived table in
+    tests/golden/quant_i8.txt (ties, saturation, zero point before rounding,
+    the fp32 decision) and exact integer brute force through the GEMM.
 
 Each pin is a plain function of an ``Oracle`` so that ``test_planted_mistakes``
 can run the same pins against oracle builds with one deliberate error each
@@ -369,10 +372,55 @@ def pin_fp8_numpy_f64(o):
         assert np.allclose(absd, [G[N - 1, 0], G[0, M - 1]], rtol=1e-12)
 
 
+def pin_quant_table(o):
+    rows = []
+    for line in open(os.path.join(GOLDEN, "quant_i8.txt")):
+        f = line.split("#")[0].split()
+        if f:
+            rows.append((float(f[0]), float(f[1]), int(f[2]), int(f[3])))
+    for x, sc, zp, want in rows:
+        got = int(o.quantize_i8(np.array([[x]]), np.array([sc], dtype=np.float32), zp)[0, 0])
+        assert got == want, (x, sc, zp, got, want)
+
+
+def _rne(q: Fraction) -> int:
+    f = q.numerator // q.denominator
+    r = q - f
+    if r > Fraction(1, 2) or (r == Fraction(1, 2) and f % 2 == 1):
+        f += 1
+    return f
+
+
+def pin_quant_gemm_integer(o):
+    """Integer inputs, power-of-two row scales and an integer bias: every
+    value is exact, so the codes must be the exact rationals rounded half to
+    even and saturated (brute force with Python integers)."""
+    M, N, K = 6, 5, 11
+    case = gi.make_case("qint", M, N, K, alpha=1.0, beta=0.0, out_dtype=gi.OUT_F32, seed=900, kind="integer")
+    scale = np.array([0.5, 0.25, 2.0, 1.0, 0.125, 4.0], dtype=np.float32)
+    bias = np.arange(N + 2, dtype=np.float32) - 3
+    for zp, act in ((0, "none"), (3, "relu"), (-7, "none")):
+        E = o.gemm_epi_f64(M, N, K, _u16(case.A), _u16(case.B), None, 1.0, 0.0, bias=bias, act=act)
+        Q = o.quantize_i8(E, scale, zp)
+        A = _as_int(_u16(case.A)[:, :K])
+        B = _as_int(_u16(case.B)[:, :K])
+        for i in range(M):
+            for j in range(N):
+                e = sum((A[i, k] * B[j, k] for k in range(K)), Fraction(0)) + Fraction(int(bias[j]))
+                if act == "relu":
+                    e = max(e, Fraction(0))
+                want = max(-128, min(127, _rne(e * Fraction(float(scale[i])) + zp)))
+                assert int(Q[j, i]) == want, (zp, act, i, j, int(Q[j, i]), want)
+        rows, cols = gi.sample_indices(M, N, 8, 1)
+        smp = o.quantize_i8_sampled(E[cols, rows], rows, scale, zp)
+        assert np.array_equal(smp, Q[cols, rows])
+
+
 PINS = [pin_integer_bruteforce, pin_numpy_f64, pin_identity_and_permutation, pin_closed_forms,
         pin_bf16_rounding, pin_beta_zero_ignores_c, pin_k_zero, pin_statistics,
         pin_sampled_matches_full, pin_epilogue_integer_bruteforce, pin_activations_library,
-        pin_activation_odd_identity, pin_fp8_codes, pin_fp8_integer_bruteforce, pin_fp8_numpy_f64]
+        pin_activation_odd_identity, pin_fp8_codes, pin_fp8_integer_bruteforce, pin_fp8_numpy_f64,
+        pin_quant_table, pin_quant_gemm_integer]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -398,6 +446,9 @@ MUTANTS = {
     15: "bias added before alpha",
     16: "E4M3 subnormals scaled by 2^-10",
     17: "E5M2 decoded with E4M3's exponent bias",
+    18: "quantisation truncates instead of rounding",
+    19: "quantisation wraps instead of saturating",
+    20: "zero point added after rounding",
 }
 
 
