@@ -49,7 +49,8 @@ extern "C" {
 
 typedef enum {
     TCGEMM_OUT_F32 = 0,
-    TCGEMM_OUT_BF16 = 1
+    TCGEMM_OUT_BF16 = 1,
+    TCGEMM_OUT_I8 = 2    /* int8 codes; only through gemm_quant_i8 */
 } tcgemm_dtype_t;
 
 typedef enum {
@@ -221,6 +222,45 @@ int gemm_fp8(int64_t M, int64_t N, int64_t K,
  * holds 64 bf16 or 128 8-bit values, which changes the plan's k-block count
  * and stream-K choice.  Host only. */
 int tcgemm_plan_kind(int64_t M, int64_t N, int64_t K, int variant, int in_kind, int num_sms, int64_t* out);
+
+/* Operand types of gemm_quant_i8. */
+typedef enum {
+    TCGEMM_IN_BF16 = 0,
+    TCGEMM_IN_E4M3 = 1,
+    TCGEMM_IN_E5M2 = 2
+} tcgemm_in_t;
+
+/* GEMM with the quantising epilogue of the "DeepGEMM" article, section 6.2
+ * (the next layer wants int8 input: y = round(x * scale + zero_point), with
+ * one scale per row -- per token -- done in the GEMM's epilogue instead of a
+ * second pass over the fp32 result):
+ *
+ *   x[i,j] = act( alpha * sum_k A[i,k] B[k,j] + bias[j] )          (fp32)
+ *   Q[i,j] = saturate_int8( rne( fmaf(x[i,j], row_scale[i], zero_point) ) )
+ *
+ * rne rounds to nearest with ties to even; saturation clamps to [-128, 127];
+ * a NaN gives 0.  The article gives the formula and the per-row scale; the
+ * zero point's granularity (one integer), the rounding (ties to even) and the
+ * saturation are this library's readings.
+ *
+ * A, B: in_type (tcgemm_in_t) operands in the layouts of gemm_bf16 / gemm_fp8
+ * (lda, ldb in elements, rows multiples of 16 bytes).
+ * Q: int8, column-major M x N, Q[i,j] at ((int8_t*)Q)[j*ldq + i], ldq >= M and
+ *    a multiple of 16; written only (there is no beta).
+ * bias, bias_dtype, activation: as gemm_bf16_bias_act (TCGEMM_BIAS_NONE and
+ *    TCGEMM_ACT_NONE for none).
+ * row_scale: M fp32 device values, 16-byte aligned, not overlapping Q.
+ * variant: 0 (by shape), TCGEMM_VARIANT_2CTA, _2CTA_W256, _1CTA_N64 or
+ *    _SWAP_N64 (the others -> TCGEMM_ERR_INVALID_ARG).
+ * Errors: an unknown in_type, a NULL row_scale -> TCGEMM_ERR_INVALID_ARG; a
+ * misaligned row_scale -> TCGEMM_ERR_ALIGNMENT; otherwise as gemm_bf16_bias_act. */
+int gemm_quant_i8(int64_t M, int64_t N, int64_t K,
+                  const void* A, int64_t lda,
+                  const void* B, int64_t ldb, int in_type,
+                  void* Q, int64_t ldq, float alpha,
+                  const void* bias, int bias_dtype, int activation,
+                  const float* row_scale, int zero_point,
+                  void* stream, int variant);
 
 /* Size in bytes of gemm_bf16_noalloc's fixed scratch array.  Host only. */
 int64_t tcgemm_noalloc_scratch_bytes(void);

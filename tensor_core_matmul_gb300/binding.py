@@ -19,6 +19,8 @@ from . import _build
 
 OUT_F32 = 0
 OUT_BF16 = 1
+OUT_I8 = 2
+IN_BF16, IN_E4M3, IN_E5M2 = range(3)
 (VARIANT_AUTO, VARIANT_1CTA, VARIANT_2CTA, VARIANT_1CTA_MC, VARIANT_1CTA_N64, VARIANT_2CTA_W256,
  VARIANT_SWAP_N64) = range(7)
 
@@ -66,6 +68,8 @@ def lib() -> ctypes.CDLL:
     L.gemm_bf16_ws.restype = i32
     L.gemm_bf16_bias_act.argtypes = gemm_args[:-1] + [p, i32, i32, p, i32]
     L.gemm_bf16_bias_act.restype = i32
+    L.gemm_quant_i8.argtypes = [i64, i64, i64, p, i64, p, i64, i32, p, i64, f32, p, i32, i32, p, i32, p, i32]
+    L.gemm_quant_i8.restype = i32
     L.gemm_fp8.argtypes = gemm_args[:-1] + [i32, p, i32]
     L.gemm_fp8.restype = i32
     L.tcgemm_plan_kind.argtypes = [i64, i64, i64, i32, i32, i32, ctypes.POINTER(ctypes.c_int64)]
@@ -243,6 +247,54 @@ def gemm_fp8(A, B, C, alpha: float = 1.0, beta: float = 0.0, *, M: Optional[int]
                       float(alpha), float(beta), out, fmts[A.dtype], _stream_ptr(stream), variant)
     _check(st)
     return C
+
+
+def gemm_quant_i8_raw(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int, in_type: int, Q: int, ldq: int,
+                      alpha: float, bias: Optional[int], bias_dtype: int, activation: int, row_scale: Optional[int],
+                      zero_point: int, stream: int, variant: int = 0) -> int:
+    """Pointer-level call of the quantising entry point; returns the status."""
+    return lib().gemm_quant_i8(M, N, K, A, lda, B, ldb, in_type, Q, ldq, alpha, bias, bias_dtype, activation,
+                               row_scale, zero_point, stream, variant)
+
+
+def gemm_quant_i8(A, B, Q, alpha: float = 1.0, *, row_scale, zero_point: int = 0, bias=None, activation="none",
+                  M: Optional[int] = None, N: Optional[int] = None, K: Optional[int] = None, stream=None,
+                  variant: int = 0):
+    """Q = saturate_int8(rne(act(alpha*A*B + bias[j]) * row_scale[i] + zero_point)) on the GPU.
+    A, B: bf16 or float8 (both the same) CUDA tensors in gemm_bf16's storage
+    convention; Q: int8 (N, ldq); row_scale: contiguous fp32 CUDA tensor of
+    at least M values."""
+    import torch
+    kinds = {torch.bfloat16: IN_BF16, torch.float8_e4m3fn: IN_E4M3, torch.float8_e5m2: IN_E5M2}
+    if not (A.is_cuda and B.is_cuda and Q.is_cuda and row_scale.is_cuda):
+        raise ValueError("A, B, Q and row_scale must be CUDA tensors")
+    if A.dtype not in kinds or B.dtype != A.dtype:
+        raise ValueError("A and B must both be bfloat16, float8_e4m3fn or float8_e5m2")
+    if Q.dtype != torch.int8 or row_scale.dtype != torch.float32 or row_scale.dim() != 1:
+        raise ValueError("Q must be int8 and row_scale 1-D float32")
+    for t in (A, B, Q):
+        if t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError("A, B, Q must be 2-D with unit inner stride")
+    M = Q.shape[1] if M is None else M
+    N = Q.shape[0] if N is None else N
+    K = A.shape[1] if K is None else K
+    if Q.shape[0] < N or row_scale.shape[0] < M or (K > 0 and (A.shape[0] < M or B.shape[0] < N)):
+        raise ValueError("tensor shapes smaller than M/N")
+    if bias is None:
+        bptr, bkind = None, BIAS_NONE
+    else:
+        if not bias.is_cuda or bias.dim() != 1 or bias.stride(0) != 1 or bias.shape[0] < N:
+            raise ValueError("bias must be a contiguous 1-D CUDA tensor of at least N values")
+        bkind = BIAS_F32 if bias.dtype == torch.float32 else BIAS_BF16 if bias.dtype == torch.bfloat16 else None
+        if bkind is None:
+            raise ValueError("bias must be float32 or bfloat16")
+        bptr = bias.data_ptr()
+    act = ACTIVATIONS[activation] if isinstance(activation, str) else int(activation)
+    st = gemm_quant_i8_raw(M, N, K, A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0), kinds[A.dtype], Q.data_ptr(),
+                           Q.stride(0), float(alpha), bptr, bkind, act, row_scale.data_ptr(), int(zero_point),
+                           _stream_ptr(stream), variant)
+    _check(st)
+    return Q
 
 
 def check_device_status(stream=None) -> tuple[int, int]:

@@ -131,6 +131,9 @@ struct GemmParams {
     const void* bias;    // one value per column of C (per row of D in the transposed product), or null
     int bias_kind;       // 0 none, 1 fp32, 2 bf16
     int act;             // kAct*
+    // int8 output: code = saturate(rne(fmaf(value, qscale[row of C], qzero))).
+    const float* qscale;
+    float qzero;
     uint64_t timeout_ns;
 };
 
@@ -364,6 +367,17 @@ __device__ __forceinline__ void store_out<__nv_bfloat16>(__nv_bfloat16* p, float
     *p = __float2bfloat16_rn(v);
 }
 
+// int8 output (the quantising epilogue): v already holds value*scale + zero
+// point; round to nearest even (NaN gives 0) and saturate to [-128, 127].
+__device__ __forceinline__ int int8_code(float v) { return max(-128, min(127, __float2int_rn(v))); }
+template <>
+__device__ __forceinline__ float load_out<int8_t>(const int8_t* p) { return static_cast<float>(*p); }
+template <>
+__device__ __forceinline__ void store_out<int8_t>(int8_t* p, float v) { *p = static_cast<int8_t>(int8_code(v)); }
+
+template <typename OutT>
+inline constexpr bool kIsI8 = sizeof(OutT) == 1;
+
 // alpha*acc (+ beta*C) for the 32 columns [col0, col0+32) of one row; `acc`
 // holds fp32 bit patterns.  Columns at or beyond N are skipped.
 template <typename OutT>
@@ -385,10 +399,11 @@ __device__ __forceinline__ void epilogue_store32(OutT* dst, int64_t ldc, int64_t
 
 // The same with the fused epilogue: + bias[column] (the 32 columns' values,
 // already in registers so no load waits behind a store), then the activation.
+// int8 output: then * qs (this row's scale) + the zero point.
 template <typename OutT>
 __device__ __forceinline__ void epilogue_store32_fused(OutT* dst, int64_t ldc, int64_t col0, const GemmParams& p,
                                                        const uint32_t (&acc)[32], const float (&cold)[32],
-                                                       bool has_beta, const float (&bias)[32]) {
+                                                       bool has_beta, const float (&bias)[32], float qs = 1.0f) {
     float v[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
@@ -396,6 +411,10 @@ __device__ __forceinline__ void epilogue_store32_fused(OutT* dst, int64_t ldc, i
                          : p.alpha * __uint_as_float(acc[j])) + bias[j];
     }
     activation_n(v, p.act);
+    if constexpr (kIsI8<OutT>) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = fmaf(v[j], qs, p.qzero);
+    }
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
         if (col0 + j < p.N) store_out<OutT>(dst + j * ldc, v[j]);
@@ -424,15 +443,36 @@ __device__ __forceinline__ void load_cold32(const OutT* dst, int64_t ldc, int64_
 // run starts 64- or 128-byte aligned: C is 16-byte aligned, ldc*sizeof(T) is a
 // multiple of 16 and the run starts at a multiple of 32 rows).
 // With FUSED, every value then gets + bias (the one bias value of this row
-// of D, a column of C) and the activation before it is stored.
+// of D, a column of C) and the activation before it is stored.  int8 output
+// (always FUSED, beta == 0): then * qs32[j] (the scales of these 32 rows of
+// C, 16-byte aligned) + zero point, 32 codes in two 16-byte stores.
 template <typename OutT, bool FUSED = false>
 __device__ __forceinline__ void store_run32(OutT* dst, int64_t valid, const uint32_t (&acc)[32], float alpha,
-                                            float beta, bool has_beta, float bias_v = 0.0f, int act = kActNone) {
+                                            float beta, bool has_beta, float bias_v = 0.0f, int act = kActNone,
+                                            const float* qs32 = nullptr, float zp = 0.0f) {
     float v[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = alpha * __uint_as_float(acc[j]);
     if (valid >= 32) {
-        if constexpr (sizeof(OutT) == 4) {
+        if constexpr (kIsI8<OutT>) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] += bias_v;
+            activation_n(v, act);
+            const float4* s4 = reinterpret_cast<const float4*>(qs32);
+            uint32_t w[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 sc = __ldg(s4 + q);
+                const uint32_t c0 = static_cast<uint8_t>(int8_code(fmaf(v[4 * q], sc.x, zp)));
+                const uint32_t c1 = static_cast<uint8_t>(int8_code(fmaf(v[4 * q + 1], sc.y, zp)));
+                const uint32_t c2 = static_cast<uint8_t>(int8_code(fmaf(v[4 * q + 2], sc.z, zp)));
+                const uint32_t c3 = static_cast<uint8_t>(int8_code(fmaf(v[4 * q + 3], sc.w, zp)));
+                w[q] = c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
+            }
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+            d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        } else if constexpr (sizeof(OutT) == 4) {
             float4* d4 = reinterpret_cast<float4*>(dst);
             if (has_beta) {
 #pragma unroll
@@ -490,6 +530,7 @@ __device__ __forceinline__ void store_run32(OutT* dst, int64_t valid, const uint
                 float x = v[j];
                 if (has_beta) x = fmaf(alpha, __uint_as_float(acc[j]), beta * load_out<OutT>(dst + j));
                 if constexpr (FUSED) x = activation(x + bias_v, act);
+                if constexpr (kIsI8<OutT>) x = fmaf(x, __ldg(qs32 + j), zp);
                 store_out<OutT>(dst + j, x);
             }
         }
@@ -725,7 +766,7 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t row_local = q * 32u + lane;  // 0..127 within this CTA's rows
         OutT* C = static_cast<OutT*>(p.C);
         const bool has_beta = p.beta != 0.0f;
-        const bool fused = has_epilogue(p);
+        const bool fused = kIsI8<OutT> || has_epilogue(p);  // int8 output always takes the fused path
         float* bias_s = reinterpret_cast<float*>(smem + Cfg::kBiasOff);
         // Two staging buffers shared by the four epilogue warps, each one
         // 128-row x 32-column chunk of C with rows fastest (the layout of the
@@ -762,6 +803,10 @@ __global__ void __launch_bounds__(192, 1)
             // barrier of that tile since its last read); transposed product:
             // this thread's row has one value.
             float bias_v = 0.0f;
+            float qs = 1.0f;  // int8 output: this row's scale (plain product)
+            if constexpr (kIsI8<OutT> && !SWAP) {
+                if (row_ok) qs = __ldg(p.qscale + row);
+            }
             if (fused && u.slot < 0) {
                 if constexpr (SWAP) {
                     if (row_ok) bias_v = bias_at(p, row);
@@ -796,7 +841,8 @@ __global__ void __launch_bounds__(192, 1)
                     if (row_ok) {
                         OutT* dst = C + row * p.ldc + col0;
                         if (fused) {
-                            store_run32<OutT, true>(dst, p.N - col0, r, p.alpha, p.beta, has_beta, bias_v, p.act);
+                            store_run32<OutT, true>(dst, p.N - col0, r, p.alpha, p.beta, has_beta, bias_v, p.act,
+                                                    p.qscale + col0, p.qzero);
                         } else {
                             store_run32<OutT>(dst, p.N - col0, r, p.alpha, p.beta, has_beta);
                         }
@@ -821,7 +867,7 @@ __global__ void __launch_bounds__(192, 1)
                             float bj[32];
 #pragma unroll
                             for (int j = 0; j < 32; ++j) bj[j] = bias_s[c + j];
-                            epilogue_store32_fused<OutT>(dst, p.ldc, col0, p, r, cold, has_beta, bj);
+                            epilogue_store32_fused<OutT>(dst, p.ldc, col0, p, r, cold, has_beta, bj, qs);
                         } else {
                             epilogue_store32<OutT>(dst, p.ldc, col0, p.N, r, p.alpha, p.beta, cold, has_beta);
                         }
@@ -906,6 +952,10 @@ __global__ void __launch_bounds__(192, 1)
                             vv[j] = v + bj[j];
                         }
                         activation_n(vv, p.act);
+                        if constexpr (kIsI8<OutT>) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) vv[j] = fmaf(vv[j], qs, p.qzero);
+                        }
 #pragma unroll
                         for (int j = 0; j < 32; ++j) store_out<OutT>(sp + j * 128 + row_local, vv[j]);
                     } else {
@@ -1023,7 +1073,7 @@ __global__ void __launch_bounds__(128)
     const int64_t row = static_cast<int64_t>(tm) * (128 * CTA_GROUP) + rank * 128 + row_local;
     const int64_t col0 = static_cast<int64_t>(tn) * BN + kSkReduceCols * c;
     // The bias is an input, not written by the GEMM: fetch it before waiting.
-    const bool fused = has_epilogue(p);
+    const bool fused = kIsI8<OutT> || has_epilogue(p);
     float bj[32];
     if (fused) {
         if constexpr (SWAP) {
@@ -1070,7 +1120,8 @@ __global__ void __launch_bounds__(128)
     if constexpr (SWAP) {
         OutT* dst = static_cast<OutT*>(p.C) + row * p.ldc + col0;
         if (fused) {
-            store_run32<OutT, true>(dst, p.N - col0, r, p.alpha, p.beta, has_beta, bj[0], p.act);
+            store_run32<OutT, true>(dst, p.N - col0, r, p.alpha, p.beta, has_beta, bj[0], p.act, p.qscale + col0,
+                                    p.qzero);
         } else {
             store_run32<OutT>(dst, p.N - col0, r, p.alpha, p.beta, has_beta);
         }
@@ -1079,7 +1130,8 @@ __global__ void __launch_bounds__(128)
         float cold[32];
         if (has_beta) load_cold32<OutT>(dst, p.ldc, col0, p.N, cold);
         if (fused) {
-            epilogue_store32_fused<OutT>(dst, p.ldc, col0, p, r, cold, has_beta, bj);
+            const float qs = kIsI8<OutT> ? __ldg(p.qscale + row) : 1.0f;
+            epilogue_store32_fused<OutT>(dst, p.ldc, col0, p, r, cold, has_beta, bj, qs);
         } else {
             epilogue_store32<OutT>(dst, p.ldc, col0, p.N, r, p.alpha, p.beta, cold, has_beta);
         }
@@ -1101,6 +1153,7 @@ __global__ void scale_c_kernel(const GemmParams p) {
         OutT* dst = C + j * p.ldc + i;
         float v = p.beta == 0.0f ? 0.0f : p.beta * load_out<OutT>(dst);
         if (fused) v = activation(v + bias_at(p, j), p.act);
+        if constexpr (kIsI8<OutT>) v = fmaf(v, __ldg(p.qscale + i), p.qzero);
         store_out<OutT>(dst, v);
     }
 }

@@ -241,19 +241,22 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pa
 // C (column-major M x N, fp32 or bf16) in 128-row x 32-column boxes, for the
 // epilogue's TMA loads, stores and L2 prefetches.  The stream-K workspace is
 // mapped the same way (fp32, 128 rows, ldc = 128).
-bool encode_c(CUtensorMap* m, void* ptr, int64_t M, int64_t N, int64_t ldc, bool bf16) {
+// out_dtype: TCGEMM_OUT_F32, _BF16 or _I8 (the workspace map uses F32).
+bool encode_c(CUtensorMap* m, void* ptr, int64_t M, int64_t N, int64_t ldc, int out_dtype) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) {
         set_error("cuTensorMapEncodeTiled is not available from the driver");
         return false;
     }
-    const uint64_t esz = bf16 ? 2 : 4;
+    const uint64_t esz = out_dtype == TCGEMM_OUT_F32 ? 4 : out_dtype == TCGEMM_OUT_BF16 ? 2 : 1;
+    const CUtensorMapDataType dt = out_dtype == TCGEMM_OUT_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : out_dtype == TCGEMM_OUT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                                  : CU_TENSOR_MAP_DATA_TYPE_UINT8;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(N)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc) * esz};
     cuuint32_t box[2] = {128u, 32u};
     cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims,
-                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+    CUresult r = fn(m, dt, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         set_error("cuTensorMapEncodeTiled failed (%d) for C %lld x %lld, ldc %lld", static_cast<int>(r),
@@ -437,8 +440,9 @@ int validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
                   static_cast<long long>(N), static_cast<long long>(K));
         return TCGEMM_ERR_INVALID_ARG;
     }
-    if (out_dtype != TCGEMM_OUT_F32 && out_dtype != TCGEMM_OUT_BF16) {
-        set_error("out_dtype must be TCGEMM_OUT_F32 (0) or TCGEMM_OUT_BF16 (1), got %d", out_dtype);
+    if (out_dtype != TCGEMM_OUT_F32 && out_dtype != TCGEMM_OUT_BF16 && out_dtype != TCGEMM_OUT_I8) {
+        set_error("out_dtype must be TCGEMM_OUT_F32 (0), TCGEMM_OUT_BF16 (1) or TCGEMM_OUT_I8 (2), got %d",
+                  out_dtype);
         return TCGEMM_ERR_INVALID_ARG;
     }
     if (lda < std::max<int64_t>(K, 1) || ldb < std::max<int64_t>(K, 1) || ldc < std::max<int64_t>(M, 1)) {
@@ -446,7 +450,7 @@ int validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
         return TCGEMM_ERR_INVALID_ARG;
     }
     if (M == 0 || N == 0) return TCGEMM_OK;
-    const int64_t esz = out_dtype == TCGEMM_OUT_F32 ? 4 : 2;
+    const int64_t esz = out_dtype == TCGEMM_OUT_F32 ? 4 : out_dtype == TCGEMM_OUT_BF16 ? 2 : 1;
     if (C == nullptr || (K > 0 && (A == nullptr || B == nullptr))) {
         set_error("null matrix pointer");
         return TCGEMM_ERR_INVALID_ARG;
@@ -567,6 +571,8 @@ struct Epilogue {
     const void* bias = nullptr;
     int bias_kind = TCGEMM_BIAS_NONE;
     int act = TCGEMM_ACT_NONE;
+    const float* qscale = nullptr;  // int8 output: one scale per row of C
+    int qzero = 0;                  // int8 output: zero point
 };
 
 int validate_epilogue(const Epilogue& ep, int64_t M, int64_t N, const void* C, int64_t ldc, int out_dtype) {
@@ -582,13 +588,28 @@ int validate_epilogue(const Epilogue& ep, int64_t M, int64_t N, const void* C, i
         set_error("bias must be NULL exactly when bias_dtype is TCGEMM_BIAS_NONE");
         return TCGEMM_ERR_INVALID_ARG;
     }
+    if (out_dtype == TCGEMM_OUT_I8) {
+        if (ep.qscale == nullptr) {
+            set_error("int8 output needs the per-row scales (gemm_quant_i8)");
+            return TCGEMM_ERR_INVALID_ARG;
+        }
+        if ((reinterpret_cast<uintptr_t>(ep.qscale) & 15u) != 0) {
+            set_error("row_scale must be 16-byte aligned");
+            return TCGEMM_ERR_ALIGNMENT;
+        }
+        if (M > 0 && N > 0 &&
+            overlaps(C, ((N - 1) * ldc + M), ep.qscale, M * static_cast<int64_t>(sizeof(float)))) {
+            set_error("row_scale overlaps the output");
+            return TCGEMM_ERR_INVALID_ARG;
+        }
+    }
     if (ep.bias_kind == TCGEMM_BIAS_NONE || M == 0 || N == 0) return TCGEMM_OK;
     const int64_t besz = ep.bias_kind == TCGEMM_BIAS_F32 ? 4 : 2;
     if ((reinterpret_cast<uintptr_t>(ep.bias) & static_cast<uintptr_t>(besz - 1)) != 0) {
         set_error("bias must be aligned to its element size (%lld bytes)", static_cast<long long>(besz));
         return TCGEMM_ERR_ALIGNMENT;
     }
-    const int64_t esz = out_dtype == TCGEMM_OUT_F32 ? 4 : 2;
+    const int64_t esz = out_dtype == TCGEMM_OUT_F32 ? 4 : out_dtype == TCGEMM_OUT_BF16 ? 2 : 1;
     if (overlaps(C, ((N - 1) * ldc + M) * esz, ep.bias, N * besz)) {
         set_error("bias overlaps C");
         return TCGEMM_ERR_INVALID_ARG;
@@ -612,6 +633,16 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
         }
         if (variant == TCGEMM_VARIANT_1CTA || variant == TCGEMM_VARIANT_1CTA_MC) {
             set_error("variant %d is not built for FP8 operands", variant);
+            return TCGEMM_ERR_INVALID_ARG;
+        }
+    }
+    if (out_dtype == TCGEMM_OUT_I8) {
+        if (beta != 0.0f) {
+            set_error("int8 output is written only: beta must be 0");
+            return TCGEMM_ERR_INVALID_ARG;
+        }
+        if (variant == TCGEMM_VARIANT_1CTA || variant == TCGEMM_VARIANT_1CTA_MC) {
+            set_error("variant %d is not built for int8 output", variant);
             return TCGEMM_ERR_INVALID_ARG;
         }
     }
@@ -640,8 +671,12 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
         sp.bias = ep.bias;
         sp.bias_kind = ep.bias_kind;
         sp.act = ep.act;
+        sp.qscale = ep.qscale;
+        sp.qzero = static_cast<float>(ep.qzero);
         if (out_dtype == TCGEMM_OUT_F32) {
             tcg::scale_c_kernel<float><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(sp);
+        } else if (out_dtype == TCGEMM_OUT_I8) {
+            tcg::scale_c_kernel<int8_t><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(sp);
         } else {
             tcg::scale_c_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(sp);
         }
@@ -703,10 +738,10 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     }
     pl.ws_ptr = wsp;
     CUtensorMap tcm, twm;
-    if (!encode_c(&tcm, C, M, N, ldc, out_dtype == TCGEMM_OUT_BF16)) return TCGEMM_ERR_INVALID_ARG;
+    if (!encode_c(&tcm, C, M, N, ldc, out_dtype)) return TCGEMM_ERR_INVALID_ARG;
     if (pl.sk_tiles > 0) {
         const int64_t wcols = 2 * static_cast<int64_t>(pl.grid / pl.cta_group) * pl.cta_group * pl.bn;
-        if (!encode_c(&twm, wsp, 128, wcols, 128, false))
+        if (!encode_c(&twm, wsp, 128, wcols, 128, TCGEMM_OUT_F32))
             return TCGEMM_ERR_INVALID_ARG;
     } else {
         twm = tcm;
@@ -729,12 +764,29 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     gp.bias_kind = ep.bias_kind;
     gp.act = ep.act;
     gp.in_fmt = in_fmt;
+    gp.qscale = ep.qscale;
+    gp.qzero = static_cast<float>(ep.qzero);
     gp.tiles_dp = pl.tiles_dp;
     gp.sk_tiles = pl.sk_tiles;
     gp.sk_iters = pl.sk_iters;
     gp.timeout_ns = timeout_ns();
 
     const bool bf16 = out_dtype == TCGEMM_OUT_BF16;
+    if (out_dtype == TCGEMM_OUT_I8) {
+        // The quantising epilogue: CTA-pair tiles, narrow tiles, the
+        // transposed product; bf16 or 8-bit operands.
+#define TCGEMM_LAUNCH_I8(CG, BN, ST, MC, AR, SW)                                                             \
+    return in_kind == 1 ? launch_gemm<CG, BN, ST, MC, AR, SW, int8_t, 1>(pl, ta, tb, tcm, twm, gp, stream, dev) \
+                        : launch_gemm<CG, BN, ST, MC, AR, SW, int8_t, 0>(pl, ta, tb, tcm, twm, gp, stream, dev)
+        if (pl.swap) TCGEMM_LAUNCH_I8(1, 64, kStagesN64, 1, 128, true);
+        if (pl.bn == 64 && pl.arows == 64) TCGEMM_LAUNCH_I8(1, 64, kStagesN64h, 1, 64, false);
+        if (pl.bn == 64) TCGEMM_LAUNCH_I8(1, 64, kStagesN64, 1, 128, false);
+        if (pl.cta_group == 2 && pl.bn == 224) TCGEMM_LAUNCH_I8(2, 224, kStages2n, 1, 128, false);
+        if (pl.cta_group == 2) TCGEMM_LAUNCH_I8(2, 256, kStages2, 1, 128, false);
+#undef TCGEMM_LAUNCH_I8
+        set_error("no int8-output kernel for this plan");
+        return TCGEMM_ERR_INVALID_ARG;
+    }
     if (in_kind == 1) {
         // 8-bit operands: the CTA-pair tiles, the narrow tiles and the
         // transposed product.
@@ -804,6 +856,26 @@ int gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
              int64_t ldc, float alpha, float beta, int out_dtype, int in_format, void* stream, int variant) {
     return run_gemm(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, stream, variant, kWsInternal, nullptr, 0,
                     Epilogue(), 1, in_format);
+}
+
+int gemm_quant_i8(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                  int in_type, void* Q, int64_t ldq, float alpha, const void* bias, int bias_dtype, int activation,
+                  const float* row_scale, int zero_point, void* stream, int variant) {
+    if (in_type < TCGEMM_IN_BF16 || in_type > TCGEMM_IN_E5M2) {
+        t_last_error[0] = '\0';
+        set_error("unknown operand type %d", in_type);
+        return TCGEMM_ERR_INVALID_ARG;
+    }
+    Epilogue ep;
+    ep.bias = bias;
+    ep.bias_kind = bias_dtype;
+    ep.act = activation;
+    ep.qscale = row_scale;
+    ep.qzero = zero_point;
+    const int in_kind = in_type == TCGEMM_IN_BF16 ? 0 : 1;
+    const int in_fmt = in_type == TCGEMM_IN_E5M2 ? TCGEMM_FP8_E5M2 : TCGEMM_FP8_E4M3;
+    return run_gemm(M, N, K, A, lda, B, ldb, Q, ldq, alpha, 0.0f, TCGEMM_OUT_I8, stream, variant, kWsInternal, nullptr,
+                    0, ep, in_kind, in_fmt);
 }
 
 int64_t tcgemm_noalloc_scratch_bytes(void) { return static_cast<int64_t>(kNoAllocScratchBytes); }

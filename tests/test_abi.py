@@ -95,6 +95,24 @@ def test_fp8_argument_errors(tc, args, fmt, variant, status):
     assert st == status, (st, tc.binding.last_error())
 
 
+@pytest.mark.parametrize("in_type,scale,variant,status", [
+    (3, FAKE * 16, 0, 1),          # unknown operand type
+    (0, None, 0, 1),               # no row scales
+    (1, FAKE * 16 + 4, 0, 2),      # row scales not 16-byte aligned
+    (0, FAKE * 16, 1, 1),          # variant not built for int8 output
+    (2, FAKE * 4, 0, 1),           # row scales overlap Q (Q at FAKE*4, 16 x 8 int8)
+])
+def test_quant_argument_errors(tc, in_type, scale, variant, status):
+    st = tc.binding.gemm_quant_i8_raw(16, 8, 16, FAKE, 16, FAKE * 2, 16, in_type, FAKE * 4, 16, 1.0, None, 0, 0,
+                                      scale, 0, 0, variant)
+    assert st == status, (st, tc.binding.last_error())
+
+
+def test_int8_output_needs_the_quantising_entry_point(tc):
+    assert tc.gemm_bf16_raw(16, 8, 16, FAKE, 16, FAKE * 2, 16, FAKE * 4, 16, 1.0, 0.0, 2, 0) == 1
+    assert "scale" in tc.binding.last_error()
+
+
 @pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (64, 8192, 8192), (600, 700, 8192), (600, 700, 4096)])
 def test_fp8_plans_count_128_value_k_blocks(tc, M, N, K):
     p8 = tc.plan(M, N, K, 0, 152, in_kind=1)
