@@ -189,19 +189,29 @@ def run_ours(args) -> None:
     M, N, K = case.M, case.N, case.K
     A = case.A.to(dev)
     B = case.B.to(dev)
-    C = (case.C_in.to(dev) if case.C_in is not None
-         else torch.zeros((N, case.ldc), dtype=case.out_torch_dtype(), device=dev))
+    if args.quant:
+        # int8 output of the quantising epilogue: written only, beta = 0.
+        if case.beta != 0.0:
+            raise SystemExit("--quant needs a workload with beta = 0")
+        C = torch.zeros((N, (M + 15) // 16 * 16), dtype=torch.int8, device=dev)
+        row_scale = (torch.rand(M, generator=torch.Generator().manual_seed(9002)) * 60 + 4).to(dev)
+    else:
+        C = (case.C_in.to(dev) if case.C_in is not None
+             else torch.zeros((N, case.ldc), dtype=case.out_torch_dtype(), device=dev))
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     bias_cpu = make_bias(args, N)
     act = EPILOGUES[args.epilogue][1]
     bias = None if bias_cpu is None else bias_cpu.to(dev)
 
-    if args.in_format != "bf16" and args.epilogue != "none":
-        raise SystemExit("--epilogue is built for bf16 operands only")
+    if args.in_format != "bf16" and args.epilogue != "none" and not args.quant:
+        raise SystemExit("--epilogue with 8-bit operands needs --quant")
 
     def gemm():
-        if args.in_format != "bf16":
+        if args.quant:
+            tc.gemm_quant_i8(A, B, C, case.alpha, row_scale=row_scale, zero_point=0, bias=bias, activation=act, M=M,
+                             N=N, K=K, stream=stream, variant=args.variant)
+        elif args.in_format != "bf16":
             tc.gemm_fp8(A, B, C, case.alpha, case.beta, M=M, N=N, K=K, stream=stream, variant=args.variant)
         elif args.epilogue == "none":
             tc.gemm_bf16(A, B, C, case.alpha, case.beta, M=M, N=N, K=K, stream=stream, variant=args.variant)
@@ -250,17 +260,17 @@ def run_ours(args) -> None:
 
     peaks, peak_src = load_peaks()
     tag = (f"gemm_{args.config}_full" + ("" if args.epilogue == "none" else f"_{args.epilogue}")
-           + ("" if args.in_format == "bf16" else f"_{args.in_format}"))
+           + ("" if args.in_format == "bf16" else f"_{args.in_format}") + ("_quant" if args.quant else ""))
     traffic = profile_traffic(tag)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     variant = args.variant or tc.pick_variant(M, N, K, sms)
     plan = tc.plan(M, N, K, variant, sms, in_kind=0 if args.in_format == "bf16" else 1)
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.quant:
         e2e = measure_e2e(args, case, dev, stream, bias_cpu, act)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quant:
         cpu = cpu_baseline(case, target_s=args.cpu_seconds, bias=bias_cpu, act=act)
 
     if rank == 0:
@@ -286,13 +296,15 @@ def run_ours(args) -> None:
                 "M": M, "N": N, "K": K,
                 "epilogue": args.epilogue,
                 "in_format": args.in_format,
+                "output": "int8 (per-row quantisation)" if args.quant else ("bf16" if case.out_dtype else "fp32"),
                 "l2": f"flushed between timed steps ({FLUSH_BYTES >> 20} MiB write, untimed)",
                 "kernel": {"variant": {1: "1cta", 2: "2cta"}.get(variant, str(variant)), **plan},
                 "parallelism": f"independent problem per GPU x{world}",
                 "wall_s_timed_loop": round(wall, 3),
             },
             "roofline": roofline(case, total_s / args.steps, peaks, peak_src, traffic,
-                                 extra_bytes=0 if bias_cpu is None else 4 * N),
+                                 extra_bytes=(0 if bias_cpu is None else 4 * N)
+                                 + (4 * M - M * N * (4 if case.out_dtype == 0 else 2) + M * N if args.quant else 0)),
             "clocks": clocks,
             "e2e": e2e,
             "gpu_launches": int(launches),
@@ -525,6 +537,8 @@ def main():
                     help="operand type: bf16 (gemm_bf16) or 8-bit floats (gemm_fp8)")
     ap.add_argument("--epilogue", default="none", choices=sorted(EPILOGUES),
                     help="fused epilogue: bias and/or activation (gemm_bf16_bias_act)")
+    ap.add_argument("--quant", action="store_true",
+                    help="int8 output through the per-row quantising epilogue (gemm_quant_i8)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
