@@ -65,6 +65,8 @@ class GemmCase:
     B: torch.Tensor  # (N, ldb) bf16 or FP8, host
     C_in: Optional[torch.Tensor]  # (N, ldc) out dtype, host; None when beta == 0
     in_format: str = "bf16"  # "bf16", "e4m3" or "e5m2" (A and B)
+    a_col: bool = False  # A stored column-major: A is (K, lda), A[i, k] = A[k, i]
+    b_row: bool = False  # B stored row-major: B is (K, ldb), B[k, j] = B[k, j]
 
     @property
     def flops(self) -> int:
@@ -142,6 +144,33 @@ def integer_fp8(rows: int, cols: int, seed: int, fmt: str, lo: int = -4, hi: int
     ld = cols if ld is None else ld
     vals = torch.randint(lo, hi + 1, (rows, cols), generator=_gen(seed), dtype=torch.int32)
     return _fp8(vals.to(torch.float32), rows, cols, fmt, ld)
+
+
+def relayout(case: GemmCase, a_col: bool, b_row: bool, lda: Optional[int] = None,
+             ldb: Optional[int] = None) -> GemmCase:
+    """The same logical A and B stored in another layout (column-major A as
+    (K, lda) with lda >= M; row-major B as (K, ldb) with ldb >= N); padding
+    holds the NaN sentinel.  Only bf16 operands."""
+    assert case.in_format == "bf16" and not case.a_col and not case.b_row
+    M, N, K = case.M, case.N, case.K
+    A, B = case.A[:, :K], case.B[:, :K]
+    if a_col:
+        lda = round_up(max(M, 1), 8) if lda is None else lda
+        At = torch.empty((K, lda), dtype=torch.bfloat16)
+        At.view(torch.int16)[:] = PAD_BF16_BITS
+        At[:, :M] = A.t()
+        A, la = At, lda
+    else:
+        A, la = case.A, case.lda
+    if b_row:
+        ldb = round_up(max(N, 1), 8) if ldb is None else ldb
+        Bt = torch.empty((K, ldb), dtype=torch.bfloat16)
+        Bt.view(torch.int16)[:] = PAD_BF16_BITS
+        Bt[:, :N] = B.t()
+        B, lb = Bt, ldb
+    else:
+        B, lb = case.B, case.ldb
+    return dataclasses.replace(case, A=A, B=B, lda=la, ldb=lb, a_col=a_col, b_row=b_row)
 
 
 def as_u8(t: torch.Tensor) -> np.ndarray:

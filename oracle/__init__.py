@@ -85,6 +85,13 @@ class Oracle:
                                                   ctypes.c_int, i64, p, p, p]
         L.oracle_absdot_kind_sampled_f64.argtypes = [i64, i64, i64, p, i64, p, i64, ctypes.c_int, i64, p, p, p]
         L.oracle_absdot_kind_sampled_f64.restype = ctypes.c_int
+        L.oracle_gemm_layout_f64.argtypes = [i64, i64, i64, p, i64, ctypes.c_int, p, i64, ctypes.c_int, p, i64,
+                                             ctypes.c_int, ctypes.c_float, ctypes.c_float, p, ctypes.c_int]
+        L.oracle_gemm_layout_f64.restype = ctypes.c_int
+        L.oracle_gemm_layout_sampled_f64.argtypes = [i64, i64, i64, p, i64, ctypes.c_int, p, i64, ctypes.c_int, p,
+                                                     i64, ctypes.c_int, ctypes.c_float, ctypes.c_float, i64, p, p, p,
+                                                     ctypes.c_int]
+        L.oracle_gemm_layout_sampled_f64.restype = ctypes.c_int
         L.oracle_quantize_i8.argtypes = [p, i64, i64, p, ctypes.c_int32, p]
         L.oracle_quantize_i8_sampled.argtypes = [p, i64, p, p, ctypes.c_int32, p]
         L.oracle_fp8_to_double.argtypes = [ctypes.c_uint8, ctypes.c_int]
@@ -287,6 +294,41 @@ class Oracle:
     def round_out(self, d: np.ndarray, out_dtype: int) -> np.ndarray:
         """out_dtype 0 -> float32 array, 1 -> uint16 bf16 bits."""
         return self.round_f32(d) if out_dtype == 0 else self.round_bf16(d)
+
+    def gemm_layout_f64(self, M: int, N: int, K: int, A: np.ndarray, B: np.ndarray, a_col: bool, b_row: bool,
+                        C_in: Optional[np.ndarray] = None, alpha: float = 1.0, beta: float = 0.0,
+                        threads: int = 0) -> np.ndarray:
+        """D for bf16 operands in any layout: A is (M, lda) row-major or, with
+        a_col, (K, lda) column-major; B is (N, ldb) column-major or, with
+        b_row, (K, ldb) row-major.  Returns D as an (N, M) array."""
+        A = np.ascontiguousarray(A, dtype=np.uint16)
+        B = np.ascontiguousarray(B, dtype=np.uint16)
+        cin, ldc, cin_bf16 = self._cin(C_in, beta)
+        D = np.empty((N, M), dtype=np.float64)
+        rc = self._L.oracle_gemm_layout_f64(M, N, K, self._ptr(A), A.shape[1], int(a_col), self._ptr(B), B.shape[1],
+                                            int(b_row), self._ptr(cin), max(ldc, M), cin_bf16, float(alpha),
+                                            float(beta), self._ptr(D), int(threads))
+        if rc != 0:
+            raise ValueError("oracle_gemm_layout_f64: bad arguments")
+        return D
+
+    def gemm_layout_sampled_f64(self, M: int, N: int, K: int, A: np.ndarray, B: np.ndarray, a_col: bool,
+                                b_row: bool, rows: np.ndarray, cols: np.ndarray, C_in: Optional[np.ndarray] = None,
+                                alpha: float = 1.0, beta: float = 0.0, absolute: bool = False) -> np.ndarray:
+        """D (or, with absolute, G = sum |a*b|) at the given positions."""
+        A = np.ascontiguousarray(A, dtype=np.uint16)
+        B = np.ascontiguousarray(B, dtype=np.uint16)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        cols = np.ascontiguousarray(cols, dtype=np.int64)
+        cin, ldc, cin_bf16 = self._cin(C_in, beta)
+        out = np.empty(rows.shape[0], dtype=np.float64)
+        rc = self._L.oracle_gemm_layout_sampled_f64(M, N, K, self._ptr(A), A.shape[1], int(a_col), self._ptr(B),
+                                                    B.shape[1], int(b_row), self._ptr(cin), max(ldc, M), cin_bf16,
+                                                    float(alpha), float(beta), rows.shape[0], self._ptr(rows),
+                                                    self._ptr(cols), self._ptr(out), int(absolute))
+        if rc != 0:
+            raise ValueError("oracle_gemm_layout_sampled_f64: bad arguments")
+        return out
 
     def quantize_i8(self, E: np.ndarray, row_scale: np.ndarray, zero_point: int) -> np.ndarray:
         """int8 codes of the quantising epilogue from E, an (N, M) array of

@@ -70,6 +70,12 @@
  * scale factors folded into alpha.  Every FP8 value decodes exactly to double
  * and every product of two is exact in double.
  *
+ * Other operand layouts (the work log fixes A row-major and B column-major in
+ * "实验设置"; the other three combinations are the same product with an
+ * operand stored transposed): A column-major puts A[i,k] at A[k*lda + i]
+ * (lda >= M), B row-major puts B[k,j] at B[k*ldb + j] (ldb >= N).  C stays
+ * column-major.
+ *
  * Quantising epilogue (the same article, section 6.2: y = round(x * scale +
  * zero_point) with one scale per row -- per token -- fused after the GEMM).
  * Readings taken: x is the epilogue's value E[i,j] above (with beta = 0: the
@@ -156,6 +162,7 @@ typedef struct {
     const void* A; int64_t lda;
     const void* B; int64_t ldb;
     int in_kind;        /* 0 bf16, 1 FP8 E4M3, 2 FP8 E5M2 (both operands) */
+    int a_col, b_row;   /* 1: A column-major (A[k*lda + i]); 1: B row-major (B[k*ldb + j]) */
     const void* Cin; int64_t ldc; int cin_bf16; /* C_in dtype: 0 fp32, 1 bf16 */
     double alpha, beta;
     int absolute;       /* 1: sum |A[i,k]*B[k,j]| instead (error model, no alpha/beta) */
@@ -278,13 +285,15 @@ static double element(const problem_t* p, int64_t i, int64_t j) {
     for (int64_t k = 0; k < kend; ++k) {
 #if ORACLE_MUTANT == 1
         double a = a_at(p, k * p->M + i);                /* planted: A as column-major */
+#elif ORACLE_MUTANT == 21
+        double a = a_at(p, p->a_col ? i * p->lda + k : i * p->lda + k);  /* planted: column-major A ignored */
 #else
-        double a = a_at(p, i * p->lda + k);
+        double a = a_at(p, p->a_col ? k * p->lda + i : i * p->lda + k);
 #endif
 #if ORACLE_MUTANT == 2
         double b = b_at(p, k * p->N + j);                /* planted: B as row-major */
 #else
-        double b = b_at(p, j * p->ldb + k);
+        double b = b_at(p, p->b_row ? k * p->ldb + j : j * p->ldb + k);
 #endif
         s += p->absolute ? fabs(a * b) : a * b;
     }
@@ -382,7 +391,7 @@ int oracle_gemm_epi_f64(int64_t M, int64_t N, int64_t K,
     if (beta != 0.0f && Cin == NULL) return -1;
     if (bias_kind < 0 || bias_kind > 2 || (bias_kind != 0 && bias == NULL) || act < 0 || act > 3) return -1;
     if (in_kind < 0 || in_kind > 2) return -1;
-    problem_t p = {M, N, K, A, lda, B, ldb, in_kind, Cin, ldc, cin_bf16, (double)alpha, (double)beta, 0,
+    problem_t p = {M, N, K, A, lda, B, ldb, in_kind, 0, 0, Cin, ldc, cin_bf16, (double)alpha, (double)beta, 0,
                    bias, bias_kind, act};
     return run_full(&p, D, nthreads);
 }
@@ -433,7 +442,7 @@ int oracle_gemm_epi_sampled_f64(int64_t M, int64_t N, int64_t K,
     if (beta != 0.0f && Cin == NULL) return -1;
     if (bias_kind < 0 || bias_kind > 2 || (bias_kind != 0 && bias == NULL) || act < 0 || act > 3) return -1;
     if (in_kind < 0 || in_kind > 2) return -1;
-    problem_t p = {M, N, K, A, lda, B, ldb, in_kind, Cin, ldc, cin_bf16, (double)alpha, (double)beta, 0,
+    problem_t p = {M, N, K, A, lda, B, ldb, in_kind, 0, 0, Cin, ldc, cin_bf16, (double)alpha, (double)beta, 0,
                    bias, bias_kind, act};
     for (int64_t s = 0; s < count; ++s) {
         if (rows[s] < 0 || rows[s] >= M || cols[s] < 0 || cols[s] >= N) return -1;
@@ -451,7 +460,7 @@ int oracle_absdot_kind_sampled_f64(int64_t M, int64_t N, int64_t K,
                                    int64_t count, const int64_t* rows, const int64_t* cols,
                                    double* out) {
     if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || in_kind < 0 || in_kind > 2) return -1;
-    problem_t p = {M, N, K, A, lda, B, ldb, in_kind, NULL, M, 0, 1.0, 0.0, 1, NULL, 0, 0};
+    problem_t p = {M, N, K, A, lda, B, ldb, in_kind, 0, 0, NULL, M, 0, 1.0, 0.0, 1, NULL, 0, 0};
     for (int64_t s = 0; s < count; ++s) {
         if (rows[s] < 0 || rows[s] >= M || cols[s] < 0 || cols[s] >= N) return -1;
         out[s] = element(&p, rows[s], cols[s]);
@@ -505,6 +514,36 @@ void oracle_quantize_i8(const double* E, int64_t M, int64_t N, const float* row_
 void oracle_quantize_i8_sampled(const double* values, int64_t count, const int64_t* rows, const float* row_scale,
                                 int32_t zero_point, int8_t* out) {
     for (int64_t s = 0; s < count; ++s) out[s] = quant_i8(values[s], row_scale[rows[s]], zero_point);
+}
+
+/* D = alpha*A*B + beta*C_in in fp64 for bf16 operands in any of the four
+ * layouts: a_col = 1 for column-major A (lda >= M), b_row = 1 for row-major
+ * B (ldb >= N).  D as in oracle_gemm_f64. */
+int oracle_gemm_layout_f64(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, int a_col,
+                           const uint16_t* B, int64_t ldb, int b_row, const void* Cin, int64_t ldc, int cin_bf16,
+                           float alpha, float beta, double* D, int nthreads) {
+    if (M < 0 || N < 0 || K < 0 || ldc < M) return -1;
+    if (lda < (a_col ? M : K) || ldb < (b_row ? N : K)) return -1;
+    if (beta != 0.0f && Cin == NULL) return -1;
+    problem_t p = {M, N, K, A, lda, B, ldb, 0, a_col != 0, b_row != 0, Cin, ldc, cin_bf16, (double)alpha,
+                   (double)beta, 0, NULL, 0, 0};
+    return run_full(&p, D, nthreads);
+}
+
+int oracle_gemm_layout_sampled_f64(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, int a_col,
+                                   const uint16_t* B, int64_t ldb, int b_row, const void* Cin, int64_t ldc,
+                                   int cin_bf16, float alpha, float beta, int64_t count, const int64_t* rows,
+                                   const int64_t* cols, double* out, int absolute) {
+    if (M < 0 || N < 0 || K < 0 || ldc < M) return -1;
+    if (lda < (a_col ? M : K) || ldb < (b_row ? N : K)) return -1;
+    if (!absolute && beta != 0.0f && Cin == NULL) return -1;
+    problem_t p = {M, N, K, A, lda, B, ldb, 0, a_col != 0, b_row != 0, absolute ? NULL : Cin, ldc, cin_bf16,
+                   absolute ? 1.0 : (double)alpha, absolute ? 0.0 : (double)beta, absolute != 0, NULL, 0, 0};
+    for (int64_t s = 0; s < count; ++s) {
+        if (rows[s] < 0 || rows[s] >= M || cols[s] < 0 || cols[s] >= N) return -1;
+        out[s] = element(&p, rows[s], cols[s]);
+    }
+    return 0;
 }
 
 int oracle_mutant_id(void) { return ORACLE_MUTANT; }

@@ -21,7 +21,9 @@ The pages print no worked numerical example, so the pins are:
     numpy's float64 matmul on the decoded values,
   * for the int8 quantising epilogue: the hand-derived table in
     tests/golden/quant_i8.txt (ties, saturation, zero point before rounding,
-    the fp32 decision) and exact integer brute force through the GEMM.
+    the fp32 decision) and exact integer brute force through the GEMM,
+  * for the other operand layouts: the same logical matrices stored
+    transposed give bit-identical D, and integer brute force in each layout.
 
 Each pin is a plain function of an ``Oracle`` so that ``test_planted_mistakes``
 can run the same pins against oracle builds with one deliberate error each
@@ -416,11 +418,38 @@ def pin_quant_gemm_integer(o):
         assert np.array_equal(smp, Q[cols, rows])
 
 
+def pin_layouts(o):
+    """The four operand layouts: the same logical matrices stored the other
+    way give the identical D (same terms, same order), and an integer case in
+    each layout equals exact brute force over the logical matrices."""
+    case = gi.make_case("lay", 13, 9, 21, alpha=1.5, beta=0.5, out_dtype=gi.OUT_F32, seed=950)
+    D0 = o.gemm_f64(case.M, case.N, case.K, _u16(case.A), _u16(case.B), _cin_np(case), case.alpha, case.beta)
+    icase = gi.make_case("layi", 7, 5, 10, alpha=2.0, beta=0.0, out_dtype=gi.OUT_F32, seed=951, kind="integer")
+    A = _as_int(_u16(icase.A)[:, :icase.K])
+    B = _as_int(_u16(icase.B)[:, :icase.K])
+    for a_col in (False, True):
+        for b_row in (False, True):
+            r = gi.relayout(case, a_col, b_row, lda=case.M + 3 if a_col else None, ldb=case.N + 7 if b_row else None)
+            D = o.gemm_layout_f64(case.M, case.N, case.K, _u16(r.A), _u16(r.B), a_col, b_row, _cin_np(case),
+                                  case.alpha, case.beta)
+            assert np.array_equal(D, D0), (a_col, b_row)
+            rows, cols = gi.sample_indices(case.M, case.N, 10, 2)
+            smp = o.gemm_layout_sampled_f64(case.M, case.N, case.K, _u16(r.A), _u16(r.B), a_col, b_row, rows, cols,
+                                            _cin_np(case), case.alpha, case.beta)
+            assert np.array_equal(smp, D0[cols, rows])
+            ri = gi.relayout(icase, a_col, b_row)
+            Di = o.gemm_layout_f64(icase.M, icase.N, icase.K, _u16(ri.A), _u16(ri.B), a_col, b_row, None, 2.0, 0.0)
+            for i in range(icase.M):
+                for j in range(icase.N):
+                    want = 2 * sum((A[i, k] * B[j, k] for k in range(icase.K)), Fraction(0))
+                    assert Di[j, i] == float(want), (a_col, b_row, i, j)
+
+
 PINS = [pin_integer_bruteforce, pin_numpy_f64, pin_identity_and_permutation, pin_closed_forms,
         pin_bf16_rounding, pin_beta_zero_ignores_c, pin_k_zero, pin_statistics,
         pin_sampled_matches_full, pin_epilogue_integer_bruteforce, pin_activations_library,
         pin_activation_odd_identity, pin_fp8_codes, pin_fp8_integer_bruteforce, pin_fp8_numpy_f64,
-        pin_quant_table, pin_quant_gemm_integer]
+        pin_quant_table, pin_quant_gemm_integer, pin_layouts]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -449,6 +478,7 @@ MUTANTS = {
     18: "quantisation truncates instead of rounding",
     19: "quantisation wraps instead of saturating",
     20: "zero point added after rounding",
+    21: "column-major A read as row-major",
 }
 
 
