@@ -262,6 +262,31 @@ int gemm_quant_i8(int64_t M, int64_t N, int64_t K,
                   const float* row_scale, int zero_point,
                   void* stream, int variant);
 
+/* Storage order of an operand (gemm_bf16_layout). */
+typedef enum {
+    TCGEMM_ROW_MAJOR = 0,
+    TCGEMM_COL_MAJOR = 1
+} tcgemm_layout_t;
+
+/* The bf16 GEMM with each operand in either storage order (the work log's
+ * layout, "实验设置", is A row-major and B column-major; the other three are
+ * the same product with an operand stored transposed):
+ *   A row-major:    A[i,k] at A[i*lda + k], lda >= K   (K contiguous)
+ *   A column-major: A[i,k] at A[k*lda + i], lda >= M   (M contiguous)
+ *   B column-major: B[k,j] at B[j*ldb + k], ldb >= K   (K contiguous)
+ *   B row-major:    B[k,j] at B[k*ldb + j], ldb >= N   (N contiguous)
+ * C is column-major as in gemm_bf16.  An operand with its M or N index
+ * contiguous is loaded by TMA in 64 x 64 boxes and read by the tensor cores
+ * as an MN-major operand (the transpose bits of the MMA's instruction
+ * descriptor); nothing is transposed in memory.  Variants as
+ * gemm_bf16_variant except TCGEMM_VARIANT_1CTA_MC (-> TCGEMM_ERR_INVALID_ARG,
+ * as is an unknown layout).  Other rules and errors as gemm_bf16_variant. */
+int gemm_bf16_layout(int64_t M, int64_t N, int64_t K,
+                     const void* A, int64_t lda, int a_layout,
+                     const void* B, int64_t ldb, int b_layout,
+                     void* C, int64_t ldc,
+                     float alpha, float beta, int out_dtype, void* stream, int variant);
+
 /* Size in bytes of gemm_bf16_noalloc's fixed scratch array.  Host only. */
 int64_t tcgemm_noalloc_scratch_bytes(void);
 

@@ -21,6 +21,7 @@ OUT_F32 = 0
 OUT_BF16 = 1
 OUT_I8 = 2
 IN_BF16, IN_E4M3, IN_E5M2 = range(3)
+ROW_MAJOR, COL_MAJOR = range(2)
 (VARIANT_AUTO, VARIANT_1CTA, VARIANT_2CTA, VARIANT_1CTA_MC, VARIANT_1CTA_N64, VARIANT_2CTA_W256,
  VARIANT_SWAP_N64) = range(7)
 
@@ -70,6 +71,8 @@ def lib() -> ctypes.CDLL:
     L.gemm_bf16_bias_act.restype = i32
     L.gemm_quant_i8.argtypes = [i64, i64, i64, p, i64, p, i64, i32, p, i64, f32, p, i32, i32, p, i32, p, i32]
     L.gemm_quant_i8.restype = i32
+    L.gemm_bf16_layout.argtypes = [i64, i64, i64, p, i64, i32, p, i64, i32, p, i64, f32, f32, i32, p, i32]
+    L.gemm_bf16_layout.restype = i32
     L.gemm_fp8.argtypes = gemm_args[:-1] + [i32, p, i32]
     L.gemm_fp8.restype = i32
     L.tcgemm_plan_kind.argtypes = [i64, i64, i64, i32, i32, i32, ctypes.POINTER(ctypes.c_int64)]
@@ -295,6 +298,41 @@ def gemm_quant_i8(A, B, Q, alpha: float = 1.0, *, row_scale, zero_point: int = 0
                            _stream_ptr(stream), variant)
     _check(st)
     return Q
+
+
+def gemm_bf16_layout_raw(M: int, N: int, K: int, A: int, lda: int, a_layout: int, B: int, ldb: int, b_layout: int,
+                         C: int, ldc: int, alpha: float, beta: float, out_dtype: int, stream: int,
+                         variant: int = 0) -> int:
+    """Pointer-level call of the any-layout entry point; returns the status."""
+    return lib().gemm_bf16_layout(M, N, K, A, lda, a_layout, B, ldb, b_layout, C, ldc, alpha, beta, out_dtype,
+                                  stream, variant)
+
+
+def gemm_bf16_layout(A, B, C, alpha: float = 1.0, beta: float = 0.0, *, a_col: bool = False, b_row: bool = False,
+                     M: Optional[int] = None, N: Optional[int] = None, K: Optional[int] = None, stream=None,
+                     variant: int = 0):
+    """C = alpha * A * B + beta * C with A row-major (M, lda) or, with a_col,
+    column-major (K, lda); B column-major (N, ldb) or, with b_row, row-major
+    (K, ldb).  C as in gemm_bf16."""
+    import torch
+    if not (A.is_cuda and B.is_cuda and C.is_cuda):
+        raise ValueError("A, B and C must be CUDA tensors")
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise ValueError("A and B must be bfloat16")
+    if C.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("C must be float32 or bfloat16")
+    for t in (A, B, C):
+        if t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError("A, B, C must be 2-D with unit inner stride")
+    M = C.shape[1] if M is None else M
+    N = C.shape[0] if N is None else N
+    K = (A.shape[0] if a_col else A.shape[1]) if K is None else K
+    out = OUT_F32 if C.dtype == torch.float32 else OUT_BF16
+    st = gemm_bf16_layout_raw(M, N, K, A.data_ptr(), A.stride(0), COL_MAJOR if a_col else ROW_MAJOR, B.data_ptr(),
+                              B.stride(0), ROW_MAJOR if b_row else COL_MAJOR, C.data_ptr(), C.stride(0), float(alpha),
+                              float(beta), out, _stream_ptr(stream), variant)
+    _check(st)
+    return C
 
 
 def check_device_status(stream=None) -> tuple[int, int]:

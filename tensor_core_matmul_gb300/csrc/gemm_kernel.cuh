@@ -127,6 +127,7 @@ struct GemmParams {
     void* C;
     float alpha, beta;
     int in_fmt;          // 8-bit operands: 0 = E4M3, 1 = E5M2 (unused for bf16)
+    int a_mn, b_mn;      // MMA operand A / B stored MN-major (M or N contiguous; bf16 only)
     // Fused epilogue: out = act(alpha*acc + beta*C + bias[column of C]).
     const void* bias;    // one value per column of C (per row of D in the transposed product), or null
     int bias_kind;       // 0 none, 1 fp32, 2 bf16
@@ -642,6 +643,21 @@ __global__ void __launch_bounds__(192, 1)
                 const int b_row = tn * BN + static_cast<int>(rank) * Cfg::kRowsB;
                 const CUtensorMap* mB = &tmB;
                 const uint32_t stage_tx = Cfg::kStageTx;
+                // One operand tile: K-major, one box of 64 K values by `rows`
+                // rows; MN-major, boxes of 64 MN values by 64 K rows, 8 KB
+                // apart.  Same bytes either way.
+                auto load_tile = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar, int kb, int row0, int rows,
+                                     bool mn) {
+                    if (!mn) {
+                        if constexpr (CTA_GROUP == 1) tma_load_2d(dst, map, bar, kb * Cfg::kBK, row0);
+                        else tma_load_2d_pair(dst, map, bar, kb * Cfg::kBK, row0);
+                    } else {
+                        for (int t = 0; t < rows; t += 64) {
+                            if constexpr (CTA_GROUP == 1) tma_load_2d(dst + t * 128, map, bar, row0 + t, kb * 64);
+                            else tma_load_2d_pair(dst + t * 128, map, bar, row0 + t, kb * 64);
+                        }
+                    }
+                };
                 for (int kb = u.kb0; kb < u.kb1; ++kb) {
                     if (!wait_phase<false>(empty_bar(stage), phase ^ 1u, wctx, kWhereProducer)) {
                         ok = false;
@@ -661,14 +677,14 @@ __global__ void __launch_bounds__(192, 1)
                                               b_row + static_cast<int>(rm) * (BN / 2), mask_b);
                     } else if constexpr (CTA_GROUP == 1) {
                         mbar_arrive_expect_tx(full_bar(stage), stage_tx);
-                        tma_load_2d(sa, &tmA, full_bar(stage), kb * Cfg::kBK, a_row);
-                        tma_load_2d(sb, mB, full_bar(stage), kb * Cfg::kBK, b_row);
+                        load_tile(sa, &tmA, full_bar(stage), kb, a_row, Cfg::kRowsA, p.a_mn != 0);
+                        load_tile(sb, mB, full_bar(stage), kb, b_row, Cfg::kRowsB, p.b_mn != 0);
                     } else {
                         // Both CTAs' bytes land on the leader's barrier.
                         if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), stage_tx);
                         const uint32_t fb = map_to_cta(full_bar(stage), 0);
-                        tma_load_2d_pair(sa, &tmA, fb, kb * Cfg::kBK, a_row);
-                        tma_load_2d_pair(sb, mB, fb, kb * Cfg::kBK, b_row);
+                        load_tile(sa, &tmA, fb, kb, a_row, Cfg::kRowsA, p.a_mn != 0);
+                        load_tile(sb, mB, fb, kb, b_row, Cfg::kRowsB, p.b_mn != 0);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -699,8 +715,13 @@ __global__ void __launch_bounds__(192, 1)
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer --
         if (lane == 0 && (CTA_GROUP == 1 || rank == 0)) {
-            const uint32_t kIdesc = IN == 1 ? idesc_f8_f32(Cfg::kBM, BN, static_cast<uint32_t>(p.in_fmt) & 1u)
-                                            : idesc_bf16_f32(Cfg::kBM, BN);
+            // Bits 15 / 16 of the instruction descriptor: A / B MN-major.
+            const uint32_t kIdesc = (IN == 1 ? idesc_f8_f32(Cfg::kBM, BN, static_cast<uint32_t>(p.in_fmt) & 1u)
+                                             : idesc_bf16_f32(Cfg::kBM, BN)) |
+                                    (p.a_mn ? (1u << 15) : 0u) | (p.b_mn ? (1u << 16) : 0u);
+            // Descriptor step per MMA: 32 bytes along a K-major row, two
+            // 1 KB K groups in an MN-major tile (in 16-byte units).
+            const uint32_t a_step = p.a_mn ? 128u : 2u, b_step = p.b_mn ? 128u : 2u;
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             UnitIter it(cluster_id, num_clusters);
@@ -717,12 +738,12 @@ __global__ void __launch_bounds__(192, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint64_t ad = sdesc_kmajor_sw128(sA0 + stage * Cfg::kABytes);
-                    const uint64_t bd = sdesc_kmajor_sw128(sB0 + stage * Cfg::kBBytes);
+                    const uint32_t sa = sA0 + stage * Cfg::kABytes, sb = sB0 + stage * Cfg::kBBytes;
+                    const uint64_t ad = p.a_mn ? sdesc_mnmajor_sw128(sa) : sdesc_kmajor_sw128(sa);
+                    const uint64_t bd = p.b_mn ? sdesc_mnmajor_sw128(sb) : sdesc_kmajor_sw128(sb);
 #pragma unroll
                     for (int k = 0; k < Cfg::kBK / Cfg::kUmmaK; ++k) {
-                        // +32 bytes along K per step: (32 >> 4) = 2 in the address field.
-                        mma_tc<CTA_GROUP, IN>(d_tmem, ad + 2u * k, bd + 2u * k, idesc,
+                        mma_tc<CTA_GROUP, IN>(d_tmem, ad + a_step * k, bd + b_step * k, idesc,
                                               (kb != u.kb0 || k != 0) ? 1u : 0u);
                     }
                     if constexpr (MC == 4) {

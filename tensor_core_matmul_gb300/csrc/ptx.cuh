@@ -272,6 +272,24 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
     return d;
 }
 
+// The same for an MN-major operand tile (M or N contiguous in memory): TMA
+// writes boxes of 64 MN values (128 B, one swizzled row) by 64 K rows, so a
+// swizzle atom is 8 K rows x 64 MN values.  In the canonical MN-major
+// 128-byte-swizzle layout, ((8,8,m),(8,k)) : ((1,8,LBO),(64,SBO)) in
+// elements, the leading byte offset is the distance between atoms along MN
+// (the next 64-value box: 64 rows x 128 B = 8 KB) and the stride byte offset
+// the distance between 8-row groups along K (1 KB).  One MMA (K = 16 bf16)
+// covers two K groups, so the next one starts 2 KB further on.
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>(8192u >> 4) << 16;
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
 // Instruction descriptor for kind::f16 with bf16 A and B, fp32 accumulator,
 // both operands K-major, no negation, dense.
 //   [4,6) D format (1 = f32)  [7,10) A format (1 = bf16)  [10,13) B format

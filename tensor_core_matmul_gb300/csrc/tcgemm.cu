@@ -147,7 +147,7 @@ bool use_stream_k(int64_t tiles, int64_t clusters, int64_t num_kb) {
 
 // in_kind 0: bf16 operands (64 per k-block); 1: 8-bit operands (128 per k-block).
 bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pairs, int max_quads, Plan& pl,
-               bool allow_split = true, int in_kind = 0) {
+               bool allow_split = true, int in_kind = 0, bool a_col = false, bool b_row = false) {
     if (sms <= 0) return false;
     if (variant == TCGEMM_VARIANT_AUTO) variant = pick_variant(M, N, K, sms);
     pl.variant = variant;
@@ -180,7 +180,9 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pa
                                    : static_cast<double>((t + pairs - 1) / pairs * num_kb);
             return kbs * static_cast<double>(bn + 32);
         };
-        pl.bn = (variant == TCGEMM_VARIANT_2CTA && cost(224) < cost(256) * 0.97) ? 224 : 256;
+        // An MN-major B tile is loaded in 64-value boxes: 112 per CTA does
+        // not fit, so it takes the 256 width.
+        pl.bn = (variant == TCGEMM_VARIANT_2CTA && !b_row && cost(224) < cost(256) * 0.97) ? 224 : 256;
         pl.smem = pl.bn == 224 ? Cfg2n::kSmemBytes : Cfg2::kSmemBytes;
     } else if (variant == TCGEMM_VARIANT_1CTA_MC) {
         pl.cta_group = 1;
@@ -285,6 +287,30 @@ bool encode_kmajor(CUtensorMap* m, const void* ptr, int64_t k_extent, int64_t ro
     if (r != CUDA_SUCCESS) {
         set_error("cuTensorMapEncodeTiled failed (%d) for extent %lld x %lld, ld %lld", static_cast<int>(r),
                   static_cast<long long>(k_extent), static_cast<long long>(rows), static_cast<long long>(ld));
+        return false;
+    }
+    return true;
+}
+
+// An MN-major operand (M or N contiguous; bf16): dims {MN, K}, boxes of 64
+// MN values (one 128-byte swizzled row) by 64 K rows.
+bool encode_mnmajor(CUtensorMap* m, const void* ptr, int64_t mn_extent, int64_t k_extent, int64_t ld) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) {
+        set_error("cuTensorMapEncodeTiled is not available from the driver");
+        return false;
+    }
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(mn_extent), static_cast<cuuint64_t>(k_extent)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
+    cuuint32_t box[2] = {64u, 64u};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled failed (%d) for an MN-major operand %lld x %lld, ld %lld",
+                  static_cast<int>(r), static_cast<long long>(mn_extent), static_cast<long long>(k_extent),
+                  static_cast<long long>(ld));
         return false;
     }
     return true;
@@ -433,7 +459,8 @@ bool overlaps(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
 }
 
 int validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
-             const void* C, int64_t ldc, int out_dtype, int64_t in_bytes = 2) {
+             const void* C, int64_t ldc, int out_dtype, int64_t in_bytes = 2, bool a_col = false,
+             bool b_row = false) {
     const int64_t lim = (int64_t{1} << 31) - 1;
     if (M < 0 || N < 0 || K < 0 || M > lim || N > lim || K > lim) {
         set_error("sizes must satisfy 0 <= M, N, K < 2^31 (got %lld, %lld, %lld)", static_cast<long long>(M),
@@ -445,8 +472,10 @@ int validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
                   out_dtype);
         return TCGEMM_ERR_INVALID_ARG;
     }
-    if (lda < std::max<int64_t>(K, 1) || ldb < std::max<int64_t>(K, 1) || ldc < std::max<int64_t>(M, 1)) {
-        set_error("leading dimensions too small: need lda >= K, ldb >= K, ldc >= M (at least 1)");
+    if (lda < std::max<int64_t>(a_col ? M : K, 1) || ldb < std::max<int64_t>(b_row ? N : K, 1) ||
+        ldc < std::max<int64_t>(M, 1)) {
+        set_error("leading dimensions too small: need lda >= %s, ldb >= %s, ldc >= M (at least 1)",
+                  a_col ? "M" : "K", b_row ? "N" : "K");
         return TCGEMM_ERR_INVALID_ARG;
     }
     if (M == 0 || N == 0) return TCGEMM_OK;
@@ -467,8 +496,9 @@ int validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
             return TCGEMM_ERR_ALIGNMENT;
         }
         const int64_t cbytes = ((N - 1) * ldc + M) * esz;
-        if (overlaps(C, cbytes, A, ((M - 1) * lda + K) * in_bytes) ||
-            overlaps(C, cbytes, B, ((N - 1) * ldb + K) * in_bytes)) {
+        const int64_t a_elems = a_col ? (K - 1) * lda + M : (M - 1) * lda + K;
+        const int64_t b_elems = b_row ? (K - 1) * ldb + N : (N - 1) * ldb + K;
+        if (overlaps(C, cbytes, A, a_elems * in_bytes) || overlaps(C, cbytes, B, b_elems * in_bytes)) {
             set_error("C overlaps A or B");
             return TCGEMM_ERR_INVALID_ARG;
         }
@@ -620,7 +650,7 @@ int validate_epilogue(const Epilogue& ep, int64_t M, int64_t N, const void* C, i
 int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
              int64_t ldc, float alpha, float beta, int out_dtype, void* stream_v, int variant,
              int ws_mode = kWsInternal, void* ws = nullptr, int64_t ws_bytes = 0, const Epilogue& ep = Epilogue(),
-             int in_kind = 0, int in_fmt = 0) {
+             int in_kind = 0, int in_fmt = 0, bool a_col = false, bool b_row = false) {
     t_last_error[0] = '\0';
     if (variant < TCGEMM_VARIANT_AUTO || variant > TCGEMM_VARIANT_SWAP_N64) {
         set_error("unknown variant %d", variant);
@@ -646,7 +676,11 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
             return TCGEMM_ERR_INVALID_ARG;
         }
     }
-    int rc = validate(M, N, K, A, lda, B, ldb, C, ldc, out_dtype, in_kind == 1 ? 1 : 2);
+    if ((a_col || b_row) && (in_kind == 1 || variant == TCGEMM_VARIANT_1CTA_MC)) {
+        set_error("column-major A / row-major B: bf16 operands and variants other than 3 only");
+        return TCGEMM_ERR_INVALID_ARG;
+    }
+    int rc = validate(M, N, K, A, lda, B, ldb, C, ldc, out_dtype, in_kind == 1 ? 1 : 2, a_col, b_row);
     if (rc != TCGEMM_OK) return rc;
     rc = validate_epilogue(ep, M, N, C, ldc, out_dtype);
     if (rc != TCGEMM_OK) return rc;
@@ -690,7 +724,8 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     }
 
     Plan pl;
-    if (!make_plan(M, N, K, variant, info.sms, info.max_pairs, info.max_quads, pl, ws_mode != kWsNone, in_kind)) {
+    if (!make_plan(M, N, K, variant, info.sms, info.max_pairs, info.max_quads, pl, ws_mode != kWsNone, in_kind,
+                   a_col, b_row)) {
         set_error("no launch plan for this shape and variant");
         return TCGEMM_ERR_INVALID_ARG;
     }
@@ -730,10 +765,16 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     const void* opB = pl.swap ? A : B;
     const int64_t rowsA = pl.swap ? N : M, rowsB = pl.swap ? M : N;
     const int64_t ldA = pl.swap ? ldb : lda, ldB = pl.swap ? lda : ldb;
+    // The MMA's A operand is A (B in the transposed product); MN-major when
+    // that matrix is stored with its M (N) index contiguous.
+    const bool mma_a_mn = pl.swap ? b_row : a_col, mma_b_mn = pl.swap ? a_col : b_row;
     CUtensorMap ta, tb;
     const int in_bytes = in_kind == 1 ? 1 : 2;
-    if (!encode_kmajor(&ta, opA, K, rowsA, ldA, a_box_rows, in_bytes) ||
-        !encode_kmajor(&tb, opB, K, rowsB, ldB, b_box_rows, in_bytes)) {
+    const bool ok_a = mma_a_mn ? encode_mnmajor(&ta, opA, rowsA, K, ldA)
+                               : encode_kmajor(&ta, opA, K, rowsA, ldA, a_box_rows, in_bytes);
+    const bool ok_b = mma_b_mn ? encode_mnmajor(&tb, opB, rowsB, K, ldB)
+                               : encode_kmajor(&tb, opB, K, rowsB, ldB, b_box_rows, in_bytes);
+    if (!ok_a || !ok_b) {
         return TCGEMM_ERR_INVALID_ARG;
     }
     pl.ws_ptr = wsp;
@@ -766,6 +807,8 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     gp.in_fmt = in_fmt;
     gp.qscale = ep.qscale;
     gp.qzero = static_cast<float>(ep.qzero);
+    gp.a_mn = mma_a_mn ? 1 : 0;
+    gp.b_mn = mma_b_mn ? 1 : 0;
     gp.tiles_dp = pl.tiles_dp;
     gp.sk_tiles = pl.sk_tiles;
     gp.sk_iters = pl.sk_iters;
@@ -876,6 +919,19 @@ int gemm_quant_i8(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, c
     const int in_fmt = in_type == TCGEMM_IN_E5M2 ? TCGEMM_FP8_E5M2 : TCGEMM_FP8_E4M3;
     return run_gemm(M, N, K, A, lda, B, ldb, Q, ldq, alpha, 0.0f, TCGEMM_OUT_I8, stream, variant, kWsInternal, nullptr,
                     0, ep, in_kind, in_fmt);
+}
+
+int gemm_bf16_layout(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_layout, const void* B,
+                     int64_t ldb, int b_layout, void* C, int64_t ldc, float alpha, float beta, int out_dtype,
+                     void* stream, int variant) {
+    if ((a_layout != TCGEMM_ROW_MAJOR && a_layout != TCGEMM_COL_MAJOR) ||
+        (b_layout != TCGEMM_ROW_MAJOR && b_layout != TCGEMM_COL_MAJOR)) {
+        t_last_error[0] = '\0';
+        set_error("layouts must be TCGEMM_ROW_MAJOR (0) or TCGEMM_COL_MAJOR (1)");
+        return TCGEMM_ERR_INVALID_ARG;
+    }
+    return run_gemm(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, stream, variant, kWsInternal, nullptr, 0,
+                    Epilogue(), 0, 0, a_layout == TCGEMM_COL_MAJOR, b_layout == TCGEMM_ROW_MAJOR);
 }
 
 int64_t tcgemm_noalloc_scratch_bytes(void) { return static_cast<int64_t>(kNoAllocScratchBytes); }

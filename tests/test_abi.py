@@ -108,6 +108,22 @@ def test_quant_argument_errors(tc, in_type, scale, variant, status):
     assert st == status, (st, tc.binding.last_error())
 
 
+@pytest.mark.parametrize("args,status", [
+    ((8, 8, 16, FAKE, 16, 2, FAKE * 2, 16, 1), 1),      # unknown A layout
+    ((8, 8, 16, FAKE, 4, 1, FAKE * 2, 16, 1), 1),       # column-major A: lda < M
+    ((8, 12, 16, FAKE, 16, 0, FAKE * 2, 8, 0), 1),      # row-major B: ldb < N
+    ((8, 8, 16, FAKE, 12, 1, FAKE * 2, 16, 1), 2),      # lda*2 not a multiple of 16
+])
+def test_layout_argument_errors(tc, args, status):
+    st = tc.binding.gemm_bf16_layout_raw(*args, FAKE * 4, 8, 1.0, 0.0, 0, 0, 0)
+    assert st == status, (st, tc.binding.last_error())
+
+
+def test_layout_multicast_variant_refused(tc):
+    assert tc.binding.gemm_bf16_layout_raw(8, 8, 16, FAKE, 8, 1, FAKE * 2, 16, 1, FAKE * 4, 8, 1.0, 0.0, 0, 0,
+                                           3) == 1
+
+
 def test_int8_output_needs_the_quantising_entry_point(tc):
     assert tc.gemm_bf16_raw(16, 8, 16, FAKE, 16, FAKE * 2, 16, FAKE * 4, 16, 1.0, 0.0, 2, 0) == 1
     assert "scale" in tc.binding.last_error()
