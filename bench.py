@@ -213,6 +213,9 @@ def run_ours(args) -> None:
                              N=N, K=K, stream=stream, variant=args.variant)
         elif args.in_format != "bf16":
             tc.gemm_fp8(A, B, C, case.alpha, case.beta, M=M, N=N, K=K, stream=stream, variant=args.variant)
+        elif args.layout != "tn":
+            tc.gemm_bf16_layout(A, B, C, case.alpha, case.beta, a_col=case.a_col, b_row=case.b_row, M=M, N=N, K=K,
+                                stream=stream, variant=args.variant)
         elif args.epilogue == "none":
             tc.gemm_bf16(A, B, C, case.alpha, case.beta, M=M, N=N, K=K, stream=stream, variant=args.variant)
         else:
@@ -264,13 +267,14 @@ def run_ours(args) -> None:
     traffic = profile_traffic(tag)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     variant = args.variant or tc.pick_variant(M, N, K, sms)
-    plan = tc.plan(M, N, K, variant, sms, in_kind=0 if args.in_format == "bf16" else 1)
+    plan = tc.plan(M, N, K, variant, sms, in_kind=0 if args.in_format == "bf16" else 1, a_col=case.a_col,
+                   b_row=case.b_row)
 
     e2e = None
-    if not args.no_e2e and not args.quant:
+    if not args.no_e2e and not args.quant and args.layout == "tn":
         e2e = measure_e2e(args, case, dev, stream, bias_cpu, act)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quant:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quant and args.layout == "tn":
         cpu = cpu_baseline(case, target_s=args.cpu_seconds, bias=bias_cpu, act=act)
 
     if rank == 0:
@@ -296,6 +300,8 @@ def run_ours(args) -> None:
                 "M": M, "N": N, "K": K,
                 "epilogue": args.epilogue,
                 "in_format": args.in_format,
+                "layout": {"tn": "A row-major, B column-major", "nn": "A column-major, B column-major",
+                           "tt": "A row-major, B row-major", "nt": "A column-major, B row-major"}[args.layout],
                 "output": "int8 (per-row quantisation)" if args.quant else ("bf16" if case.out_dtype else "fp32"),
                 "l2": f"flushed between timed steps ({FLUSH_BYTES >> 20} MiB write, untimed)",
                 "kernel": {"variant": {1: "1cta", 2: "2cta"}.get(variant, str(variant)), **plan},
@@ -320,8 +326,12 @@ def bench_case(args):
     --in-format asks for them (same shapes, seeds and distribution)."""
     import gemm_inputs as gi
     c = gi.CONFIGS[args.config]
-    return gi.make_case(args.config, c["M"], c["N"], c["K"], alpha=c["alpha"], beta=c["beta"],
+    case = gi.make_case(args.config, c["M"], c["N"], c["K"], alpha=c["alpha"], beta=c["beta"],
                         out_dtype=c["out_dtype"], seed=c["seed"], in_format=args.in_format)
+    if args.layout != "tn":
+        # nn: A column-major; tt: B row-major; nt: both (the same logical matrices).
+        case = gi.relayout(case, a_col=args.layout in ("nn", "nt"), b_row=args.layout in ("tt", "nt"))
+    return case
 
 
 def algorithmic_bytes(case) -> int:
@@ -537,6 +547,9 @@ def main():
                     help="operand type: bf16 (gemm_bf16) or 8-bit floats (gemm_fp8)")
     ap.add_argument("--epilogue", default="none", choices=sorted(EPILOGUES),
                     help="fused epilogue: bias and/or activation (gemm_bf16_bias_act)")
+    ap.add_argument("--layout", default="tn", choices=["tn", "nn", "tt", "nt"],
+                    help="operand storage, first letter A (t row-major, n column-major), second B (n "
+                         "column-major, t row-major): tn is the pages' layout; others use gemm_bf16_layout")
     ap.add_argument("--quant", action="store_true",
                     help="int8 output through the per-row quantising epilogue (gemm_quant_i8)")
     ap.add_argument("--no-e2e", action="store_true")

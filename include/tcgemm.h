@@ -218,10 +218,7 @@ int gemm_fp8(int64_t M, int64_t N, int64_t K,
              float alpha, float beta, int out_dtype, int in_format,
              void* stream, int variant);
 
-/* tcgemm_plan for bf16 (in_kind 0) or 8-bit (in_kind 1) operands: a k-block
- * holds 64 bf16 or 128 8-bit values, which changes the plan's k-block count
- * and stream-K choice.  Host only. */
-int tcgemm_plan_kind(int64_t M, int64_t N, int64_t K, int variant, int in_kind, int num_sms, int64_t* out);
+
 
 /* Operand types of gemm_quant_i8. */
 typedef enum {
@@ -286,6 +283,14 @@ int gemm_bf16_layout(int64_t M, int64_t N, int64_t K,
                      const void* B, int64_t ldb, int b_layout,
                      void* C, int64_t ldc,
                      float alpha, float beta, int out_dtype, void* stream, int variant);
+
+/* tcgemm_plan for bf16 (in_kind 0) or 8-bit (in_kind 1) operands and the
+ * operand layouts of gemm_bf16_layout (a_layout TCGEMM_ROW_MAJOR and b_layout
+ * TCGEMM_COL_MAJOR are gemm_bf16's): a k-block holds 64 bf16 or 128 8-bit
+ * values, which changes the k-block count and the stream-K choice, and a
+ * row-major B takes 256-wide pair tiles.  Host only. */
+int tcgemm_plan_kind(int64_t M, int64_t N, int64_t K, int variant, int in_kind, int a_layout, int b_layout,
+                     int num_sms, int64_t* out);
 
 /* Size in bytes of gemm_bf16_noalloc's fixed scratch array.  Host only. */
 int64_t tcgemm_noalloc_scratch_bytes(void);

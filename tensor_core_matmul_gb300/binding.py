@@ -75,7 +75,7 @@ def lib() -> ctypes.CDLL:
     L.gemm_bf16_layout.restype = i32
     L.gemm_fp8.argtypes = gemm_args[:-1] + [i32, p, i32]
     L.gemm_fp8.restype = i32
-    L.tcgemm_plan_kind.argtypes = [i64, i64, i64, i32, i32, i32, ctypes.POINTER(ctypes.c_int64)]
+    L.tcgemm_plan_kind.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int64)]
     L.tcgemm_plan_kind.restype = i32
     L.gemm_bf16_noalloc.argtypes = gemm_args + [i32]
     L.gemm_bf16_noalloc.restype = i32
@@ -358,12 +358,15 @@ PLAN_KEYS = ["grid", "cluster", "tiles_m", "tiles_n", "bm", "bn", "num_kb", "sme
              "stream_k", "arows", "swap"]
 
 
-def plan(M: int, N: int, K: int, variant: int = 0, num_sms: int = 152, in_kind: int = 0) -> dict:
+def plan(M: int, N: int, K: int, variant: int = 0, num_sms: int = 152, in_kind: int = 0, a_col: bool = False,
+         b_row: bool = False) -> dict:
     """Launch plan for a device with `num_sms` SMs (host only; assumes every
-    pair / 4-cluster of SMs can be resident).  in_kind 1: 8-bit operands."""
+    pair / 4-cluster of SMs can be resident).  in_kind 1: 8-bit operands;
+    a_col / b_row: the layouts of gemm_bf16_layout."""
     out = (ctypes.c_int64 * len(PLAN_KEYS))()
-    if in_kind:
-        _check(lib().tcgemm_plan_kind(M, N, K, variant, in_kind, num_sms, out))
+    if in_kind or a_col or b_row:
+        _check(lib().tcgemm_plan_kind(M, N, K, variant, in_kind, COL_MAJOR if a_col else ROW_MAJOR,
+                                      ROW_MAJOR if b_row else COL_MAJOR, num_sms, out))
     else:
         _check(lib().tcgemm_plan(M, N, K, variant, num_sms, out))
     return dict(zip(PLAN_KEYS, [int(v) for v in out]))

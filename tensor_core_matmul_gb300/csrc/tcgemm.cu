@@ -953,11 +953,14 @@ int tcgemm_plan(int64_t M, int64_t N, int64_t K, int variant, int num_sms, int64
     return TCGEMM_OK;
 }
 
-int tcgemm_plan_kind(int64_t M, int64_t N, int64_t K, int variant, int in_kind, int num_sms, int64_t* out) {
+int tcgemm_plan_kind(int64_t M, int64_t N, int64_t K, int variant, int in_kind, int a_layout, int b_layout,
+                     int num_sms, int64_t* out) {
     if (out == nullptr || M <= 0 || N <= 0 || K <= 0 || num_sms <= 0 || in_kind < 0 || in_kind > 1)
         return TCGEMM_ERR_INVALID_ARG;
     Plan pl;
-    if (!make_plan(M, N, K, variant, num_sms, num_sms / 2, num_sms / 4, pl, true, in_kind)) return TCGEMM_ERR_INVALID_ARG;
+    if (!make_plan(M, N, K, variant, num_sms, num_sms / 2, num_sms / 4, pl, true, in_kind,
+                   a_layout == TCGEMM_COL_MAJOR, b_layout == TCGEMM_ROW_MAJOR))
+        return TCGEMM_ERR_INVALID_ARG;
     fill_plan_out(pl, out);
     return TCGEMM_OK;
 }

@@ -119,6 +119,12 @@ def test_layout_argument_errors(tc, args, status):
     assert st == status, (st, tc.binding.last_error())
 
 
+def test_row_major_b_takes_256_wide_pairs(tc):
+    assert tc.plan(4096, 4096, 4096, 0, 152)["bn"] == 224
+    assert tc.plan(4096, 4096, 4096, 0, 152, b_row=True)["bn"] == 256
+    assert tc.plan(4096, 4096, 4096, 0, 152, a_col=True)["bn"] == 224
+
+
 def test_layout_multicast_variant_refused(tc):
     assert tc.binding.gemm_bf16_layout_raw(8, 8, 16, FAKE, 8, 1, FAKE * 2, 16, 1, FAKE * 4, 8, 1.0, 0.0, 0, 0,
                                            3) == 1
