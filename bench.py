@@ -222,6 +222,13 @@ def run_ours(args) -> None:
             tc.gemm_bf16_bias_act(A, B, C, case.alpha, case.beta, bias=bias, activation=act, M=M, N=N, K=K,
                                   stream=stream, variant=args.variant)
 
+    tuned = None
+    if args.autotune:
+        if args.quant or args.epilogue != "none":
+            raise SystemExit("--autotune times the plain GEMM (no --quant / --epilogue)")
+        v, us = tc.autotune(A, B, C, case.alpha, case.beta, a_col=case.a_col, b_row=case.b_row, M=M, N=N, K=K,
+                            iters=10, flush=flush, stream=stream)
+        tuned = {"variant": v, "us_flushed": round(us, 2)}
     for _ in range(args.warmup):
         flush.fill_(1)
         gemm()
@@ -266,7 +273,7 @@ def run_ours(args) -> None:
            + ("" if args.in_format == "bf16" else f"_{args.in_format}") + ("_quant" if args.quant else ""))
     traffic = profile_traffic(tag)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    variant = args.variant or tc.pick_variant(M, N, K, sms)
+    variant = args.variant or (tuned["variant"] if tuned else tc.pick_variant(M, N, K, sms))
     plan = tc.plan(M, N, K, variant, sms, in_kind=0 if args.in_format == "bf16" else 1, a_col=case.a_col,
                    b_row=case.b_row)
 
@@ -305,6 +312,7 @@ def run_ours(args) -> None:
                 "output": "int8 (per-row quantisation)" if args.quant else ("bf16" if case.out_dtype else "fp32"),
                 "l2": f"flushed between timed steps ({FLUSH_BYTES >> 20} MiB write, untimed)",
                 "kernel": {"variant": {1: "1cta", 2: "2cta"}.get(variant, str(variant)), **plan},
+                "autotuned": tuned,
                 "parallelism": f"independent problem per GPU x{world}",
                 "wall_s_timed_loop": round(wall, 3),
             },
@@ -550,6 +558,8 @@ def main():
     ap.add_argument("--layout", default="tn", choices=["tn", "nn", "tt", "nt"],
                     help="operand storage, first letter A (t row-major, n column-major), second B (n "
                          "column-major, t row-major): tn is the pages' layout; others use gemm_bf16_layout")
+    ap.add_argument("--autotune", action="store_true",
+                    help="time every variant first (tcgemm_autotune) and let the automatic choice use the fastest")
     ap.add_argument("--quant", action="store_true",
                     help="int8 output through the per-row quantising epilogue (gemm_quant_i8)")
     ap.add_argument("--no-e2e", action="store_true")

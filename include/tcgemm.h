@@ -292,6 +292,39 @@ int gemm_bf16_layout(int64_t M, int64_t N, int64_t K,
 int tcgemm_plan_kind(int64_t M, int64_t N, int64_t K, int variant, int in_kind, int a_layout, int b_layout,
                      int num_sms, int64_t* out);
 
+/* Autotuning (the work log attributes its remaining per-shape gaps to the
+ * lack of it): time every kernel variant built for this problem on the
+ * caller's buffers and remember the fastest.  Every later call for the same
+ * device, M, N, K, operand type (tcgemm_in_t), operand layouts
+ * (tcgemm_layout_t; gemm_bf16's are TCGEMM_ROW_MAJOR A and TCGEMM_COL_MAJOR
+ * B), output type (fp32 or bf16) and beta == 0 or not that asks for the
+ * automatic choice (variant 0) then uses it.  Each candidate runs once, then
+ * `iters` (1..1000) times, each call between its own pair of CUDA events on
+ * `stream`; with flush_bytes > 0 the device buffer `flush` is written
+ * (cudaMemsetAsync, untimed) before every timed call, so that a buffer
+ * larger than L2 makes the timing that of a cold call (NULL / 0: back-to-back
+ * calls, operands partly in L2).  The call synchronises the stream, so it
+ * cannot be captured in a CUDA graph.  C is
+ * overwritten (with beta != 0 it accumulates): its contents afterwards are
+ * undefined.  Writes the chosen variant to *best_variant and, if best_us is
+ * not NULL, its mean time in microseconds.  Errors: bad arguments ->
+ * TCGEMM_ERR_INVALID_ARG; a failed timed call -> TCGEMM_ERR_CUDA; a device
+ * timeout in the timed runs -> TCGEMM_ERR_TIMEOUT. */
+int tcgemm_autotune(int64_t M, int64_t N, int64_t K,
+                    const void* A, int64_t lda, int a_layout,
+                    const void* B, int64_t ldb, int b_layout, int in_type,
+                    void* C, int64_t ldc, float alpha, float beta, int out_dtype,
+                    int iters, void* flush, int64_t flush_bytes, void* stream,
+                    int* best_variant, float* best_us);
+
+/* The variant tcgemm_autotune chose for this problem on the current device,
+ * or 0 if none was tuned.  Host only. */
+int tcgemm_autotune_lookup(int64_t M, int64_t N, int64_t K, int in_type, int out_dtype, int a_layout,
+                           int b_layout, int beta_nonzero);
+
+/* Forget every tuned choice.  Host only. */
+void tcgemm_autotune_clear(void);
+
 /* Size in bytes of gemm_bf16_noalloc's fixed scratch array.  Host only. */
 int64_t tcgemm_noalloc_scratch_bytes(void);
 

@@ -73,6 +73,13 @@ def lib() -> ctypes.CDLL:
     L.gemm_quant_i8.restype = i32
     L.gemm_bf16_layout.argtypes = [i64, i64, i64, p, i64, i32, p, i64, i32, p, i64, f32, f32, i32, p, i32]
     L.gemm_bf16_layout.restype = i32
+    L.tcgemm_autotune.argtypes = [i64, i64, i64, p, i64, i32, p, i64, i32, i32, p, i64, f32, f32, i32, i32, p, i64,
+                                  p, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_float)]
+    L.tcgemm_autotune.restype = i32
+    L.tcgemm_autotune_lookup.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32]
+    L.tcgemm_autotune_lookup.restype = i32
+    L.tcgemm_autotune_clear.argtypes = []
+    L.tcgemm_autotune_clear.restype = None
     L.gemm_fp8.argtypes = gemm_args[:-1] + [i32, p, i32]
     L.gemm_fp8.restype = i32
     L.tcgemm_plan_kind.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int64)]
@@ -333,6 +340,46 @@ def gemm_bf16_layout(A, B, C, alpha: float = 1.0, beta: float = 0.0, *, a_col: b
                               float(beta), out, _stream_ptr(stream), variant)
     _check(st)
     return C
+
+
+def autotune(A, B, C, alpha: float = 1.0, beta: float = 0.0, *, a_col: bool = False, b_row: bool = False,
+             M: Optional[int] = None, N: Optional[int] = None, K: Optional[int] = None, iters: int = 10,
+             flush=None, stream=None) -> tuple[int, float]:
+    """Time every variant built for this problem on these tensors (storage
+    convention of gemm_bf16 / gemm_bf16_layout / gemm_fp8) and remember the
+    fastest for later automatic calls.  Returns (variant, microseconds).
+    ``flush``: an optional CUDA tensor larger than L2, written before every
+    timed call (cold-call timing).  C is overwritten."""
+    import torch
+    kinds = {torch.bfloat16: IN_BF16, torch.float8_e4m3fn: IN_E4M3, torch.float8_e5m2: IN_E5M2}
+    if A.dtype not in kinds or B.dtype != A.dtype:
+        raise ValueError("A and B must both be bfloat16, float8_e4m3fn or float8_e5m2")
+    if C.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("C must be float32 or bfloat16")
+    M = C.shape[1] if M is None else M
+    N = C.shape[0] if N is None else N
+    K = (A.shape[0] if a_col else A.shape[1]) if K is None else K
+    best = ctypes.c_int(0)
+    us = ctypes.c_float(0.0)
+    st = lib().tcgemm_autotune(M, N, K, A.data_ptr(), A.stride(0), COL_MAJOR if a_col else ROW_MAJOR, B.data_ptr(),
+                               B.stride(0), ROW_MAJOR if b_row else COL_MAJOR, kinds[A.dtype], C.data_ptr(),
+                               C.stride(0), float(alpha), float(beta),
+                               OUT_F32 if C.dtype == torch.float32 else OUT_BF16, int(iters),
+                               None if flush is None else flush.data_ptr(),
+                               0 if flush is None else flush.numel() * flush.element_size(), _stream_ptr(stream),
+                               ctypes.byref(best), ctypes.byref(us))
+    _check(st)
+    return best.value, us.value
+
+
+def autotune_lookup(M: int, N: int, K: int, in_type: int = 0, out_dtype: int = 1, a_col: bool = False,
+                    b_row: bool = False, beta_nonzero: bool = False) -> int:
+    return lib().tcgemm_autotune_lookup(M, N, K, in_type, out_dtype, COL_MAJOR if a_col else ROW_MAJOR,
+                                        ROW_MAJOR if b_row else COL_MAJOR, int(beta_nonzero))
+
+
+def autotune_clear() -> None:
+    lib().tcgemm_autotune_clear()
 
 
 def check_device_status(stream=None) -> tuple[int, int]:

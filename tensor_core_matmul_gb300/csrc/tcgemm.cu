@@ -12,7 +12,9 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <utility>
+#include <vector>
 
 #include "../../include/tcgemm.h"
 #include "gemm_kernel.cuh"
@@ -121,18 +123,46 @@ bool split_enabled() {
     return on;
 }
 
-// CTA pairs (M = 256 per MMA) halve the operand traffic per SM; they pay off
-// once there are more than 128 rows.  Up to 128 rows ("skinny" products, B
-// streamed from memory once) narrow 128 x 64 tiles give every SM its own
-// columns of B and a deep pipeline; up to 64 rows the product is computed
-// transposed (C^T = B^T A^T), so that B's columns fill all 128 MMA rows and
-// the 64 rows of A become the MMA's N.
-int pick_variant(int64_t M, int64_t N, int64_t K, int sms) {
-    (void)K;
-    (void)sms;
-    if (M > 128) return TCGEMM_VARIANT_2CTA;
+bool use_stream_k(int64_t tiles, int64_t clusters, int64_t num_kb);
+
+// Estimated microseconds of a persistent launch (the variable part): rounds
+// of tiles (or a stream-K share) times k-blocks times the time per k-block,
+// which is the larger of the MMA's and the time to bring the k-block's
+// operand bytes into the SM.  Measured on GB300: an SM receives operands at
+// about 100 GB/s from L2 when every SM streams at once, the SM clock runs
+// near 1.9 GHz, and a launch costs about 12 us (CTA pairs) or 10 us (single
+// CTAs) on top (pipeline fill, last epilogue, launch).
+double est_launch_us(int64_t tiles, int64_t units, int64_t num_kb, double mma_cycles_per_kb, double bytes_per_kb) {
+    constexpr double kClockGHz = 1.9, kBytesPerUs = 100e3;
+    const bool sk = use_stream_k(tiles, units, num_kb);
+    const double kbs = sk ? static_cast<double>(tiles * num_kb) / static_cast<double>(units)
+                          : static_cast<double>((tiles + units - 1) / units * num_kb);
+    const double per_kb = std::max(mma_cycles_per_kb / (kClockGHz * 1e3), bytes_per_kb / kBytesPerUs);
+    return kbs * per_kb + (sk ? 3.0 : 0.0);
+}
+
+// Automatic variant.  Up to 64 rows the product is computed transposed
+// (C^T = B^T A^T), so that B's columns fill all 128 MMA rows and A's rows
+// become the MMA's N; up to 128 rows the narrow 128 x 64 tiles give every SM
+// its own columns of B.  Above that, CTA pairs (256-row tiles, M = 256 MMAs)
+// unless the narrow tiles spread a small problem over many more SMs by
+// enough to win: for 1024^3 they take 13.6 us against 17.1 us, for 2048^3
+// 47.5 us against 24.2 us (GB300).  in_kind 1: 8-bit operands (a k-block of
+// 128 values, the MMA twice as fast).
+int pick_variant(int64_t M, int64_t N, int64_t K, int sms, int in_kind = 0) {
     if (M <= 64 && N >= 256) return TCGEMM_VARIANT_SWAP_N64;
-    return TCGEMM_VARIANT_1CTA_N64;
+    if (M <= 128) return TCGEMM_VARIANT_1CTA_N64;
+    const int64_t num_kb = (K + (in_kind == 1 ? 127 : 63)) / (in_kind == 1 ? 128 : 64);
+    const double mma_scale = in_kind == 1 ? 0.5 : 1.0;
+    const int64_t pairs = std::max(1, sms / 2);
+    double pair_us = 1e300;
+    for (int64_t bn : {224, 256}) {
+        const int64_t tiles = (M + 255) / 256 * ((N + bn - 1) / bn);
+        pair_us = std::min(pair_us, est_launch_us(tiles, pairs, num_kb, 2.0 * bn * mma_scale, (128 + bn / 2) * 128.0));
+    }
+    const int64_t n64_tiles = (M + 127) / 128 * ((N + 63) / 64);
+    const double n64_us = est_launch_us(n64_tiles, std::max(1, sms), num_kb, 128.0 * mma_scale, 192 * 128.0);
+    return n64_us + 10.0 < pair_us + 12.0 ? TCGEMM_VARIANT_1CTA_N64 : TCGEMM_VARIANT_2CTA;
 }
 
 // Stream-K sharing: a piece pays the same fixed costs as a whole tile
@@ -149,7 +179,7 @@ bool use_stream_k(int64_t tiles, int64_t clusters, int64_t num_kb) {
 bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pairs, int max_quads, Plan& pl,
                bool allow_split = true, int in_kind = 0, bool a_col = false, bool b_row = false) {
     if (sms <= 0) return false;
-    if (variant == TCGEMM_VARIANT_AUTO) variant = pick_variant(M, N, K, sms);
+    if (variant == TCGEMM_VARIANT_AUTO) variant = pick_variant(M, N, K, sms, in_kind);
     pl.variant = variant;
     allow_split = allow_split && split_enabled();
     if (variant == TCGEMM_VARIANT_SWAP_N64) {
@@ -647,6 +677,29 @@ int validate_epilogue(const Epilogue& ep, int64_t M, int64_t N, const void* C, i
     return TCGEMM_OK;
 }
 
+// ------------------------------------------------------------ autotuning --
+
+// The variant measured fastest for a problem, per device: filled by
+// tcgemm_autotune, consulted by every call that asks for the automatic
+// choice.
+struct TuneKey {
+    int dev;
+    int64_t M, N, K;
+    int in_kind, in_fmt, out_dtype, a_col, b_row, has_beta;
+    bool operator<(const TuneKey& o) const {
+        return std::tie(dev, M, N, K, in_kind, in_fmt, out_dtype, a_col, b_row, has_beta) <
+               std::tie(o.dev, o.M, o.N, o.K, o.in_kind, o.in_fmt, o.out_dtype, o.a_col, o.b_row, o.has_beta);
+    }
+};
+std::mutex g_tune_mu;
+std::map<TuneKey, int> g_tuned;
+
+int tuned_variant(const TuneKey& k) {
+    std::lock_guard<std::mutex> lk(g_tune_mu);
+    auto it = g_tuned.find(k);
+    return it == g_tuned.end() ? TCGEMM_VARIANT_AUTO : it->second;
+}
+
 int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
              int64_t ldc, float alpha, float beta, int out_dtype, void* stream_v, int variant,
              int ws_mode = kWsInternal, void* ws = nullptr, int64_t ws_bytes = 0, const Epilogue& ep = Epilogue(),
@@ -690,6 +743,11 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     rc = probe_device(dev, info);
     if (rc != TCGEMM_OK) return rc;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    if (variant == TCGEMM_VARIANT_AUTO) {
+        const TuneKey key{dev, M, N, K, in_kind, in_kind == 1 ? in_fmt : 0, out_dtype, a_col ? 1 : 0, b_row ? 1 : 0,
+                          beta != 0.0f ? 1 : 0};
+        variant = tuned_variant(key);
+    }
 
     if (K == 0) {
         const int64_t total = M * N;
@@ -932,6 +990,118 @@ int gemm_bf16_layout(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda
     }
     return run_gemm(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, stream, variant, kWsInternal, nullptr, 0,
                     Epilogue(), 0, 0, a_layout == TCGEMM_COL_MAJOR, b_layout == TCGEMM_ROW_MAJOR);
+}
+
+int tcgemm_autotune(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_layout, const void* B,
+                    int64_t ldb, int b_layout, int in_type, void* C, int64_t ldc, float alpha, float beta,
+                    int out_dtype, int iters, void* flush, int64_t flush_bytes, void* stream_v, int* best_variant,
+                    float* best_us) {
+    t_last_error[0] = '\0';
+    if (best_variant == nullptr || iters <= 0 || iters > 1000 || in_type < TCGEMM_IN_BF16 ||
+        in_type > TCGEMM_IN_E5M2 || (out_dtype != TCGEMM_OUT_F32 && out_dtype != TCGEMM_OUT_BF16) ||
+        (a_layout != TCGEMM_ROW_MAJOR && a_layout != TCGEMM_COL_MAJOR) ||
+        (b_layout != TCGEMM_ROW_MAJOR && b_layout != TCGEMM_COL_MAJOR) || M <= 0 || N <= 0 || K <= 0 ||
+        flush_bytes < 0 || (flush_bytes > 0 && flush == nullptr)) {
+        set_error("autotune: bad arguments (sizes > 0, 1 <= iters <= 1000, fp32 or bf16 output)");
+        return TCGEMM_ERR_INVALID_ARG;
+    }
+    const int in_kind = in_type == TCGEMM_IN_BF16 ? 0 : 1;
+    const int in_fmt = in_type == TCGEMM_IN_E5M2 ? TCGEMM_FP8_E5M2 : TCGEMM_FP8_E4M3;
+    const bool a_col = a_layout == TCGEMM_COL_MAJOR, b_row = b_layout == TCGEMM_ROW_MAJOR;
+    int dev = 0;
+    DeviceInfo info;
+    int rc = probe_device(dev, info);
+    if (rc != TCGEMM_OK) return rc;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    auto call = [&](int v) {
+        return run_gemm(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, stream_v, v, kWsInternal, nullptr, 0,
+                        Epilogue(), in_kind, in_fmt, a_col, b_row);
+    };
+    // One event pair per timed call: with a flush buffer, each call is timed
+    // alone after the buffer (larger than L2) has been written, so the
+    // operands come from memory as in a cold call.
+    std::vector<cudaEvent_t> ev(2 * static_cast<size_t>(iters), nullptr);
+    for (auto& e : ev) {
+        if (cudaEventCreate(&e) != cudaSuccess) {
+            for (auto& f : ev)
+                if (f) cudaEventDestroy(f);
+            set_error("autotune: cudaEventCreate failed");
+            return TCGEMM_ERR_CUDA;
+        }
+    }
+    const int candidates[] = {TCGEMM_VARIANT_2CTA, TCGEMM_VARIANT_2CTA_W256, TCGEMM_VARIANT_1CTA,
+                              TCGEMM_VARIANT_1CTA_MC, TCGEMM_VARIANT_1CTA_N64, TCGEMM_VARIANT_SWAP_N64};
+    int best = TCGEMM_VARIANT_AUTO;
+    float best_t = 0.0f;
+    rc = TCGEMM_OK;
+    for (int v : candidates) {
+        if (call(v) != TCGEMM_OK) continue;  // not built for these operands / layouts
+        bool ok = true;
+        for (int i = 0; i < iters && ok; ++i) {
+            if (flush_bytes > 0 && cudaMemsetAsync(flush, i & 0xFF, static_cast<size_t>(flush_bytes), stream) !=
+                                       cudaSuccess) {
+                ok = false;
+                break;
+            }
+            ok = cudaEventRecord(ev[2 * i], stream) == cudaSuccess && call(v) == TCGEMM_OK &&
+                 cudaEventRecord(ev[2 * i + 1], stream) == cudaSuccess;
+        }
+        if (!ok || cudaEventSynchronize(ev.back()) != cudaSuccess) {
+            rc = TCGEMM_ERR_CUDA;
+            break;
+        }
+        float total_ms = 0.0f;
+        for (int i = 0; i < iters; ++i) {
+            float ms = 0.0f;
+            cudaEventElapsedTime(&ms, ev[2 * i], ev[2 * i + 1]);
+            total_ms += ms;
+        }
+        const float us = total_ms * 1000.0f / static_cast<float>(iters);
+        if (best == TCGEMM_VARIANT_AUTO || us < best_t) {
+            best = v;
+            best_t = us;
+        }
+    }
+    for (auto& e : ev) cudaEventDestroy(e);
+    if (rc != TCGEMM_OK) {
+        set_error("autotune: a timed call failed");
+        return rc;
+    }
+    if (best == TCGEMM_VARIANT_AUTO) {
+        set_error("autotune: no variant ran for this problem");
+        return TCGEMM_ERR_INVALID_ARG;
+    }
+    // The device status word records any timeout of the runs above.
+    uint32_t where = 0;
+    rc = tcgemm_check_device_status(stream_v, &where);
+    if (rc != TCGEMM_OK) return rc;
+    {
+        std::lock_guard<std::mutex> lk(g_tune_mu);
+        g_tuned[TuneKey{dev, M, N, K, in_kind, in_kind == 1 ? in_fmt : 0, out_dtype, a_col ? 1 : 0, b_row ? 1 : 0,
+                        beta != 0.0f ? 1 : 0}] = best;
+    }
+    *best_variant = best;
+    if (best_us) *best_us = best_t;
+    return TCGEMM_OK;
+}
+
+int tcgemm_autotune_lookup(int64_t M, int64_t N, int64_t K, int in_type, int out_dtype, int a_layout, int b_layout,
+                           int beta_nonzero) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        dev = 0;
+    }
+    const int in_kind = in_type == TCGEMM_IN_BF16 ? 0 : 1;
+    const int in_fmt = in_type == TCGEMM_IN_E5M2 ? TCGEMM_FP8_E5M2 : TCGEMM_FP8_E4M3;
+    return tuned_variant(TuneKey{dev, M, N, K, in_kind, in_kind == 1 ? in_fmt : 0, out_dtype,
+                                 a_layout == TCGEMM_COL_MAJOR ? 1 : 0, b_layout == TCGEMM_ROW_MAJOR ? 1 : 0,
+                                 beta_nonzero ? 1 : 0});
+}
+
+void tcgemm_autotune_clear(void) {
+    std::lock_guard<std::mutex> lk(g_tune_mu);
+    g_tuned.clear();
 }
 
 int64_t tcgemm_noalloc_scratch_bytes(void) { return static_cast<int64_t>(kNoAllocScratchBytes); }

@@ -130,6 +130,20 @@ def test_layout_multicast_variant_refused(tc):
                                            3) == 1
 
 
+def test_autotune_table_starts_empty_and_rejects_bad_arguments(tc):
+    tc.autotune_clear()
+    assert tc.autotune_lookup(4096, 4096, 4096) == 0
+    best = ctypes.c_int(-1)
+    L = tc.lib()
+    assert L.tcgemm_autotune(8, 8, 16, FAKE, 16, 0, FAKE * 2, 16, 1, 0, FAKE * 4, 8, 1.0, 0.0, 0, 0, None, 0, None,
+                             ctypes.byref(best), None) == 1          # iters = 0
+    assert L.tcgemm_autotune(8, 8, 16, FAKE, 16, 0, FAKE * 2, 16, 1, 0, FAKE * 4, 8, 1.0, 0.0, 2, 5, None, 0, None,
+                             ctypes.byref(best), None) == 1          # int8 output is not tuned
+    assert L.tcgemm_autotune(8, 8, 16, FAKE, 16, 0, FAKE * 2, 16, 1, 0, FAKE * 4, 8, 1.0, 0.0, 0, 5, None, 64, None,
+                             ctypes.byref(best), None) == 1          # flush size without a buffer
+    assert best.value == -1
+
+
 def test_int8_output_needs_the_quantising_entry_point(tc):
     assert tc.gemm_bf16_raw(16, 8, 16, FAKE, 16, FAKE * 2, 16, FAKE * 4, 16, 1.0, 0.0, 2, 0) == 1
     assert "scale" in tc.binding.last_error()
