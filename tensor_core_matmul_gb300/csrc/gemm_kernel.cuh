@@ -46,6 +46,8 @@
 #include <cuda_bf16.h>
 #include <cstdint>
 
+#include <type_traits>
+
 #include "ptx.cuh"
 
 namespace tcg {
@@ -715,14 +717,20 @@ __global__ void __launch_bounds__(192, 1)
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer --
         if (lane == 0 && (CTA_GROUP == 1 || rank == 0)) {
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            // The units' MMAs.  MN: either operand MN-major (descriptors and
+            // steps chosen per operand at run time); otherwise the K-major
+            // code with constant steps.  The single thread issuing MMAs is on
+            // the critical path, so the common layout keeps its own copy.
+            auto issue_units = [&](auto mn_tag) {
+            constexpr bool MN = decltype(mn_tag)::value;
             // Bits 15 / 16 of the instruction descriptor: A / B MN-major.
             const uint32_t kIdesc = (IN == 1 ? idesc_f8_f32(Cfg::kBM, BN, static_cast<uint32_t>(p.in_fmt) & 1u)
                                              : idesc_bf16_f32(Cfg::kBM, BN)) |
-                                    (p.a_mn ? (1u << 15) : 0u) | (p.b_mn ? (1u << 16) : 0u);
+                                    (MN && p.a_mn ? (1u << 15) : 0u) | (MN && p.b_mn ? (1u << 16) : 0u);
             // Descriptor step per MMA: 32 bytes along a K-major row, two
             // 1 KB K groups in an MN-major tile (in 16-byte units).
-            const uint32_t a_step = p.a_mn ? 128u : 2u, b_step = p.b_mn ? 128u : 2u;
-            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            const uint32_t a_step = MN && p.a_mn ? 128u : 2u, b_step = MN && p.b_mn ? 128u : 2u;
             bool ok = true;
             UnitIter it(cluster_id, num_clusters);
             it.start(p);
@@ -739,12 +747,18 @@ __global__ void __launch_bounds__(192, 1)
                     }
                     tc_fence_after_sync();
                     const uint32_t sa = sA0 + stage * Cfg::kABytes, sb = sB0 + stage * Cfg::kBBytes;
-                    const uint64_t ad = p.a_mn ? sdesc_mnmajor_sw128(sa) : sdesc_kmajor_sw128(sa);
-                    const uint64_t bd = p.b_mn ? sdesc_mnmajor_sw128(sb) : sdesc_kmajor_sw128(sb);
+                    const uint64_t ad = MN && p.a_mn ? sdesc_mnmajor_sw128(sa) : sdesc_kmajor_sw128(sa);
+                    const uint64_t bd = MN && p.b_mn ? sdesc_mnmajor_sw128(sb) : sdesc_kmajor_sw128(sb);
 #pragma unroll
                     for (int k = 0; k < Cfg::kBK / Cfg::kUmmaK; ++k) {
-                        mma_tc<CTA_GROUP, IN>(d_tmem, ad + a_step * k, bd + b_step * k, idesc,
-                                              (kb != u.kb0 || k != 0) ? 1u : 0u);
+                        if constexpr (MN) {
+                            mma_tc<CTA_GROUP, IN>(d_tmem, ad + a_step * k, bd + b_step * k, idesc,
+                                                  (kb != u.kb0 || k != 0) ? 1u : 0u);
+                        } else {
+                            // +32 bytes along K per step: (32 >> 4) = 2 in the address field.
+                            mma_tc<CTA_GROUP, IN>(d_tmem, ad + 2u * k, bd + 2u * k, idesc,
+                                                  (kb != u.kb0 || k != 0) ? 1u : 0u);
+                        }
                     }
                     if constexpr (MC == 4) {
                         // The stage is free once this CTA and both partners
@@ -772,6 +786,13 @@ __global__ void __launch_bounds__(192, 1)
                 acc ^= 1u;
                 if (acc == 0) acc_phase ^= 1u;
             }
+            };
+            if (p.a_mn || p.b_mn) {
+                issue_units(std::true_type{});
+            } else {
+                issue_units(std::false_type{});
+            }
+
             // Drain: all MMAs issued by this thread have completed.
             if constexpr (CTA_GROUP == 1) {
                 mma_commit(drain_bar);
