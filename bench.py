@@ -282,7 +282,8 @@ def run_ours(args) -> None:
 
     peaks, peak_src = load_peaks()
     tag = (f"gemm_{args.config}_full" + ("" if args.epilogue == "none" else f"_{args.epilogue}")
-           + ("" if args.in_format == "bf16" else f"_{args.in_format}") + ("_quant" if args.quant else ""))
+           + ("" if args.in_format == "bf16" else f"_{args.in_format}") + ("_quant" if args.quant else "")
+           + ("" if args.layout == "tn" else f"_{args.layout}"))
     traffic = profile_traffic(tag)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     variant = args.variant or (tuned["variant"] if tuned else tc.pick_variant(M, N, K, sms))
