@@ -75,8 +75,14 @@ typedef enum {
                                    stages and 64-row A tiles when M <= 64): the choice for
                                    M <= 128, where B is streamed from memory once */
     TCGEMM_VARIANT_2CTA_W256 = 5, /* as TCGEMM_VARIANT_2CTA with the tile width fixed at 256 */
-    TCGEMM_VARIANT_SWAP_N64 = 6   /* the transposed product C^T = B^T A^T on 128 x 64 tiles (128
+    TCGEMM_VARIANT_SWAP_N64 = 6,  /* the transposed product C^T = B^T A^T on 128 x 64 tiles (128
                                     columns of C by up to 64 rows): the choice for M <= 64 */
+    TCGEMM_VARIANT_SWAP_N64_KS2 = 7 /* as TCGEMM_VARIANT_SWAP_N64, each tile computed by a cluster
+                                      of 2 CTAs that split its k-blocks in halves; the second
+                                      CTA's fp32 partial is added to the first's through
+                                      distributed shared memory (first half + second half), so no
+                                      workspace and no second kernel: the choice for M <= 64 when
+                                      the tiles fill 3/4 to 1 round of 2-CTA clusters */
 } tcgemm_variant_t;
 
 /* C = alpha*A*B + beta*C as described above.  Returns TCGEMM_OK once the work
@@ -348,8 +354,9 @@ int tcgemm_pick_variant(int64_t M, int64_t N, int64_t K, int num_sms);
  * visiting order walks (tiles, or 2 x 2 tile blocks for variant 3), out[17] =
  * 1 when stream-K is used, out[18] = rows of A loaded per CTA (64 for M <= 64
  * with variant 4, else 128), out[19] = 1 when the launch computes the
- * transposed product (variant 6; then out[2..] describe C^T).  `out` must
- * hold 20 values.  Returns TCGEMM_OK or TCGEMM_ERR_INVALID_ARG.  Needs no
+ * transposed product (variants 6 and 7; then out[2..] describe C^T),
+ * out[20] = CTAs of a cluster that split each tile's k-blocks (2 for
+ * variant 7, else 1).  `out` must hold 21 values.  Returns TCGEMM_OK or TCGEMM_ERR_INVALID_ARG.  Needs no
  * GPU. */
 int tcgemm_plan(int64_t M, int64_t N, int64_t K, int variant, int num_sms, int64_t* out);
 

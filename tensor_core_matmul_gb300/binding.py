@@ -23,7 +23,7 @@ OUT_I8 = 2
 IN_BF16, IN_E4M3, IN_E5M2 = range(3)
 ROW_MAJOR, COL_MAJOR = range(2)
 (VARIANT_AUTO, VARIANT_1CTA, VARIANT_2CTA, VARIANT_1CTA_MC, VARIANT_1CTA_N64, VARIANT_2CTA_W256,
- VARIANT_SWAP_N64) = range(7)
+ VARIANT_SWAP_N64, VARIANT_SWAP_N64_KS2) = range(8)
 
 ACT_NONE, ACT_RELU, ACT_GELU, ACT_GELU_TANH = range(4)
 ACTIVATIONS = {"none": ACT_NONE, "relu": ACT_RELU, "gelu": ACT_GELU, "gelu_tanh": ACT_GELU_TANH}
@@ -402,7 +402,7 @@ def pick_variant(M: int, N: int, K: int, num_sms: int) -> int:
 
 PLAN_KEYS = ["grid", "cluster", "tiles_m", "tiles_n", "bm", "bn", "num_kb", "smem", "tiles_dp",
              "sk_tiles", "sk_iters", "ws_bytes", "group_m", "variant", "cta_group", "grid_m", "grid_n",
-             "stream_k", "arows", "swap"]
+             "stream_k", "arows", "swap", "ks"]
 
 
 def plan(M: int, N: int, K: int, variant: int = 0, num_sms: int = 152, in_kind: int = 0, a_col: bool = False,

@@ -339,7 +339,7 @@ struct GemmCfg {
     static constexpr uint32_t kEpiOff = STAGES * (kABytes + kBBytes);
     static constexpr uint32_t kEpiBytes = 2 * kEpiBufBytes;
     static constexpr uint32_t kBarOff = kEpiOff + kEpiBytes;
-    static constexpr uint32_t kNumBars = 2 * STAGES + 4 + 1 + 2;
+    static constexpr uint32_t kNumBars = 2 * STAGES + 4 + 1 + 2 + 2;
     // The fused epilogue's bias values for the current tile's BN columns
     // (fp32), staged once per tile.
     static constexpr uint32_t kBiasOff = (kBarOff + kNumBars * 8 + 16 + 15) / 16 * 16;
@@ -558,7 +558,15 @@ constexpr uint32_t kEpiThreads = 128;
 // SWAP: the launch computes D = C^T (the host swapped A with B and M with N);
 // D's rows are C's columns, so the epilogue writes each TMEM row as a
 // contiguous run of one column of C (D row-major with leading dimension ldc).
-template <int CTA_GROUP, int BN, int STAGES, int MC, int AROWS, bool SWAP, typename OutT, int IN = 0>
+// KS = 2 (transposed product only): a cluster of two CTAs computes each tile,
+// CTA 0 over the first half of its k-blocks and CTA 1 over the second half.
+// CTA 1 leaves its fp32 partial tile in its shared memory (the epilogue
+// staging area, [column][row]); CTA 0 adds it to its own accumulator through
+// distributed shared memory (first half + second half, always in that
+// order) and runs the epilogue.  Two barriers hand the buffer back and forth:
+// xfull on CTA 0 (one arrival per epilogue warp of CTA 1), xfree on CTA 1
+// (one per epilogue warp of CTA 0).
+template <int CTA_GROUP, int BN, int STAGES, int MC, int AROWS, bool SWAP, typename OutT, int IN = 0, int KS = 1>
 __global__ void __launch_bounds__(192, 1)
     gemm_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
@@ -566,7 +574,9 @@ __global__ void __launch_bounds__(192, 1)
     using Cfg = GemmCfg<CTA_GROUP, BN, STAGES, AROWS, IN>;
     static_assert(MC == 1 || (MC == 4 && CTA_GROUP == 1 && AROWS == 128), "multicast clusters use single-CTA MMAs");
     static_assert(!SWAP || (CTA_GROUP == 1 && MC == 1), "the swapped product runs on single-CTA tiles");
-    constexpr int kCluster = CTA_GROUP * MC;
+    static_assert(KS == 1 || (KS == 2 && SWAP && Cfg::kEpiBytes >= 128u * BN * 4u),
+                  "the K split exchanges a whole fp32 tile through the staging area");
+    constexpr int kCluster = CTA_GROUP * MC * KS;
     extern __shared__ uint8_t smem_raw[];
 
     // 1 KB-aligned carve-up: [A stages][B stages][barriers][tmem slot][abort][last flag]
@@ -582,6 +592,8 @@ __global__ void __launch_bounds__(192, 1)
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
     const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
     auto cold_bar = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 5 + b); };  // C chunk loads
+    const uint32_t xfull_bar = bar0 + 8u * (2 * STAGES + 7);  // KS = 2, on CTA 0: CTA 1's partial is staged
+    const uint32_t xfree_bar = bar0 + 8u * (2 * STAGES + 8);  // KS = 2, on CTA 1: CTA 0 has read it
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kBarOff + Cfg::kNumBars * 8);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
@@ -591,6 +603,16 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t rank = (CTA_GROUP == 2) ? crank : 0u;  // position in the MMA pair
     const uint32_t rm = (MC == 4) ? (crank & 1u) : 0u;    // position in the 2 x 2 block
     const uint32_t rn = (MC == 4) ? (crank >> 1) : 0u;
+    const uint32_t ks_rank = (KS == 2) ? crank : 0u;       // which half of each tile's k-blocks
+    // This CTA's share of a unit's k-blocks: the first half (rounded up) for
+    // CTA 0 of a K-split cluster, the rest for CTA 1.
+    auto ks_range = [&](WorkUnit& u) {
+        if constexpr (KS == 2) {
+            const int mid = u.kb0 + (u.kb1 - u.kb0 + 1) / 2;
+            if (ks_rank == 0) u.kb1 = mid;
+            else u.kb0 = mid;
+        }
+    };
     const int cluster_id = blockIdx.x / kCluster;
     const int num_clusters = gridDim.x / kCluster;
     auto tile_of = [&](int unit_tile, int& tm, int& tn) {
@@ -613,6 +635,8 @@ __global__ void __launch_bounds__(192, 1)
         mbar_init(drain_bar, 1);
         mbar_init(cold_bar(0), 1);
         mbar_init(cold_bar(1), 1);
+        mbar_init(xfull_bar, 4);
+        mbar_init(xfree_bar, 4);
         *abort_flag = 0u;
         fence_barrier_init();
     }
@@ -639,6 +663,7 @@ __global__ void __launch_bounds__(192, 1)
             it.start(p);
             WorkUnit u;
             while (ok && it.next(p, u)) {
+                ks_range(u);
                 int tm, tn;
                 tile_of(u.tile, tm, tn);
                 const int a_row = tm * Cfg::kBM + static_cast<int>(rank) * Cfg::kRowsA;
@@ -736,6 +761,7 @@ __global__ void __launch_bounds__(192, 1)
             it.start(p);
             WorkUnit u;
             while (ok && it.next(p, u)) {
+                ks_range(u);
                 if (!wait_phase<CTA_GROUP == 2>(tempty_bar(acc), acc_phase ^ 1u, wctx, kWhereMma)) break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * BN;
@@ -822,6 +848,7 @@ __global__ void __launch_bounds__(192, 1)
         bool aborted = false;
         if (leader) tma_prefetch_desc(&tmC);
         uint32_t acc = 0, acc_phase = 0;
+        uint32_t xph = 0;  // KS = 2: parity of the next exchange
         UnitIter it(cluster_id, num_clusters);
             it.start(p);
         WorkUnit u;
@@ -871,15 +898,58 @@ __global__ void __launch_bounds__(192, 1)
             // granule at row M would also write rows M.. of the ldc padding:
             // that block is stored with masked plain stores instead.
             const bool tma_rows = row_blk + 128 <= p.M || ((static_cast<int64_t>(p.M) * sizeof(OutT)) % 16) == 0;
-            if (SWAP && u.slot < 0) {
+            if (KS == 2 && ks_rank == 1) {
+                // Second half of a K-split tile: stage the fp32 partial for
+                // CTA 0 once it has read the previous one.
+                uint32_t okx = 1;
+                if (lane == 0) okx = wait_phase<true>(xfree_bar, xph ^ 1u, wctx, kWhereEpilogue) ? 1u : 0u;
+                okx = __shfl_sync(0xffffffffu, okx, 0);
+                if (!named_barrier_and(kEpiBarrier, kEpiThreads, okx != 0u)) break;
+                float* xb = reinterpret_cast<float*>(smem + Cfg::kEpiOff) + row_local;
+#pragma unroll 1
+                for (int c = 0; c < ncols; c += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tbase + c, r);
+                    tmem_ld_wait32(r);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) xb[(c + j) * 128] = __uint_as_float(r[j]);
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(tempty_bar(acc));
+                    mbar_arrive_cluster(map_to_cta(xfull_bar, 0));
+                }
+                xph ^= 1u;
+            } else if (SWAP && u.slot < 0) {
                 // D row `row` = column `row` of C; D columns = rows of C.
+                // K split: CTA 1's partial (the second half of the k-blocks,
+                // read from its staging area through distributed shared
+                // memory) is added to this CTA's (the first half).
+                uint32_t xrow = 0;
+                if constexpr (KS == 2) {
+                    uint32_t okx = 1;
+                    if (lane == 0) okx = wait_phase<true>(xfull_bar, xph, wctx, kWhereEpilogue) ? 1u : 0u;
+                    okx = __shfl_sync(0xffffffffu, okx, 0);
+                    if (!named_barrier_and(kEpiBarrier, kEpiThreads, okx != 0u)) break;
+                    xrow = map_to_cta(base + Cfg::kEpiOff, 1) + row_local * 4u;
+                }
 #pragma unroll 1
                 for (int c = 0; c < ncols; c += 32) {
                     const int64_t col0 = colt + c;
                     if (col0 >= p.N) break;
                     uint32_t r[32];
                     tmem_ld32(tbase + c, r);
-                    tmem_ld_wait32(r);
+                    if constexpr (KS == 2) {
+                        float x[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) x[j] = ld_dsmem_f32(xrow + static_cast<uint32_t>(c + j) * 512u);
+                        tmem_ld_wait32(r);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + x[j]);
+                    } else {
+                        tmem_ld_wait32(r);
+                    }
                     if (row_ok) {
                         OutT* dst = C + row * p.ldc + col0;
                         if (fused) {
@@ -892,7 +962,11 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty_bar(acc));
+                if (lane == 0) {
+                    mbar_arrive(tempty_bar(acc));
+                    if constexpr (KS == 2) mbar_arrive_cluster(map_to_cta(xfree_bar, 1));
+                }
+                if constexpr (KS == 2) xph ^= 1u;
             } else if (u.slot < 0 && !tma_rows) {
 #pragma unroll 1
                 for (int c = 0; c < ncols; c += 32) {

@@ -95,6 +95,7 @@ struct Plan {
     uint32_t smem = 0;
     uint64_t slot_bytes = 0;  // workspace bytes per stream-K partial piece
     uint64_t ws_bytes = 0;    // workspace this plan needs (0 without stream-K)
+    int ks = 1;               // CTAs of a cluster that split each tile's k-blocks (2: variant 7)
     void* ws_ptr = nullptr;   // the workspace of this launch
 };
 
@@ -150,7 +151,17 @@ double est_launch_us(int64_t tiles, int64_t units, int64_t num_kb, double mma_cy
 // 47.5 us against 24.2 us (GB300).  in_kind 1: 8-bit operands (a k-block of
 // 128 values, the MMA twice as fast).
 int pick_variant(int64_t M, int64_t N, int64_t K, int sms, int in_kind = 0) {
-    if (M <= 64 && N >= 256) return TCGEMM_VARIANT_SWAP_N64;
+    if (M <= 64 && N >= 256) {
+        // The transposed product.  When its 128-row tiles fill between three
+        // quarters of a round and a whole round of 2-CTA clusters, each tile's
+        // k-blocks are split over the two CTAs of a cluster (no reduction
+        // pass); otherwise stream-K shares them out when it pays.
+        const int64_t tiles = (N + 127) / 128;
+        const int64_t num_kb = (K + (in_kind == 1 ? 127 : 63)) / (in_kind == 1 ? 128 : 64);
+        if (num_kb >= 8 && 2 * tiles <= sms && 8 * tiles >= 3 * static_cast<int64_t>(sms))
+            return TCGEMM_VARIANT_SWAP_N64_KS2;
+        return TCGEMM_VARIANT_SWAP_N64;
+    }
     if (M <= 128) return TCGEMM_VARIANT_1CTA_N64;
     const int64_t num_kb = (K + (in_kind == 1 ? 127 : 63)) / (in_kind == 1 ? 128 : 64);
     const double mma_scale = in_kind == 1 ? 0.5 : 1.0;
@@ -182,7 +193,7 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pa
     if (variant == TCGEMM_VARIANT_AUTO) variant = pick_variant(M, N, K, sms, in_kind);
     pl.variant = variant;
     allow_split = allow_split && split_enabled();
-    if (variant == TCGEMM_VARIANT_SWAP_N64) {
+    if (variant == TCGEMM_VARIANT_SWAP_N64 || variant == TCGEMM_VARIANT_SWAP_N64_KS2) {
         // The transposed product: its M is N, its N is M.
         pl.swap = 1;
         std::swap(M, N);
@@ -220,10 +231,13 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pa
         pl.bm = Cfg1::kBM;
         pl.bn = 256;
         pl.smem = Cfg1::kSmemBytes;
-    } else if (variant == TCGEMM_VARIANT_1CTA_N64 || variant == TCGEMM_VARIANT_SWAP_N64) {
+    } else if (variant == TCGEMM_VARIANT_1CTA_N64 || variant == TCGEMM_VARIANT_SWAP_N64 ||
+               variant == TCGEMM_VARIANT_SWAP_N64_KS2) {
         pl.cta_group = 1;
         pl.bm = CfgN64::kBM;
         pl.bn = 64;
+        // Each CTA of the cluster needs at least one k-block.
+        if (variant == TCGEMM_VARIANT_SWAP_N64_KS2 && num_kb >= 2) pl.ks = 2;
         pl.arows = (!pl.swap && M <= 64) ? 64 : 128;
         pl.smem = pl.arows == 64 ? CfgN64h::kSmemBytes : CfgN64::kSmemBytes;
     } else {
@@ -238,12 +252,13 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pa
     const int64_t tiles = static_cast<int64_t>(pl.grid_m) * pl.grid_n;  // units of the order
     if (tiles > (int64_t{1} << 30)) return false;
     int64_t clusters = sms;
-    if (pl.cta_group == 2) clusters = std::max(1, max_pairs > 0 ? max_pairs : sms / 2);
+    if (pl.cta_group == 2 || pl.ks == 2) clusters = std::max(1, max_pairs > 0 ? max_pairs : sms / 2);
+    if (pl.ks == 2) allow_split = false;  // the split is the cluster's
     if (pl.mc == 4) {
         clusters = std::max(1, max_quads > 0 ? max_quads : sms / 4);
         allow_split = false;  // the 2 x 2 blocks are scheduled whole
     }
-    const int csize = pl.cta_group * pl.mc;
+    const int csize = pl.cta_group * pl.mc * pl.ks;
     pl.tiles_dp = static_cast<int>(tiles);
     pl.sk_tiles = 0;
     pl.sk_iters = 0;
@@ -350,13 +365,13 @@ bool encode_mnmajor(CUtensorMap* m, const void* ptr, int64_t mn_extent, int64_t 
 
 // The dynamic shared-memory opt-in is a per-kernel attribute; it is set once
 // per device for each kernel instantiation.
-template <int CG, int BN, int ST, int MC, int AR, bool SW, typename OutT, int IN = 0>
+template <int CG, int BN, int ST, int MC, int AR, bool SW, typename OutT, int IN = 0, int KS = 1>
 bool ensure_smem_attr(int dev) {
     static std::mutex mu;
     static bool done[kMaxDevices] = {};
     std::lock_guard<std::mutex> lk(mu);
     if (done[dev]) return true;
-    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, MC, AR, SW, OutT, IN>;
+    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, MC, AR, SW, OutT, IN, KS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(tcg::GemmCfg<CG, BN, ST, AR, IN>::kSmemBytes));
     if (e != cudaSuccess) {
@@ -367,11 +382,11 @@ bool ensure_smem_attr(int dev) {
     return true;
 }
 
-template <int CG, int BN, int ST, int MC, int AR, bool SW, typename OutT, int IN = 0>
+template <int CG, int BN, int ST, int MC, int AR, bool SW, typename OutT, int IN = 0, int KS = 1>
 int launch_gemm(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tcm,
                 const CUtensorMap& twm, const tcg::GemmParams& gp, cudaStream_t stream, int dev) {
-    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, MC, AR, SW, OutT, IN>;
-    if (!ensure_smem_attr<CG, BN, ST, MC, AR, SW, OutT, IN>(dev)) return TCGEMM_ERR_CUDA;
+    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, MC, AR, SW, OutT, IN, KS>;
+    if (!ensure_smem_attr<CG, BN, ST, MC, AR, SW, OutT, IN, KS>(dev)) return TCGEMM_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(pl.grid), 1, 1);
     cfg.blockDim = dim3(tcg::GemmCfg<CG, BN, ST, AR>::kThreads, 1, 1);
@@ -379,9 +394,9 @@ int launch_gemm(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, co
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     cfg.numAttrs = 0;
-    if (CG * MC > 1) {
+    if (CG * MC * KS > 1) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = CG * MC;
+        attr[0].val.clusterDim.x = CG * MC * KS;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
@@ -599,7 +614,7 @@ int noalloc_scratch(int dev, void** out) {
 
 void fill_plan_out(const Plan& pl, int64_t* out) {
     out[0] = pl.grid;
-    out[1] = pl.cta_group * pl.mc;
+    out[1] = pl.cta_group * pl.mc * pl.ks;
     out[2] = pl.tiles_m;
     out[3] = pl.tiles_n;
     out[4] = pl.bm;
@@ -618,6 +633,7 @@ void fill_plan_out(const Plan& pl, int64_t* out) {
     out[17] = pl.sk_tiles > 0 ? 1 : 0;
     out[18] = pl.arows;
     out[19] = pl.swap;
+    out[20] = pl.ks;
 }
 
 constexpr int kWsInternal = 0;
@@ -705,7 +721,7 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
              int ws_mode = kWsInternal, void* ws = nullptr, int64_t ws_bytes = 0, const Epilogue& ep = Epilogue(),
              int in_kind = 0, int in_fmt = 0, bool a_col = false, bool b_row = false) {
     t_last_error[0] = '\0';
-    if (variant < TCGEMM_VARIANT_AUTO || variant > TCGEMM_VARIANT_SWAP_N64) {
+    if (variant < TCGEMM_VARIANT_AUTO || variant > TCGEMM_VARIANT_SWAP_N64_KS2) {
         set_error("unknown variant %d", variant);
         return TCGEMM_ERR_INVALID_ARG;
     }
@@ -879,6 +895,9 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
 #define TCGEMM_LAUNCH_I8(CG, BN, ST, MC, AR, SW)                                                             \
     return in_kind == 1 ? launch_gemm<CG, BN, ST, MC, AR, SW, int8_t, 1>(pl, ta, tb, tcm, twm, gp, stream, dev) \
                         : launch_gemm<CG, BN, ST, MC, AR, SW, int8_t, 0>(pl, ta, tb, tcm, twm, gp, stream, dev)
+        if (pl.swap && pl.ks == 2)
+            return in_kind == 1 ? launch_gemm<1, 64, kStagesN64, 1, 128, true, int8_t, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
+                                : launch_gemm<1, 64, kStagesN64, 1, 128, true, int8_t, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
         if (pl.swap) TCGEMM_LAUNCH_I8(1, 64, kStagesN64, 1, 128, true);
         if (pl.bn == 64 && pl.arows == 64) TCGEMM_LAUNCH_I8(1, 64, kStagesN64h, 1, 64, false);
         if (pl.bn == 64) TCGEMM_LAUNCH_I8(1, 64, kStagesN64, 1, 128, false);
@@ -894,6 +913,9 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
 #define TCGEMM_LAUNCH8(CG, BN, ST, MC, AR, SW)                                                                  \
     return bf16 ? launch_gemm<CG, BN, ST, MC, AR, SW, __nv_bfloat16, 1>(pl, ta, tb, tcm, twm, gp, stream, dev) \
                 : launch_gemm<CG, BN, ST, MC, AR, SW, float, 1>(pl, ta, tb, tcm, twm, gp, stream, dev)
+        if (pl.swap && pl.ks == 2)
+            return bf16 ? launch_gemm<1, 64, kStagesN64, 1, 128, true, __nv_bfloat16, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
+                        : launch_gemm<1, 64, kStagesN64, 1, 128, true, float, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
         if (pl.swap) TCGEMM_LAUNCH8(1, 64, kStagesN64, 1, 128, true);
         if (pl.bn == 64 && pl.arows == 64) TCGEMM_LAUNCH8(1, 64, kStagesN64h, 1, 64, false);
         if (pl.bn == 64) TCGEMM_LAUNCH8(1, 64, kStagesN64, 1, 128, false);
@@ -907,6 +929,9 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     return bf16 ? launch_gemm<CG, BN, ST, MC, AR, SW, __nv_bfloat16>(pl, ta, tb, tcm, twm, gp, stream, dev) \
                 : launch_gemm<CG, BN, ST, MC, AR, SW, float>(pl, ta, tb, tcm, twm, gp, stream, dev)
     if (pl.mc == 4) TCGEMM_LAUNCH(1, 256, kStages1, 4, 128, false);
+    if (pl.swap && pl.ks == 2)
+        return bf16 ? launch_gemm<1, 64, kStagesN64, 1, 128, true, __nv_bfloat16, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
+                    : launch_gemm<1, 64, kStagesN64, 1, 128, true, float, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
     if (pl.swap) TCGEMM_LAUNCH(1, 64, kStagesN64, 1, 128, true);
     if (pl.bn == 64 && pl.arows == 64) TCGEMM_LAUNCH(1, 64, kStagesN64h, 1, 64, false);
     if (pl.bn == 64) TCGEMM_LAUNCH(1, 64, kStagesN64, 1, 128, false);
@@ -1029,8 +1054,9 @@ int tcgemm_autotune(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
             return TCGEMM_ERR_CUDA;
         }
     }
-    const int candidates[] = {TCGEMM_VARIANT_2CTA, TCGEMM_VARIANT_2CTA_W256, TCGEMM_VARIANT_1CTA,
-                              TCGEMM_VARIANT_1CTA_MC, TCGEMM_VARIANT_1CTA_N64, TCGEMM_VARIANT_SWAP_N64};
+    const int candidates[] = {TCGEMM_VARIANT_2CTA,    TCGEMM_VARIANT_2CTA_W256, TCGEMM_VARIANT_1CTA,
+                              TCGEMM_VARIANT_1CTA_MC, TCGEMM_VARIANT_1CTA_N64,  TCGEMM_VARIANT_SWAP_N64,
+                              TCGEMM_VARIANT_SWAP_N64_KS2};
     int best = TCGEMM_VARIANT_AUTO;
     float best_t = 0.0f;
     rc = TCGEMM_OK;
@@ -1165,7 +1191,7 @@ int tcgemm_units(int64_t M, int64_t N, int64_t K, int variant, int num_sms, int 
     if (out == nullptr || M <= 0 || N <= 0 || K <= 0 || num_sms <= 0 || max_units < 0) return -1;
     Plan pl;
     if (!make_plan(M, N, K, variant, num_sms, num_sms / 2, num_sms / 4, pl)) return -1;
-    const int clusters = pl.grid / (pl.cta_group * pl.mc);
+    const int clusters = pl.grid / (pl.cta_group * pl.mc * pl.ks);
     if (cluster < 0 || cluster >= clusters) return -1;
     tcg::GemmParams gp = {};
     gp.num_kb = pl.num_kb;

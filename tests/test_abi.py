@@ -190,7 +190,7 @@ def test_tile_order_groups_for_l2(tc):
 
 @pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (8192, 8192, 8192), (4000, 4100, 4104),
                                    (64, 8192, 8192), (256, 256, 256), (1, 1, 1)])
-@pytest.mark.parametrize("variant", [1, 2, 3, 4, 5, 6])
+@pytest.mark.parametrize("variant", [1, 2, 3, 4, 5, 6, 7])
 def test_plans(tc, M, N, K, variant):
     p = tc.plan(M, N, K, variant, 152)
     if p["swap"]:
@@ -208,7 +208,7 @@ SK_SHAPES = [(4096, 4096, 4096), (8192, 8192, 8192), (4000, 4100, 4104), (64, 81
 
 
 @pytest.mark.parametrize("M,N,K", SK_SHAPES)
-@pytest.mark.parametrize("variant", [1, 2, 3, 4, 5, 6])
+@pytest.mark.parametrize("variant", [1, 2, 3, 4, 5, 6, 7])
 @pytest.mark.parametrize("sms", [152, 148, 20])
 def test_stream_k_plan_invariants(tc, M, N, K, variant, sms):
     p = tc.plan(M, N, K, variant, sms)
@@ -298,8 +298,25 @@ def test_width_choice(tc):
     assert tc.plan(512, 512, 16384, 2, 152)["stream_k"] == 1    # 4 tiles, long K
 
 
+def test_k_split_plan(tc):
+    """Variant 7: the transposed product with each tile's k-blocks split over
+    a 2-CTA cluster: two CTAs per tile, no stream-K, no workspace; a single
+    k-block cannot be split and runs on one CTA per tile."""
+    p = tc.plan(64, 8192, 8192, 7, 152)
+    assert (p["swap"], p["ks"], p["cluster"], p["grid"], p["stream_k"], p["ws_bytes"]) == (1, 2, 2, 128, 0, 0)
+    assert p["tiles_m"] == 64 and p["tiles_n"] == 1 and p["bn"] == 64
+    p = tc.plan(40, 30000, 640, 7, 152)      # 235 tiles: rounds of 76 clusters
+    assert p["ks"] == 2 and p["grid"] == 152 and p["stream_k"] == 0
+    p = tc.plan(64, 8192, 64, 7, 152)
+    assert p["ks"] == 1 and p["cluster"] == 1
+    assert tc.plan(64, 8192, 8192, 6, 152)["ks"] == 1
+
+
 def test_auto_variant_choice(tc):
-    assert tc.pick_variant(64, 8192, 8192, 152) == 6
+    assert tc.pick_variant(64, 8192, 8192, 152) == 7      # 64 tiles: 128 of 152 SMs, K split in halves
+    assert tc.pick_variant(64, 4096, 8192, 152) == 6      # 32 tiles: stream-K over all SMs instead
+    assert tc.pick_variant(64, 8192, 256, 152) == 6       # 4 k-blocks: too short to split
+    assert tc.pick_variant(64, 12288, 8192, 152) == 6     # 96 tiles: more than a round of clusters
     assert tc.pick_variant(128, 4096, 4096, 152) == 4
     assert tc.pick_variant(64, 128, 4096, 152) == 4
     assert tc.pick_variant(129, 4096, 4096, 152) == 2

@@ -17,7 +17,7 @@ from tests import parity
 
 pytestmark = pytest.mark.gpu
 
-FP8_VARIANTS = [int(v) for v in os.environ.get("FP8_VARIANTS", "0,2,4,5,6").split(",")]
+FP8_VARIANTS = [int(v) for v in os.environ.get("FP8_VARIANTS", "0,2,4,5,6,7").split(",")]
 FORMATS = ["e4m3", "e5m2"]
 
 

@@ -16,7 +16,7 @@ from tests import parity
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = [int(v) for v in os.environ.get("LAYOUT_VARIANTS", "0,1,2,4,5,6").split(",")]
+VARIANTS = [int(v) for v in os.environ.get("LAYOUT_VARIANTS", "0,1,2,4,5,6,7").split(",")]
 LAYOUTS = [(True, False), (False, True), (True, True)]
 IDS = ["NN(A col)", "TT(B row)", "NT(both)"]
 

@@ -26,7 +26,7 @@ from tests import parity
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = [int(v) for v in os.environ.get("QUANT_VARIANTS", "0,2,4,5,6").split(",")]
+VARIANTS = [int(v) for v in os.environ.get("QUANT_VARIANTS", "0,2,4,5,6,7").split(",")]
 GUARD = 4096
 SENT = 0x5A
 
