@@ -623,6 +623,16 @@ __global__ void __launch_bounds__(192, 1)
         }
     };
 
+    // Single-CTA MMAs: the producer needs nothing but its own barriers, so it
+    // starts loading as soon as they are initialised, while the TMEM
+    // allocation and the (cluster) barrier complete for the other warps.
+    constexpr bool kEarlyProducer = CTA_GROUP == 1 && MC == 1;
+    if (threadIdx.x == 0) {
+        // The descriptors' first fetch overlaps the set-up.
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 2 && lane == 0) tma_prefetch_desc(&tmC);
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
@@ -641,21 +651,33 @@ __global__ void __launch_bounds__(192, 1)
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc<CTA_GROUP>(smem_u32(tmem_slot), Cfg::kTmemAlloc);
-    tc_fence_before_sync();
-    if constexpr (kCluster == 1) {
-        __syncthreads();
+    if (kEarlyProducer && warp == 0) {
+        // Arrive now, wait (cluster) after the loads are issued.
+        __syncwarp();
+        if constexpr (kCluster == 1) {
+            named_barrier_arrive(0, Cfg::kThreads);
+        } else {
+            cluster_arrive();
+        }
     } else {
-        cluster_sync();
+        tc_fence_before_sync();
+        if constexpr (kCluster == 1) {
+            if constexpr (kEarlyProducer) {
+                named_barrier_sync(0, Cfg::kThreads);
+            } else {
+                __syncthreads();
+            }
+        } else {
+            cluster_sync();
+        }
+        tc_fence_after_sync();
     }
-    tc_fence_after_sync();
-    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t tmem_base = *tmem_slot;  // not read by an early producer
     const WaitCtx wctx{abort_flag, p.timeout_ns};
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer --
         if (lane == 0) {
-            tma_prefetch_desc(&tmA);
-            tma_prefetch_desc(&tmB);
             uint32_t stage = 0, phase = 0;
             uint64_t issued = 0;
             bool ok = true;
@@ -738,6 +760,11 @@ __global__ void __launch_bounds__(192, 1)
                     wait_phase<false>(empty_bar(s), par, wctx, kWhereDrain);
                 }
             }
+        }
+        if constexpr (kEarlyProducer && kCluster > 1) {
+            // The wait that goes with the early arrive above.
+            __syncwarp();
+            cluster_wait();
         }
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer --
@@ -846,7 +873,6 @@ __global__ void __launch_bounds__(192, 1)
         uint32_t nchunk = 0;      // chunks staged so far; chunk i uses buffer i & 1
         uint32_t cold_phase = 0;  // bit b: parity of the next completion of cold_bar(b)
         bool aborted = false;
-        if (leader) tma_prefetch_desc(&tmC);
         uint32_t acc = 0, acc_phase = 0;
         uint32_t xph = 0;  // KS = 2: parity of the next exchange
         UnitIter it(cluster_id, num_clusters);

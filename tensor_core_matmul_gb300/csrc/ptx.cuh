@@ -123,6 +123,16 @@ __device__ __forceinline__ void cluster_sync() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The two halves of cluster_sync, for a warp that arrives early and waits
+// later (every arrive must be followed by a wait before the next arrive).
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // -------------------------------------------------------------------- TMA --
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
@@ -209,6 +219,12 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 // Named barrier among a subset of warps.
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Arrive on a named barrier without waiting (the warp is counted as
+// nthreads' share; the others wait with named_barrier_sync).
+__device__ __forceinline__ void named_barrier_arrive(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // Named barrier that also ANDs a predicate over the participating threads.
