@@ -276,7 +276,12 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pa
     }
     // Band height so that the tiles in flight at once cover a roughly square
     // patch of C: group_m^2 ~ concurrent tiles * (tile width / tile height).
-    const double ideal = std::sqrt(static_cast<double>(pl.grid / csize) * pl.bn / pl.bm);
+    // Pair tiles take a band twice that tall (measured on GB300: 16 instead
+    // of 8 rows of tiles, 4000x4100x4104 110.5 -> 108.3 us, 16384x8192x4096
+    // 594 -> 584 us, the square shapes unchanged): B is fetched from memory
+    // once per band, so fewer bands re-read it less often.
+    const double ideal = std::sqrt(static_cast<double>(pl.grid / csize) * pl.bn / pl.bm) *
+                         (pl.cta_group == 2 ? 2.0 : 1.0);
     int g = 1;
     while (g * 2 <= ideal) g *= 2;
     pl.group_m = std::max(1, std::min(g, pl.grid_m));
