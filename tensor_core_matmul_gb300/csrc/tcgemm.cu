@@ -52,6 +52,51 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+// cuTensorMapEncodeTiled with a small per-thread memo: repeated calls on the
+// same buffers and shapes (the common case in a loop) reuse the descriptor
+// instead of encoding it again.  A descriptor depends only on the arguments
+// below, so a hit is always the descriptor the driver would return.
+struct MapKey {
+    CUtensorMapDataType dt;
+    const void* ptr;
+    cuuint64_t dims[2];
+    cuuint64_t stride;
+    cuuint32_t box[2];
+    CUtensorMapSwizzle swizzle;
+    CUtensorMapL2promotion promo;
+    bool operator==(const MapKey& o) const {
+        return dt == o.dt && ptr == o.ptr && dims[0] == o.dims[0] && dims[1] == o.dims[1] && stride == o.stride &&
+               box[0] == o.box[0] && box[1] == o.box[1] && swizzle == o.swizzle && promo == o.promo;
+    }
+};
+
+CUresult encode_2d(CUtensorMap* m, const MapKey& k) {
+    constexpr int kMemo = 16;
+    thread_local MapKey keys[kMemo];
+    thread_local CUtensorMap maps[kMemo];
+    thread_local bool used[kMemo] = {};
+    thread_local int next = 0;
+    for (int i = 0; i < kMemo; ++i) {
+        if (used[i] && keys[i] == k) {
+            *m = maps[i];
+            return CUDA_SUCCESS;
+        }
+    }
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return CUDA_ERROR_NOT_FOUND;
+    const cuuint64_t strides[1] = {k.stride};
+    const cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = fn(m, k.dt, 2, const_cast<void*>(k.ptr), k.dims, strides, k.box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, k.swizzle, k.promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS) {
+        keys[next] = k;
+        maps[next] = *m;
+        used[next] = true;
+        next = (next + 1) % kMemo;
+    }
+    return r;
+}
+
 uint64_t timeout_ns() {
     static uint64_t ns = [] {
         const char* s = std::getenv("TCGEMM_TIMEOUT_MS");
@@ -295,8 +340,7 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pa
 // mapped the same way (fp32, 128 rows, ldc = 128).
 // out_dtype: TCGEMM_OUT_F32, _BF16 or _I8 (the workspace map uses F32).
 bool encode_c(CUtensorMap* m, void* ptr, int64_t M, int64_t N, int64_t ldc, int out_dtype) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) {
+    if (!encode_fn()) {
         set_error("cuTensorMapEncodeTiled is not available from the driver");
         return false;
     }
@@ -304,12 +348,10 @@ bool encode_c(CUtensorMap* m, void* ptr, int64_t M, int64_t N, int64_t ldc, int 
     const CUtensorMapDataType dt = out_dtype == TCGEMM_OUT_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                    : out_dtype == TCGEMM_OUT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                                   : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(N)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc) * esz};
-    cuuint32_t box[2] = {128u, 32u};
-    cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = fn(m, dt, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const MapKey k{dt, ptr, {static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(N)},
+                   static_cast<cuuint64_t>(ldc) * esz, {128u, 32u}, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE};
+    const CUresult r = encode_2d(m, k);
     if (r != CUDA_SUCCESS) {
         set_error("cuTensorMapEncodeTiled failed (%d) for C %lld x %lld, ldc %lld", static_cast<int>(r),
                   static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(ldc));
@@ -320,20 +362,17 @@ bool encode_c(CUtensorMap* m, void* ptr, int64_t M, int64_t N, int64_t ldc, int 
 
 bool encode_kmajor(CUtensorMap* m, const void* ptr, int64_t k_extent, int64_t rows, int64_t ld,
                    uint32_t box_rows, int elem_bytes = 2) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) {
+    if (!encode_fn()) {
         set_error("cuTensorMapEncodeTiled is not available from the driver");
         return false;
     }
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(k_extent), static_cast<cuuint64_t>(rows)};
     // One 128-byte row per box row: 64 bf16 or 128 8-bit values.
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * static_cast<cuuint64_t>(elem_bytes)};
-    cuuint32_t box[2] = {128u / static_cast<cuuint32_t>(elem_bytes), box_rows};
-    cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = fn(m, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                    const_cast<void*>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const MapKey k{elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ptr,
+                   {static_cast<cuuint64_t>(k_extent), static_cast<cuuint64_t>(rows)},
+                   static_cast<cuuint64_t>(ld) * static_cast<cuuint64_t>(elem_bytes),
+                   {128u / static_cast<cuuint32_t>(elem_bytes), box_rows}, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B};
+    const CUresult r = encode_2d(m, k);
     if (r != CUDA_SUCCESS) {
         set_error("cuTensorMapEncodeTiled failed (%d) for extent %lld x %lld, ld %lld", static_cast<int>(r),
                   static_cast<long long>(k_extent), static_cast<long long>(rows), static_cast<long long>(ld));
@@ -345,18 +384,15 @@ bool encode_kmajor(CUtensorMap* m, const void* ptr, int64_t k_extent, int64_t ro
 // An MN-major operand (M or N contiguous; bf16): dims {MN, K}, boxes of 64
 // MN values (one 128-byte swizzled row) by 64 K rows.
 bool encode_mnmajor(CUtensorMap* m, const void* ptr, int64_t mn_extent, int64_t k_extent, int64_t ld) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) {
+    if (!encode_fn()) {
         set_error("cuTensorMapEncodeTiled is not available from the driver");
         return false;
     }
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(mn_extent), static_cast<cuuint64_t>(k_extent)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
-    cuuint32_t box[2] = {64u, 64u};
-    cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const MapKey k{CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ptr,
+                   {static_cast<cuuint64_t>(mn_extent), static_cast<cuuint64_t>(k_extent)},
+                   static_cast<cuuint64_t>(ld) * 2u, {64u, 64u}, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B};
+    const CUresult r = encode_2d(m, k);
     if (r != CUDA_SUCCESS) {
         set_error("cuTensorMapEncodeTiled failed (%d) for an MN-major operand %lld x %lld, ld %lld",
                   static_cast<int>(r), static_cast<long long>(mn_extent), static_cast<long long>(k_extent),
