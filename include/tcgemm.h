@@ -77,12 +77,13 @@ typedef enum {
     TCGEMM_VARIANT_2CTA_W256 = 5, /* as TCGEMM_VARIANT_2CTA with the tile width fixed at 256 */
     TCGEMM_VARIANT_SWAP_N64 = 6,  /* the transposed product C^T = B^T A^T on 128 x 64 tiles (128
                                     columns of C by up to 64 rows): the choice for M <= 64 */
-    TCGEMM_VARIANT_SWAP_N64_KS2 = 7 /* as TCGEMM_VARIANT_SWAP_N64, each tile computed by a cluster
-                                      of 2 CTAs that split its k-blocks in halves; the second
-                                      CTA's fp32 partial is added to the first's through
-                                      distributed shared memory (first half + second half), so no
-                                      workspace and no second kernel: the choice for M <= 64 when
-                                      the tiles fill 3/4 to 1 round of 2-CTA clusters */
+    TCGEMM_VARIANT_SWAP_N64_KS2 = 7 /* as TCGEMM_VARIANT_SWAP_N64 (128 x 128 tiles of C^T when
+                                      M > 64), each tile computed by a cluster of 2 CTAs that
+                                      split its k-blocks in halves; the second CTA's fp32 partial
+                                      is added to the first's through distributed shared memory
+                                      (first half + second half), so no workspace and no second
+                                      kernel: the choice for M <= 128 when the tiles fill 3/4 to
+                                      1 round of 2-CTA clusters */
 } tcgemm_variant_t;
 
 /* C = alpha*A*B + beta*C as described above.  Returns TCGEMM_OK once the work

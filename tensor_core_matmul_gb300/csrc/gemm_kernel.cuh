@@ -318,7 +318,7 @@ struct UnitIter {
 // stored, so whatever they hold does not matter, and A's traffic halves.
 // IN = 0: bf16 operands; IN = 1: 8-bit float operands (E4M3 or E5M2).  A
 // k-block is one 128-byte swizzle row either way: 64 bf16 or 128 FP8 values.
-template <int CTA_GROUP, int BN, int STAGES, int AROWS = 128, int IN = 0>
+template <int CTA_GROUP, int BN, int STAGES, int AROWS = 128, int IN = 0, int KS = 1>
 struct GemmCfg {
     static constexpr int kInBytes = IN == 1 ? 1 : 2;       // bytes per operand element
     static constexpr int kBK = 128 / kInBytes;             // elements per k-block (one 128-byte row)
@@ -337,7 +337,9 @@ struct GemmCfg {
     // 128-row x 32-column chunk of C (sized for fp32 output).
     static constexpr uint32_t kEpiBufBytes = 128 * 32 * 4;
     static constexpr uint32_t kEpiOff = STAGES * (kABytes + kBBytes);
-    static constexpr uint32_t kEpiBytes = 2 * kEpiBufBytes;
+    // A K-split cluster (KS = 2) also receives the partner's whole fp32 tile there.
+    static constexpr uint32_t kEpiBytes = (KS == 2 && 128u * BN * 4u > 2 * kEpiBufBytes) ? 128u * BN * 4u
+                                                                                         : 2 * kEpiBufBytes;
     static constexpr uint32_t kBarOff = kEpiOff + kEpiBytes;
     static constexpr uint32_t kNumBars = 2 * STAGES + 4 + 1 + 2 + 2;
     // The fused epilogue's bias values for the current tile's BN columns
@@ -571,7 +573,7 @@ __global__ void __launch_bounds__(192, 1)
     gemm_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
                         const GemmParams p) {
-    using Cfg = GemmCfg<CTA_GROUP, BN, STAGES, AROWS, IN>;
+    using Cfg = GemmCfg<CTA_GROUP, BN, STAGES, AROWS, IN, KS>;
     static_assert(MC == 1 || (MC == 4 && CTA_GROUP == 1 && AROWS == 128), "multicast clusters use single-CTA MMAs");
     static_assert(!SWAP || (CTA_GROUP == 1 && MC == 1), "the swapped product runs on single-CTA tiles");
     static_assert(KS == 1 || (KS == 2 && SWAP && Cfg::kEpiBytes >= 128u * BN * 4u),

@@ -157,6 +157,12 @@ using Cfg2 = tcg::GemmCfg<2, 256, kStages2>;
 using Cfg2n = tcg::GemmCfg<2, 224, kStages2n>;
 using CfgN64 = tcg::GemmCfg<1, 64, kStagesN64>;
 using CfgN64h = tcg::GemmCfg<1, 64, kStagesN64h, 64>;
+// The transposed product with 128-row x 128-column tiles and the K split over
+// a 2-CTA cluster (64 < M <= 128): 5 x (16 KB + 16 KB) per CTA, next to the
+// 64 KB that receives the partner's fp32 tile.
+constexpr int kStagesS128 = 5;
+using CfgS128 = tcg::GemmCfg<1, 128, kStagesS128, 128, 0, 2>;
+static_assert(CfgS128::kSmemBytes <= 227 * 1024, "shared memory");
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
@@ -196,16 +202,17 @@ double est_launch_us(int64_t tiles, int64_t units, int64_t num_kb, double mma_cy
 // 47.5 us against 24.2 us (GB300).  in_kind 1: 8-bit operands (a k-block of
 // 128 values, the MMA twice as fast).
 int pick_variant(int64_t M, int64_t N, int64_t K, int sms, int in_kind = 0) {
-    if (M <= 64 && N >= 256) {
-        // The transposed product.  When its 128-row tiles fill between three
-        // quarters of a round and a whole round of 2-CTA clusters, each tile's
-        // k-blocks are split over the two CTAs of a cluster (no reduction
-        // pass); otherwise stream-K shares them out when it pays.
+    if (M <= 128 && N >= 256) {
+        // The transposed product (B's columns fill the 128 MMA rows).  When
+        // its 128-row tiles fill between three quarters of a round and a
+        // whole round of 2-CTA clusters, each tile's k-blocks are split over
+        // the two CTAs of a cluster (no reduction pass); otherwise, up to 64
+        // rows, stream-K shares them out when it pays.
         const int64_t tiles = (N + 127) / 128;
         const int64_t num_kb = (K + (in_kind == 1 ? 127 : 63)) / (in_kind == 1 ? 128 : 64);
         if (num_kb >= 8 && 2 * tiles <= sms && 8 * tiles >= 3 * static_cast<int64_t>(sms))
             return TCGEMM_VARIANT_SWAP_N64_KS2;
-        return TCGEMM_VARIANT_SWAP_N64;
+        if (M <= 64) return TCGEMM_VARIANT_SWAP_N64;
     }
     if (M <= 128) return TCGEMM_VARIANT_1CTA_N64;
     const int64_t num_kb = (K + (in_kind == 1 ? 127 : 63)) / (in_kind == 1 ? 128 : 64);
@@ -285,6 +292,11 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pa
         if (variant == TCGEMM_VARIANT_SWAP_N64_KS2 && num_kb >= 2) pl.ks = 2;
         pl.arows = (!pl.swap && M <= 64) ? 64 : 128;
         pl.smem = pl.arows == 64 ? CfgN64h::kSmemBytes : CfgN64::kSmemBytes;
+        if (pl.ks == 2 && N > 64) {
+            // More than 64 rows of C (the transposed product's N): 128-wide tiles.
+            pl.bn = 128;
+            pl.smem = CfgS128::kSmemBytes;
+        }
     } else {
         return false;
     }
@@ -414,7 +426,7 @@ bool ensure_smem_attr(int dev) {
     if (done[dev]) return true;
     auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, MC, AR, SW, OutT, IN, KS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(tcg::GemmCfg<CG, BN, ST, AR, IN>::kSmemBytes));
+                                         static_cast<int>(tcg::GemmCfg<CG, BN, ST, AR, IN, KS>::kSmemBytes));
     if (e != cudaSuccess) {
         set_error("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         return false;
@@ -936,6 +948,9 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
 #define TCGEMM_LAUNCH_I8(CG, BN, ST, MC, AR, SW)                                                             \
     return in_kind == 1 ? launch_gemm<CG, BN, ST, MC, AR, SW, int8_t, 1>(pl, ta, tb, tcm, twm, gp, stream, dev) \
                         : launch_gemm<CG, BN, ST, MC, AR, SW, int8_t, 0>(pl, ta, tb, tcm, twm, gp, stream, dev)
+        if (pl.swap && pl.ks == 2 && pl.bn == 128)
+            return in_kind == 1 ? launch_gemm<1, 128, kStagesS128, 1, 128, true, int8_t, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
+                                : launch_gemm<1, 128, kStagesS128, 1, 128, true, int8_t, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
         if (pl.swap && pl.ks == 2)
             return in_kind == 1 ? launch_gemm<1, 64, kStagesN64, 1, 128, true, int8_t, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
                                 : launch_gemm<1, 64, kStagesN64, 1, 128, true, int8_t, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
@@ -954,6 +969,9 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
 #define TCGEMM_LAUNCH8(CG, BN, ST, MC, AR, SW)                                                                  \
     return bf16 ? launch_gemm<CG, BN, ST, MC, AR, SW, __nv_bfloat16, 1>(pl, ta, tb, tcm, twm, gp, stream, dev) \
                 : launch_gemm<CG, BN, ST, MC, AR, SW, float, 1>(pl, ta, tb, tcm, twm, gp, stream, dev)
+        if (pl.swap && pl.ks == 2 && pl.bn == 128)
+            return bf16 ? launch_gemm<1, 128, kStagesS128, 1, 128, true, __nv_bfloat16, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
+                        : launch_gemm<1, 128, kStagesS128, 1, 128, true, float, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
         if (pl.swap && pl.ks == 2)
             return bf16 ? launch_gemm<1, 64, kStagesN64, 1, 128, true, __nv_bfloat16, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
                         : launch_gemm<1, 64, kStagesN64, 1, 128, true, float, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
@@ -970,6 +988,9 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     return bf16 ? launch_gemm<CG, BN, ST, MC, AR, SW, __nv_bfloat16>(pl, ta, tb, tcm, twm, gp, stream, dev) \
                 : launch_gemm<CG, BN, ST, MC, AR, SW, float>(pl, ta, tb, tcm, twm, gp, stream, dev)
     if (pl.mc == 4) TCGEMM_LAUNCH(1, 256, kStages1, 4, 128, false);
+    if (pl.swap && pl.ks == 2 && pl.bn == 128)
+        return bf16 ? launch_gemm<1, 128, kStagesS128, 1, 128, true, __nv_bfloat16, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
+                    : launch_gemm<1, 128, kStagesS128, 1, 128, true, float, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
     if (pl.swap && pl.ks == 2)
         return bf16 ? launch_gemm<1, 64, kStagesN64, 1, 128, true, __nv_bfloat16, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
                     : launch_gemm<1, 64, kStagesN64, 1, 128, true, float, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);

@@ -308,7 +308,11 @@ def test_k_split_plan(tc):
     p = tc.plan(40, 30000, 640, 7, 152)      # 235 tiles: rounds of 76 clusters
     assert p["ks"] == 2 and p["grid"] == 152 and p["stream_k"] == 0
     p = tc.plan(64, 8192, 64, 7, 152)
-    assert p["ks"] == 1 and p["cluster"] == 1
+    assert p["ks"] == 1 and p["cluster"] == 1 and p["bn"] == 64
+    p = tc.plan(128, 8192, 8192, 7, 152)      # 64 < M <= 128: 128 x 128 tiles of C^T
+    assert (p["ks"], p["bn"], p["grid"], p["tiles_n"]) == (2, 128, 128, 1) and p["smem"] <= 227 * 1024
+    p = tc.plan(300, 200, 320, 7, 152)        # C^T is 200 x 300: 2 x 3 tiles of 128 x 128
+    assert (p["ks"], p["bn"], p["tiles_m"], p["tiles_n"]) == (2, 128, 2, 3)
     assert tc.plan(64, 8192, 8192, 6, 152)["ks"] == 1
 
 
@@ -317,6 +321,9 @@ def test_auto_variant_choice(tc):
     assert tc.pick_variant(64, 4096, 8192, 152) == 6      # 32 tiles: stream-K over all SMs instead
     assert tc.pick_variant(64, 8192, 256, 152) == 6       # 4 k-blocks: too short to split
     assert tc.pick_variant(64, 12288, 8192, 152) == 6     # 96 tiles: more than a round of clusters
+    assert tc.pick_variant(128, 8192, 8192, 152) == 7     # 128-wide tiles of C^T, K split
+    assert tc.pick_variant(100, 8192, 8192, 152) == 7
+    assert tc.pick_variant(128, 12288, 8192, 152) == 4
     assert tc.pick_variant(128, 4096, 4096, 152) == 4
     assert tc.pick_variant(64, 128, 4096, 152) == 4
     assert tc.pick_variant(129, 4096, 4096, 152) == 2
