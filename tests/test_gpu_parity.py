@@ -102,6 +102,28 @@ def test_configs_sampled(oracle_lib, name):
                         ((got & 0x7FFF) > 0x7F80)).any()
 
 
+@pytest.mark.parametrize("M,N,K,out,beta", [(128, 8192, 8192, gi.OUT_BF16, 0.0), (100, 8192, 8192, gi.OUT_F32, 0.5),
+                                          (40, 9000, 8200, gi.OUT_BF16, 0.0)])
+def test_k_split_cluster_sizes_sampled(oracle_lib, M, N, K, out, beta):
+    """Skinny shapes the automatic choice gives to the K split over 2-CTA
+    clusters (variant 7: 64- and 128-wide tiles of C^T, K tails): sampled at
+    2 points of every 128 x 128 cell and along whole rows and columns, and
+    repeatable bit for bit."""
+    import tensor_core_matmul_gb300 as tc
+    assert tc.binding.plan_device(M, N, K, 0)["ks"] == 2
+    case = gi.make_case(f"ks{M}", M, N, K, alpha=0.5, beta=beta, out_dtype=out, seed=77 + M)
+    got = H.run_case(case, 0).result_np()
+    rows, cols = gi.cell_sample_indices(case.M, case.N, 128, 128, 2, seed=21)
+    H.compare_sampled(oracle_lib, case, got, rows, cols, what=f"k-split {M}")
+    r = np.arange(case.M, dtype=np.int64)
+    for j in [0, case.N - 1]:
+        H.compare_sampled(oracle_lib, case, got, r, np.full_like(r, j), what=f"k-split {M} col {j}")
+    c = np.arange(case.N, dtype=np.int64)
+    H.compare_sampled(oracle_lib, case, got, np.full_like(c, case.M - 1), c, what=f"k-split {M} last row")
+    again = H.run_case(case, 0).result_np()
+    assert np.array_equal(got.view(np.uint8), again.view(np.uint8)), "K split not repeatable"
+
+
 @pytest.mark.parametrize("name", ["edge", "s8k"])
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_configs_integer_exact_sampled(oracle_lib, name, variant):
