@@ -373,8 +373,9 @@ def run_ours(args) -> None:
 
 
 def bench_case(args):
-    """The workload: BASELINE's configuration, with 8-bit operands when
-    --in-format asks for them (same shapes, seeds and distribution)."""
+    """The workload named by --config (shape, alpha/beta, output type, seed),
+    with 8-bit operands when --in-format asks for them (same shapes, seeds and
+    distribution)."""
     import gemm_inputs as gi
     c = gi.CONFIGS[args.config]
     case = gi.make_case(args.config, c["M"], c["N"], c["K"], alpha=c["alpha"], beta=c["beta"],
