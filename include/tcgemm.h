@@ -103,6 +103,30 @@ int gemm_bf16_variant(int64_t M, int64_t N, int64_t K,
                       void* C, int64_t ldc,
                       float alpha, float beta, int out_dtype, void* stream, int variant);
 
+/* Same operation on HOST buffers: A, B and C are host pointers (pinned
+ * memory, e.g. from cudaHostAlloc, lets the copies run asynchronously; pageable
+ * memory works too, with the copies staged by the driver).  On `stream` the
+ * call enqueues one pitched host-to-device copy of A and of B (their M x K and
+ * N x K elements; padding is not copied) and of C when beta != 0, the GEMM
+ * (automatic variant) on the library's device copies, and one pitched
+ * device-to-host copy of C's M x N elements (its ldc padding on the host is
+ * never written), then returns.  C holds the result once `stream` has completed that work;
+ * the caller must neither write A, B, C nor read C before then.  The device
+ * copies belong to the library: one set per device and stream, allocated by
+ * cudaMalloc on the first call that needs them (or needs more), held until
+ * the process exits; calls that overlap on the GPU must use different
+ * streams.  out_dtype TCGEMM_OUT_F32 or _BF16.  Rules and errors as
+ * gemm_bf16, applied to the host pointers (16-byte alignment, leading
+ * dimensions, no overlap of C with A or B); a failed copy or allocation ->
+ * TCGEMM_ERR_CUDA.  The pages this library follows time device-resident
+ * operands only; this entry point serves callers whose matrices live in host
+ * memory. */
+int gemm_bf16_host(int64_t M, int64_t N, int64_t K,
+                   const void* A, int64_t lda,
+                   const void* B, int64_t ldb,
+                   void* C, int64_t ldc,
+                   float alpha, float beta, int out_dtype, void* stream);
+
 /* Same operation with a caller-supplied workspace instead of the library's
  * own.  When the tiles do not fill the last round of the persistent CTAs, the
  * k-blocks of that round's tiles are shared out evenly ("stream-K"); the fp32

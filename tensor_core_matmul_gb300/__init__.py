@@ -7,14 +7,15 @@
     gemm_fp8: the same GEMM on 8-bit float operands (E4M3 / E5M2)
     gemm_quant_i8: int8 codes of act(alpha*A*B + bias) * row_scale + zero_point
     gemm_bf16_layout: A row- or column-major, B column- or row-major
+    gemm_bf16_host: the plain GEMM on host buffers (copies in and out included)
 
 The CUDA library (``_lib/libtcgemm.so``, built from ``csrc/``) does all the
 work; ``binding`` only marshals arguments.  Build with ``_build.build()``.
 """
 from .binding import (OUT_BF16, autotune, autotune_clear, autotune_lookup, OUT_F32, VARIANT_1CTA, VARIANT_1CTA_MC, VARIANT_1CTA_N64, VARIANT_2CTA, VARIANT_AUTO, TcgemmError,
-                      check_device_status, gemm_bf16, gemm_bf16_bias_act, gemm_bf16_layout, gemm_bf16_raw, gemm_fp8, gemm_quant_i8, gemm_bf16_ws_raw, launch_count, lib, pick_variant,
+                      check_device_status, gemm_bf16, gemm_bf16_bias_act, gemm_bf16_host, gemm_bf16_layout, gemm_bf16_raw, gemm_fp8, gemm_quant_i8, gemm_bf16_ws_raw, launch_count, lib, pick_variant,
                       plan, selftest_timeout, tile_order, version, workspace_bytes)
 
 __all__ = ["OUT_BF16", "autotune", "autotune_clear", "autotune_lookup", "OUT_F32", "VARIANT_1CTA", "VARIANT_1CTA_MC", "VARIANT_1CTA_N64", "VARIANT_2CTA", "VARIANT_AUTO", "TcgemmError",
-           "check_device_status", "gemm_bf16", "gemm_bf16_bias_act", "gemm_bf16_layout", "gemm_bf16_raw", "gemm_fp8", "gemm_quant_i8", "gemm_bf16_ws_raw", "launch_count", "lib", "pick_variant",
+           "check_device_status", "gemm_bf16", "gemm_bf16_bias_act", "gemm_bf16_host", "gemm_bf16_layout", "gemm_bf16_raw", "gemm_fp8", "gemm_quant_i8", "gemm_bf16_ws_raw", "launch_count", "lib", "pick_variant",
            "plan", "selftest_timeout", "tile_order", "version", "workspace_bytes"]

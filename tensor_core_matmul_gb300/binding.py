@@ -86,6 +86,8 @@ def lib() -> ctypes.CDLL:
     L.tcgemm_plan_kind.restype = i32
     L.gemm_bf16_noalloc.argtypes = gemm_args + [i32]
     L.gemm_bf16_noalloc.restype = i32
+    L.gemm_bf16_host.argtypes = gemm_args
+    L.gemm_bf16_host.restype = i32
     L.tcgemm_noalloc_scratch_bytes.argtypes = []
     L.tcgemm_noalloc_scratch_bytes.restype = i64
     L.tcgemm_workspace_bytes.argtypes = [i64, i64, i64, i32, i32]
@@ -171,6 +173,43 @@ def gemm_bf16(A, B, C, alpha: float = 1.0, beta: float = 0.0, *, M: Optional[int
         raise ValueError("tensor shapes smaller than M/N")  # A and B are not read when K == 0
     st = gemm_bf16_raw(M, N, K, A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0), C.data_ptr(),
                        C.stride(0), float(alpha), float(beta), out, _stream_ptr(stream), variant)
+    _check(st)
+    return C
+
+
+def gemm_bf16_host_raw(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int, C: int, ldc: int,
+                       alpha: float, beta: float, out_dtype: int, stream: int) -> int:
+    """Pointer-level call of the host-buffer entry point; returns the status."""
+    return lib().gemm_bf16_host(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, stream)
+
+
+def gemm_bf16_host(A, B, C, alpha: float = 1.0, beta: float = 0.0, *, M: Optional[int] = None,
+                   N: Optional[int] = None, K: Optional[int] = None, stream=None):
+    """C = alpha * A * B + beta * C with A, B, C in host memory (CPU tensors,
+    pinned for asynchronous copies): the library copies them to the device,
+    runs the GEMM and copies C back, all enqueued on `stream`.  C is valid
+    once the stream has completed that work."""
+    import torch
+    if A.is_cuda or B.is_cuda or C.is_cuda:
+        raise ValueError("A, B and C must be CPU tensors")
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise ValueError("A and B must be bfloat16")
+    if C.dtype == torch.float32:
+        out = OUT_F32
+    elif C.dtype == torch.bfloat16:
+        out = OUT_BF16
+    else:
+        raise ValueError("C must be float32 or bfloat16")
+    for t in (A, B, C):
+        if t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError("A, B, C must be 2-D with unit inner stride")
+    M = C.shape[1] if M is None else M
+    N = C.shape[0] if N is None else N
+    K = A.shape[1] if K is None else K
+    if C.shape[0] < N or (K > 0 and (A.shape[0] < M or B.shape[0] < N)):
+        raise ValueError("tensor shapes smaller than M/N")
+    st = gemm_bf16_host_raw(M, N, K, A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0), C.data_ptr(),
+                            C.stride(0), float(alpha), float(beta), out, _stream_ptr(stream))
     _check(st)
     return C
 

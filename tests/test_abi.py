@@ -59,6 +59,24 @@ def test_argument_errors(tc, args, status):
     assert tc.binding.last_error()
 
 
+@pytest.mark.parametrize("args,out,status", [
+    ((8, 8, 8, FAKE, 8, FAKE * 2, 8, FAKE * 4, 8), 2, 1),   # int8 output is not offered on host buffers
+    ((8, 8, 8, FAKE, 4, FAKE * 2, 8, FAKE * 4, 8), 0, 1),   # lda < K
+    ((8, 8, 8, FAKE + 2, 8, FAKE * 2, 8, FAKE * 4, 8), 0, 2),  # A misaligned
+    ((8, 8, 8, FAKE, 8, FAKE * 2, 8, FAKE + 64, 8), 0, 1),  # C overlaps A
+    ((8, 8, 8, FAKE, 8, 0, 8, FAKE * 4, 8), 0, 1),          # null B
+])
+def test_host_entry_argument_errors(tc, args, out, status):
+    """The host-buffer entry point checks its arguments before any CUDA call."""
+    st = tc.binding.gemm_bf16_host_raw(*args, 1.0, 0.0, out, 0)
+    assert st == status, (st, tc.binding.last_error())
+    assert tc.binding.last_error()
+
+
+def test_host_entry_empty_is_noop(tc):
+    assert tc.binding.gemm_bf16_host_raw(0, 8, 8, FAKE, 8, FAKE * 2, 8, FAKE * 4, 8, 1.0, 0.0, 0, 0) == 0
+
+
 def test_bad_dtype_and_variant(tc):
     assert tc.gemm_bf16_raw(8, 8, 8, FAKE, 8, FAKE * 2, 8, FAKE * 4, 8, 1.0, 0.0, 7, 0) == 1
     assert tc.gemm_bf16_raw(8, 8, 8, FAKE, 8, FAKE * 2, 8, FAKE * 4, 8, 1.0, 0.0, 0, 0, 9) == 1
