@@ -337,9 +337,9 @@ struct GemmCfg {
     // 128-row x 32-column chunk of C (sized for fp32 output).
     static constexpr uint32_t kEpiBufBytes = 128 * 32 * 4;
     static constexpr uint32_t kEpiOff = STAGES * (kABytes + kBBytes);
-    // A K-split cluster (KS = 2) also receives the partner's whole fp32 tile there.
-    static constexpr uint32_t kEpiBytes = (KS == 2 && 128u * BN * 4u > 2 * kEpiBufBytes) ? 128u * BN * 4u
-                                                                                         : 2 * kEpiBufBytes;
+    // A K-split cluster (KS = 2) also stages half an fp32 tile there for the peer.
+    static constexpr uint32_t kEpiBytes = (KS == 2 && 128u * (BN / 2) * 4u > 2 * kEpiBufBytes) ? 128u * (BN / 2) * 4u
+                                                                                               : 2 * kEpiBufBytes;
     static constexpr uint32_t kBarOff = kEpiOff + kEpiBytes;
     static constexpr uint32_t kNumBars = 2 * STAGES + 4 + 1 + 2 + 2;
     // The fused epilogue's bias values for the current tile's BN columns
@@ -562,12 +562,12 @@ constexpr uint32_t kEpiThreads = 128;
 // contiguous run of one column of C (D row-major with leading dimension ldc).
 // KS = 2 (transposed product only): a cluster of two CTAs computes each tile,
 // CTA 0 over the first half of its k-blocks and CTA 1 over the second half.
-// CTA 1 leaves its fp32 partial tile in its shared memory (the epilogue
-// staging area, [column][row]); CTA 0 adds it to its own accumulator through
-// distributed shared memory (first half + second half, always in that
-// order) and runs the epilogue.  Two barriers hand the buffer back and forth:
-// xfull on CTA 0 (one arrival per epilogue warp of CTA 1), xfree on CTA 1
-// (one per epilogue warp of CTA 0).
+// Each CTA then finishes half of the tile's columns: it leaves its fp32
+// partial of the other half in its shared memory (the epilogue staging area,
+// [column][row]), adds the peer's partial of its own half to its accumulator
+// through distributed shared memory, and stores.  Per CTA, xfull (one arrival
+// per epilogue warp of the peer) says the peer's partial is staged, xfree
+// says the peer has read this CTA's.
 template <int CTA_GROUP, int BN, int STAGES, int MC, int AROWS, bool SWAP, typename OutT, int IN = 0, int KS = 1>
 __global__ void __launch_bounds__(192, 1)
     gemm_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -576,8 +576,8 @@ __global__ void __launch_bounds__(192, 1)
     using Cfg = GemmCfg<CTA_GROUP, BN, STAGES, AROWS, IN, KS>;
     static_assert(MC == 1 || (MC == 4 && CTA_GROUP == 1 && AROWS == 128), "multicast clusters use single-CTA MMAs");
     static_assert(!SWAP || (CTA_GROUP == 1 && MC == 1), "the swapped product runs on single-CTA tiles");
-    static_assert(KS == 1 || (KS == 2 && SWAP && Cfg::kEpiBytes >= 128u * BN * 4u),
-                  "the K split exchanges a whole fp32 tile through the staging area");
+    static_assert(KS == 1 || (KS == 2 && SWAP && BN % 64 == 0 && Cfg::kEpiBytes >= 128u * (BN / 2) * 4u),
+                  "the K split exchanges half an fp32 tile through the staging area");
     constexpr int kCluster = CTA_GROUP * MC * KS;
     extern __shared__ uint8_t smem_raw[];
 
@@ -926,58 +926,48 @@ __global__ void __launch_bounds__(192, 1)
             // granule at row M would also write rows M.. of the ldc padding:
             // that block is stored with masked plain stores instead.
             const bool tma_rows = row_blk + 128 <= p.M || ((static_cast<int64_t>(p.M) * sizeof(OutT)) % 16) == 0;
-            if (KS == 2 && ks_rank == 1) {
-                // Second half of a K-split tile: stage the fp32 partial for
-                // CTA 0 once it has read the previous one.
+            if (KS == 2) {
+                // K-split tile: each CTA finishes half of the tile's columns
+                // (D columns = rows of C).  It stages the fp32 partial of the
+                // other half for its peer, then adds the peer's partial of
+                // its own half (read through distributed shared memory) to
+                // its accumulator and stores.  Two partials, so the sum does
+                // not depend on which CTA adds it up.
+                const uint32_t peer = ks_rank ^ 1u;
+                const int half = ncols / 2;
+                const int mine = static_cast<int>(ks_rank) * half, theirs = static_cast<int>(peer) * half;
                 uint32_t okx = 1;
                 if (lane == 0) okx = wait_phase<true>(xfree_bar, xph ^ 1u, wctx, kWhereEpilogue) ? 1u : 0u;
                 okx = __shfl_sync(0xffffffffu, okx, 0);
                 if (!named_barrier_and(kEpiBarrier, kEpiThreads, okx != 0u)) break;
                 float* xb = reinterpret_cast<float*>(smem + Cfg::kEpiOff) + row_local;
 #pragma unroll 1
-                for (int c = 0; c < ncols; c += 32) {
+                for (int c = 0; c < half; c += 32) {
                     uint32_t r[32];
-                    tmem_ld32(tbase + c, r);
+                    tmem_ld32(tbase + theirs + c, r);
                     tmem_ld_wait32(r);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) xb[(c + j) * 128] = __uint_as_float(r[j]);
                 }
-                tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(tempty_bar(acc));
-                    mbar_arrive_cluster(map_to_cta(xfull_bar, 0));
-                }
-                xph ^= 1u;
-            } else if (SWAP && u.slot < 0) {
-                // D row `row` = column `row` of C; D columns = rows of C.
-                // K split: CTA 1's partial (the second half of the k-blocks,
-                // read from its staging area through distributed shared
-                // memory) is added to this CTA's (the first half).
-                uint32_t xrow = 0;
-                if constexpr (KS == 2) {
-                    uint32_t okx = 1;
-                    if (lane == 0) okx = wait_phase<true>(xfull_bar, xph, wctx, kWhereEpilogue) ? 1u : 0u;
-                    okx = __shfl_sync(0xffffffffu, okx, 0);
-                    if (!named_barrier_and(kEpiBarrier, kEpiThreads, okx != 0u)) break;
-                    xrow = map_to_cta(base + Cfg::kEpiOff, 1) + row_local * 4u;
-                }
+                if (lane == 0) mbar_arrive_cluster(map_to_cta(xfull_bar, peer));
+                okx = 1;
+                if (lane == 0) okx = wait_phase<true>(xfull_bar, xph, wctx, kWhereEpilogue) ? 1u : 0u;
+                okx = __shfl_sync(0xffffffffu, okx, 0);
+                if (!named_barrier_and(kEpiBarrier, kEpiThreads, okx != 0u)) break;
+                const uint32_t xrow = map_to_cta(base + Cfg::kEpiOff, peer) + row_local * 4u;
 #pragma unroll 1
-                for (int c = 0; c < ncols; c += 32) {
-                    const int64_t col0 = colt + c;
+                for (int c = 0; c < half; c += 32) {
+                    const int64_t col0 = colt + mine + c;
                     if (col0 >= p.N) break;
                     uint32_t r[32];
-                    tmem_ld32(tbase + c, r);
-                    if constexpr (KS == 2) {
-                        float x[32];
+                    tmem_ld32(tbase + mine + c, r);
+                    float x[32];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) x[j] = ld_dsmem_f32(xrow + static_cast<uint32_t>(c + j) * 512u);
-                        tmem_ld_wait32(r);
+                    for (int j = 0; j < 32; ++j) x[j] = ld_dsmem_f32(xrow + static_cast<uint32_t>(c + j) * 512u);
+                    tmem_ld_wait32(r);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + x[j]);
-                    } else {
-                        tmem_ld_wait32(r);
-                    }
+                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + x[j]);
                     if (row_ok) {
                         OutT* dst = C + row * p.ldc + col0;
                         if (fused) {
@@ -992,9 +982,31 @@ __global__ void __launch_bounds__(192, 1)
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(tempty_bar(acc));
-                    if constexpr (KS == 2) mbar_arrive_cluster(map_to_cta(xfree_bar, 1));
+                    mbar_arrive_cluster(map_to_cta(xfree_bar, peer));
                 }
-                if constexpr (KS == 2) xph ^= 1u;
+                xph ^= 1u;
+            } else if (SWAP && u.slot < 0) {
+                // D row `row` = column `row` of C; D columns = rows of C.
+#pragma unroll 1
+                for (int c = 0; c < ncols; c += 32) {
+                    const int64_t col0 = colt + c;
+                    if (col0 >= p.N) break;
+                    uint32_t r[32];
+                    tmem_ld32(tbase + c, r);
+                    tmem_ld_wait32(r);
+                    if (row_ok) {
+                        OutT* dst = C + row * p.ldc + col0;
+                        if (fused) {
+                            store_run32<OutT, true>(dst, p.N - col0, r, p.alpha, p.beta, has_beta, bias_v, p.act,
+                                                    p.qscale + col0, p.qzero);
+                        } else {
+                            store_run32<OutT>(dst, p.N - col0, r, p.alpha, p.beta, has_beta);
+                        }
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(acc));
             } else if (u.slot < 0 && !tma_rows) {
 #pragma unroll 1
                 for (int c = 0; c < ncols; c += 32) {

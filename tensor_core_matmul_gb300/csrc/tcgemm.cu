@@ -158,9 +158,9 @@ using Cfg2n = tcg::GemmCfg<2, 224, kStages2n>;
 using CfgN64 = tcg::GemmCfg<1, 64, kStagesN64>;
 using CfgN64h = tcg::GemmCfg<1, 64, kStagesN64h, 64>;
 // The transposed product with 128-row x 128-column tiles and the K split over
-// a 2-CTA cluster (64 < M <= 128): 5 x (16 KB + 16 KB) per CTA, next to the
-// 64 KB that receives the partner's fp32 tile.
-constexpr int kStagesS128 = 5;
+// a 2-CTA cluster (64 < M <= 128): 6 x (16 KB + 16 KB) per CTA, next to the
+// 32 KB that stages half of the fp32 tile for the peer.
+constexpr int kStagesS128 = 6;
 using CfgS128 = tcg::GemmCfg<1, 128, kStagesS128, 128, 0, 2>;
 static_assert(CfgS128::kSmemBytes <= 227 * 1024, "shared memory");
 
