@@ -1005,45 +1005,6 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
 
 }  // namespace
 
-// ------------------------------------------------- host-buffer staging --
-//
-// Device copies of the operands and of C for gemm_bf16_host, one set per
-// (device, stream) so that calls on different streams never share them.
-// Grown (never shrunk) when a call needs more; cudaFree waits for the device,
-// so a buffer is never freed under a copy or kernel still using it.
-struct HostStage {
-    void* p[3] = {nullptr, nullptr, nullptr};  // A, B, C
-    uint64_t bytes[3] = {0, 0, 0};
-};
-std::mutex g_stage_mu;
-std::map<std::pair<int, uintptr_t>, HostStage> g_stage;
-
-int host_stage(int dev, cudaStream_t stream, const uint64_t need[3], void* out[3]) {
-    std::lock_guard<std::mutex> lk(g_stage_mu);
-    HostStage& st = g_stage[{dev, reinterpret_cast<uintptr_t>(stream)}];
-    for (int i = 0; i < 3; ++i) {
-        if (need[i] > st.bytes[i]) {
-            const uint64_t grain = uint64_t{2} << 20;
-            const uint64_t bytes = (need[i] + grain - 1) / grain * grain;
-            if (st.p[i]) {
-                cudaFree(st.p[i]);
-                st.p[i] = nullptr;
-                st.bytes[i] = 0;
-            }
-            cudaError_t e = cudaMalloc(&st.p[i], bytes);
-            if (e != cudaSuccess) {
-                st.p[i] = nullptr;
-                set_error("staging cudaMalloc(%llu): %s", static_cast<unsigned long long>(bytes),
-                          cudaGetErrorString(e));
-                return TCGEMM_ERR_CUDA;
-            }
-            st.bytes[i] = bytes;
-        }
-        out[i] = st.p[i];
-    }
-    return TCGEMM_OK;
-}
-
 extern "C" {
 
 int gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
@@ -1066,54 +1027,6 @@ int gemm_bf16_ws(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, co
 int gemm_bf16_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
                       void* C, int64_t ldc, float alpha, float beta, int out_dtype, void* stream, int variant) {
     return run_gemm(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, stream, variant, kWsNoAlloc);
-}
-
-int gemm_bf16_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
-                   void* C, int64_t ldc, float alpha, float beta, int out_dtype, void* stream) {
-    t_last_error[0] = '\0';
-    if (out_dtype != TCGEMM_OUT_F32 && out_dtype != TCGEMM_OUT_BF16) {
-        set_error("out_dtype must be TCGEMM_OUT_F32 (0) or TCGEMM_OUT_BF16 (1), got %d", out_dtype);
-        return TCGEMM_ERR_INVALID_ARG;
-    }
-    // The host buffers follow the device entry points' rules (sizes, leading
-    // dimensions, 16-byte alignment, no overlap of C with A or B).
-    int rc = validate(M, N, K, A, lda, B, ldb, C, ldc, out_dtype);
-    if (rc != TCGEMM_OK) return rc;
-    if (M == 0 || N == 0) return TCGEMM_OK;
-    int dev = 0;
-    DeviceInfo info;
-    rc = probe_device(dev, info);
-    if (rc != TCGEMM_OK) return rc;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const uint64_t esz = out_dtype == TCGEMM_OUT_F32 ? 4 : 2;
-    const uint64_t need[3] = {K > 0 ? static_cast<uint64_t>((M - 1) * lda + K) * 2 : 0,
-                              K > 0 ? static_cast<uint64_t>((N - 1) * ldb + K) * 2 : 0,
-                              static_cast<uint64_t>((N - 1) * ldc + M) * esz};
-    void* d[3] = {nullptr, nullptr, nullptr};
-    rc = host_stage(dev, s, need, d);
-    if (rc != TCGEMM_OK) return rc;
-    // One pitched copy per matrix, all on the caller's stream: only the
-    // matrices' own elements move (the device copies keep the caller's
-    // leading dimensions), so C's padding on the host is never written.
-    cudaError_t e = cudaSuccess;
-    if (K > 0) {
-        e = cudaMemcpy2DAsync(d[0], lda * 2, A, lda * 2, K * 2, M, cudaMemcpyHostToDevice, s);
-        if (e == cudaSuccess) e = cudaMemcpy2DAsync(d[1], ldb * 2, B, ldb * 2, K * 2, N, cudaMemcpyHostToDevice, s);
-    }
-    if (e == cudaSuccess && beta != 0.0f)
-        e = cudaMemcpy2DAsync(d[2], ldc * esz, C, ldc * esz, M * esz, N, cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) {
-        set_error("host-to-device copy: %s", cudaGetErrorString(e));
-        return TCGEMM_ERR_CUDA;
-    }
-    rc = run_gemm(M, N, K, d[0], lda, d[1], ldb, d[2], ldc, alpha, beta, out_dtype, stream, TCGEMM_VARIANT_AUTO);
-    if (rc != TCGEMM_OK) return rc;
-    e = cudaMemcpy2DAsync(C, ldc * esz, d[2], ldc * esz, M * esz, N, cudaMemcpyDeviceToHost, s);
-    if (e != cudaSuccess) {
-        set_error("device-to-host copy: %s", cudaGetErrorString(e));
-        return TCGEMM_ERR_CUDA;
-    }
-    return TCGEMM_OK;
 }
 
 int gemm_bf16_bias_act(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
@@ -1438,3 +1351,6 @@ uint64_t tcgemm_launch_count(void) { return g_launches.load(std::memory_order_re
 int tcgemm_version(void) { return 100; }
 
 }  // extern "C"
+
+// The host-buffer entry point (gemm_bf16_host) and its device copies.
+#include "host_entry.cuh"
