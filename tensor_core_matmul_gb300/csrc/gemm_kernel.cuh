@@ -594,8 +594,8 @@ __global__ void __launch_bounds__(192, 1)
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
     const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
     auto cold_bar = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 5 + b); };  // C chunk loads
-    const uint32_t xfull_bar = bar0 + 8u * (2 * STAGES + 7);  // KS = 2, on CTA 0: CTA 1's partial is staged
-    const uint32_t xfree_bar = bar0 + 8u * (2 * STAGES + 8);  // KS = 2, on CTA 1: CTA 0 has read it
+    const uint32_t xfull_bar = bar0 + 8u * (2 * STAGES + 7);  // KS = 2: the peer's partial is staged
+    const uint32_t xfree_bar = bar0 + 8u * (2 * STAGES + 8);  // KS = 2: the peer has read this CTA's
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kBarOff + Cfg::kNumBars * 8);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
