@@ -356,6 +356,31 @@ int tcgemm_autotune_lookup(int64_t M, int64_t N, int64_t K, int in_type, int out
 /* Forget every tuned choice.  Host only. */
 void tcgemm_autotune_clear(void);
 
+/* Records `variant` as the tuned choice for this problem on the current
+ * device (device 0 when no device is visible), as tcgemm_autotune would — for
+ * a choice measured elsewhere; variant 0 removes the entry.  Arguments as
+ * tcgemm_autotune_lookup.  A variant not built for that kind of problem (the
+ * single-CTA variants 1 and 3 for 8-bit operands or int8 output, variant 3
+ * with a column-major A or row-major B, 8-bit operands with those layouts) or
+ * a size outside 1..2^31-1 -> TCGEMM_ERR_INVALID_ARG.  Host only. */
+int tcgemm_autotune_set(int64_t M, int64_t N, int64_t K, int in_type, int out_dtype, int a_layout, int b_layout,
+                        int beta_nonzero, int variant);
+
+/* Writes every tuned choice (all devices) to the text file `path`: a header
+ * line, then one line per choice (device ordinal, M, N, K, operand kind and
+ * format, output type, A column-major, B row-major, beta != 0, variant).
+ * Returns the number of choices written, or -1 if the file cannot be written
+ * (tcgemm_last_error says why).  Host only. */
+int64_t tcgemm_autotune_save(const char* path);
+
+/* Adds the choices in a file written by tcgemm_autotune_save, replacing any
+ * for the same problem; automatic calls use them from then on.  Returns the
+ * number read, or -1 (nothing added) if the file cannot be read, lacks the
+ * header or holds a line that is not a valid choice.  Choices are keyed by
+ * device ordinal: load a table on the kind of GPU it was measured on.  Host
+ * only. */
+int64_t tcgemm_autotune_load(const char* path);
+
 /* Size in bytes of gemm_bf16_noalloc's fixed scratch array.  Host only. */
 int64_t tcgemm_noalloc_scratch_bytes(void);
 

@@ -80,6 +80,12 @@ def lib() -> ctypes.CDLL:
     L.tcgemm_autotune_lookup.restype = i32
     L.tcgemm_autotune_clear.argtypes = []
     L.tcgemm_autotune_clear.restype = None
+    L.tcgemm_autotune_set.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, i32]
+    L.tcgemm_autotune_set.restype = i32
+    L.tcgemm_autotune_save.argtypes = [ctypes.c_char_p]
+    L.tcgemm_autotune_save.restype = i64
+    L.tcgemm_autotune_load.argtypes = [ctypes.c_char_p]
+    L.tcgemm_autotune_load.restype = i64
     L.gemm_fp8.argtypes = gemm_args[:-1] + [i32, p, i32]
     L.gemm_fp8.restype = i32
     L.tcgemm_plan_kind.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int64)]
@@ -419,6 +425,29 @@ def autotune_lookup(M: int, N: int, K: int, in_type: int = 0, out_dtype: int = 1
 
 def autotune_clear() -> None:
     lib().tcgemm_autotune_clear()
+
+
+def autotune_set(M: int, N: int, K: int, variant: int, in_type: int = 0, out_dtype: int = 1, a_col: bool = False,
+                 b_row: bool = False, beta_nonzero: bool = False) -> None:
+    """Record `variant` as the tuned choice for this problem (0 removes it)."""
+    _check(lib().tcgemm_autotune_set(M, N, K, in_type, out_dtype, COL_MAJOR if a_col else ROW_MAJOR,
+                                     ROW_MAJOR if b_row else COL_MAJOR, int(beta_nonzero), variant))
+
+
+def autotune_save(path: str) -> int:
+    """Write the tuned-choice table to a text file; returns the number of choices."""
+    n = int(lib().tcgemm_autotune_save(str(path).encode()))
+    if n < 0:
+        raise TcgemmError(1, last_error())
+    return n
+
+
+def autotune_load(path: str) -> int:
+    """Add the choices stored by autotune_save; returns how many were read."""
+    n = int(lib().tcgemm_autotune_load(str(path).encode()))
+    if n < 0:
+        raise TcgemmError(1, last_error())
+    return n
 
 
 def check_device_status(stream=None) -> tuple[int, int]:

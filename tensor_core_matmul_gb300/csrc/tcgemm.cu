@@ -1354,3 +1354,6 @@ int tcgemm_version(void) { return 100; }
 
 // The host-buffer entry point (gemm_bf16_host) and its device copies.
 #include "host_entry.cuh"
+
+// Saving, loading and setting the tuned-choice table.
+#include "tune_table.cuh"

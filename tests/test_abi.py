@@ -346,3 +346,50 @@ def test_auto_variant_choice(tc):
     assert tc.pick_variant(64, 128, 4096, 152) == 4
     assert tc.pick_variant(129, 4096, 4096, 152) == 2
     assert tc.pick_variant(4096, 4096, 4096, 152) == 2
+
+
+def test_autotune_table_set_save_load(tc, tmp_path):
+    """The tuned-choice table: a choice set by hand is what an automatic call
+    would use (lookup), survives a save / clear / load round trip, and a
+    variant not built for the problem is refused.  No GPU needed."""
+    b = tc.binding
+    b.autotune_clear()
+    b.autotune_set(1000, 1200, 2048, 5)
+    b.autotune_set(512, 640, 4096, 4, in_type=1, out_dtype=0)
+    b.autotune_set(384, 448, 1024, 2, out_dtype=0, a_col=True, b_row=True, beta_nonzero=True)
+    assert b.autotune_lookup(1000, 1200, 2048) == 5
+    assert b.autotune_lookup(512, 640, 4096, in_type=1, out_dtype=0) == 4
+    assert b.autotune_lookup(512, 640, 4096, in_type=2, out_dtype=0) == 0   # E5M2 is another problem
+    path = tmp_path / "tuned.txt"
+    assert b.autotune_save(path) == 3
+    b.autotune_clear()
+    assert b.autotune_lookup(1000, 1200, 2048) == 0
+    assert b.autotune_load(path) == 3
+    assert b.autotune_lookup(1000, 1200, 2048) == 5
+    assert b.autotune_lookup(384, 448, 1024, out_dtype=0, a_col=True, b_row=True, beta_nonzero=True) == 2
+    b.autotune_set(1000, 1200, 2048, 0)                                      # variant 0 removes the choice
+    assert b.autotune_lookup(1000, 1200, 2048) == 0
+    b.autotune_clear()
+
+
+@pytest.mark.parametrize("kwargs", [dict(variant=1, in_type=1, out_dtype=0),   # one-CTA kernels: no FP8
+                                    dict(variant=3, out_dtype=2),                 # nor int8 output
+                                    dict(variant=3, a_col=True),                  # multicast: row-major A only
+                                    dict(variant=8), dict(variant=-1),
+                                    dict(variant=2, out_dtype=2, beta_nonzero=True)])  # int8 output has no beta
+def test_autotune_set_refuses_unbuilt(tc, kwargs):
+    with pytest.raises(tc.TcgemmError):
+        tc.binding.autotune_set(256, 256, 256, **kwargs)
+
+
+def test_autotune_load_rejects_bad_files(tc, tmp_path):
+    b = tc.binding
+    b.autotune_clear()
+    bad_header = tmp_path / "a.txt"
+    bad_header.write_text("something else\n0 64 64 64 0 0 1 0 0 0 2\n")
+    bad_line = tmp_path / "b.txt"
+    bad_line.write_text("tcgemm-autotune 1\n0 64 64 64 0 0 1 0 0 0 2\n0 64 64 64 0 0 1 0 0 0 9\n")
+    for p in (bad_header, bad_line, tmp_path / "missing.txt"):
+        with pytest.raises(tc.TcgemmError):
+            b.autotune_load(p)
+    assert b.autotune_lookup(64, 64, 64) == 0        # nothing from the half-valid file was added
