@@ -79,11 +79,12 @@ typedef enum {
                                     columns of C by up to 64 rows): the choice for M <= 64 */
     TCGEMM_VARIANT_SWAP_N64_KS2 = 7 /* as TCGEMM_VARIANT_SWAP_N64 (128 x 128 tiles of C^T when
                                       M > 64), each tile computed by a cluster of 2 CTAs that
-                                      split its k-blocks in halves; the second CTA's fp32 partial
-                                      is added to the first's through distributed shared memory
-                                      (first half + second half), so no workspace and no second
-                                      kernel: the choice for M <= 128 when the tiles fill 3/4 to
-                                      1 round of 2-CTA clusters */
+                                      split its k-blocks in halves; each CTA then finishes half of
+                                      the tile, adding the peer's fp32 partial of that half
+                                      through distributed shared memory (a sum of two terms: the
+                                      same bits whichever CTA adds), so no workspace and no
+                                      second kernel: the choice for M <= 128 when the tiles fill
+                                      3/4 to 1 round of 2-CTA clusters */
 } tcgemm_variant_t;
 
 /* C = alpha*A*B + beta*C as described above.  Returns TCGEMM_OK once the work
