@@ -68,9 +68,8 @@ typedef enum {
     TCGEMM_VARIANT_1CTA = 1,  /* one CTA per SM, 128 x 256 tiles, cta_group::1 MMA   */
     TCGEMM_VARIANT_2CTA = 2,  /* CTA pairs, cta_group::2 MMA (M=256), tiles 256 x 256 or 256 x 224,
                                  whichever finishes the persistent rounds sooner */
-    TCGEMM_VARIANT_1CTA_MC = 3, /* 4-CTA clusters on 2 x 2 blocks of 128 x 256 tiles; each CTA
-                                  loads half of its A and B tiles and multicasts them to the
-                                  CTA sharing its tile row / tile column */
+    /* 3 is not a variant: the number is kept unused so that no other variant
+       is renumbered; passing it is TCGEMM_ERR_INVALID_ARG. */
     TCGEMM_VARIANT_1CTA_N64 = 4, /* one CTA per SM, narrow 128 x 64 tiles, 8-stage pipeline (12
                                    stages and 64-row A tiles when M <= 64): the choice for
                                    M <= 128, where B is streamed from memory once */
@@ -240,8 +239,8 @@ typedef enum {
  * gemm_bf16.  The article gives no formats or scaling rules: the OCP formats
  * and alpha as the scale are this library's readings.
  * variant: 0 (chosen by shape), TCGEMM_VARIANT_2CTA, _2CTA_W256, _1CTA_N64 or
- * _SWAP_N64; TCGEMM_VARIANT_1CTA and _1CTA_MC are not built for 8-bit
- * operands -> TCGEMM_ERR_INVALID_ARG, as is an unknown in_format.  Other
+ * _SWAP_N64; TCGEMM_VARIANT_1CTA is not built for 8-bit operands
+ * -> TCGEMM_ERR_INVALID_ARG, as is an unknown in_format.  Other
  * rules and errors as gemm_bf16_variant (16-byte rules in bytes). */
 int gemm_fp8(int64_t M, int64_t N, int64_t K,
              const void* A, int64_t lda,
@@ -308,8 +307,8 @@ typedef enum {
  * contiguous is loaded by TMA in 64 x 64 boxes and read by the tensor cores
  * as an MN-major operand (the transpose bits of the MMA's instruction
  * descriptor); nothing is transposed in memory.  Variants as
- * gemm_bf16_variant except TCGEMM_VARIANT_1CTA_MC (-> TCGEMM_ERR_INVALID_ARG,
- * as is an unknown layout).  Other rules and errors as gemm_bf16_variant. */
+ * gemm_bf16_variant; an unknown layout is TCGEMM_ERR_INVALID_ARG.  Other
+ * rules and errors as gemm_bf16_variant. */
 int gemm_bf16_layout(int64_t M, int64_t N, int64_t K,
                      const void* A, int64_t lda, int a_layout,
                      const void* B, int64_t ldb, int b_layout,
@@ -416,8 +415,8 @@ int tcgemm_plan(int64_t M, int64_t N, int64_t K, int variant, int num_sms, int64
  * itself uses).  Needs a supported GPU. */
 int tcgemm_plan_device(int64_t M, int64_t N, int64_t K, int variant, int64_t* out);
 
-/* Current device: out[0] = SMs, out[1] = CTA pairs and out[2] = 4-CTA clusters
- * that can be resident at once with this library's kernels, out[3] = device
+/* Current device: out[0] = SMs, out[1] = CTA pairs that can be resident at
+ * once with this library's kernels, out[2] = 0 (unused), out[3] = device
  * ordinal.  `out` must hold 4 values.  Needs a supported GPU. */
 int tcgemm_device_info(int64_t* out);
 

@@ -22,8 +22,8 @@ OUT_BF16 = 1
 OUT_I8 = 2
 IN_BF16, IN_E4M3, IN_E5M2 = range(3)
 ROW_MAJOR, COL_MAJOR = range(2)
-(VARIANT_AUTO, VARIANT_1CTA, VARIANT_2CTA, VARIANT_1CTA_MC, VARIANT_1CTA_N64, VARIANT_2CTA_W256,
- VARIANT_SWAP_N64, VARIANT_SWAP_N64_KS2) = range(8)
+VARIANT_AUTO, VARIANT_1CTA, VARIANT_2CTA = 0, 1, 2        # 3 names no kernel
+VARIANT_1CTA_N64, VARIANT_2CTA_W256, VARIANT_SWAP_N64, VARIANT_SWAP_N64_KS2 = 4, 5, 6, 7
 
 ACT_NONE, ACT_RELU, ACT_GELU, ACT_GELU_TANH = range(4)
 ACTIVATIONS = {"none": ACT_NONE, "relu": ACT_RELU, "gelu": ACT_GELU, "gelu_tanh": ACT_GELU_TANH}
@@ -497,7 +497,7 @@ def plan_device(M: int, N: int, K: int, variant: int = 0) -> dict:
 def device_info() -> dict:
     out = (ctypes.c_int64 * 4)()
     _check(lib().tcgemm_device_info(out))
-    return {"sms": int(out[0]), "max_pairs": int(out[1]), "max_quads": int(out[2]), "device": int(out[3])}
+    return {"sms": int(out[0]), "max_pairs": int(out[1]), "device": int(out[3])}
 
 
 def gemm_bf16_noalloc_raw(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int, C: int, ldc: int,

@@ -121,7 +121,7 @@ __host__ __device__ __forceinline__ void grouped_tile(int t, int tiles_m, int ti
 struct GemmParams {
     int M, N, K;
     int tiles_m, tiles_n, num_kb, group_m;
-    int grid_m, grid_n;  // grid the unit order walks: tiles, or 2 x 2 tile blocks of a multicast cluster
+    int grid_m, grid_n;  // grid of tiles the unit order walks
     int tiles_dp;        // tiles computed whole, round-robin over the clusters
     int sk_tiles;        // trailing tiles whose k-blocks are shared out by stream-K (0: none)
     int64_t sk_iters;    // sk_tiles * num_kb
@@ -545,15 +545,6 @@ __device__ __forceinline__ void store_run32(OutT* dst, int64_t valid, const uint
 constexpr uint32_t kEpiBarrier = 1;     // named barrier id for the 4 epilogue warps
 constexpr uint32_t kEpiThreads = 128;
 
-// MC = 1: no multicast.  MC = 4 (single-CTA MMAs only): a cluster of 4 CTAs
-// computes a 2 x 2 block of tiles; CTA (rm, rn) = (rank & 1, rank >> 1) owns
-// tile (2*TM + rm, 2*TN + rn).  The two CTAs of a tile row need the same A
-// rows, the two of a tile column the same B columns, so each CTA loads half of
-// its A tile and half of its B tile and multicasts each half to itself and to
-// its partner: a quarter less traffic from L2 per CTA than a CTA pair, half of
-// a lone CTA's.  (The work log's "内核 8：线程块集群" multicasts the shared B
-// tile to two vertically adjacent tiles; this is the same idea in both
-// directions.)
 // tmC maps C (column-major M x N) in 128-row x 32-column boxes for the
 // epilogue's TMA loads / stores and L2 prefetches; tmW maps the stream-K
 // workspace (fp32, 128 rows x [slot][CTA of pair][BN] columns) the same way.
@@ -568,17 +559,16 @@ constexpr uint32_t kEpiThreads = 128;
 // through distributed shared memory, and stores.  Per CTA, xfull (one arrival
 // per epilogue warp of the peer) says the peer's partial is staged, xfree
 // says the peer has read this CTA's.
-template <int CTA_GROUP, int BN, int STAGES, int MC, int AROWS, bool SWAP, typename OutT, int IN = 0, int KS = 1>
+template <int CTA_GROUP, int BN, int STAGES, int AROWS, bool SWAP, typename OutT, int IN = 0, int KS = 1>
 __global__ void __launch_bounds__(192, 1)
     gemm_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
                         const GemmParams p) {
     using Cfg = GemmCfg<CTA_GROUP, BN, STAGES, AROWS, IN, KS>;
-    static_assert(MC == 1 || (MC == 4 && CTA_GROUP == 1 && AROWS == 128), "multicast clusters use single-CTA MMAs");
-    static_assert(!SWAP || (CTA_GROUP == 1 && MC == 1), "the swapped product runs on single-CTA tiles");
+    static_assert(!SWAP || CTA_GROUP == 1, "the swapped product runs on single-CTA tiles");
     static_assert(KS == 1 || (KS == 2 && SWAP && BN % 64 == 0 && Cfg::kEpiBytes >= 128u * (BN / 2) * 4u),
                   "the K split exchanges half an fp32 tile through the staging area");
-    constexpr int kCluster = CTA_GROUP * MC * KS;
+    constexpr int kCluster = CTA_GROUP * KS;
     extern __shared__ uint8_t smem_raw[];
 
     // 1 KB-aligned carve-up: [A stages][B stages][barriers][tmem slot][abort][last flag]
@@ -603,8 +593,6 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t crank = (kCluster > 1) ? cluster_ctarank() : 0u;
     const uint32_t rank = (CTA_GROUP == 2) ? crank : 0u;  // position in the MMA pair
-    const uint32_t rm = (MC == 4) ? (crank & 1u) : 0u;    // position in the 2 x 2 block
-    const uint32_t rn = (MC == 4) ? (crank >> 1) : 0u;
     const uint32_t ks_rank = (KS == 2) ? crank : 0u;       // which half of each tile's k-blocks
     // This CTA's share of a unit's k-blocks: the first half (rounded up) for
     // CTA 0 of a K-split cluster, the rest for CTA 1.
@@ -619,16 +607,12 @@ __global__ void __launch_bounds__(192, 1)
     const int num_clusters = gridDim.x / kCluster;
     auto tile_of = [&](int unit_tile, int& tm, int& tn) {
         grouped_tile(unit_tile, p.grid_m, p.grid_n, p.group_m, tm, tn);
-        if (MC == 4) {
-            tm = 2 * tm + static_cast<int>(rm);
-            tn = 2 * tn + static_cast<int>(rn);
-        }
     };
 
     // Single-CTA MMAs: the producer needs nothing but its own barriers, so it
     // starts loading as soon as they are initialised, while the TMEM
     // allocation and the (cluster) barrier complete for the other warps.
-    constexpr bool kEarlyProducer = CTA_GROUP == 1 && MC == 1;
+    constexpr bool kEarlyProducer = CTA_GROUP == 1;
     if (threadIdx.x == 0) {
         // The descriptors' first fetch overlaps the set-up.
         tma_prefetch_desc(&tmA);
@@ -638,7 +622,7 @@ __global__ void __launch_bounds__(192, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), MC == 4 ? 3 : 1);  // MC: self, row partner, column partner
+            mbar_init(empty_bar(s), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
@@ -716,17 +700,7 @@ __global__ void __launch_bounds__(192, 1)
                     }
                     const uint32_t sa = sA0 + stage * Cfg::kABytes;
                     const uint32_t sb = sB0 + stage * Cfg::kBBytes;
-                    if constexpr (MC == 4) {
-                        // Own half of A -> this CTA and its row partner; own
-                        // half of B -> this CTA and its column partner.
-                        const uint16_t mask_a = static_cast<uint16_t>((1u << rm) | (1u << (rm + 2u)));
-                        const uint16_t mask_b = static_cast<uint16_t>(3u << (2u * rn));
-                        mbar_arrive_expect_tx(full_bar(stage), Cfg::kStageTx);
-                        tma_load_2d_multicast(sa + rn * (Cfg::kABytes / 2), &tmA, full_bar(stage), kb * Cfg::kBK,
-                                              a_row + static_cast<int>(rn) * (Cfg::kRowsA / 2), mask_a);
-                        tma_load_2d_multicast(sb + rm * (Cfg::kBBytes / 2), &tmB, full_bar(stage), kb * Cfg::kBK,
-                                              b_row + static_cast<int>(rm) * (BN / 2), mask_b);
-                    } else if constexpr (CTA_GROUP == 1) {
+                    if constexpr (CTA_GROUP == 1) {
                         mbar_arrive_expect_tx(full_bar(stage), stage_tx);
                         load_tile(sa, &tmA, full_bar(stage), kb, a_row, Cfg::kRowsA, p.a_mn != 0);
                         load_tile(sb, mB, full_bar(stage), kb, b_row, Cfg::kRowsB, p.b_mn != 0);
@@ -815,14 +789,7 @@ __global__ void __launch_bounds__(192, 1)
                                                   (kb != u.kb0 || k != 0) ? 1u : 0u);
                         }
                     }
-                    if constexpr (MC == 4) {
-                        // The stage is free once this CTA and both partners
-                        // that multicast into it are done with it.
-                        const uint32_t row_partner = rm + 2u * (1u - rn);
-                        const uint32_t col_partner = (1u - rm) + 2u * rn;
-                        mma_commit_multicast(empty_bar(stage), static_cast<uint16_t>((1u << crank) | (1u << row_partner) |
-                                                                                     (1u << col_partner)));
-                    } else if constexpr (CTA_GROUP == 1) {
+                    if constexpr (CTA_GROUP == 1) {
                         mma_commit(empty_bar(stage));
                     } else {
                         mma_commit_pair(empty_bar(stage), 0x3);

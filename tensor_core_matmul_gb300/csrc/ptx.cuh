@@ -150,18 +150,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
         : "memory");
 }
 
-// Same tile delivered to every CTA of `cta_mask` in the cluster, at the same
-// shared-memory offset, with complete_tx on the barrier at the same offset in
-// each destination CTA.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* m, uint32_t bar,
-                                                      int32_t c0, int32_t c1, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "h"(cta_mask)
-        : "memory");
-}
-
 // Same, for a CTA pair: the completion may be signalled on the barrier of the
 // peer CTA (`bar_cluster` is a shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m,
@@ -382,16 +370,6 @@ __device__ __forceinline__ void mma_tc(uint32_t d_tmem, uint64_t adesc, uint64_t
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
-}
-
-// Arrive once on the barrier at the same offset in every CTA of `cta_mask`
-// (single-CTA MMAs in a multicast cluster).
-__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
-            "r"(bar),
-        "h"(cta_mask)
-        : "memory");
 }
 
 // Pair version: arrive on the barrier at the same offset in every CTA of

@@ -116,7 +116,6 @@ struct DeviceInfo {
     bool supported = false;
     int sms = 0;
     int max_pairs = 0;  // co-resident CTA pairs for the 2-CTA kernel
-    int max_quads = 0;  // co-resident 4-CTA clusters for the multicast kernel
 };
 
 std::mutex g_dev_mu;
@@ -127,7 +126,6 @@ DeviceInfo g_dev[kMaxDevices];
 struct Plan {
     int variant = 0;
     int cta_group = 1;
-    int mc = 1;            // 4: 2 x 2 multicast cluster of single-CTA tiles
     int arows = 128;       // A rows loaded per CTA (64: M <= 64, narrow kernel)
     int swap = 0;          // 1: the launch computes C^T = B^T A^T (M and N, A and B exchanged)
     int grid_m = 0, grid_n = 0;
@@ -163,6 +161,9 @@ using CfgN64h = tcg::GemmCfg<1, 64, kStagesN64h, 64>;
 constexpr int kStagesS128 = 6;
 using CfgS128 = tcg::GemmCfg<1, 128, kStagesS128, 128, 0, 2>;
 static_assert(CfgS128::kSmemBytes <= 227 * 1024, "shared memory");
+
+// Variant numbers that name a kernel (3 is unused).
+bool variant_known(int v) { return v >= TCGEMM_VARIANT_AUTO && v <= TCGEMM_VARIANT_SWAP_N64_KS2 && v != 3; }
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
@@ -239,7 +240,7 @@ bool use_stream_k(int64_t tiles, int64_t clusters, int64_t num_kb) {
 }
 
 // in_kind 0: bf16 operands (64 per k-block); 1: 8-bit operands (128 per k-block).
-bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pairs, int max_quads, Plan& pl,
+bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pairs, Plan& pl,
                bool allow_split = true, int in_kind = 0, bool a_col = false, bool b_row = false) {
     if (sms <= 0) return false;
     if (variant == TCGEMM_VARIANT_AUTO) variant = pick_variant(M, N, K, sms, in_kind);
@@ -277,12 +278,6 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pa
         // not fit, so it takes the 256 width.
         pl.bn = (variant == TCGEMM_VARIANT_2CTA && !b_row && cost(224) < cost(256) * 0.97) ? 224 : 256;
         pl.smem = pl.bn == 224 ? Cfg2n::kSmemBytes : Cfg2::kSmemBytes;
-    } else if (variant == TCGEMM_VARIANT_1CTA_MC) {
-        pl.cta_group = 1;
-        pl.mc = 4;
-        pl.bm = Cfg1::kBM;
-        pl.bn = 256;
-        pl.smem = Cfg1::kSmemBytes;
     } else if (variant == TCGEMM_VARIANT_1CTA_N64 || variant == TCGEMM_VARIANT_SWAP_N64 ||
                variant == TCGEMM_VARIANT_SWAP_N64_KS2) {
         pl.cta_group = 1;
@@ -304,18 +299,14 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pa
     pl.tiles_n = ceil_div(N, pl.bn);
     pl.num_kb = static_cast<int>(num_kb);
     pl.slot_bytes = static_cast<uint64_t>(pl.cta_group) * 128 * pl.bn * 4;
-    pl.grid_m = pl.mc == 4 ? (pl.tiles_m + 1) / 2 : pl.tiles_m;
-    pl.grid_n = pl.mc == 4 ? (pl.tiles_n + 1) / 2 : pl.tiles_n;
+    pl.grid_m = pl.tiles_m;
+    pl.grid_n = pl.tiles_n;
     const int64_t tiles = static_cast<int64_t>(pl.grid_m) * pl.grid_n;  // units of the order
     if (tiles > (int64_t{1} << 30)) return false;
     int64_t clusters = sms;
     if (pl.cta_group == 2 || pl.ks == 2) clusters = std::max(1, max_pairs > 0 ? max_pairs : sms / 2);
     if (pl.ks == 2) allow_split = false;  // the split is the cluster's
-    if (pl.mc == 4) {
-        clusters = std::max(1, max_quads > 0 ? max_quads : sms / 4);
-        allow_split = false;  // the 2 x 2 blocks are scheduled whole
-    }
-    const int csize = pl.cta_group * pl.mc * pl.ks;
+    const int csize = pl.cta_group * pl.ks;
     pl.tiles_dp = static_cast<int>(tiles);
     pl.sk_tiles = 0;
     pl.sk_iters = 0;
@@ -418,13 +409,13 @@ bool encode_mnmajor(CUtensorMap* m, const void* ptr, int64_t mn_extent, int64_t 
 
 // The dynamic shared-memory opt-in is a per-kernel attribute; it is set once
 // per device for each kernel instantiation.
-template <int CG, int BN, int ST, int MC, int AR, bool SW, typename OutT, int IN = 0, int KS = 1>
+template <int CG, int BN, int ST, int AR, bool SW, typename OutT, int IN = 0, int KS = 1>
 bool ensure_smem_attr(int dev) {
     static std::mutex mu;
     static bool done[kMaxDevices] = {};
     std::lock_guard<std::mutex> lk(mu);
     if (done[dev]) return true;
-    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, MC, AR, SW, OutT, IN, KS>;
+    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, AR, SW, OutT, IN, KS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(tcg::GemmCfg<CG, BN, ST, AR, IN, KS>::kSmemBytes));
     if (e != cudaSuccess) {
@@ -435,11 +426,11 @@ bool ensure_smem_attr(int dev) {
     return true;
 }
 
-template <int CG, int BN, int ST, int MC, int AR, bool SW, typename OutT, int IN = 0, int KS = 1>
+template <int CG, int BN, int ST, int AR, bool SW, typename OutT, int IN = 0, int KS = 1>
 int launch_gemm(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tcm,
                 const CUtensorMap& twm, const tcg::GemmParams& gp, cudaStream_t stream, int dev) {
-    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, MC, AR, SW, OutT, IN, KS>;
-    if (!ensure_smem_attr<CG, BN, ST, MC, AR, SW, OutT, IN, KS>(dev)) return TCGEMM_ERR_CUDA;
+    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, AR, SW, OutT, IN, KS>;
+    if (!ensure_smem_attr<CG, BN, ST, AR, SW, OutT, IN, KS>(dev)) return TCGEMM_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(pl.grid), 1, 1);
     cfg.blockDim = dim3(tcg::GemmCfg<CG, BN, ST, AR>::kThreads, 1, 1);
@@ -447,9 +438,9 @@ int launch_gemm(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, co
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     cfg.numAttrs = 0;
-    if (CG * MC * KS > 1) {
+    if (CG * KS > 1) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = CG * MC * KS;
+        attr[0].val.clusterDim.x = CG * KS;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
@@ -474,7 +465,7 @@ int launch_gemm(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, co
         rcfg.attrs = rattr;
         rcfg.numAttrs = 1;
         e = cudaLaunchKernelEx(&rcfg, tcg::sk_reduce_kernel<CG, BN, SW, OutT>, static_cast<const float*>(pl.ws_ptr),
-                               gp, pl.grid / (CG * MC));
+                               gp, pl.grid / CG);
         if (e != cudaSuccess) {
             set_error("reduction kernel launch: %s", cudaGetErrorString(e));
             return TCGEMM_ERR_CUDA;
@@ -525,19 +516,13 @@ int probe_device(int& dev_out, DeviceInfo& info) {
         d.supported = (major == 10 && minor == 3);
         d.sms = sms;
         d.max_pairs = sms / 2;
-        d.max_quads = sms / 4;
         if (d.supported) {
             // How many clusters of each kind can be resident at once (cluster
             // placement may leave some SMs of a GPC unused).
-            if (ensure_smem_attr<2, 256, kStages2, 1, 128, false, __nv_bfloat16>(dev)) {
-                const int n = max_active_clusters(tcg::gemm_bf16_tn_kernel<2, 256, kStages2, 1, 128, false, __nv_bfloat16>,
+            if (ensure_smem_attr<2, 256, kStages2, 128, false, __nv_bfloat16>(dev)) {
+                const int n = max_active_clusters(tcg::gemm_bf16_tn_kernel<2, 256, kStages2, 128, false, __nv_bfloat16>,
                                                   2, Cfg2::kSmemBytes, sms);
                 if (n > 0) d.max_pairs = n;
-            }
-            if (ensure_smem_attr<1, 256, kStages1, 4, 128, false, __nv_bfloat16>(dev)) {
-                const int n = max_active_clusters(tcg::gemm_bf16_tn_kernel<1, 256, kStages1, 4, 128, false, __nv_bfloat16>,
-                                                  4, Cfg1::kSmemBytes, sms);
-                if (n > 0) d.max_quads = n;
             }
         }
         d.probed = true;
@@ -667,7 +652,7 @@ int noalloc_scratch(int dev, void** out) {
 
 void fill_plan_out(const Plan& pl, int64_t* out) {
     out[0] = pl.grid;
-    out[1] = pl.cta_group * pl.mc * pl.ks;
+    out[1] = pl.cta_group * pl.ks;
     out[2] = pl.tiles_m;
     out[3] = pl.tiles_n;
     out[4] = pl.bm;
@@ -774,7 +759,7 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
              int ws_mode = kWsInternal, void* ws = nullptr, int64_t ws_bytes = 0, const Epilogue& ep = Epilogue(),
              int in_kind = 0, int in_fmt = 0, bool a_col = false, bool b_row = false) {
     t_last_error[0] = '\0';
-    if (variant < TCGEMM_VARIANT_AUTO || variant > TCGEMM_VARIANT_SWAP_N64_KS2) {
+    if (!variant_known(variant)) {
         set_error("unknown variant %d", variant);
         return TCGEMM_ERR_INVALID_ARG;
     }
@@ -783,7 +768,7 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
             set_error("unknown FP8 format %d", in_fmt);
             return TCGEMM_ERR_INVALID_ARG;
         }
-        if (variant == TCGEMM_VARIANT_1CTA || variant == TCGEMM_VARIANT_1CTA_MC) {
+        if (variant == TCGEMM_VARIANT_1CTA) {
             set_error("variant %d is not built for FP8 operands", variant);
             return TCGEMM_ERR_INVALID_ARG;
         }
@@ -793,13 +778,13 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
             set_error("int8 output is written only: beta must be 0");
             return TCGEMM_ERR_INVALID_ARG;
         }
-        if (variant == TCGEMM_VARIANT_1CTA || variant == TCGEMM_VARIANT_1CTA_MC) {
+        if (variant == TCGEMM_VARIANT_1CTA) {
             set_error("variant %d is not built for int8 output", variant);
             return TCGEMM_ERR_INVALID_ARG;
         }
     }
-    if ((a_col || b_row) && (in_kind == 1 || variant == TCGEMM_VARIANT_1CTA_MC)) {
-        set_error("column-major A / row-major B: bf16 operands and variants other than 3 only");
+    if ((a_col || b_row) && in_kind == 1) {
+        set_error("column-major A / row-major B: bf16 operands only");
         return TCGEMM_ERR_INVALID_ARG;
     }
     int rc = validate(M, N, K, A, lda, B, ldb, C, ldc, out_dtype, in_kind == 1 ? 1 : 2, a_col, b_row);
@@ -851,7 +836,7 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     }
 
     Plan pl;
-    if (!make_plan(M, N, K, variant, info.sms, info.max_pairs, info.max_quads, pl, ws_mode != kWsNone, in_kind,
+    if (!make_plan(M, N, K, variant, info.sms, info.max_pairs, pl, ws_mode != kWsNone, in_kind,
                    a_col, b_row)) {
         set_error("no launch plan for this shape and variant");
         return TCGEMM_ERR_INVALID_ARG;
@@ -882,10 +867,9 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
             if (rc != TCGEMM_OK) return rc;
         }
     }
-    // Box heights: a CTA pair loads half of the B tile per CTA; a multicast
-    // CTA loads half of its A tile and half of its B tile.
-    const uint32_t a_box_rows = (pl.mc == 4 || pl.arows == 64) ? 64u : 128u;
-    const uint32_t b_box_rows = static_cast<uint32_t>(pl.bn / pl.cta_group / (pl.mc == 4 ? 2 : 1));
+    // Box heights: a CTA pair loads half of the B tile per CTA.
+    const uint32_t a_box_rows = pl.arows == 64 ? 64u : 128u;
+    const uint32_t b_box_rows = static_cast<uint32_t>(pl.bn / pl.cta_group);
     // The transposed product multiplies B^T (N x K, rows of B contiguous in
     // k) by A^T: the operands trade places.
     const void* opA = pl.swap ? B : A;
@@ -945,20 +929,20 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     if (out_dtype == TCGEMM_OUT_I8) {
         // The quantising epilogue: CTA-pair tiles, narrow tiles, the
         // transposed product; bf16 or 8-bit operands.
-#define TCGEMM_LAUNCH_I8(CG, BN, ST, MC, AR, SW)                                                             \
-    return in_kind == 1 ? launch_gemm<CG, BN, ST, MC, AR, SW, int8_t, 1>(pl, ta, tb, tcm, twm, gp, stream, dev) \
-                        : launch_gemm<CG, BN, ST, MC, AR, SW, int8_t, 0>(pl, ta, tb, tcm, twm, gp, stream, dev)
+#define TCGEMM_LAUNCH_I8(CG, BN, ST, AR, SW)                                                             \
+    return in_kind == 1 ? launch_gemm<CG, BN, ST, AR, SW, int8_t, 1>(pl, ta, tb, tcm, twm, gp, stream, dev) \
+                        : launch_gemm<CG, BN, ST, AR, SW, int8_t, 0>(pl, ta, tb, tcm, twm, gp, stream, dev)
         if (pl.swap && pl.ks == 2 && pl.bn == 128)
-            return in_kind == 1 ? launch_gemm<1, 128, kStagesS128, 1, 128, true, int8_t, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
-                                : launch_gemm<1, 128, kStagesS128, 1, 128, true, int8_t, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
+            return in_kind == 1 ? launch_gemm<1, 128, kStagesS128, 128, true, int8_t, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
+                                : launch_gemm<1, 128, kStagesS128, 128, true, int8_t, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
         if (pl.swap && pl.ks == 2)
-            return in_kind == 1 ? launch_gemm<1, 64, kStagesN64, 1, 128, true, int8_t, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
-                                : launch_gemm<1, 64, kStagesN64, 1, 128, true, int8_t, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
-        if (pl.swap) TCGEMM_LAUNCH_I8(1, 64, kStagesN64, 1, 128, true);
-        if (pl.bn == 64 && pl.arows == 64) TCGEMM_LAUNCH_I8(1, 64, kStagesN64h, 1, 64, false);
-        if (pl.bn == 64) TCGEMM_LAUNCH_I8(1, 64, kStagesN64, 1, 128, false);
-        if (pl.cta_group == 2 && pl.bn == 224) TCGEMM_LAUNCH_I8(2, 224, kStages2n, 1, 128, false);
-        if (pl.cta_group == 2) TCGEMM_LAUNCH_I8(2, 256, kStages2, 1, 128, false);
+            return in_kind == 1 ? launch_gemm<1, 64, kStagesN64, 128, true, int8_t, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
+                                : launch_gemm<1, 64, kStagesN64, 128, true, int8_t, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
+        if (pl.swap) TCGEMM_LAUNCH_I8(1, 64, kStagesN64, 128, true);
+        if (pl.bn == 64 && pl.arows == 64) TCGEMM_LAUNCH_I8(1, 64, kStagesN64h, 64, false);
+        if (pl.bn == 64) TCGEMM_LAUNCH_I8(1, 64, kStagesN64, 128, false);
+        if (pl.cta_group == 2 && pl.bn == 224) TCGEMM_LAUNCH_I8(2, 224, kStages2n, 128, false);
+        if (pl.cta_group == 2) TCGEMM_LAUNCH_I8(2, 256, kStages2, 128, false);
 #undef TCGEMM_LAUNCH_I8
         set_error("no int8-output kernel for this plan");
         return TCGEMM_ERR_INVALID_ARG;
@@ -966,40 +950,39 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     if (in_kind == 1) {
         // 8-bit operands: the CTA-pair tiles, the narrow tiles and the
         // transposed product.
-#define TCGEMM_LAUNCH8(CG, BN, ST, MC, AR, SW)                                                                  \
-    return bf16 ? launch_gemm<CG, BN, ST, MC, AR, SW, __nv_bfloat16, 1>(pl, ta, tb, tcm, twm, gp, stream, dev) \
-                : launch_gemm<CG, BN, ST, MC, AR, SW, float, 1>(pl, ta, tb, tcm, twm, gp, stream, dev)
+#define TCGEMM_LAUNCH8(CG, BN, ST, AR, SW)                                                                  \
+    return bf16 ? launch_gemm<CG, BN, ST, AR, SW, __nv_bfloat16, 1>(pl, ta, tb, tcm, twm, gp, stream, dev) \
+                : launch_gemm<CG, BN, ST, AR, SW, float, 1>(pl, ta, tb, tcm, twm, gp, stream, dev)
         if (pl.swap && pl.ks == 2 && pl.bn == 128)
-            return bf16 ? launch_gemm<1, 128, kStagesS128, 1, 128, true, __nv_bfloat16, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
-                        : launch_gemm<1, 128, kStagesS128, 1, 128, true, float, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
+            return bf16 ? launch_gemm<1, 128, kStagesS128, 128, true, __nv_bfloat16, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
+                        : launch_gemm<1, 128, kStagesS128, 128, true, float, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
         if (pl.swap && pl.ks == 2)
-            return bf16 ? launch_gemm<1, 64, kStagesN64, 1, 128, true, __nv_bfloat16, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
-                        : launch_gemm<1, 64, kStagesN64, 1, 128, true, float, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
-        if (pl.swap) TCGEMM_LAUNCH8(1, 64, kStagesN64, 1, 128, true);
-        if (pl.bn == 64 && pl.arows == 64) TCGEMM_LAUNCH8(1, 64, kStagesN64h, 1, 64, false);
-        if (pl.bn == 64) TCGEMM_LAUNCH8(1, 64, kStagesN64, 1, 128, false);
-        if (pl.cta_group == 2 && pl.bn == 224) TCGEMM_LAUNCH8(2, 224, kStages2n, 1, 128, false);
-        if (pl.cta_group == 2) TCGEMM_LAUNCH8(2, 256, kStages2, 1, 128, false);
+            return bf16 ? launch_gemm<1, 64, kStagesN64, 128, true, __nv_bfloat16, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
+                        : launch_gemm<1, 64, kStagesN64, 128, true, float, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
+        if (pl.swap) TCGEMM_LAUNCH8(1, 64, kStagesN64, 128, true);
+        if (pl.bn == 64 && pl.arows == 64) TCGEMM_LAUNCH8(1, 64, kStagesN64h, 64, false);
+        if (pl.bn == 64) TCGEMM_LAUNCH8(1, 64, kStagesN64, 128, false);
+        if (pl.cta_group == 2 && pl.bn == 224) TCGEMM_LAUNCH8(2, 224, kStages2n, 128, false);
+        if (pl.cta_group == 2) TCGEMM_LAUNCH8(2, 256, kStages2, 128, false);
 #undef TCGEMM_LAUNCH8
         set_error("no FP8 kernel for this plan");
         return TCGEMM_ERR_INVALID_ARG;
     }
-#define TCGEMM_LAUNCH(CG, BN, ST, MC, AR, SW)                                                               \
-    return bf16 ? launch_gemm<CG, BN, ST, MC, AR, SW, __nv_bfloat16>(pl, ta, tb, tcm, twm, gp, stream, dev) \
-                : launch_gemm<CG, BN, ST, MC, AR, SW, float>(pl, ta, tb, tcm, twm, gp, stream, dev)
-    if (pl.mc == 4) TCGEMM_LAUNCH(1, 256, kStages1, 4, 128, false);
+#define TCGEMM_LAUNCH(CG, BN, ST, AR, SW)                                                               \
+    return bf16 ? launch_gemm<CG, BN, ST, AR, SW, __nv_bfloat16>(pl, ta, tb, tcm, twm, gp, stream, dev) \
+                : launch_gemm<CG, BN, ST, AR, SW, float>(pl, ta, tb, tcm, twm, gp, stream, dev)
     if (pl.swap && pl.ks == 2 && pl.bn == 128)
-        return bf16 ? launch_gemm<1, 128, kStagesS128, 1, 128, true, __nv_bfloat16, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
-                    : launch_gemm<1, 128, kStagesS128, 1, 128, true, float, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
+        return bf16 ? launch_gemm<1, 128, kStagesS128, 128, true, __nv_bfloat16, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
+                    : launch_gemm<1, 128, kStagesS128, 128, true, float, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
     if (pl.swap && pl.ks == 2)
-        return bf16 ? launch_gemm<1, 64, kStagesN64, 1, 128, true, __nv_bfloat16, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
-                    : launch_gemm<1, 64, kStagesN64, 1, 128, true, float, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
-    if (pl.swap) TCGEMM_LAUNCH(1, 64, kStagesN64, 1, 128, true);
-    if (pl.bn == 64 && pl.arows == 64) TCGEMM_LAUNCH(1, 64, kStagesN64h, 1, 64, false);
-    if (pl.bn == 64) TCGEMM_LAUNCH(1, 64, kStagesN64, 1, 128, false);
-    if (pl.cta_group == 1) TCGEMM_LAUNCH(1, 256, kStages1, 1, 128, false);
-    if (pl.bn == 224) TCGEMM_LAUNCH(2, 224, kStages2n, 1, 128, false);
-    TCGEMM_LAUNCH(2, 256, kStages2, 1, 128, false);
+        return bf16 ? launch_gemm<1, 64, kStagesN64, 128, true, __nv_bfloat16, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
+                    : launch_gemm<1, 64, kStagesN64, 128, true, float, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
+    if (pl.swap) TCGEMM_LAUNCH(1, 64, kStagesN64, 128, true);
+    if (pl.bn == 64 && pl.arows == 64) TCGEMM_LAUNCH(1, 64, kStagesN64h, 64, false);
+    if (pl.bn == 64) TCGEMM_LAUNCH(1, 64, kStagesN64, 128, false);
+    if (pl.cta_group == 1) TCGEMM_LAUNCH(1, 256, kStages1, 128, false);
+    if (pl.bn == 224) TCGEMM_LAUNCH(2, 224, kStages2n, 128, false);
+    TCGEMM_LAUNCH(2, 256, kStages2, 128, false);
 #undef TCGEMM_LAUNCH
 }
 
@@ -1116,9 +1099,8 @@ int tcgemm_autotune(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
             return TCGEMM_ERR_CUDA;
         }
     }
-    const int candidates[] = {TCGEMM_VARIANT_2CTA,    TCGEMM_VARIANT_2CTA_W256, TCGEMM_VARIANT_1CTA,
-                              TCGEMM_VARIANT_1CTA_MC, TCGEMM_VARIANT_1CTA_N64,  TCGEMM_VARIANT_SWAP_N64,
-                              TCGEMM_VARIANT_SWAP_N64_KS2};
+    const int candidates[] = {TCGEMM_VARIANT_2CTA,      TCGEMM_VARIANT_2CTA_W256, TCGEMM_VARIANT_1CTA,
+                              TCGEMM_VARIANT_1CTA_N64,  TCGEMM_VARIANT_SWAP_N64,  TCGEMM_VARIANT_SWAP_N64_KS2};
     int best = TCGEMM_VARIANT_AUTO;
     float best_t = 0.0f;
     rc = TCGEMM_OK;
@@ -1197,7 +1179,7 @@ int64_t tcgemm_noalloc_scratch_bytes(void) { return static_cast<int64_t>(kNoAllo
 int64_t tcgemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int variant, int num_sms) {
     if (M <= 0 || N <= 0 || K <= 0 || num_sms <= 0) return 0;
     Plan pl;
-    if (!make_plan(M, N, K, variant, num_sms, num_sms / 2, num_sms / 4, pl)) return -1;
+    if (!make_plan(M, N, K, variant, num_sms, num_sms / 2, pl)) return -1;
     return static_cast<int64_t>(pl.ws_bytes);
 }
 
@@ -1206,7 +1188,7 @@ int tcgemm_pick_variant(int64_t M, int64_t N, int64_t K, int num_sms) { return p
 int tcgemm_plan(int64_t M, int64_t N, int64_t K, int variant, int num_sms, int64_t* out) {
     if (out == nullptr || M <= 0 || N <= 0 || K <= 0 || num_sms <= 0) return TCGEMM_ERR_INVALID_ARG;
     Plan pl;
-    if (!make_plan(M, N, K, variant, num_sms, num_sms / 2, num_sms / 4, pl)) return TCGEMM_ERR_INVALID_ARG;
+    if (!make_plan(M, N, K, variant, num_sms, num_sms / 2, pl)) return TCGEMM_ERR_INVALID_ARG;
     fill_plan_out(pl, out);
     return TCGEMM_OK;
 }
@@ -1216,7 +1198,7 @@ int tcgemm_plan_kind(int64_t M, int64_t N, int64_t K, int variant, int in_kind, 
     if (out == nullptr || M <= 0 || N <= 0 || K <= 0 || num_sms <= 0 || in_kind < 0 || in_kind > 1)
         return TCGEMM_ERR_INVALID_ARG;
     Plan pl;
-    if (!make_plan(M, N, K, variant, num_sms, num_sms / 2, num_sms / 4, pl, true, in_kind,
+    if (!make_plan(M, N, K, variant, num_sms, num_sms / 2, pl, true, in_kind,
                    a_layout == TCGEMM_COL_MAJOR, b_layout == TCGEMM_ROW_MAJOR))
         return TCGEMM_ERR_INVALID_ARG;
     fill_plan_out(pl, out);
@@ -1231,7 +1213,7 @@ int tcgemm_device_info(int64_t* out) {
     if (rc != TCGEMM_OK) return rc;
     out[0] = info.sms;
     out[1] = info.max_pairs;
-    out[2] = info.max_quads;
+    out[2] = 0;  // formerly the 4-CTA cluster count; no 4-CTA kernel is built
     out[3] = dev;
     return TCGEMM_OK;
 }
@@ -1242,7 +1224,7 @@ int tcgemm_plan_device(int64_t M, int64_t N, int64_t K, int variant, int64_t* ou
     if (rc != TCGEMM_OK) return rc;
     if (out == nullptr || M <= 0 || N <= 0 || K <= 0) return TCGEMM_ERR_INVALID_ARG;
     Plan pl;
-    if (!make_plan(M, N, K, variant, static_cast<int>(d[0]), static_cast<int>(d[1]), static_cast<int>(d[2]), pl))
+    if (!make_plan(M, N, K, variant, static_cast<int>(d[0]), static_cast<int>(d[1]), pl))
         return TCGEMM_ERR_INVALID_ARG;
     fill_plan_out(pl, out);
     return TCGEMM_OK;
@@ -1252,8 +1234,8 @@ int tcgemm_units(int64_t M, int64_t N, int64_t K, int variant, int num_sms, int 
                  int32_t* out) {
     if (out == nullptr || M <= 0 || N <= 0 || K <= 0 || num_sms <= 0 || max_units < 0) return -1;
     Plan pl;
-    if (!make_plan(M, N, K, variant, num_sms, num_sms / 2, num_sms / 4, pl)) return -1;
-    const int clusters = pl.grid / (pl.cta_group * pl.mc * pl.ks);
+    if (!make_plan(M, N, K, variant, num_sms, num_sms / 2, pl)) return -1;
+    const int clusters = pl.grid / (pl.cta_group * pl.ks);
     if (cluster < 0 || cluster >= clusters) return -1;
     tcg::GemmParams gp = {};
     gp.num_kb = pl.num_kb;

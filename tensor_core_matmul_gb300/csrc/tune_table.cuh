@@ -31,10 +31,8 @@ bool tune_entry_valid(const TuneKey& k, int variant) {
     if (k.in_kind == 1 && k.in_fmt != TCGEMM_FP8_E4M3 && k.in_fmt != TCGEMM_FP8_E5M2) return false;
     if (k.out_dtype != TCGEMM_OUT_F32 && k.out_dtype != TCGEMM_OUT_BF16 && k.out_dtype != TCGEMM_OUT_I8) return false;
     if ((k.a_col | k.b_row | k.has_beta) & ~1) return false;
-    if (variant < TCGEMM_VARIANT_1CTA || variant > TCGEMM_VARIANT_SWAP_N64_KS2) return false;
-    const bool single_cta_only = variant == TCGEMM_VARIANT_1CTA || variant == TCGEMM_VARIANT_1CTA_MC;
-    if (single_cta_only && (k.in_kind == 1 || k.out_dtype == TCGEMM_OUT_I8)) return false;
-    if (variant == TCGEMM_VARIANT_1CTA_MC && (k.a_col || k.b_row)) return false;
+    if (!variant_known(variant) || variant == TCGEMM_VARIANT_AUTO) return false;
+    if (variant == TCGEMM_VARIANT_1CTA && (k.in_kind == 1 || k.out_dtype == TCGEMM_OUT_I8)) return false;
     if ((k.a_col || k.b_row) && k.in_kind == 1) return false;
     if (k.out_dtype == TCGEMM_OUT_I8 && k.has_beta) return false;
     return true;

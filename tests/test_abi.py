@@ -104,7 +104,7 @@ def test_epilogue_argument_errors(tc, bias, bias_dtype, act, status):
 @pytest.mark.parametrize("args,fmt,variant,status", [
     ((8, 8, 16, FAKE, 16, FAKE * 2, 16, FAKE * 4, 8), 2, 0, 1),     # unknown FP8 format
     ((8, 8, 16, FAKE, 16, FAKE * 2, 16, FAKE * 4, 8), 0, 1, 1),     # variant not built for FP8
-    ((8, 8, 16, FAKE, 16, FAKE * 2, 16, FAKE * 4, 8), 1, 3, 1),     # variant not built for FP8
+    ((8, 8, 16, FAKE, 16, FAKE * 2, 16, FAKE * 4, 8), 1, 3, 1),     # 3 names no kernel
     ((8, 8, 8, FAKE, 8, FAKE * 2, 16, FAKE * 4, 8), 0, 0, 2),       # lda = 8 bytes: not a 16-byte multiple
     ((8, 8, 16, FAKE + 8, 16, FAKE * 2, 16, FAKE * 4, 8), 1, 0, 2), # A misaligned
 ])
@@ -143,9 +143,16 @@ def test_row_major_b_takes_256_wide_pairs(tc):
     assert tc.plan(4096, 4096, 4096, 0, 152, a_col=True)["bn"] == 224
 
 
-def test_layout_multicast_variant_refused(tc):
+def test_variant_number_3_names_no_kernel(tc):
+    """Variant number 3 is unused: every entry point refuses it on the host,
+    and no plan exists for it."""
     assert tc.binding.gemm_bf16_layout_raw(8, 8, 16, FAKE, 8, 1, FAKE * 2, 16, 1, FAKE * 4, 8, 1.0, 0.0, 0, 0,
                                            3) == 1
+    assert tc.lib().gemm_bf16_variant(8, 8, 16, FAKE, 16, FAKE * 2, 16, FAKE * 4, 8, ctypes.c_float(1.0),
+                                      ctypes.c_float(0.0), 0, None, 3) == 1
+    assert b"unknown variant" in tc.lib().tcgemm_last_error()
+    with pytest.raises(tc.TcgemmError):
+        tc.plan(4096, 4096, 4096, 3, 152)
 
 
 def test_autotune_table_starts_empty_and_rejects_bad_arguments(tc):
@@ -208,7 +215,7 @@ def test_tile_order_groups_for_l2(tc):
 
 @pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (8192, 8192, 8192), (4000, 4100, 4104),
                                    (64, 8192, 8192), (256, 256, 256), (1, 1, 1)])
-@pytest.mark.parametrize("variant", [1, 2, 3, 4, 5, 6, 7])
+@pytest.mark.parametrize("variant", [1, 2, 4, 5, 6, 7])
 def test_plans(tc, M, N, K, variant):
     p = tc.plan(M, N, K, variant, 152)
     if p["swap"]:
@@ -226,7 +233,7 @@ SK_SHAPES = [(4096, 4096, 4096), (8192, 8192, 8192), (4000, 4100, 4104), (64, 81
 
 
 @pytest.mark.parametrize("M,N,K", SK_SHAPES)
-@pytest.mark.parametrize("variant", [1, 2, 3, 4, 5, 6, 7])
+@pytest.mark.parametrize("variant", [1, 2, 4, 5, 6, 7])
 @pytest.mark.parametrize("sms", [152, 148, 20])
 def test_stream_k_plan_invariants(tc, M, N, K, variant, sms):
     p = tc.plan(M, N, K, variant, sms)
@@ -252,8 +259,8 @@ def _sk_slot(c, t_begin, iters, clusters):
 
 @pytest.mark.parametrize("M,N,K,v", [(4096, 4096, 4096, 2), (8192, 8192, 8192, 2), (512, 512, 16384, 2),
                                      (256, 2048, 8192, 1), (600, 700, 8192, 5), (1024, 1280, 2048, 2),
-                                     (64, 8192, 8192, 1), (513, 200, 1000, 1), (4000, 4100, 4104, 3),
-                                     (129, 257, 65, 3), (64, 8192, 8192, 4), (4096, 4096, 4096, 1),
+                                     (64, 8192, 8192, 1), (513, 200, 1000, 1), (4000, 4100, 4104, 4),
+                                     (129, 257, 65, 7), (64, 8192, 8192, 4), (4096, 4096, 4096, 1),
                                      (4096, 4096, 4096, 5), (8192, 8192, 8192, 5), (4000, 4100, 4104, 2),
                                      (200, 300, 2392, 2), (3000, 5000, 777, 2), (64, 8192, 8192, 6),
                                      (50, 3000, 5000, 6)])
@@ -289,15 +296,6 @@ def test_unit_schedule_covers_every_k_block_once(tc, M, N, K, v):
             assert slot not in slots
             slots.add(slot)
     assert all(0 <= sl < 2 * G for sl in slots)
-
-
-@pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (4000, 4100, 4104), (129, 257, 65), (1, 1, 1)])
-def test_multicast_plan_blocks(tc, M, N, K):
-    """Variant 3 walks 2 x 2 blocks of 128 x 256 tiles with 4-CTA clusters."""
-    p = tc.plan(M, N, K, 3, 152)
-    assert p["cluster"] == 4 and p["cta_group"] == 1 and p["bm"] == 128 and p["bn"] == 256
-    assert p["grid_m"] == (p["tiles_m"] + 1) // 2 and p["grid_n"] == (p["tiles_n"] + 1) // 2
-    assert p["sk_tiles"] == 0 and p["ws_bytes"] == 0
 
 
 def test_width_choice(tc):
@@ -373,8 +371,8 @@ def test_autotune_table_set_save_load(tc, tmp_path):
 
 
 @pytest.mark.parametrize("kwargs", [dict(variant=1, in_type=1, out_dtype=0),   # one-CTA kernels: no FP8
-                                    dict(variant=3, out_dtype=2),                 # nor int8 output
-                                    dict(variant=3, a_col=True),                  # multicast: row-major A only
+                                    dict(variant=1, out_dtype=2),                 # nor int8 output
+                                    dict(variant=3),                              # 3 names no kernel
                                     dict(variant=8), dict(variant=-1),
                                     dict(variant=2, out_dtype=2, beta_nonzero=True)])  # int8 output has no beta
 def test_autotune_set_refuses_unbuilt(tc, kwargs):
