@@ -12,9 +12,16 @@ Timing: W untimed warm-up steps, then K timed steps between a barrier plus
 torch.cuda.synchronize() on both sides.  The 96 MiB working set of the 4096
 case fits in the 126 MiB L2, so a 512 MiB buffer is written between timed
 steps (untimed) and each GEMM is timed alone with CUDA events on its stream.
-With N > 1 (torchrun), every rank multiplies its own independent matrices on
-its own GPU (no collective on the data path), the max over ranks is taken
-and `value` is the aggregate over all ranks.
+The other large workloads (8192^3 with beta = 0.5, the 4000x4100x4104 edge
+shape, the 64x8192x8192 skinny shape) are timed the same way after the main
+line and reported under "subrecords", each with its own roofline and clocks.
+
+With N > 1 (torchrun), the default (--multi slabs) splits one GEMM N times
+wider than the workload into N contiguous column slabs of B and C, A
+replicated: rank g computes C[:, g*N:(g+1)*N] (weak scaling, no collective on
+the data path).  --multi replicas gives every rank its own copy of the
+workload instead.  The max over ranks is taken and `value` is the aggregate
+over all ranks.
 
 `--impl reference` times the CPU oracle (the plain C definition) on a bounded
 column slab of the same workload, on the host cores.
@@ -170,10 +177,133 @@ def make_bias(args, N: int):
     return torch.randn(N, generator=torch.Generator().manual_seed(9001), dtype=torch.float32)
 
 
+def flush_buffers(dev):
+    import torch
+    return (torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev),
+            torch.ones(FLUSH_BYTES // 8, dtype=torch.int64, device=dev))
+
+
+def make_flush(bufs):
+    flush, flush_rd = bufs
+
+    def flush_l2(i: int, read: bool = True):
+        # Write a buffer larger than L2 (evicts A, B and C), then read a
+        # second one, so that L2 is left holding clean lines: the write-back
+        # of the first buffer's dirty lines then happens here, untimed,
+        # instead of inside the next timed call.
+        flush.fill_(i & 0xFF)
+        if read:
+            flush_rd.sum()
+    return flush_l2
+
+
+def time_steps(gemm, flush_l2, stream, steps: int, dev, pg=None, sample_clocks: bool = True):
+    """K timed steps, each one GEMM between its own CUDA events on `stream`
+    after an untimed L2 flush; a barrier and a synchronize on both sides.
+    Returns per-step milliseconds, the wall time of the loop, the library's
+    kernel launches inside it and the sampled clocks."""
+    import torch
+
+    import tensor_core_matmul_gb300 as tc
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    sampler = ClockSampler(torch.cuda.current_device()) if sample_clocks else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.25)  # let the sampler take a first reading
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    n_launch0 = tc.launch_count()
+    wall0 = time.perf_counter()
+    for i in range(steps):
+        flush_l2(i)                    # evict A, B, C from L2 (untimed)
+        starts[i].record(stream)
+        gemm()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if pg:
+        pg.barrier()
+    launches = tc.launch_count() - n_launch0
+    clocks = sampler.stop() if sampler else None
+    st, where = tc.check_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} in the timed region (role {where})")
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)], wall, launches, clocks
+
+
+def gemm_call(args, case, A, B, C, stream, bias=None, act="none", row_scale=None, variant=0):
+    """The public entry point this workload's options name, bound to its buffers."""
+    import tensor_core_matmul_gb300 as tc
+    M, N, K = case.M, case.N, case.K
+
+    def gemm():
+        if args.quant:
+            tc.gemm_quant_i8(A, B, C, case.alpha, row_scale=row_scale, zero_point=0, bias=bias, activation=act, M=M,
+                             N=N, K=K, stream=stream, variant=variant)
+        elif case.in_format != "bf16":
+            tc.gemm_fp8(A, B, C, case.alpha, case.beta, M=M, N=N, K=K, stream=stream, variant=variant)
+        elif case.a_col or case.b_row:
+            tc.gemm_bf16_layout(A, B, C, case.alpha, case.beta, a_col=case.a_col, b_row=case.b_row, M=M, N=N, K=K,
+                                stream=stream, variant=variant)
+        elif bias is None and act == "none":
+            tc.gemm_bf16(A, B, C, case.alpha, case.beta, M=M, N=N, K=K, stream=stream, variant=variant)
+        else:
+            tc.gemm_bf16_bias_act(A, B, C, case.alpha, case.beta, bias=bias, activation=act, M=M, N=N, K=K,
+                                  stream=stream, variant=variant)
+    return gemm
+
+
+def device_buffers(case, dev):
+    import torch
+    A = case.A.to(dev)
+    B = case.B.to(dev)
+    C = (case.C_in.to(dev) if case.C_in is not None
+         else torch.zeros((case.N, case.ldc), dtype=case.out_torch_dtype(), device=dev))
+    return A, B, C
+
+
+def sub_record(args, name: str, dev, stream, flush_l2, world: int, pg, peaks, peak_src, sms: int) -> dict:
+    """Another workload, plain bf16 GEMM through gemm_bf16, timed with the
+    main line's protocol (flushed L2, CUDA events per call, clocks sampled):
+    its own TFLOP/s, roofline and clocks.  Same slab rule as the main line."""
+    import tensor_core_matmul_gb300 as tc
+    sub_args = argparse.Namespace(**{**vars(args), "config": name, "in_format": "bf16", "layout": "tn",
+                                     "epilogue": "none", "quant": False})
+    case = bench_case(sub_args, world, dist_setup()[1])
+    A, B, C = device_buffers(case, dev)
+    gemm = gemm_call(sub_args, case, A, B, C, stream, variant=args.variant)
+    for _ in range(args.warmup):
+        flush_l2(1)
+        gemm()
+    times_ms, wall, launches, clocks = time_steps(gemm, flush_l2, stream, args.steps, dev, pg)
+    total_s = max_over_ranks(sum(times_ms) / 1e3)
+    variant = args.variant or tc.pick_variant(case.M, case.N, case.K, sms)
+    plan = tc.plan(case.M, case.N, case.K, variant, sms)
+    traffic = profile_traffic(f"gemm_{name}_full")
+    del A, B, C
+    return {
+        "value": round(job_throughput(case.flops, args.steps, world, total_s), 2), "unit": "TFLOP/s",
+        "ms_per_step": round(total_s / args.steps * 1e3, 5),
+        "ms_per_step_median": round(float(sorted(times_ms)[len(times_ms) // 2]), 5),
+        "steps": args.steps, "warmup": args.warmup, "gpu_launches": int(launches),
+        "config": {"workload": workload_text(case, name), "M": case.M, "N": case.N, "K": case.K,
+                   "kernel": {"variant": variant, **plan}},
+        "roofline": roofline(case, total_s / args.steps, peaks, peak_src, traffic, sms=sms, clocks=clocks),
+        "clocks": clocks,
+    }
+
+
+def workload_text(case, name: str) -> str:
+    return (f"gemm {name}: M={case.M} N={case.N} K={case.K}, {case.in_format} A row-major x B col-major, "
+            f"fp32 accumulate, {'bf16' if case.out_dtype else 'fp32'} C col-major, "
+            f"alpha={case.alpha} beta={case.beta}, N(0,1) inputs")
+
+
 def run_ours(args) -> None:
     import torch
 
-    import gemm_inputs as gi
     import tensor_core_matmul_gb300 as tc
 
     world, rank, local = dist_setup()
@@ -185,52 +315,29 @@ def run_ours(args) -> None:
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
 
-    case = bench_case(args)
+    case = bench_case(args, world, rank)
     M, N, K = case.M, case.N, case.K
-    A = case.A.to(dev)
-    B = case.B.to(dev)
     if args.quant:
         # int8 output of the quantising epilogue: written only, beta = 0.
         if case.beta != 0.0:
             raise SystemExit("--quant needs a workload with beta = 0")
+        A, B = case.A.to(dev), case.B.to(dev)
         C = torch.zeros((N, (M + 15) // 16 * 16), dtype=torch.int8, device=dev)
         row_scale = (torch.rand(M, generator=torch.Generator().manual_seed(9002)) * 60 + 4).to(dev)
     else:
-        C = (case.C_in.to(dev) if case.C_in is not None
-             else torch.zeros((N, case.ldc), dtype=case.out_torch_dtype(), device=dev))
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    flush_rd = torch.ones(FLUSH_BYTES // 8, dtype=torch.int64, device=dev)
+        A, B, C = device_buffers(case, dev)
+        row_scale = None
+    flush_bufs = flush_buffers(dev)
+    flush, _ = flush_bufs
+    flush_l2 = make_flush(flush_bufs)
     stream = torch.cuda.current_stream(dev)
-
-    def flush_l2(i: int, read: bool = True):
-        # Write a buffer larger than L2 (evicts A, B and C), then read a
-        # second one, so that L2 is left holding clean lines: the write-back
-        # of the first buffer's dirty lines then happens here, untimed,
-        # instead of inside the next timed call.
-        flush.fill_(i & 0xFF)
-        if read:
-            flush_rd.sum()
     bias_cpu = make_bias(args, N)
     act = EPILOGUES[args.epilogue][1]
     bias = None if bias_cpu is None else bias_cpu.to(dev)
 
     if args.in_format != "bf16" and args.epilogue != "none" and not args.quant:
         raise SystemExit("--epilogue with 8-bit operands needs --quant")
-
-    def gemm():
-        if args.quant:
-            tc.gemm_quant_i8(A, B, C, case.alpha, row_scale=row_scale, zero_point=0, bias=bias, activation=act, M=M,
-                             N=N, K=K, stream=stream, variant=args.variant)
-        elif args.in_format != "bf16":
-            tc.gemm_fp8(A, B, C, case.alpha, case.beta, M=M, N=N, K=K, stream=stream, variant=args.variant)
-        elif args.layout != "tn":
-            tc.gemm_bf16_layout(A, B, C, case.alpha, case.beta, a_col=case.a_col, b_row=case.b_row, M=M, N=N, K=K,
-                                stream=stream, variant=args.variant)
-        elif args.epilogue == "none":
-            tc.gemm_bf16(A, B, C, case.alpha, case.beta, M=M, N=N, K=K, stream=stream, variant=args.variant)
-        else:
-            tc.gemm_bf16_bias_act(A, B, C, case.alpha, case.beta, bias=bias, activation=act, M=M, N=N, K=K,
-                                  stream=stream, variant=args.variant)
+    gemm = gemm_call(args, case, A, B, C, stream, bias=bias, act=act, row_scale=row_scale, variant=args.variant)
 
     tuned = None
     if args.autotune:
@@ -247,32 +354,7 @@ def run_ours(args) -> None:
     if st != 0:
         raise RuntimeError(f"device status {st} during warm-up (role {where})")
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.25)  # let the sampler take a first reading
-    if pg:
-        pg.barrier()
-    torch.cuda.synchronize(dev)
-    n_launch0 = tc.launch_count()
-    wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush_l2(i)                    # evict A, B, C from L2 (untimed)
-        starts[i].record(stream)
-        gemm()
-        ends[i].record(stream)
-    torch.cuda.synchronize(dev)
-    wall = time.perf_counter() - wall0
-    if pg:
-        pg.barrier()
-    launches = tc.launch_count() - n_launch0
-    clocks = sampler.stop()
-    st, where = tc.check_device_status(stream)
-    if st != 0:
-        raise RuntimeError(f"device status {st} in the timed region (role {where})")
-
-    times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    times_ms, wall, launches, clocks = time_steps(gemm, flush_l2, stream, args.steps, dev, pg)
     total_s = max_over_ranks(sum(times_ms) / 1e3)
     # The work log's own protocol times back-to-back calls without flushing
     # L2 between them; reported beside the flushed number (same work).
@@ -312,12 +394,22 @@ def run_ours(args) -> None:
 
     e2e = None
     if not args.no_e2e and not args.quant and args.layout == "tn":
-        e2e = measure_e2e(args, case, dev, stream, bias_cpu, act)
+        e2e = measure_e2e(args, case, dev, stream, bias_cpu, act, world)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quant and args.layout == "tn":
         cpu = cpu_baseline(case, target_s=args.cpu_seconds, bias=bias_cpu, act=act)
 
+    subs = {}
+    names = [n for n in (args.subrecords.split(",") if args.subrecords else []) if n and n != args.config]
+    if names:
+        del A, B, C, gemm
+        torch.cuda.empty_cache()
+        for name in names:
+            subs[name] = sub_record(args, name, dev, stream, flush_l2, world, pg, peaks, peak_src, sms)
+            torch.cuda.empty_cache()
+
     if rank == 0:
+        slab = args.multi == "slabs" and world > 1
         out = {
             "metric": METRIC,
             "value": round(value, 2),
@@ -341,9 +433,7 @@ def run_ours(args) -> None:
             "dtype": "bf16" if args.in_format == "bf16" else f"fp8_{args.in_format}",
             "data": "synthetic",
             "config": {
-                "workload": f"gemm {args.config}: M={M} N={N} K={K}, {args.in_format} A row-major x B col-major, "
-                            f"fp32 accumulate, {'bf16' if case.out_dtype else 'fp32'} C col-major, "
-                            f"alpha={case.alpha} beta={case.beta}, N(0,1) inputs"
+                "workload": workload_text(case, args.config)
                             + ("" if args.epilogue == "none" else
                                f", fused epilogue C = {act}(alpha*A*B + beta*C + bias[j]), fp32 N(0,1) bias"),
                 "M": M, "N": N, "K": K,
@@ -356,28 +446,41 @@ def run_ours(args) -> None:
                       f"{FLUSH_BYTES >> 20} MiB read, untimed: inputs evicted, L2 left clean)",
                 "kernel": {"variant": {1: "1cta", 2: "2cta"}.get(variant, str(variant)), **plan},
                 "autotuned": tuned,
-                "parallelism": f"independent problem per GPU x{world}",
+                "parallelism": (f"one M x (N*{world}) x K GEMM in {world} contiguous column slabs of B and C, "
+                                f"A replicated, no collective on the data path" if slab else
+                                f"independent problem per GPU x{world}"),
                 "wall_s_timed_loop": round(wall, 3),
             },
             "roofline": roofline(case, total_s / args.steps, peaks, peak_src, traffic,
                                  extra_bytes=(0 if bias_cpu is None else 4 * N)
-                                 + (4 * M - M * N * (4 if case.out_dtype == 0 else 2) + M * N if args.quant else 0)),
+                                 + (4 * M - M * N * (4 if case.out_dtype == 0 else 2) + M * N if args.quant else 0),
+                                 sms=sms, clocks=clocks),
             "clocks": clocks,
             "e2e": e2e,
             "gpu_launches": int(launches),
             "cpu_baseline": cpu,
         }
+        if subs:
+            out["subrecords"] = subs
         print(json.dumps(out), flush=True)
     if pg:
         pg.destroy_process_group()
 
 
-def bench_case(args):
+def bench_case(args, world: int = 1, rank: int = 0):
     """The workload named by --config (shape, alpha/beta, output type, seed),
     with 8-bit operands when --in-format asks for them (same shapes, seeds and
-    distribution)."""
+    distribution).  Under --multi slabs with more than one rank, this rank's
+    contiguous column slab of one GEMM `world` times wider (A replicated; the
+    slabs are the column ranges gemm_inputs.slab_bounds gives)."""
     import gemm_inputs as gi
     c = gi.CONFIGS[args.config]
+    if world > 1 and args.multi == "slabs":
+        if args.in_format != "bf16" or args.layout != "tn":
+            raise SystemExit("--multi slabs uses bf16 operands in the tn layout")
+        n0, n1 = gi.slab_bounds(c["N"] * world, world, rank, align=c["N"])
+        assert (n0, n1) == (rank * c["N"], (rank + 1) * c["N"])
+        return gi.column_slab_case(args.config, world, rank)
     case = gi.make_case(args.config, c["M"], c["N"], c["K"], alpha=c["alpha"], beta=c["beta"],
                         out_dtype=c["out_dtype"], seed=c["seed"], in_format=args.in_format)
     if args.layout != "tn":
@@ -395,11 +498,24 @@ def algorithmic_bytes(case) -> int:
     return isz * case.M * case.K + isz * case.N * case.K + c + (c if case.beta != 0.0 else 0)
 
 
-def roofline(case, t_launch: float, peaks: dict, peak_src: str, traffic, extra_bytes: int = 0) -> dict:
+# Dense bf16 tensor-core rate of one Blackwell SM taken by the formula peak
+# SMs x rate x clock: 8192 FLOP (4096 multiply-adds) per clock; 8-bit
+# operands at twice that.  Reported beside the measured cuBLAS peak.
+BF16_FLOP_PER_CLK_SM = 8192
+
+
+def formula_peak_tflops(sms: int, mhz: float, fp8: bool = False) -> float:
+    return sms * BF16_FLOP_PER_CLK_SM * (2 if fp8 else 1) * mhz * 1e6 / 1e12
+
+
+def roofline(case, t_launch: float, peaks: dict, peak_src: str, traffic, extra_bytes: int = 0, sms: int = 152,
+             clocks: dict | None = None) -> dict:
     """Dominant kernel (the GEMM itself) against its bound: the tensor cores
     for the square / edge shapes, HBM for the skinny shape (intensity
     2MNK / bytes far below the ridge point).  extra_bytes: the fused
-    epilogue's bias vector."""
+    epilogue's bias vector.  Tensor-bound lines also carry the formula peak
+    SMs x 8192 FLOP/clk x clock, at the maximum SM clock and at the median
+    clock sampled during the timed region."""
     flops = case.flops
     nbytes = algorithmic_bytes(case) + extra_bytes
     peak_flops = float(peaks["bf16_tflops"])
@@ -418,15 +534,24 @@ def roofline(case, t_launch: float, peaks: dict, peak_src: str, traffic, extra_b
                 "algorithmic_bytes": nbytes, "tflops": round(flops / t_launch / 1e12, 2),
                 "peak_source": f"{src} hbm_gbs (copy bandwidth)"}
     achieved = flops / t_launch / 1e12
-    nominal = 4500.0 if fp8 else 2250.0
-    return {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_flops, "unit": "TFLOP/s",
-            "frac": round(achieved / peak_flops, 4), "traffic": traffic, "algorithmic_bytes": nbytes,
-            "peak_source": (f"{src} bf16_tflops (cuBLAS bf16 8192^3 burst)" if not fp8 else
-                            f"{src} bf16_tflops x 2 (nominal dense fp8/bf16 ratio 4.5/2.25)"),
-            "nominal_dense_tflops": nominal, "frac_of_nominal": round(achieved / nominal, 4)}
+    max_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    med_mhz = (clocks or {}).get("sm_mhz") or None
+    formula = formula_peak_tflops(sms, max_mhz, fp8)
+    out = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_flops, "unit": "TFLOP/s",
+           "frac": round(achieved / peak_flops, 4), "traffic": traffic, "algorithmic_bytes": nbytes,
+           "peak_source": (f"{src} bf16_tflops (cuBLAS bf16 8192^3 burst)" if not fp8 else
+                           f"{src} bf16_tflops x 2 (nominal dense fp8/bf16 ratio 4.5/2.25)"),
+           "formula_peak": {"tflops": round(formula, 1), "sm_mhz": max_mhz,
+                            "rule": f"{sms} SMs x {BF16_FLOP_PER_CLK_SM * (2 if fp8 else 1)} FLOP/clk x max SM clock",
+                            "frac": round(achieved / formula, 4)}}
+    if med_mhz:
+        f_med = formula_peak_tflops(sms, float(med_mhz), fp8)
+        out["formula_peak_at_median_clock"] = {"tflops": round(f_med, 1), "sm_mhz": med_mhz,
+                                               "frac": round(achieved / f_med, 4)}
+    return out
 
 
-def measure_e2e(args, case, dev, stream, bias_cpu=None, act="none") -> dict:
+def measure_e2e(args, case, dev, stream, bias_cpu=None, act="none", world: int = 1) -> dict:
     """Same metric through the public API with host buffers: every step copies
     A and B (and C when beta != 0) from pinned host memory to the device, runs
     the GEMM and copies C back to pinned host memory.  For the plain GEMM that
@@ -500,7 +625,8 @@ def measure_e2e(args, case, dev, stream, bias_cpu=None, act="none") -> dict:
            + (C0.numel() * C0.element_size() if has_beta else 0))
     h2d += 0 if bias_cpu is None else bias_cpu.numel() * 4
     d2h = C0.numel() * C0.element_size()
-    return {"value": round(case.flops * steps / t / 1e12, 2), "unit": "TFLOP/s",
+    t = max_over_ranks(t)
+    return {"value": round(world * case.flops * steps / t / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
             "ms_per_step": round(t / steps * 1e3, 4), "streams": nbuf,
             "api": "gemm_bf16_host (C ABI, host buffers)" if host_entry else "torch copies + device entry point",
@@ -643,6 +769,12 @@ def main():
                     help="time every variant first (tcgemm_autotune) and let the automatic choice use the fastest")
     ap.add_argument("--quant", action="store_true",
                     help="int8 output through the per-row quantising epilogue (gemm_quant_i8)")
+    ap.add_argument("--subrecords", default="s8k,edge,skinny",
+                    help="other workloads timed the same way (plain bf16 GEMM) and reported under 'subrecords' "
+                         "(comma-separated; empty for none)")
+    ap.add_argument("--multi", default="slabs", choices=["slabs", "replicas"],
+                    help="with N > 1 ranks: 'slabs' splits one GEMM N times wider into contiguous column slabs "
+                         "of B and C (A replicated); 'replicas' gives every rank its own copy of the workload")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")

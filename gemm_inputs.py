@@ -248,6 +248,45 @@ def config_case(name: str, kind: str = "normal") -> GemmCase:
                      out_dtype=c["out_dtype"], seed=c["seed"], kind=kind)
 
 
+def slab_bounds(n_total: int, world: int, rank: int, align: int = 1) -> tuple[int, int]:
+    """Columns [n0, n1) of an n_total-column output that rank `rank` of
+    `world` owns: contiguous slabs in rank order, each a multiple of `align`
+    columns except possibly the last, as even as that allows (a rank may get
+    none when n_total is small)."""
+    if world < 1 or not 0 <= rank < world or align < 1 or n_total < 0:
+        raise ValueError("bad slab arguments")
+    units = (n_total + align - 1) // align
+    u0 = units * rank // world
+    u1 = units * (rank + 1) // world
+    return min(n_total, u0 * align), min(n_total, u1 * align)
+
+
+def slab_seed(seed: int, rank: int) -> int:
+    """Seed of rank `rank`'s slab of a matrix whose slab 0 uses `seed` (so a
+    one-rank job draws exactly the single-GPU workload)."""
+    return int(seed) if rank == 0 else int(seed) + 7919 * rank
+
+
+def column_slab_case(name: str, world: int, rank: int) -> GemmCase:
+    """Rank `rank`'s part of one GEMM that is `world` times wider than the
+    named workload: C = alpha*A*B + beta*C with M x (N*world) output, A
+    replicated on every rank, and this rank holding the contiguous columns
+    [rank*N, (rank+1)*N) of B and C (drawn from their own seeds; rank 0's
+    slab is the named workload itself)."""
+    c = CONFIGS[name]
+    case = config_case(name)
+    if rank == 0:
+        return case
+    s = c["seed"]
+    M, N, K = c["M"], c["N"], c["K"]
+    B = normal_bf16(N, K, slab_seed(s * 1000 + 2, rank), case.ldb)
+    C_in = None
+    if case.beta != 0.0:
+        C_in = (normal_f32(N, M, slab_seed(s * 1000 + 3, rank), case.ldc) if case.out_dtype == OUT_F32
+                else normal_bf16(N, M, slab_seed(s * 1000 + 3, rank), case.ldc))
+    return dataclasses.replace(case, B=B, C_in=C_in)
+
+
 def as_u16(t: torch.Tensor) -> np.ndarray:
     """bf16 torch tensor -> numpy uint16 view of the same bytes."""
     assert t.dtype == torch.bfloat16

@@ -67,6 +67,17 @@ def run_case(case: gi.GemmCase, variant: int = 0, stream=None) -> GuardedC:
     return g
 
 
+def record_stats(what: str, stats: dict) -> None:
+    """Append one comparison's statistics as a JSON line to the file named by
+    TCGEMM_PARITY_STATS, if set (for the record of second-clause counts)."""
+    import json
+    import os
+    path = os.environ.get("TCGEMM_PARITY_STATS")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"what": what, **stats}) + "\n")
+
+
 def cin_np(case):
     if case.C_in is None:
         return None
@@ -78,31 +89,34 @@ def cin_np(case):
 def compare_full(o, case: gi.GemmCase, got: np.ndarray, exact: bool = False, what: str = ""):
     D = o.gemm_f64(case.M, case.N, case.K, gi.as_u16(case.A), gi.as_u16(case.B), cin_np(case),
                    case.alpha, case.beta)
-    cols, rows = np.divmod(np.arange(case.M * case.N, dtype=np.int64), case.M)  # flat (N, M) order
-    _compare(o, case, got, D, rows, cols, exact, what)
+    return _compare(o, case, got, D, None, None, exact, what)
 
 
 def compare_sampled(o, case: gi.GemmCase, got: np.ndarray, rows: np.ndarray, cols: np.ndarray,
                     exact: bool = False, what: str = ""):
     D = o.gemm_sampled_f64(case.M, case.N, case.K, gi.as_u16(case.A), gi.as_u16(case.B), rows, cols,
                            cin_np(case), case.alpha, case.beta)
-    _compare(o, case, got[cols, rows], D, rows, cols, exact, what)
+    return _compare(o, case, got[cols, rows], D, rows, cols, exact, what)
 
 
 def _compare(o, case, got, D, rows, cols, exact, what):
     if case.out_dtype == gi.OUT_F32:
         if exact:
             parity.check_exact(got, o.round_f32(D), what)
-        else:
-            parity.check_f32(got, D, case.K, what)
+            return {"size": int(np.size(got)), "exact": True}
+        return parity.check_f32(got, D, case.K, what)
     else:
         ref = o.round_bf16(D)
         if exact:
             parity.check_exact(got, ref, what)
+            return {"size": int(np.size(got)), "exact": True}
         else:
             def fallback(flat):
-                r, c = rows.reshape(-1)[flat], cols.reshape(-1)[flat]
+                if rows is None:  # the whole of C, flat in (N, M) order
+                    c, r = np.divmod(flat.astype(np.int64), case.M)
+                else:
+                    r, c = rows.reshape(-1)[flat], cols.reshape(-1)[flat]
                 G = o.absdot_sampled_f64(case.M, case.N, case.K, gi.as_u16(case.A), gi.as_u16(case.B), r, c)
                 # |alpha| scales the product's error; beta*C adds one exact-ish term.
                 return D.reshape(-1)[flat], abs(case.alpha) * G, case.K
-            parity.check_bf16(got, ref, what, fallback=fallback)
+            return parity.check_bf16(got, ref, what, fallback=fallback)

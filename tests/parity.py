@@ -23,6 +23,12 @@
   the accumulation bound plus the fp32 epilogue's few roundings.
 
 C_ref is the oracle's fp64 value D (for fp32 output) or its bf16 rounding.
+
+The check functions return a dict of statistics, so that a test can bound
+how often the second clause was needed: ``size``, ``beyond_1ulp`` (bf16
+elements more than one ulp from the oracle's rounding), ``second_clause``
+(those accepted by the second clause), ``max_ulp`` (largest ordered-integer
+distance) and, for fp32 output, ``max_err_over_tol``.
 """
 from __future__ import annotations
 
@@ -45,12 +51,12 @@ def f32_tolerance(ref: np.ndarray, K: int) -> np.ndarray:
     return 1e-3 * np.sqrt(max(K, 1)) * np.maximum(1.0, np.abs(ref))
 
 
-def check_f32(got: np.ndarray, ref_f64: np.ndarray, K: int, what: str = "") -> None:
+def check_f32(got: np.ndarray, ref_f64: np.ndarray, K: int, what: str = "") -> dict:
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref_f64, dtype=np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
     if got.size == 0:
-        return
+        return {"size": 0, "max_err_over_tol": 0.0}
     err = np.abs(got - ref)
     tol = f32_tolerance(ref, K)
     bad = ~(err <= tol)  # NaN counts as bad
@@ -58,6 +64,7 @@ def check_f32(got: np.ndarray, ref_f64: np.ndarray, K: int, what: str = "") -> N
         idx = np.argwhere(bad)[:5]
         raise AssertionError(f"{what}: {int(bad.sum())} of {got.size} fp32 outputs out of "
                              f"tolerance; first {idx.tolist()} got {got[bad][:5]} ref {ref[bad][:5]}")
+    return {"size": int(got.size), "max_err_over_tol": float(np.max(err / tol))}
 
 
 def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
@@ -76,18 +83,20 @@ ACC_UNIT = 2.0 ** -24  # unit roundoff of the fp32 accumulator
 
 
 def check_bf16(got_bits: np.ndarray, ref_bits: np.ndarray, what: str = "", max_ulp: int = 1,
-               fallback=None) -> None:
+               fallback=None) -> dict:
     """``fallback(flat_indices) -> (D, G, K)`` supplies the exact value D and
     G = sum|a*b| at the elements that miss the 1-ulp bar (see module doc)."""
     got_bits = np.asarray(got_bits, dtype=np.uint16)
     ref_bits = np.asarray(ref_bits, dtype=np.uint16)
     assert got_bits.shape == ref_bits.shape
     if got_bits.size == 0:
-        return
+        return {"size": 0, "beyond_1ulp": 0, "second_clause": 0, "max_ulp": 0}
     d = bf16_ulp_distance(got_bits, ref_bits)
     bad = d > max_ulp
     nan_got = (got_bits & 0x7FFF) > 0x7F80
     bad |= nan_got
+    beyond = int(bad.sum())
+    second = 0
     if bad.any() and fallback is not None and not nan_got.any():
         flat = np.flatnonzero(bad)
         limit = int(0.005 * got_bits.size) + 2
@@ -96,11 +105,13 @@ def check_bf16(got_bits: np.ndarray, ref_bits: np.ndarray, what: str = "", max_u
             got = bf16_to_f64(got_bits.reshape(-1)[flat])
             ok = np.abs(got - D) <= bf16_ulp(D) + K * ACC_UNIT * G
             bad.reshape(-1)[flat[ok]] = False
+            second = int(ok.sum())
     if bad.any():
         idx = np.argwhere(bad)[:5]
         raise AssertionError(f"{what}: {int(bad.sum())} of {got_bits.size} bf16 outputs more than "
                              f"{max_ulp} ulp away; first {idx.tolist()} got "
                              f"{[hex(x) for x in got_bits[bad][:5]]} ref {[hex(x) for x in ref_bits[bad][:5]]}")
+    return {"size": int(got_bits.size), "beyond_1ulp": beyond, "second_clause": second, "max_ulp": int(d.max())}
 
 
 LIPSCHITZ = {"none": 1.0, "relu": 1.0, "gelu": 1.13, "gelu_tanh": 1.13}
@@ -127,19 +138,22 @@ def check_f32_epilogue(got: np.ndarray, E: np.ndarray, pre: np.ndarray, K: int, 
 
 
 def check_bf16_bound(got_bits: np.ndarray, ref_bits: np.ndarray, bound_fn, what: str = "",
-                     max_ulp: int = 1) -> None:
+                     max_ulp: int = 1) -> dict:
     """As check_bf16, the second clause given as ``bound_fn(flat) -> (E,
     bound)``: an element is also accepted if |C - E| <= ulp_bf16(E) + bound."""
     got_bits = np.asarray(got_bits, dtype=np.uint16)
     ref_bits = np.asarray(ref_bits, dtype=np.uint16)
     assert got_bits.shape == ref_bits.shape
     if got_bits.size == 0:
-        return
-    bad = bf16_ulp_distance(got_bits, ref_bits) > max_ulp
+        return {"size": 0, "beyond_1ulp": 0, "second_clause": 0, "max_ulp": 0}
+    d = bf16_ulp_distance(got_bits, ref_bits)
+    bad = d > max_ulp
     nan_got = (got_bits & 0x7FFF) > 0x7F80
     nan_ref = (ref_bits & 0x7FFF) > 0x7F80
     bad |= nan_got != nan_ref
     bad &= ~(nan_got & nan_ref)
+    beyond = int(bad.sum())
+    second = 0
     if bad.any():
         flat = np.flatnonzero(bad)
         if flat.size <= int(0.005 * got_bits.size) + 2:
@@ -147,11 +161,15 @@ def check_bf16_bound(got_bits: np.ndarray, ref_bits: np.ndarray, bound_fn, what:
             got = bf16_to_f64(got_bits.reshape(-1)[flat])
             ok = np.abs(got - E) <= bf16_ulp(E) + bound
             bad.reshape(-1)[flat[ok]] = False
+            second = int(ok.sum())
     if bad.any():
         idx = np.argwhere(bad)[:5]
         raise AssertionError(f"{what}: {int(bad.sum())} of {got_bits.size} bf16 outputs more than "
                              f"{max_ulp} ulp away; first {idx.tolist()} got "
                              f"{[hex(x) for x in got_bits[bad][:5]]} ref {[hex(x) for x in ref_bits[bad][:5]]}")
+    fin = ~(nan_got | nan_ref)
+    return {"size": int(got_bits.size), "beyond_1ulp": beyond, "second_clause": second,
+            "max_ulp": int(d[fin].max()) if fin.any() else 0}
 
 
 def check_exact(got: np.ndarray, ref: np.ndarray, what: str = "") -> None:

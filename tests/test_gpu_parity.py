@@ -82,22 +82,25 @@ def test_padded_leading_dimensions(oracle_lib, variant):
     H.compare_full(oracle_lib, case, g.result_np(), what="padded ld")
 
 
+# Largest share of a full-size workload's bf16 elements allowed to need the
+# derived second clause (more than one ulp from the oracle's rounding, within
+# the fp32 accumulation bound).  For N(0,1) inputs such elements are those
+# whose exact value is near zero, where cancellation leaves fp32 accumulation
+# error comparable to a bf16 ulp of the result.
+SECOND_CLAUSE_SHARE = 1e-4
+
+
 @pytest.mark.parametrize("name", ["s4k", "s8k", "edge", "skinny"])
-def test_configs_sampled(oracle_lib, name):
+def test_configs_full(oracle_lib, name):
     """The full-size workloads in the launch configuration the benchmark times
-    (automatic variant), checked at 2 random points in every 128 x 128 cell of
-    C plus the corners, and at every position of a few whole rows/columns."""
+    (automatic variant), compared with the oracle at every element of C."""
     case = gi.config_case(name)
     g = H.run_case(case, 0)
     got = g.result_np()
-    rows, cols = gi.cell_sample_indices(case.M, case.N, 128, 128, 2, seed=11)
-    H.compare_sampled(oracle_lib, case, got, rows, cols, what=name)
-    for j in [0, case.N // 2 + 3, case.N - 1]:
-        r = np.arange(case.M, dtype=np.int64)
-        H.compare_sampled(oracle_lib, case, got, r, np.full_like(r, j), what=f"{name} col {j}")
-    for i in [0, case.M - 1]:
-        c = np.arange(case.N, dtype=np.int64)
-        H.compare_sampled(oracle_lib, case, got, np.full_like(c, i), c, what=f"{name} row {i}")
+    stats = H.compare_full(oracle_lib, case, got, what=name)
+    H.record_stats(f"full {name}", stats)
+    if case.out_dtype == gi.OUT_BF16:
+        assert stats["second_clause"] <= SECOND_CLAUSE_SHARE * stats["size"] + 2, stats
     assert not np.isnan(got.astype(np.float32) if got.dtype != np.uint16 else
                         ((got & 0x7FFF) > 0x7F80)).any()
 
