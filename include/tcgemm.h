@@ -83,7 +83,14 @@ typedef enum {
                                       through distributed shared memory (a sum of two terms: the
                                       same bits whichever CTA adds), so no workspace and no
                                       second kernel: the choice for M <= 128 when the tiles fill
-                                      3/4 to 1 round of 2-CTA clusters */
+                                      3/4 to 1 round of 2-CTA clusters */,
+    TCGEMM_VARIANT_SWAP_PAIR = 8 /* the transposed product on CTA pairs (M <= 128): one
+                                   cta_group::2 MMA per k-block over a tile of 2*r columns of C
+                                   (r per CTA, r a multiple of 8 chosen so that the tiles give
+                                   every SM of the device one) by all M rows; each CTA streams its
+                                   r columns of B over the whole of K and half of A's rows, so
+                                   there is no K split and no exchange; bf16 operands in the
+                                   layouts of gemm_bf16, fp32 or bf16 output */
 } tcgemm_variant_t;
 
 /* C = alpha*A*B + beta*C as described above.  Returns TCGEMM_OK once the work
@@ -384,6 +391,12 @@ int64_t tcgemm_autotune_load(const char* path);
 /* Size in bytes of gemm_bf16_noalloc's fixed scratch array.  Host only. */
 int64_t tcgemm_noalloc_scratch_bytes(void);
 
+/* 1 if gemm_bf16_noalloc's scratch array holds what the plan of this problem
+ * needs on a device with `num_sms` SMs (the test that entry point applies
+ * before launching; plans without a split need none), 0 if the call would be
+ * refused, -1 on bad arguments.  Host only; needs no GPU. */
+int tcgemm_noalloc_fits(int64_t M, int64_t N, int64_t K, int variant, int num_sms);
+
 /* Workspace bytes the launch for this shape and variant needs on a device
  * with `num_sms` SMs (0: none).  Host only. */
 int64_t tcgemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int variant, int num_sms);
@@ -401,12 +414,16 @@ int tcgemm_pick_variant(int64_t M, int64_t N, int64_t K, int num_sms);
  * workspace bytes, out[12] = tile
  * band height of the visiting order, out[13] = variant, out[14] = CTAs per
  * MMA (cta_group), out[15], out[16] = rows and columns of the unit grid the
- * visiting order walks (tiles, or 2 x 2 tile blocks for variant 3), out[17] =
- * 1 when stream-K is used, out[18] = rows of A loaded per CTA (64 for M <= 64
- * with variant 4, else 128), out[19] = 1 when the launch computes the
- * transposed product (variants 6 and 7; then out[2..] describe C^T),
+ * visiting order walks (the tile grid), out[17] =
+ * 1 when stream-K is used, out[18] = rows of the MMA's A operand loaded per
+ * CTA (64 for M <= 64 with variant 4, the chosen r for variant 8, else 128),
+ * out[19] = 1 when the launch computes the transposed product (variants 6, 7
+ * and 8; then out[2..] describe C^T),
  * out[20] = CTAs of a cluster that split each tile's k-blocks (2 for
- * variant 7, else 1).  `out` must hold 21 values.  Returns TCGEMM_OK or TCGEMM_ERR_INVALID_ARG.  Needs no
+ * variant 7, else 1), out[21] = the visiting order: 0 for the grouped band
+ * order, k > 0 for the Hilbert curve over the enclosing 2^k x 2^k square
+ * (environment TCGEMM_ORDER=grouped or =hilbert overrides the default).
+ * `out` must hold 22 values.  Returns TCGEMM_OK or TCGEMM_ERR_INVALID_ARG.  Needs no
  * GPU. */
 int tcgemm_plan(int64_t M, int64_t N, int64_t K, int variant, int num_sms, int64_t* out);
 
@@ -429,10 +446,20 @@ int tcgemm_device_info(int64_t* out);
 int tcgemm_units(int64_t M, int64_t N, int64_t K, int variant, int num_sms, int cluster, int max_units,
                  int32_t* out);
 
-/* Tile visiting order used by the persistent kernels (host copy of the device
- * function): writes the tile row and column of order index t = 0..count-1
- * into tm[t], tn[t].  Needs no GPU. */
+/* Grouped band order of the persistent kernels (host copy of the device
+ * function; the work log's "调度与 L2 缓存"): writes the tile row and column
+ * of order index t = 0..count-1 into tm[t], tn[t]; consecutive indices run
+ * down a band of group_m tile rows, then one tile column right.  Needs no
+ * GPU. */
 int tcgemm_tile_order(int tiles_m, int tiles_n, int group_m, int64_t count, int32_t* tm, int32_t* tn);
+
+/* The Hilbert order of the work log's "内核 11：希尔伯特曲线" (host copy of the
+ * device function): the tiles_m x tiles_n tiles in the order the Hilbert
+ * curve over the enclosing 2^k x 2^k square visits them, cells outside the
+ * grid skipped; tile row and column of order index t = 0..count-1 into
+ * tm[t], tn[t] (count <= tiles_m * tiles_n).  Returns TCGEMM_OK or
+ * TCGEMM_ERR_INVALID_ARG.  Needs no GPU. */
+int tcgemm_tile_order_hilbert(int tiles_m, int tiles_n, int64_t count, int32_t* tm, int32_t* tn);
 
 /* Human-readable name of a status code (static string). */
 const char* tcgemm_status_string(int status);

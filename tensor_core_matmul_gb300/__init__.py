@@ -14,8 +14,8 @@ work; ``binding`` only marshals arguments.  Build with ``_build.build()``.
 """
 from .binding import (OUT_BF16, autotune, autotune_clear, autotune_lookup, OUT_F32, VARIANT_1CTA, VARIANT_1CTA_N64, VARIANT_2CTA, VARIANT_AUTO, TcgemmError,
                       check_device_status, gemm_bf16, gemm_bf16_bias_act, gemm_bf16_host, gemm_bf16_layout, gemm_bf16_raw, gemm_fp8, gemm_quant_i8, gemm_bf16_ws_raw, launch_count, lib, pick_variant,
-                      plan, selftest_timeout, tile_order, version, workspace_bytes)
+                      plan, selftest_timeout, tile_order, tile_order_hilbert, version, workspace_bytes)
 
 __all__ = ["OUT_BF16", "autotune", "autotune_clear", "autotune_lookup", "OUT_F32", "VARIANT_1CTA", "VARIANT_1CTA_N64", "VARIANT_2CTA", "VARIANT_AUTO", "TcgemmError",
            "check_device_status", "gemm_bf16", "gemm_bf16_bias_act", "gemm_bf16_host", "gemm_bf16_layout", "gemm_bf16_raw", "gemm_fp8", "gemm_quant_i8", "gemm_bf16_ws_raw", "launch_count", "lib", "pick_variant",
-           "plan", "selftest_timeout", "tile_order", "version", "workspace_bytes"]
+           "plan", "selftest_timeout", "tile_order", "tile_order_hilbert", "version", "workspace_bytes"]

@@ -96,6 +96,8 @@ def lib() -> ctypes.CDLL:
     L.gemm_bf16_host.restype = i32
     L.tcgemm_noalloc_scratch_bytes.argtypes = []
     L.tcgemm_noalloc_scratch_bytes.restype = i64
+    L.tcgemm_noalloc_fits.argtypes = [i64, i64, i64, i32, i32]
+    L.tcgemm_noalloc_fits.restype = i32
     L.tcgemm_workspace_bytes.argtypes = [i64, i64, i64, i32, i32]
     L.tcgemm_workspace_bytes.restype = i64
     L.tcgemm_pick_variant.argtypes = [i64, i64, i64, i32]
@@ -111,6 +113,9 @@ def lib() -> ctypes.CDLL:
     L.tcgemm_tile_order.argtypes = [i32, i32, i32, i64, ctypes.POINTER(ctypes.c_int32),
                                     ctypes.POINTER(ctypes.c_int32)]
     L.tcgemm_tile_order.restype = i32
+    L.tcgemm_tile_order_hilbert.argtypes = [i32, i32, i64, ctypes.POINTER(ctypes.c_int32),
+                                            ctypes.POINTER(ctypes.c_int32)]
+    L.tcgemm_tile_order_hilbert.restype = i32
     L.tcgemm_status_string.argtypes = [i32]
     L.tcgemm_status_string.restype = ctypes.c_char_p
     L.tcgemm_last_error.argtypes = []
@@ -470,7 +475,7 @@ def pick_variant(M: int, N: int, K: int, num_sms: int) -> int:
 
 PLAN_KEYS = ["grid", "cluster", "tiles_m", "tiles_n", "bm", "bn", "num_kb", "smem", "tiles_dp",
              "sk_tiles", "sk_iters", "ws_bytes", "group_m", "variant", "cta_group", "grid_m", "grid_n",
-             "stream_k", "arows", "swap", "ks"]
+             "stream_k", "arows", "swap", "ks", "hilbert"]
 
 
 def plan(M: int, N: int, K: int, variant: int = 0, num_sms: int = 152, in_kind: int = 0, a_col: bool = False,
@@ -511,6 +516,15 @@ def noalloc_scratch_bytes() -> int:
     return int(lib().tcgemm_noalloc_scratch_bytes())
 
 
+def noalloc_fits(M: int, N: int, K: int, variant: int = 0, num_sms: int = 152) -> bool:
+    """Whether gemm_bf16_noalloc's fixed scratch holds this problem's plan
+    on a device with num_sms SMs (host only)."""
+    r = int(lib().tcgemm_noalloc_fits(M, N, K, variant, num_sms))
+    if r < 0:
+        raise TcgemmError(1, "bad arguments")
+    return r == 1
+
+
 def workspace_bytes(M: int, N: int, K: int, variant: int = 0, num_sms: int = 152) -> int:
     return int(lib().tcgemm_workspace_bytes(M, N, K, variant, num_sms))
 
@@ -543,6 +557,15 @@ def tile_order(tiles_m: int, tiles_n: int, group_m: int, count: Optional[int] = 
     tn = (ctypes.c_int32 * count)()
     _check(lib().tcgemm_tile_order(tiles_m, tiles_n, group_m, count, tm, tn))
     return list(tm), list(tn)
+
+
+def tile_order_hilbert(tiles_m: int, tiles_n: int, count: Optional[int] = None):
+    """The Hilbert visiting order (tcgemm_tile_order_hilbert): tile rows and columns."""
+    count = tiles_m * tiles_n if count is None else count
+    tm = (ctypes.c_int32 * max(count, 1))()
+    tn = (ctypes.c_int32 * max(count, 1))()
+    _check(lib().tcgemm_tile_order_hilbert(tiles_m, tiles_n, count, tm, tn))
+    return list(tm)[:count], list(tn)[:count]
 
 
 def version() -> int:

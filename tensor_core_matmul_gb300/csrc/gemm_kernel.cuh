@@ -118,9 +118,64 @@ __host__ __device__ __forceinline__ void grouped_tile(int t, int tiles_m, int ti
     tn = r / rows;
 }
 
+// Cell d of the Hilbert curve over a 2^order x 2^order grid (the iterative
+// form that consumes d two bits at a time, lowest first, reflecting and
+// transposing the partial coordinates at each level).  The curve starts at
+// (0, 0) and ends at (2^order - 1, 0).
+__host__ __device__ __forceinline__ void hilbert_d2xy(int order, int d, int& x, int& y) {
+    x = 0;
+    y = 0;
+    for (int s = 1; s < (1 << order); s <<= 1) {
+        const int rx = 1 & (d >> 1);
+        const int ry = 1 & (d ^ rx);
+        if (ry == 0) {
+            if (rx == 1) {
+                x = s - 1 - x;
+                y = s - 1 - y;
+            }
+            const int t = x;
+            x = y;
+            y = t;
+        }
+        x += s * rx;
+        y += s * ry;
+        d >>= 2;
+    }
+}
+
+// Tile order of the H100 work log's "内核 11：希尔伯特曲线": the tiles of the
+// tiles_m x tiles_n grid in the order in which the Hilbert curve of the
+// enclosing 2^order square visits them, cells outside the grid skipped.  The
+// t-th tile is found from the top down: the curve covers the aligned
+// quarter-squares in the order the coarser curve visits its cells, so at
+// each level the child that holds the t-th tile is the first whose running
+// count of in-grid cells exceeds t.  Consecutive indices are neighbouring
+// tiles, so the tiles the persistent CTAs work on at once form a compact
+// patch (rows of A and columns of B shared in L2), and the next round's
+// patch borders it.
+__host__ __device__ __forceinline__ void hilbert_tile(int t, int tiles_m, int tiles_n, int order, int& tm, int& tn) {
+    int q = 0;
+    for (int j = order - 1; j >= 0; --j) {
+        const int side = 1 << j;
+        for (int c = 0; c < 4; ++c) {
+            int x, y;
+            hilbert_d2xy(order - j, 4 * q + c, x, y);
+            const int w = min(max(tiles_m - (x << j), 0), side);
+            const int h = min(max(tiles_n - (y << j), 0), side);
+            if (t < w * h || c == 3) {
+                q = 4 * q + c;
+                break;
+            }
+            t -= w * h;
+        }
+    }
+    hilbert_d2xy(order, q, tm, tn);
+}
+
 struct GemmParams {
     int M, N, K;
     int tiles_m, tiles_n, num_kb, group_m;
+    int hilbert;         // 0: grouped band order; else the Hilbert order over a 2^hilbert square
     int grid_m, grid_n;  // grid of tiles the unit order walks
     int tiles_dp;        // tiles computed whole, round-robin over the clusters
     int sk_tiles;        // trailing tiles whose k-blocks are shared out by stream-K (0: none)
@@ -137,8 +192,21 @@ struct GemmParams {
     // int8 output: code = saturate(rne(fmaf(value, qscale[row of C], qzero))).
     const float* qscale;
     float qzero;
+    // Transposed product on CTA pairs: rows of the MMA's A operand (columns
+    // of C) loaded per CTA, a multiple of 8 up to the stage's capacity; a
+    // pair's tile is 2 * rows_a rows of D.  Unused by the other kernels.
+    int rows_a;
     uint64_t timeout_ns;
 };
+
+// The tile of unit index t under the launch's visiting order.
+__host__ __device__ __forceinline__ void unit_tile_of(const GemmParams& p, int t, int& tm, int& tn) {
+    if (p.hilbert > 0) {
+        hilbert_tile(t, p.grid_m, p.grid_n, p.hilbert, tm, tn);
+    } else {
+        grouped_tile(t, p.grid_m, p.grid_n, p.group_m, tm, tn);
+    }
+}
 
 // ------------------------------------------------------ fused epilogue --
 // The "DeepGEMM" article (section 6.1) fuses the bias add and the ReLU/GELU
@@ -349,7 +417,7 @@ struct GemmCfg {
     // Workspace bytes per split piece (both CTAs of a pair).
     static constexpr uint64_t kSlotBytes = static_cast<uint64_t>(CTA_GROUP) * 128 * BN * 4;
     static_assert(kTmemCols <= 512, "TMEM has 512 columns");
-    static_assert(AROWS == 128 || (AROWS == 64 && CTA_GROUP == 1), "half-height A tiles are single-CTA only");
+    static_assert(AROWS == 128 || AROWS == 64, "A stages hold 128 or 64 rows");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "epilogue works in 32-column chunks");
     static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
 };
@@ -565,10 +633,20 @@ __global__ void __launch_bounds__(192, 1)
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
                         const GemmParams p) {
     using Cfg = GemmCfg<CTA_GROUP, BN, STAGES, AROWS, IN, KS>;
-    static_assert(!SWAP || CTA_GROUP == 1, "the swapped product runs on single-CTA tiles");
+    static_assert(!SWAP || CTA_GROUP == 1 || (KS == 1 && AROWS == 64), "pairs run the swapped product with "
+                  "64-row A stages and no K split");
+    static_assert(AROWS == 128 || SWAP || CTA_GROUP == 1, "half-height A tiles: single CTAs or the swapped pairs");
     static_assert(KS == 1 || (KS == 2 && SWAP && BN % 64 == 0 && Cfg::kEpiBytes >= 128u * (BN / 2) * 4u),
                   "the K split exchanges half an fp32 tile through the staging area");
     constexpr int kCluster = CTA_GROUP * KS;
+    // Transposed product on a CTA pair: each CTA loads rows_a (<= 64) rows of
+    // the MMA's A operand into a 64-row stage; the pair's M = 256 MMA reads
+    // 128 rows per CTA, the rows past rows_a (stale rows, or the next stage)
+    // give accumulator rows that are never stored.  A pair tile is 2*rows_a
+    // rows of D, so the tiles can be sized to give every SM one.
+    constexpr bool kPairSwap = SWAP && CTA_GROUP == 2;
+    const int rows_a = kPairSwap ? p.rows_a : Cfg::kRowsA;
+    const int tile_m = kPairSwap ? 2 * p.rows_a : Cfg::kBM;
     extern __shared__ uint8_t smem_raw[];
 
     // 1 KB-aligned carve-up: [A stages][B stages][barriers][tmem slot][abort][last flag]
@@ -605,9 +683,7 @@ __global__ void __launch_bounds__(192, 1)
     };
     const int cluster_id = blockIdx.x / kCluster;
     const int num_clusters = gridDim.x / kCluster;
-    auto tile_of = [&](int unit_tile, int& tm, int& tn) {
-        grouped_tile(unit_tile, p.grid_m, p.grid_n, p.group_m, tm, tn);
-    };
+    auto tile_of = [&](int unit_tile, int& tm, int& tn) { unit_tile_of(p, unit_tile, tm, tn); };
 
     // Single-CTA MMAs: the producer needs nothing but its own barriers, so it
     // starts loading as soon as they are initialised, while the TMEM
@@ -674,10 +750,11 @@ __global__ void __launch_bounds__(192, 1)
                 ks_range(u);
                 int tm, tn;
                 tile_of(u.tile, tm, tn);
-                const int a_row = tm * Cfg::kBM + static_cast<int>(rank) * Cfg::kRowsA;
+                const int a_row = tm * tile_m + static_cast<int>(rank) * rows_a;
                 const int b_row = tn * BN + static_cast<int>(rank) * Cfg::kRowsB;
                 const CUtensorMap* mB = &tmB;
-                const uint32_t stage_tx = Cfg::kStageTx;
+                const uint32_t stage_tx = kPairSwap ? CTA_GROUP * (static_cast<uint32_t>(rows_a) * 128u + Cfg::kBBytes)
+                                                    : Cfg::kStageTx;
                 // One operand tile: K-major, one box of 64 K values by `rows`
                 // rows; MN-major, boxes of 64 MN values by 64 K rows, 8 KB
                 // apart.  Same bytes either way.
@@ -850,7 +927,7 @@ __global__ void __launch_bounds__(192, 1)
         while (!aborted && it.next(p, u)) {
             int tm, tn;
             tile_of(u.tile, tm, tn);
-            const int row_blk = tm * Cfg::kBM + static_cast<int>(rank) * 128;  // this CTA's 128 rows
+            const int row_blk = tm * tile_m + static_cast<int>(rank) * (kPairSwap ? rows_a : 128);  // this CTA's rows
             const int64_t colt = static_cast<int64_t>(tn) * BN;  // first column of the tile
             const int ncols = BN;
             // beta*C: start pulling the C tile into L2 now; the tile's mainloop
@@ -860,7 +937,7 @@ __global__ void __launch_bounds__(192, 1)
                     tma_prefetch_l2_2d(&tmC, row_blk, static_cast<int32_t>(colt + c));
             }
             const int64_t row = static_cast<int64_t>(row_blk) + row_local;
-            const bool row_ok = row < p.M;
+            const bool row_ok = row < p.M && (!kPairSwap || static_cast<int>(row_local) < rows_a);
             // Fused epilogue: fetch the tile's bias now, while the mainloop
             // runs.  Plain product: the tile's BN column values go to shared
             // memory (every reader of the previous tile's values has passed a
@@ -973,7 +1050,13 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty_bar(acc));
+                if (lane == 0) {
+                    if constexpr (CTA_GROUP == 1) {
+                        mbar_arrive(tempty_bar(acc));
+                    } else {
+                        mbar_arrive_cluster(map_to_cta(tempty_bar(acc), 0));
+                    }
+                }
             } else if (u.slot < 0 && !tma_rows) {
 #pragma unroll 1
                 for (int c = 0; c < ncols; c += 32) {
@@ -1192,7 +1275,7 @@ __global__ void __launch_bounds__(128)
     if (t >= p.sk_tiles) return;
     const int row_local = threadIdx.x;
     int tm, tn;
-    grouped_tile(p.tiles_dp + t, p.grid_m, p.grid_n, p.group_m, tm, tn);
+    unit_tile_of(p, p.tiles_dp + t, tm, tn);
     const int64_t row = static_cast<int64_t>(tm) * (128 * CTA_GROUP) + rank * 128 + row_local;
     const int64_t col0 = static_cast<int64_t>(tn) * BN + kSkReduceCols * c;
     // The bias is an input, not written by the GEMM: fetch it before waiting.

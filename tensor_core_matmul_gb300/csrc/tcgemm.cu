@@ -139,6 +139,7 @@ struct Plan {
     uint64_t slot_bytes = 0;  // workspace bytes per stream-K partial piece
     uint64_t ws_bytes = 0;    // workspace this plan needs (0 without stream-K)
     int ks = 1;               // CTAs of a cluster that split each tile's k-blocks (2: variant 7)
+    int hilbert = 0;          // visiting order: 0 grouped bands, k > 0 the Hilbert curve of a 2^k square
     void* ws_ptr = nullptr;   // the workspace of this launch
 };
 
@@ -161,11 +162,33 @@ using CfgN64h = tcg::GemmCfg<1, 64, kStagesN64h, 64>;
 constexpr int kStagesS128 = 6;
 using CfgS128 = tcg::GemmCfg<1, 128, kStagesS128, 128, 0, 2>;
 static_assert(CfgS128::kSmemBytes <= 227 * 1024, "shared memory");
+// The transposed product on CTA pairs: 64-row A stages (8 KB) and half of the
+// B tile per CTA: 16 x (8 + 4) KB for up to 64 rows of C, 12 x (8 + 8) KB up
+// to 128.
+constexpr int kStagesSP = 16;
+constexpr int kStagesSP128 = 12;
+using CfgSP = tcg::GemmCfg<2, 64, kStagesSP, 64>;
+using CfgSP128 = tcg::GemmCfg<2, 128, kStagesSP128, 64>;
+static_assert(CfgSP::kSmemBytes <= 227 * 1024 && CfgSP128::kSmemBytes <= 227 * 1024, "shared memory");
 
 // Variant numbers that name a kernel (3 is unused).
-bool variant_known(int v) { return v >= TCGEMM_VARIANT_AUTO && v <= TCGEMM_VARIANT_SWAP_N64_KS2 && v != 3; }
+bool variant_known(int v) { return v >= TCGEMM_VARIANT_AUTO && v <= TCGEMM_VARIANT_SWAP_PAIR && v != 3; }
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+
+// Visiting order of the tiles: TCGEMM_ORDER=grouped or =hilbert in the
+// environment chooses one for every launch (for A/B measurements); unset,
+// the default order below is used.
+int order_override() {
+    static const int v = [] {
+        const char* s = std::getenv("TCGEMM_ORDER");
+        if (s && std::strcmp(s, "hilbert") == 0) return 1;
+        if (s && std::strcmp(s, "grouped") == 0) return 0;
+        return -1;
+    }();
+    return v;
+}
+constexpr bool kHilbertDefault = false;
 
 // TCGEMM_SPLIT=0 in the environment turns the tail split off (for A/B timing).
 bool split_enabled() {
@@ -246,7 +269,8 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pa
     if (variant == TCGEMM_VARIANT_AUTO) variant = pick_variant(M, N, K, sms, in_kind);
     pl.variant = variant;
     allow_split = allow_split && split_enabled();
-    if (variant == TCGEMM_VARIANT_SWAP_N64 || variant == TCGEMM_VARIANT_SWAP_N64_KS2) {
+    if (variant == TCGEMM_VARIANT_SWAP_N64 || variant == TCGEMM_VARIANT_SWAP_N64_KS2 ||
+        variant == TCGEMM_VARIANT_SWAP_PAIR) {
         // The transposed product: its M is N, its N is M.
         pl.swap = 1;
         std::swap(M, N);
@@ -292,6 +316,19 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pa
             pl.bn = 128;
             pl.smem = CfgS128::kSmemBytes;
         }
+    } else if (variant == TCGEMM_VARIANT_SWAP_PAIR) {
+        // Here M is C's N and N is C's M (at most 128 rows of C).
+        if (N > 128 || a_col || b_row || in_kind != 0) return false;
+        pl.cta_group = 2;
+        pl.bn = N <= 64 ? 64 : 128;
+        // r rows per CTA: the smallest multiple of 8 that covers M with one
+        // tile of 2r rows per resident pair, at most the 64-row stage.
+        const int64_t pairs = std::max(1, max_pairs > 0 ? max_pairs : sms / 2);
+        const int64_t r = std::min<int64_t>(64, std::max<int64_t>(8, (ceil_div(M, 2 * pairs) + 7) / 8 * 8));
+        pl.arows = static_cast<int>(r);
+        pl.bm = static_cast<int>(2 * r);
+        pl.smem = pl.bn == 64 ? CfgSP::kSmemBytes : CfgSP128::kSmemBytes;
+        allow_split = false;
     } else {
         return false;
     }
@@ -333,6 +370,12 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pa
     int g = 1;
     while (g * 2 <= ideal) g *= 2;
     pl.group_m = std::max(1, std::min(g, pl.grid_m));
+    const int ov = order_override();
+    if (ov == 1 || (ov < 0 && kHilbertDefault)) {
+        int k = 0;
+        while ((1 << k) < std::max(pl.grid_m, pl.grid_n)) ++k;
+        pl.hilbert = k;  // 0 for a single tile: the two orders agree
+    }
     return true;
 }
 
@@ -632,6 +675,9 @@ int internal_workspace(int dev, int sms, cudaStream_t stream, uint64_t need, voi
 constexpr uint64_t kNoAllocScratchBytes = uint64_t{40} << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
+// The fixed array holds a plan's workspace.
+bool noalloc_fits(uint64_t ws_bytes) { return ws_bytes <= kNoAllocScratchBytes; }
+
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kMaxDevices] = {};
 
@@ -672,6 +718,7 @@ void fill_plan_out(const Plan& pl, int64_t* out) {
     out[18] = pl.arows;
     out[19] = pl.swap;
     out[20] = pl.ks;
+    out[21] = pl.hilbert;
 }
 
 constexpr int kWsInternal = 0;
@@ -768,7 +815,7 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
             set_error("unknown FP8 format %d", in_fmt);
             return TCGEMM_ERR_INVALID_ARG;
         }
-        if (variant == TCGEMM_VARIANT_1CTA) {
+        if (variant == TCGEMM_VARIANT_1CTA || variant == TCGEMM_VARIANT_SWAP_PAIR) {
             set_error("variant %d is not built for FP8 operands", variant);
             return TCGEMM_ERR_INVALID_ARG;
         }
@@ -778,7 +825,7 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
             set_error("int8 output is written only: beta must be 0");
             return TCGEMM_ERR_INVALID_ARG;
         }
-        if (variant == TCGEMM_VARIANT_1CTA) {
+        if (variant == TCGEMM_VARIANT_1CTA || variant == TCGEMM_VARIANT_SWAP_PAIR) {
             set_error("variant %d is not built for int8 output", variant);
             return TCGEMM_ERR_INVALID_ARG;
         }
@@ -852,7 +899,7 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
             }
             wsp = ws;
         } else if (ws_mode == kWsNoAlloc) {
-            if (pl.ws_bytes > kNoAllocScratchBytes) {
+            if (!noalloc_fits(pl.ws_bytes)) {
                 set_error("this shape needs %llu bytes of scratch, more than the fixed %llu of gemm_bf16_noalloc",
                           static_cast<unsigned long long>(pl.ws_bytes),
                           static_cast<unsigned long long>(kNoAllocScratchBytes));
@@ -868,7 +915,8 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
         }
     }
     // Box heights: a CTA pair loads half of the B tile per CTA.
-    const uint32_t a_box_rows = pl.arows == 64 ? 64u : 128u;
+    const uint32_t a_box_rows = (pl.arows == 64 || (pl.swap && pl.cta_group == 2)) ? static_cast<uint32_t>(pl.arows)
+                                                                                    : 128u;
     const uint32_t b_box_rows = static_cast<uint32_t>(pl.bn / pl.cta_group);
     // The transposed product multiplies B^T (N x K, rows of B contiguous in
     // k) by A^T: the operands trade places.
@@ -906,6 +954,7 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     gp.tiles_n = pl.tiles_n;
     gp.num_kb = pl.num_kb;
     gp.group_m = pl.group_m;
+    gp.hilbert = pl.hilbert;
     gp.grid_m = pl.grid_m;
     gp.grid_n = pl.grid_n;
     gp.ldc = ldc;
@@ -923,6 +972,7 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     gp.tiles_dp = pl.tiles_dp;
     gp.sk_tiles = pl.sk_tiles;
     gp.sk_iters = pl.sk_iters;
+    gp.rows_a = pl.arows;
     gp.timeout_ns = timeout_ns();
 
     const bool bf16 = out_dtype == TCGEMM_OUT_BF16;
@@ -971,6 +1021,8 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
 #define TCGEMM_LAUNCH(CG, BN, ST, AR, SW)                                                               \
     return bf16 ? launch_gemm<CG, BN, ST, AR, SW, __nv_bfloat16>(pl, ta, tb, tcm, twm, gp, stream, dev) \
                 : launch_gemm<CG, BN, ST, AR, SW, float>(pl, ta, tb, tcm, twm, gp, stream, dev)
+    if (pl.swap && pl.cta_group == 2 && pl.bn == 128) TCGEMM_LAUNCH(2, 128, kStagesSP128, 64, true);
+    if (pl.swap && pl.cta_group == 2) TCGEMM_LAUNCH(2, 64, kStagesSP, 64, true);
     if (pl.swap && pl.ks == 2 && pl.bn == 128)
         return bf16 ? launch_gemm<1, 128, kStagesS128, 128, true, __nv_bfloat16, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
                     : launch_gemm<1, 128, kStagesS128, 128, true, float, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
@@ -1099,8 +1151,9 @@ int tcgemm_autotune(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
             return TCGEMM_ERR_CUDA;
         }
     }
-    const int candidates[] = {TCGEMM_VARIANT_2CTA,      TCGEMM_VARIANT_2CTA_W256, TCGEMM_VARIANT_1CTA,
-                              TCGEMM_VARIANT_1CTA_N64,  TCGEMM_VARIANT_SWAP_N64,  TCGEMM_VARIANT_SWAP_N64_KS2};
+    const int candidates[] = {TCGEMM_VARIANT_2CTA,      TCGEMM_VARIANT_2CTA_W256,    TCGEMM_VARIANT_1CTA,
+                              TCGEMM_VARIANT_1CTA_N64,  TCGEMM_VARIANT_SWAP_N64,     TCGEMM_VARIANT_SWAP_N64_KS2,
+                              TCGEMM_VARIANT_SWAP_PAIR};
     int best = TCGEMM_VARIANT_AUTO;
     float best_t = 0.0f;
     rc = TCGEMM_OK;
@@ -1175,6 +1228,13 @@ void tcgemm_autotune_clear(void) {
 }
 
 int64_t tcgemm_noalloc_scratch_bytes(void) { return static_cast<int64_t>(kNoAllocScratchBytes); }
+
+int tcgemm_noalloc_fits(int64_t M, int64_t N, int64_t K, int variant, int num_sms) {
+    if (M <= 0 || N <= 0 || K <= 0 || num_sms <= 0 || !variant_known(variant)) return -1;
+    Plan pl;
+    if (!make_plan(M, N, K, variant, num_sms, num_sms / 2, pl)) return -1;
+    return noalloc_fits(pl.ws_bytes) ? 1 : 0;
+}
 
 int64_t tcgemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int variant, int num_sms) {
     if (M <= 0 || N <= 0 || K <= 0 || num_sms <= 0) return 0;
@@ -1260,6 +1320,21 @@ int tcgemm_units(int64_t M, int64_t N, int64_t K, int variant, int num_sms, int 
         ++n;
     }
     return n;
+}
+
+int tcgemm_tile_order_hilbert(int tiles_m, int tiles_n, int64_t count, int32_t* tm, int32_t* tn) {
+    if (tiles_m <= 0 || tiles_n <= 0 || count < 0 || count > static_cast<int64_t>(tiles_m) * tiles_n ||
+        tm == nullptr || tn == nullptr)
+        return TCGEMM_ERR_INVALID_ARG;
+    int k = 0;
+    while ((1 << k) < std::max(tiles_m, tiles_n)) ++k;
+    for (int64_t t = 0; t < count; ++t) {
+        int a, b;
+        tcg::hilbert_tile(static_cast<int>(t), tiles_m, tiles_n, k, a, b);
+        tm[t] = a;
+        tn[t] = b;
+    }
+    return TCGEMM_OK;
 }
 
 int tcgemm_tile_order(int tiles_m, int tiles_n, int group_m, int64_t count, int32_t* tm, int32_t* tn) {

@@ -33,6 +33,9 @@ bool tune_entry_valid(const TuneKey& k, int variant) {
     if ((k.a_col | k.b_row | k.has_beta) & ~1) return false;
     if (!variant_known(variant) || variant == TCGEMM_VARIANT_AUTO) return false;
     if (variant == TCGEMM_VARIANT_1CTA && (k.in_kind == 1 || k.out_dtype == TCGEMM_OUT_I8)) return false;
+    if (variant == TCGEMM_VARIANT_SWAP_PAIR &&
+        (k.in_kind == 1 || k.out_dtype == TCGEMM_OUT_I8 || k.a_col || k.b_row || k.M > 128))
+        return false;
     if ((k.a_col || k.b_row) && k.in_kind == 1) return false;
     if (k.out_dtype == TCGEMM_OUT_I8 && k.has_beta) return false;
     return true;

@@ -207,6 +207,56 @@ def test_tile_order_is_a_permutation(tc, tiles_m, tiles_n, group_m):
     assert all(0 <= a < tiles_m and 0 <= b < tiles_n for a, b in cells)
 
 
+def _hilbert_reference(k: int):
+    """Cells of the 2^k x 2^k Hilbert curve by the recursive construction
+    (each square split into four quarter-squares traversed with their axes
+    exchanged, unchanged, unchanged, and reversed-exchanged), an
+    independent restatement of the curve, started along the second axis."""
+    out = []
+
+    def rec(x0, y0, xi, xj, yi, yj, n):
+        if n == 0:
+            out.append((int(x0 + (xi + yi) / 2), int(y0 + (xj + yj) / 2)))
+            return
+        rec(x0, y0, yi / 2, yj / 2, xi / 2, xj / 2, n - 1)
+        rec(x0 + xi / 2, y0 + xj / 2, xi / 2, xj / 2, yi / 2, yj / 2, n - 1)
+        rec(x0 + xi / 2 + yi / 2, y0 + xj / 2 + yj / 2, xi / 2, xj / 2, yi / 2, yj / 2, n - 1)
+        rec(x0 + xi / 2 + yi, y0 + xj / 2 + yj, -yi / 2, -yj / 2, -xi / 2, -xj / 2, n - 1)
+
+    s = 2 ** k
+    rec(0.0, 0.0, 0.0, float(s), float(s), 0.0, k)
+    return out
+
+
+@pytest.mark.parametrize("tiles_m,tiles_n", [(1, 1), (2, 2), (4, 4), (32, 32), (16, 19), (16, 17), (19, 16),
+                                             (5, 3), (1, 32), (33, 2), (64, 64), (7, 100)])
+def test_hilbert_order_matches_recursive_curve(tc, tiles_m, tiles_n):
+    """The Hilbert visiting order (host copy of the device function) is the
+    recursive curve of the enclosing power-of-two square with the cells
+    outside the grid dropped: a permutation of the grid, and on full squares
+    every step moves to a neighbouring tile."""
+    tm, tn = tc.tile_order_hilbert(tiles_m, tiles_n)
+    k = max(0, (max(tiles_m, tiles_n) - 1).bit_length())
+    ref = [(x, y) for x, y in _hilbert_reference(k) if x < tiles_m and y < tiles_n]
+    assert list(zip(tm, tn)) == ref
+    assert len(set(ref)) == tiles_m * tiles_n
+    if tiles_m == tiles_n and tiles_m & (tiles_m - 1) == 0:
+        assert all(abs(a - c) + abs(b - d) == 1 for (a, b), (c, d) in zip(ref, ref[1:]))
+
+
+def test_hilbert_rounds_are_compact(tc):
+    """A round of 76 pair tiles on the 32 x 32 grid of 8192^3 covers a patch
+    no larger than the grouped order's, and consecutive rounds share edges."""
+    tm, tn = tc.tile_order_hilbert(32, 32)
+    for r in range(1024 // 76):
+        cells = list(zip(tm[76 * r:76 * (r + 1)], tn[76 * r:76 * (r + 1)]))
+        rows = len({a for a, _ in cells})
+        cols = len({b for _, b in cells})
+        assert rows * cols <= 2 * 76 + 64, (r, rows, cols)
+    with pytest.raises(tc.TcgemmError):
+        tc.tile_order_hilbert(4, 4, 17)
+
+
 def test_tile_order_groups_for_l2(tc):
     """The first `grid` tiles (one wave) stay inside a band of group_m tile rows."""
     tm, tn = tc.tile_order(32, 16, 16, 152)
@@ -330,6 +380,55 @@ def test_k_split_plan(tc):
     p = tc.plan(300, 200, 320, 7, 152)        # C^T is 200 x 300: 2 x 3 tiles of 128 x 128
     assert (p["ks"], p["bn"], p["tiles_m"], p["tiles_n"]) == (2, 128, 2, 3)
     assert tc.plan(64, 8192, 8192, 6, 152)["ks"] == 1
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 8192, 8192), (1, 1, 1), (128, 8192, 8192), (100, 20000, 640),
+                                   (40, 9000, 8200), (64, 16, 64)])
+@pytest.mark.parametrize("sms", [152, 148, 20])
+def test_swap_pair_plan(tc, M, N, K, sms):
+    """Variant 8: C^T on CTA pairs, r = rows of C^T per CTA (a multiple of 8,
+    at most 64) so that the 2r-row pair tiles cover C^T with about one tile
+    per resident pair; whole K per pair, no stream-K, no workspace."""
+    p = tc.plan(M, N, K, 8, sms)
+    r = p["arows"]
+    assert (p["swap"], p["cta_group"], p["cluster"], p["ks"], p["stream_k"], p["ws_bytes"]) == (1, 2, 2, 1, 0, 0)
+    assert r % 8 == 0 and 8 <= r <= 64 and p["bm"] == 2 * r
+    assert p["tiles_m"] == -(-N // (2 * r)) and p["tiles_n"] == 1 and p["bn"] == (64 if M <= 64 else 128)
+    pairs = sms // 2
+    if r < 64:
+        assert p["tiles_m"] <= pairs                      # one tile per pair at most
+        assert r == 8 or -(-N // (2 * (r - 8))) > pairs   # and r is the smallest that fits
+    assert p["grid"] == 2 * min(p["tiles_m"], pairs) and p["smem"] <= 227 * 1024
+    assert p["num_kb"] == -(-K // 64)
+
+
+def test_swap_pair_refusals(tc):
+    for kwargs in [dict(M=129, N=1000, K=64), dict(M=64, N=1000, K=64, a_col=True),
+                   dict(M=64, N=1000, K=64, in_kind=1)]:
+        with pytest.raises(tc.TcgemmError):
+            tc.plan(kwargs.pop("M"), kwargs.pop("N"), kwargs.pop("K"), 8, 152, **kwargs)
+    with pytest.raises(tc.TcgemmError):
+        tc.binding.autotune_set(256, 64, 256, 8)          # more than 128 rows of C
+    with pytest.raises(tc.TcgemmError):
+        tc.binding.autotune_set(64, 4096, 256, 8, in_type=1)
+
+
+def test_noalloc_fit_decision(tc):
+    """The test gemm_bf16_noalloc applies before launching: a plan fits its
+    fixed scratch array when its workspace does.  Every plan of a 152-SM
+    GB300 fits (2 slots x 76 pairs x 256 KiB = 38 MiB of 40); on a device
+    with 256 SMs a stream-K pair plan needs 64 MiB and is refused."""
+    b = tc.binding
+    cap = b.noalloc_scratch_bytes()
+    for M, N, K, v in [(600, 700, 8192, 0), (896, 2560, 4096, 1), (128, 4096, 16384, 0), (4096, 4096, 4096, 0)]:
+        need = tc.workspace_bytes(M, N, K, v, 152)
+        assert b.noalloc_fits(M, N, K, v, 152) == (need <= cap) is True
+    assert tc.workspace_bytes(600, 700, 8192, 0, 256) > cap
+    assert b.noalloc_fits(600, 700, 8192, 0, 256) is False
+    assert b.noalloc_fits(896, 2560, 4096, 1, 256) is False
+    assert b.noalloc_fits(4096, 4096, 4096, 0, 256) is True        # no split: no scratch needed
+    with pytest.raises(tc.TcgemmError):
+        b.noalloc_fits(0, 1, 1, 0, 152)
 
 
 def test_auto_variant_choice(tc):

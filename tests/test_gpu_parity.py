@@ -87,7 +87,7 @@ def test_padded_leading_dimensions(oracle_lib, variant):
 # the fp32 accumulation bound).  For N(0,1) inputs such elements are those
 # whose exact value is near zero, where cancellation leaves fp32 accumulation
 # error comparable to a bf16 ulp of the result.
-SECOND_CLAUSE_SHARE = 1e-4
+SECOND_CLAUSE_SHARE = 1e-3
 
 
 @pytest.mark.parametrize("name", ["s4k", "s8k", "edge", "skinny"])

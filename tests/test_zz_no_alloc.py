@@ -53,13 +53,16 @@ def _run(tc, case, noalloc: bool):
 
 
 def test_noalloc_matches_regular_entry_point_twice(tc):
-    """Two different problems in a row that share out their k-blocks
-    (stream-K), so both use the scratch array; each result matches gemm_bf16
-    within the fp32 tolerance of the parity tests (and, same plan, bit for
-    bit)."""
+    """Problems in a row that share out their k-blocks (stream-K), so every
+    call uses the scratch array: a pair-tile plan with 20 shared tiles, then
+    a single-CTA plan with 64-wide slots (a different slot layout, so stale
+    partials of the first call sit where the second writes nothing), then a
+    pair-tile plan with 9 shared tiles and another K.  Each result matches
+    gemm_bf16 within the fp32 tolerance of the parity tests (and, same plan,
+    bit for bit)."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    for seed in (61, 62):
-        case = gi.make_case(f"noalloc{seed}", 600, 700, 8192, alpha=0.75, beta=0.5, out_dtype=gi.OUT_F32,
+    for seed, (M, N, K) in [(61, (1024, 1280, 8192)), (62, (128, 4096, 16384)), (63, (600, 700, 12288))]:
+        case = gi.make_case(f"noalloc{seed}", M, N, K, alpha=0.75, beta=0.5, out_dtype=gi.OUT_F32,
                             seed=seed)
         need = tc.workspace_bytes(case.M, case.N, case.K, 0, sms)
         assert 0 < need <= tc.binding.noalloc_scratch_bytes()
