@@ -409,11 +409,18 @@ struct GemmCfg {
     static constexpr uint32_t kEpiBytes = (KS == 2 && 128u * (BN / 2) * 4u > 2 * kEpiBufBytes) ? 128u * (BN / 2) * 4u
                                                                                                : 2 * kEpiBufBytes;
     static constexpr uint32_t kBarOff = kEpiOff + kEpiBytes;
-    static constexpr uint32_t kNumBars = 2 * STAGES + 4 + 1 + 2 + 2;
+    // full/empty per stage, tfull/tempty x 2, drain, C chunk loads (2 per
+    // epilogue warp), xfull/xfree.
+    static constexpr uint32_t kNumBars = 2 * STAGES + 4 + 1 + 8 + 2;
     // The fused epilogue's bias values for the current tile's BN columns
     // (fp32), staged once per tile.
     static constexpr uint32_t kBiasOff = (kBarOff + kNumBars * 8 + 16 + 15) / 16 * 16;
     static constexpr uint32_t kSmemBytes = kBiasOff + BN * 4 + 1024;  // + alignment slack
+    // Per-warp epilogue staging of the plain product: two 32-row x 32-column
+    // buffers per epilogue warp (sized for fp32) inside the staging area.
+    static constexpr uint32_t kWarpBufBytes = 32 * 32 * 4;
+    static_assert(8 * kWarpBufBytes <= kEpiBytes, "per-warp staging fits the staging area");
+    static_assert(kSmemBytes <= 227 * 1024, "dynamic shared memory of one CTA");
     // Workspace bytes per split piece (both CTAs of a pair).
     static constexpr uint64_t kSlotBytes = static_cast<uint64_t>(CTA_GROUP) * 128 * BN * 4;
     static_assert(kTmemCols <= 512, "TMEM has 512 columns");
@@ -661,9 +668,10 @@ __global__ void __launch_bounds__(192, 1)
     auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
     const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
-    auto cold_bar = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 5 + b); };  // C chunk loads
-    const uint32_t xfull_bar = bar0 + 8u * (2 * STAGES + 7);  // KS = 2: the peer's partial is staged
-    const uint32_t xfree_bar = bar0 + 8u * (2 * STAGES + 8);  // KS = 2: the peer has read this CTA's
+    // C chunk loads of epilogue warp q (0..3) into its buffer b.
+    auto cold_bar = [&](uint32_t q, uint32_t b) { return bar0 + 8u * (2 * STAGES + 5 + 2 * q + b); };
+    const uint32_t xfull_bar = bar0 + 8u * (2 * STAGES + 13);  // KS = 2: the peer's partial is staged
+    const uint32_t xfree_bar = bar0 + 8u * (2 * STAGES + 14);  // KS = 2: the peer has read this CTA's
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kBarOff + Cfg::kNumBars * 8);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
@@ -705,8 +713,7 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(tempty_bar(a), 4 * CTA_GROUP);  // one arrive per epilogue warp of each CTA
         }
         mbar_init(drain_bar, 1);
-        mbar_init(cold_bar(0), 1);
-        mbar_init(cold_bar(1), 1);
+        for (uint32_t c = 0; c < 8; ++c) mbar_init(cold_bar(c >> 1, c & 1u), 1);
         mbar_init(xfull_bar, 4);
         mbar_init(xfree_bar, 4);
         *abort_flag = 0u;
@@ -909,15 +916,13 @@ __global__ void __launch_bounds__(192, 1)
         const bool has_beta = p.beta != 0.0f;
         const bool fused = kIsI8<OutT> || has_epilogue(p);  // int8 output always takes the fused path
         float* bias_s = reinterpret_cast<float*>(smem + Cfg::kBiasOff);
-        // Two staging buffers shared by the four epilogue warps, each one
-        // 128-row x 32-column chunk of C with rows fastest (the layout of the
-        // TMA box).  One thread (warp 2, lane 0) issues the TMA copies.
+        // Stream-K pieces: two staging buffers shared by the four epilogue
+        // warps, each one 128-row x 32-column fp32 chunk with rows fastest
+        // (the layout of the TMA box); one thread (warp 2, lane 0) issues
+        // their TMA stores.  Whole tiles use per-warp buffers (below).
         const bool leader = (warp == 2 && lane == 0);
-        OutT* stage_ptr0 = reinterpret_cast<OutT*>(smem + Cfg::kEpiOff);
-        constexpr uint32_t kBufElems = Cfg::kEpiBufBytes / sizeof(OutT);
-        constexpr uint32_t kChunkBytes = 128 * 32 * sizeof(OutT);
-        uint32_t nchunk = 0;      // chunks staged so far; chunk i uses buffer i & 1
-        uint32_t cold_phase = 0;  // bit b: parity of the next completion of cold_bar(b)
+        uint32_t nchunk = 0;      // stream-K chunks staged so far; chunk i uses buffer i & 1
+        uint32_t cold_phase = 0;  // bit b: parity of the next completion of this warp's cold_bar(q, b)
         bool aborted = false;
         uint32_t acc = 0, acc_phase = 0;
         uint32_t xph = 0;  // KS = 2: parity of the next exchange
@@ -930,19 +935,23 @@ __global__ void __launch_bounds__(192, 1)
             const int row_blk = tm * tile_m + static_cast<int>(rank) * (kPairSwap ? rows_a : 128);  // this CTA's rows
             const int64_t colt = static_cast<int64_t>(tn) * BN;  // first column of the tile
             const int ncols = BN;
-            // beta*C: start pulling the C tile into L2 now; the tile's mainloop
-            // hides the memory latency.
-            if (!SWAP && has_beta && leader && row_blk < p.M) {
+            // beta*C: each warp starts pulling its rows of the C tile into L2
+            // now; the tile's mainloop hides the memory latency.
+            const int wrow = row_blk + 32 * static_cast<int>(q);  // this warp's first row (plain product)
+            if (!SWAP && has_beta && lane == 0 && wrow < p.M) {
                 for (int c = 0; c < ncols && colt + c < p.N; c += 32)
-                    tma_prefetch_l2_2d(&tmC, row_blk, static_cast<int32_t>(colt + c));
+                    tma_prefetch_l2_2d(&tmC, wrow, static_cast<int32_t>(colt + c));
             }
+            // The staging area is reused by this unit: every store of earlier
+            // units has finished reading it (the barrier below publishes that).
+            if (lane == 0) tma_store_wait_read<0>();
             const int64_t row = static_cast<int64_t>(row_blk) + row_local;
             const bool row_ok = row < p.M && (!kPairSwap || static_cast<int>(row_local) < rows_a);
             // Fused epilogue: fetch the tile's bias now, while the mainloop
             // runs.  Plain product: the tile's BN column values go to shared
-            // memory (every reader of the previous tile's values has passed a
-            // barrier of that tile since its last read); transposed product:
-            // this thread's row has one value.
+            // memory (every reader of the previous tile's values has passed
+            // the barrier that ends that tile); transposed product: this
+            // thread's row has one value.
             float bias_v = 0.0f;
             float qs = 1.0f;  // int8 output: this row's scale (plain product)
             if constexpr (kIsI8<OutT> && !SWAP) {
@@ -965,11 +974,6 @@ __global__ void __launch_bounds__(192, 1)
             tc_fence_after_sync();
             const uint32_t tbase = tmem_base + ((q * 32u) << 16) + acc * BN;
 
-            // The TMA store clips at 16-byte granules along the contiguous
-            // (row) dimension, so a 128-row block that ends inside such a
-            // granule at row M would also write rows M.. of the ldc padding:
-            // that block is stored with masked plain stores instead.
-            const bool tma_rows = row_blk + 128 <= p.M || ((static_cast<int64_t>(p.M) * sizeof(OutT)) % 16) == 0;
             if (KS == 2) {
                 // K-split tile: each CTA finishes half of the tile's columns
                 // (D columns = rows of C).  It stages the fp32 partial of the
@@ -1057,132 +1061,140 @@ __global__ void __launch_bounds__(192, 1)
                         mbar_arrive_cluster(map_to_cta(tempty_bar(acc), 0));
                     }
                 }
-            } else if (u.slot < 0 && !tma_rows) {
-#pragma unroll 1
-                for (int c = 0; c < ncols; c += 32) {
-                    const int64_t col0 = colt + c;
-                    if (col0 >= p.N) break;
-                    OutT* dst = C + col0 * p.ldc + row;
-                    float cold[32];
-                    if (has_beta && row_ok) load_cold32<OutT>(dst, p.ldc, col0, p.N, cold);
-                    uint32_t r[32];
-                    tmem_ld32(tbase + c, r);
-                    tmem_ld_wait32(r);
-                    if (row_ok) {
-                        if (fused) {
-                            float bj[32];
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) bj[j] = bias_s[c + j];
-                            epilogue_store32_fused<OutT>(dst, p.ldc, col0, p, r, cold, has_beta, bj, qs);
-                        } else {
-                            epilogue_store32<OutT>(dst, p.ldc, col0, p.N, r, p.alpha, p.beta, cold, has_beta);
-                        }
-                    }
-                }
-                // The next tile overwrites the staged bias: all reads first.
-                if (fused) named_barrier_sync(kEpiBarrier, kEpiThreads);
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) {
-                    if constexpr (CTA_GROUP == 1) {
-                        mbar_arrive(tempty_bar(acc));
-                    } else {
-                        mbar_arrive_cluster(map_to_cta(tempty_bar(acc), 0));
-                    }
-                }
             } else if (u.slot < 0) {
-                // Whole tile, chunk by chunk: (TMA load of C ->) TMEM ->
-                // alpha*acc (+ beta*C) in place in the staging buffer -> TMA
-                // store of the 128 x 32 chunk (it clips columns >= N).
+                // Whole tile, chunk by chunk, each epilogue warp on its own 32
+                // rows: (TMA load of its rows of C ->) TMEM -> alpha*acc
+                // (+ beta*C) in the warp's staging buffer -> TMA store of its
+                // 32-row x 32-column box (the store clips columns >= N and
+                // rows >= M).  The warps do not wait for one another: lane 0
+                // of each warp issues, and waits for, its own copies.  The
+                // next chunk's TMEM load is issued before this chunk is
+                // converted.  A warp whose rows end inside a 16-byte granule
+                // at row M stores with masked plain stores instead (the TMA
+                // store would also write rows M.. of the ldc padding).
                 const int64_t width = (p.N - colt) < ncols ? (p.N - colt) : ncols;
                 const int nch = static_cast<int>((width + 31) / 32);
-                const bool rows_in = row_blk < p.M;  // same for the whole CTA
-                const bool load_c = has_beta && rows_in;
-                if (load_c && leader) {
-                    tma_store_wait_read<0>();  // no older store still reads a buffer
-                    const uint32_t b = nchunk & 1u;
-                    mbar_arrive_expect_tx(cold_bar(b), kChunkBytes);
-                    tma_load_2d(base + Cfg::kEpiOff + b * Cfg::kEpiBufBytes, &tmC, cold_bar(b), row_blk,
-                                static_cast<int32_t>(colt));
-                }
+                const bool w_rows = wrow < p.M;
+                const bool w_tma = wrow + 32 <= p.M || ((static_cast<int64_t>(p.M) * sizeof(OutT)) % 16) == 0;
+                const uint32_t wbuf = base + Cfg::kEpiOff + q * 2u * Cfg::kWarpBufBytes;
+                OutT* wsp0 = reinterpret_cast<OutT*>(smem + Cfg::kEpiOff + q * 2u * Cfg::kWarpBufBytes);
+                constexpr uint32_t kWarpBufElems = Cfg::kWarpBufBytes / sizeof(OutT);
+                constexpr uint32_t kWarpChunkBytes = 32 * 32 * sizeof(OutT);
+                bool wok = true;
+                if (w_rows && !w_tma) {
 #pragma unroll 1
-                for (int i = 0; i < nch; ++i) {
-                    const int64_t col0 = colt + 32 * i;
-                    const uint32_t b = nchunk & 1u;
-                    OutT* sp = stage_ptr0 + b * kBufElems;
-                    uint32_t r[32];
-                    tmem_ld32(tbase + 32 * i, r);
-                    if (load_c) {
-                        if (leader && i + 1 < nch) {
-                            // The other buffer's last store must be done reading it.
-                            tma_store_wait_read<0>();
-                            mbar_arrive_expect_tx(cold_bar(b ^ 1u), kChunkBytes);
-                            tma_load_2d(base + Cfg::kEpiOff + (b ^ 1u) * Cfg::kEpiBufBytes, &tmC, cold_bar(b ^ 1u),
-                                        row_blk, static_cast<int32_t>(col0 + 32));
-                        }
-                        uint32_t okc = 1;
-                        if (lane == 0) okc = wait_phase<false>(cold_bar(b), (cold_phase >> b) & 1u, wctx,
-                                                               kWhereEpilogue) ? 1u : 0u;
-                        okc = __shfl_sync(0xffffffffu, okc, 0);
-                        cold_phase ^= 1u << b;
-                        if (!named_barrier_and(kEpiBarrier, kEpiThreads, okc != 0u)) {
-                            aborted = true;
-                            break;
-                        }
-                    } else {
-                        // The buffer's previous store (two chunks ago) must be
-                        // done reading it before it is overwritten.
-                        if (leader && nchunk >= 2) tma_store_wait_read<1>();
-                        named_barrier_sync(kEpiBarrier, kEpiThreads);
-                    }
-                    tmem_ld_wait32(r);
-                    if (fused) {
-                        // + bias[column] (staged; 0 beyond N, where the store
-                        // clips anyway), activation.  The 32 values are read
-                        // into registers before the first store.
-                        float bj[32];
-                        const float4* b4 = reinterpret_cast<const float4*>(bias_s + 32 * i);
+                    for (int c = 0; c < ncols; c += 32) {
+                        const int64_t col0 = colt + c;
+                        if (col0 >= p.N) break;
+                        OutT* dst = C + col0 * p.ldc + row;
+                        float cold[32];
+                        if (has_beta && row_ok) load_cold32<OutT>(dst, p.ldc, col0, p.N, cold);
+                        uint32_t r[32];
+                        tmem_ld32(tbase + c, r);
+                        tmem_ld_wait32(r);
+                        if (row_ok) {
+                            if (fused) {
+                                float bj[32];
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const float4 t4 = b4[q];
-                            bj[4 * q] = t4.x;
-                            bj[4 * q + 1] = t4.y;
-                            bj[4 * q + 2] = t4.z;
-                            bj[4 * q + 3] = t4.w;
-                        }
-                        float vv[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            float v = p.alpha * __uint_as_float(r[j]);
-                            if (load_c) v = fmaf(p.alpha, __uint_as_float(r[j]), p.beta * load_out<OutT>(sp + j * 128 + row_local));
-                            vv[j] = v + bj[j];
-                        }
-                        activation_n(vv, p.act);
-                        if constexpr (kIsI8<OutT>) {
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) vv[j] = fmaf(vv[j], qs, p.qzero);
-                        }
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) store_out<OutT>(sp + j * 128 + row_local, vv[j]);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            OutT* e = sp + j * 128 + row_local;
-                            float v = p.alpha * __uint_as_float(r[j]);
-                            if (load_c) v = fmaf(p.alpha, __uint_as_float(r[j]), p.beta * load_out<OutT>(e));
-                            store_out<OutT>(e, v);
+                                for (int j = 0; j < 32; ++j) bj[j] = bias_s[c + j];
+                                epilogue_store32_fused<OutT>(dst, p.ldc, col0, p, r, cold, has_beta, bj, qs);
+                            } else {
+                                epilogue_store32<OutT>(dst, p.ldc, col0, p.N, r, p.alpha, p.beta, cold, has_beta);
+                            }
                         }
                     }
-                    fence_proxy_async_smem();
-                    named_barrier_sync(kEpiBarrier, kEpiThreads);
-                    if (leader && rows_in) {
-                        tma_store_2d(&tmC, base + Cfg::kEpiOff + b * Cfg::kEpiBufBytes, row_blk,
-                                     static_cast<int32_t>(col0));
-                        tma_store_commit();
+                } else if (w_rows) {
+                    const bool load_c = has_beta;
+                    if (load_c && lane == 0) {
+                        mbar_arrive_expect_tx(cold_bar(q, 0), kWarpChunkBytes);
+                        tma_load_2d(wbuf, &tmC, cold_bar(q, 0), wrow, static_cast<int32_t>(colt));
                     }
-                    ++nchunk;
+                    uint32_t rn[32];
+                    tmem_ld32(tbase, rn);
+#pragma unroll 1
+                    for (int i = 0; i < nch; ++i) {
+                        const int64_t col0 = colt + 32 * i;
+                        const uint32_t b = static_cast<uint32_t>(i) & 1u;
+                        OutT* sp = wsp0 + b * kWarpBufElems;
+                        uint32_t r[32];
+                        tmem_ld_wait32(rn);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) r[j] = rn[j];
+                        if (i + 1 < nch) tmem_ld32(tbase + 32 * (i + 1), rn);
+                        if (load_c) {
+                            if (lane == 0 && i + 1 < nch) {
+                                // The other buffer's last store (chunk i - 1)
+                                // must be done reading it.
+                                tma_store_wait_read<0>();
+                                mbar_arrive_expect_tx(cold_bar(q, b ^ 1u), kWarpChunkBytes);
+                                tma_load_2d(wbuf + (b ^ 1u) * Cfg::kWarpBufBytes, &tmC, cold_bar(q, b ^ 1u), wrow,
+                                            static_cast<int32_t>(col0 + 32));
+                            }
+                            uint32_t okc = 1;
+                            if (lane == 0) okc = wait_phase<false>(cold_bar(q, b), (cold_phase >> b) & 1u, wctx,
+                                                                   kWhereEpilogue) ? 1u : 0u;
+                            okc = __shfl_sync(0xffffffffu, okc, 0);
+                            cold_phase ^= 1u << b;
+                            if (okc == 0u) {
+                                wok = false;
+                                if (i + 1 < nch) tmem_ld_wait32(rn);
+                                break;
+                            }
+                        } else {
+                            // This buffer's previous store (two chunks ago)
+                            // must be done reading it.
+                            if (lane == 0 && i >= 2) tma_store_wait_read<1>();
+                            __syncwarp();
+                        }
+                        if (fused) {
+                            // + bias[column] (staged; 0 beyond N, where the
+                            // store clips anyway), activation.
+                            float bj[32];
+                            const float4* b4 = reinterpret_cast<const float4*>(bias_s + 32 * i);
+#pragma unroll
+                            for (int t = 0; t < 8; ++t) {
+                                const float4 t4 = b4[t];
+                                bj[4 * t] = t4.x;
+                                bj[4 * t + 1] = t4.y;
+                                bj[4 * t + 2] = t4.z;
+                                bj[4 * t + 3] = t4.w;
+                            }
+                            float vv[32];
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                float v = p.alpha * __uint_as_float(r[j]);
+                                if (load_c) v = fmaf(p.alpha, __uint_as_float(r[j]), p.beta * load_out<OutT>(sp + j * 32 + lane));
+                                vv[j] = v + bj[j];
+                            }
+                            activation_n(vv, p.act);
+                            if constexpr (kIsI8<OutT>) {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) vv[j] = fmaf(vv[j], qs, p.qzero);
+                            }
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) store_out<OutT>(sp + j * 32 + lane, vv[j]);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                OutT* e = sp + j * 32 + lane;
+                                float v = p.alpha * __uint_as_float(r[j]);
+                                if (load_c) v = fmaf(p.alpha, __uint_as_float(r[j]), p.beta * load_out<OutT>(e));
+                                store_out<OutT>(e, v);
+                            }
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmC, wbuf + b * Cfg::kWarpBufBytes, wrow, static_cast<int32_t>(col0));
+                            tma_store_commit();
+                        }
+                    }
                 }
-                if (aborted) break;
+                // Every warp is done with the tile (or one gave up).
+                if (!named_barrier_and(kEpiBarrier, kEpiThreads, wok)) {
+                    aborted = true;
+                    break;
+                }
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) {
@@ -1231,7 +1243,7 @@ __global__ void __launch_bounds__(192, 1)
             if (acc == 0) acc_phase ^= 1u;
         }
         // Every TMA store has completed before the CTA exits.
-        if (leader) tma_store_wait_all();
+        if (lane == 0) tma_store_wait_all();
         __syncwarp();
     }
 

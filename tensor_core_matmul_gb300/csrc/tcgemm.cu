@@ -381,11 +381,11 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pa
 
 // --------------------------------------------------------- tensor maps --
 
-// C (column-major M x N, fp32 or bf16) in 128-row x 32-column boxes, for the
-// epilogue's TMA loads, stores and L2 prefetches.  The stream-K workspace is
-// mapped the same way (fp32, 128 rows, ldc = 128).
-// out_dtype: TCGEMM_OUT_F32, _BF16 or _I8 (the workspace map uses F32).
-bool encode_c(CUtensorMap* m, void* ptr, int64_t M, int64_t N, int64_t ldc, int out_dtype) {
+// C (column-major M x N, fp32, bf16 or int8) in boxes of box_rows rows x 32
+// columns: 32-row boxes for the epilogue warps' TMA loads, stores and L2
+// prefetches of C; 128-row boxes for the stream-K workspace (fp32, 128 rows,
+// ldc = 128).
+bool encode_c(CUtensorMap* m, void* ptr, int64_t M, int64_t N, int64_t ldc, int out_dtype, uint32_t box_rows) {
     if (!encode_fn()) {
         set_error("cuTensorMapEncodeTiled is not available from the driver");
         return false;
@@ -395,7 +395,7 @@ bool encode_c(CUtensorMap* m, void* ptr, int64_t M, int64_t N, int64_t ldc, int 
                                    : out_dtype == TCGEMM_OUT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                                   : CU_TENSOR_MAP_DATA_TYPE_UINT8;
     const MapKey k{dt, ptr, {static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(N)},
-                   static_cast<cuuint64_t>(ldc) * esz, {128u, 32u}, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   static_cast<cuuint64_t>(ldc) * esz, {box_rows, 32u}, CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_NONE};
     const CUresult r = encode_2d(m, k);
     if (r != CUDA_SUCCESS) {
@@ -938,10 +938,10 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     }
     pl.ws_ptr = wsp;
     CUtensorMap tcm, twm;
-    if (!encode_c(&tcm, C, M, N, ldc, out_dtype)) return TCGEMM_ERR_INVALID_ARG;
+    if (!encode_c(&tcm, C, M, N, ldc, out_dtype, 32u)) return TCGEMM_ERR_INVALID_ARG;
     if (pl.sk_tiles > 0) {
         const int64_t wcols = 2 * static_cast<int64_t>(pl.grid / pl.cta_group) * pl.cta_group * pl.bn;
-        if (!encode_c(&twm, wsp, 128, wcols, 128, TCGEMM_OUT_F32))
+        if (!encode_c(&twm, wsp, 128, wcols, 128, TCGEMM_OUT_F32, 128u))
             return TCGEMM_ERR_INVALID_ARG;
     } else {
         twm = tcm;

@@ -114,6 +114,27 @@ def check_bf16(got_bits: np.ndarray, ref_bits: np.ndarray, what: str = "", max_u
     return {"size": int(got_bits.size), "beyond_1ulp": beyond, "second_clause": second, "max_ulp": int(d.max())}
 
 
+def second_clause_cap(K: int) -> float:
+    """Largest share of an N(0,1) workload's bf16 elements allowed to need
+    the derived second clause (more than one ulp from the oracle's rounding,
+    within the fp32 accumulation bound).
+
+    Model: the fp32 accumulator (K/16 MMA additions into partial sums of size
+    about sqrt(K)) carries an error e of standard deviation sigma ~ 2^-24 K/4.
+    The bf16 result lands more than one ulp from the correct rounding only
+    where |e| exceeds an ulp of D, i.e. |D| < 256 |e|; with D ~ N(0, K) that
+    share is about (512 / sqrt(2 pi)) E|e| / sqrt(K) = 163 sigma / sqrt(K)
+    = 2.4e-6 sqrt(K).  The cap is three times that (4.7e-4 at K = 4096,
+    6.6e-4 at 8192): on the GB300 the full-size workloads need the clause for
+    1.5e-4 (4096^3) and 3.4e-4 (8192^3) of their elements; emulated on the
+    CPU (tests/test_second_clause_cap.py), an fp32 accumulator that rounds to
+    nearest needs it for 2e-5, one that truncates for 2.4e-4, and one that
+    keeps two fewer mantissa bits for 1e-3, over the cap although each of its
+    elements is within the clause's worst-case bound."""
+    sigma = 2.0 ** -24 * K / 4.0
+    return 3.0 * 163.0 * sigma / np.sqrt(K)
+
+
 LIPSCHITZ = {"none": 1.0, "relu": 1.0, "gelu": 1.13, "gelu_tanh": 1.13}
 ACT_FN_REL = 2.0 ** -20  # allowance for the fp32 activation function's error (erfcf, expf: a few ulp)
 

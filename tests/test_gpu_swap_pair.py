@@ -12,6 +12,7 @@ import torch
 
 import gemm_inputs as gi
 from tests import gpu_harness as H
+from tests import parity
 
 pytestmark = pytest.mark.gpu
 
@@ -83,6 +84,8 @@ def test_full_size_every_element(oracle_lib, M, N, K, out):
     got = H.run_case(case, PAIR).result_np()
     stats = H.compare_full(oracle_lib, case, got, what=f"pair full {M}x{N}x{K}")
     H.record_stats(f"pair full {M}x{N}x{K}", stats)
+    if out == gi.OUT_BF16:
+        assert stats["second_clause"] <= parity.second_clause_cap(K) * stats["size"] + 2, stats
     again = H.run_case(case, PAIR).result_np()
     assert np.array_equal(got.view(np.uint8), again.view(np.uint8))
 
