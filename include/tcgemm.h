@@ -481,6 +481,24 @@ int tcgemm_check_device_status(void* stream, uint32_t* where_out);
  * works.  Touches no user memory. */
 int tcgemm_selftest_timeout(void* stream, uint64_t timeout_ns);
 
+/* Self test of the GEMM's own give-up path (the hang guard inside the
+ * kernels, not the one-thread wait of tcgemm_selftest_timeout).  Runs
+ * C = A*B (alpha 1, beta 0, fp32 output, the layouts and rules of gemm_bf16)
+ * with kernel variant `variant` (1, 2, 4 or 5: the plain-product kernels,
+ * no split of K) while the TMA producer of CTA 0 withholds the arrival and
+ * the loads of its first k-block, so that the MMA thread's wait for that
+ * stage runs out after `timeout_ns` (in (0, 10 s]).  The waiting roles give
+ * up, every CTA drains its own copies and MMAs, frees its TMEM and exits;
+ * the call synchronizes `stream` and returns what tcgemm_check_device_status
+ * reports: TCGEMM_ERR_TIMEOUT when the path works (the status word is then
+ * cleared and the context stays usable).  C is left unspecified.  Other
+ * errors: TCGEMM_ERR_INVALID_ARG for another variant, non-positive sizes or
+ * a limit out of range; as gemm_bf16 otherwise.  No counterpart on the
+ * pages: it exists to test the bounded waits. */
+int tcgemm_selftest_withheld_load(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                                  int64_t ldb, void* C, int64_t ldc, int variant, uint64_t timeout_ns,
+                                  void* stream);
+
 /* Number of kernels this library has launched in this process. */
 uint64_t tcgemm_launch_count(void);
 

@@ -124,6 +124,8 @@ def lib() -> ctypes.CDLL:
     L.tcgemm_check_device_status.restype = i32
     L.tcgemm_selftest_timeout.argtypes = [p, ctypes.c_uint64]
     L.tcgemm_selftest_timeout.restype = i32
+    L.tcgemm_selftest_withheld_load.argtypes = [i64, i64, i64, p, i64, p, i64, p, i64, i32, ctypes.c_uint64, p]
+    L.tcgemm_selftest_withheld_load.restype = i32
     L.tcgemm_launch_count.argtypes = []
     L.tcgemm_launch_count.restype = ctypes.c_uint64
     L.tcgemm_version.argtypes = []
@@ -459,6 +461,15 @@ def check_device_status(stream=None) -> tuple[int, int]:
     where = ctypes.c_uint32(0)
     st = lib().tcgemm_check_device_status(_stream_ptr(stream), ctypes.byref(where))
     return st, where.value
+
+
+def selftest_withheld_load(A, B, C, *, M: int, N: int, K: int, variant: int, timeout_ns: int,
+                           stream=None) -> int:
+    """tcgemm_selftest_withheld_load on torch tensors laid out as gemm_bf16's
+    (C fp32); returns the status code (5 = TCGEMM_ERR_TIMEOUT expected)."""
+    return int(lib().tcgemm_selftest_withheld_load(M, N, K, A.data_ptr(), A.shape[1], B.data_ptr(), B.shape[1],
+                                                   C.data_ptr(), C.shape[1], variant, timeout_ns,
+                                                   _stream_ptr(stream)))
 
 
 def selftest_timeout(timeout_ns: int, stream=None) -> int:

@@ -197,6 +197,11 @@ struct GemmParams {
     // pair's tile is 2 * rows_a rows of D.  Unused by the other kernels.
     int rows_a;
     uint64_t timeout_ns;
+    // Self test of the give-up path (tcgemm_selftest_withheld_load): the
+    // producer of CTA 0 withholds the arrival and the loads of its k-block
+    // number `withhold_kb` (-1: never), so that the MMA's wait for it runs
+    // out.
+    int withhold_kb;
 };
 
 // The tile of unit index t under the launch's visiting order.
@@ -634,12 +639,27 @@ constexpr uint32_t kEpiThreads = 128;
 // through distributed shared memory, and stores.  Per CTA, xfull (one arrival
 // per epilogue warp of the peer) says the peer's partial is staged, xfree
 // says the peer has read this CTA's.
-template <int CTA_GROUP, int BN, int STAGES, int AROWS, bool SWAP, typename OutT, int IN = 0, int KS = 1>
+// NS: MMAs per K step.  NS = 2 issues each K step as two MMAs of width
+// BN/2 that share the A operand and write the two column halves of the
+// accumulator.  Measured on GB300, a K step with one MMA into one
+// accumulator costs 150-175 clocks whatever its width (an N = 224 MMA does
+// 112 clocks of work), while two that share A and write different columns
+// overlap and run at the full rate of 8192 FLOP per clock per SM once they
+// cover 256 columns.  For a CTA pair the halves of the tile that each MMA
+// reads must sit at the same shared-memory offset in both CTAs, so each CTA
+// loads its B rows as NS boxes: box h holds tile columns
+// [h*BN/NS + rank*BN/(2*NS), ...), and the accumulator columns stay in tile
+// order.
+template <int CTA_GROUP, int BN, int STAGES, int AROWS, bool SWAP, typename OutT, int IN = 0, int KS = 1, int NS = 1>
 __global__ void __launch_bounds__(192, 1)
     gemm_bf16_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
                         const GemmParams p) {
     using Cfg = GemmCfg<CTA_GROUP, BN, STAGES, AROWS, IN, KS>;
+    static_assert(NS == 1 || (NS == 2 && (!SWAP || CTA_GROUP == 1) && (Cfg::kRowsB / 2) % 8 == 0 &&
+                              (BN / 2) % 16 == 0),
+                  "split MMAs: whole swizzle atoms of B per half, MMA widths a multiple of 16");
+    constexpr int kRowsBh = Cfg::kRowsB / NS;  // B rows of one split MMA in this CTA
     static_assert(!SWAP || CTA_GROUP == 1 || (KS == 1 && AROWS == 64), "pairs run the swapped product with "
                   "64-row A stages and no K split");
     static_assert(AROWS == 128 || SWAP || CTA_GROUP == 1, "half-height A tiles: single CTAs or the swapped pairs");
@@ -674,6 +694,7 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t xfree_bar = bar0 + 8u * (2 * STAGES + 14);  // KS = 2: the peer has read this CTA's
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kBarOff + Cfg::kNumBars * 8);
     volatile uint32_t* abort_flag = tmem_slot + 1;
+    volatile uint32_t* never_flag = tmem_slot + 2;  // stays 0: drains wait for copies even after an abort
 
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31u;
@@ -703,6 +724,21 @@ __global__ void __launch_bounds__(192, 1)
         tma_prefetch_desc(&tmB);
     }
     if (warp == 2 && lane == 0) tma_prefetch_desc(&tmC);
+    // The producer's first unit is worked out before the set-up, so that the
+    // kernel parameters it reads (first reads of the launch, from memory)
+    // arrive while the barriers are initialised and TMEM is allocated.
+    UnitIter pit(cluster_id, num_clusters);
+    WorkUnit pu{};
+    bool p_have = false;
+    int p_tm = 0, p_tn = 0;
+    if (warp == 0 && lane == 0) {
+        pit.start(p);
+        p_have = pit.next(p, pu);
+        if (p_have) {
+            ks_range(pu);
+            tile_of(pu.tile, p_tm, p_tn);
+        }
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
@@ -717,6 +753,7 @@ __global__ void __launch_bounds__(192, 1)
         mbar_init(xfull_bar, 4);
         mbar_init(xfree_bar, 4);
         *abort_flag = 0u;
+        *never_flag = 0u;
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc<CTA_GROUP>(smem_u32(tmem_slot), Cfg::kTmemAlloc);
@@ -743,6 +780,10 @@ __global__ void __launch_bounds__(192, 1)
     }
     const uint32_t tmem_base = *tmem_slot;  // not read by an early producer
     const WaitCtx wctx{abort_flag, p.timeout_ns};
+    // Drains wait for this CTA's own copies and MMAs to finish whether or not
+    // another role gave up (bounded by the same limit): the CTA may not exit,
+    // nor free its TMEM, while a TMA copy or an MMA still uses them.
+    const WaitCtx dctx{never_flag, p.timeout_ns};
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer --
@@ -750,15 +791,14 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t stage = 0, phase = 0;
             uint64_t issued = 0;
             bool ok = true;
-            UnitIter it(cluster_id, num_clusters);
-            it.start(p);
-            WorkUnit u;
-            while (ok && it.next(p, u)) {
-                ks_range(u);
-                int tm, tn;
-                tile_of(u.tile, tm, tn);
+            // Launched as a programmatic dependent of the previous kernel on
+            // the stream, the set-up above may have overlapped its tail; no
+            // global memory is read before that kernel has completed.
+            grid_dependency_wait();
+            while (ok && p_have) {
+                const WorkUnit u = pu;
+                const int tm = p_tm, tn = p_tn;
                 const int a_row = tm * tile_m + static_cast<int>(rank) * rows_a;
-                const int b_row = tn * BN + static_cast<int>(rank) * Cfg::kRowsB;
                 const CUtensorMap* mB = &tmB;
                 const uint32_t stage_tx = kPairSwap ? CTA_GROUP * (static_cast<uint32_t>(rows_a) * 128u + Cfg::kBBytes)
                                                     : Cfg::kStageTx;
@@ -784,22 +824,34 @@ __global__ void __launch_bounds__(192, 1)
                     }
                     const uint32_t sa = sA0 + stage * Cfg::kABytes;
                     const uint32_t sb = sB0 + stage * Cfg::kBBytes;
-                    if constexpr (CTA_GROUP == 1) {
+                    if (p.withhold_kb >= 0 && blockIdx.x == 0 && issued == static_cast<uint64_t>(p.withhold_kb)) {
+                        // Self test: this stage's phase is never completed.
+                    } else if constexpr (CTA_GROUP == 1) {
                         mbar_arrive_expect_tx(full_bar(stage), stage_tx);
                         load_tile(sa, &tmA, full_bar(stage), kb, a_row, Cfg::kRowsA, p.a_mn != 0);
-                        load_tile(sb, mB, full_bar(stage), kb, b_row, Cfg::kRowsB, p.b_mn != 0);
+                        load_tile(sb, mB, full_bar(stage), kb, tn * BN, Cfg::kRowsB, p.b_mn != 0);
                     } else {
                         // Both CTAs' bytes land on the leader's barrier.
                         if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), stage_tx);
                         const uint32_t fb = map_to_cta(full_bar(stage), 0);
                         load_tile(sa, &tmA, fb, kb, a_row, Cfg::kRowsA, p.a_mn != 0);
-                        load_tile(sb, mB, fb, kb, b_row, Cfg::kRowsB, p.b_mn != 0);
+#pragma unroll
+                        for (int h = 0; h < NS; ++h)
+                            load_tile(sb + h * kRowsBh * 128, mB, fb, kb,
+                                      tn * BN + h * (BN / NS) + static_cast<int>(rank) * kRowsBh, kRowsBh,
+                                      p.b_mn != 0);
                     }
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
+                }
+                // The next unit, worked out while this one's loads are in flight.
+                p_have = pit.next(p, pu);
+                if (p_have) {
+                    ks_range(pu);
+                    tile_of(pu.tile, p_tm, p_tn);
                 }
             }
             // Every load is issued: a dependent kernel (the stream-K
@@ -815,9 +867,9 @@ __global__ void __launch_bounds__(192, 1)
                 const uint64_t times = (issued - s - 1) / STAGES + 1;
                 const uint32_t par = static_cast<uint32_t>((times - 1) & 1u);
                 if (CTA_GROUP == 1 || rank == 0) {
-                    wait_phase<false>(full_bar(s), par, wctx, kWhereDrain);
+                    wait_phase<false>(full_bar(s), par, dctx, kWhereDrain);
                 } else {
-                    wait_phase<false>(empty_bar(s), par, wctx, kWhereDrain);
+                    wait_phase<false>(empty_bar(s), par, dctx, kWhereDrain);
                 }
             }
         }
@@ -837,8 +889,8 @@ __global__ void __launch_bounds__(192, 1)
             auto issue_units = [&](auto mn_tag) {
             constexpr bool MN = decltype(mn_tag)::value;
             // Bits 15 / 16 of the instruction descriptor: A / B MN-major.
-            const uint32_t kIdesc = (IN == 1 ? idesc_f8_f32(Cfg::kBM, BN, static_cast<uint32_t>(p.in_fmt) & 1u)
-                                             : idesc_bf16_f32(Cfg::kBM, BN)) |
+            const uint32_t kIdesc = (IN == 1 ? idesc_f8_f32(Cfg::kBM, BN / NS, static_cast<uint32_t>(p.in_fmt) & 1u)
+                                             : idesc_bf16_f32(Cfg::kBM, BN / NS)) |
                                     (MN && p.a_mn ? (1u << 15) : 0u) | (MN && p.b_mn ? (1u << 16) : 0u);
             // Descriptor step per MMA: 32 bytes along a K-major row, two
             // 1 KB K groups in an MN-major tile (in 16-byte units).
@@ -864,13 +916,21 @@ __global__ void __launch_bounds__(192, 1)
                     const uint64_t bd = MN && p.b_mn ? sdesc_mnmajor_sw128(sb) : sdesc_kmajor_sw128(sb);
 #pragma unroll
                     for (int k = 0; k < Cfg::kBK / Cfg::kUmmaK; ++k) {
-                        if constexpr (MN) {
-                            mma_tc<CTA_GROUP, IN>(d_tmem, ad + a_step * k, bd + b_step * k, idesc,
-                                                  (kb != u.kb0 || k != 0) ? 1u : 0u);
-                        } else {
-                            // +32 bytes along K per step: (32 >> 4) = 2 in the address field.
-                            mma_tc<CTA_GROUP, IN>(d_tmem, ad + 2u * k, bd + 2u * k, idesc,
-                                                  (kb != u.kb0 || k != 0) ? 1u : 0u);
+#pragma unroll
+                        for (int h = 0; h < NS; ++h) {
+                            // Split MMA h: its B rows start kRowsBh rows (whole
+                            // 1 KB swizzle atoms, or 8 KB MN-major boxes of 64
+                            // rows) further on; it writes columns h*BN/NS.. .
+                            const uint32_t bh = static_cast<uint32_t>(h) * kRowsBh * 8u;
+                            const uint32_t dh = d_tmem + static_cast<uint32_t>(h) * (BN / NS);
+                            if constexpr (MN) {
+                                mma_tc<CTA_GROUP, IN>(dh, ad + a_step * k, bd + bh + b_step * k, idesc,
+                                                      (kb != u.kb0 || k != 0) ? 1u : 0u);
+                            } else {
+                                // +32 bytes along K per step: (32 >> 4) = 2 in the address field.
+                                mma_tc<CTA_GROUP, IN>(dh, ad + 2u * k, bd + bh + 2u * k, idesc,
+                                                      (kb != u.kb0 || k != 0) ? 1u : 0u);
+                            }
                         }
                     }
                     if constexpr (CTA_GROUP == 1) {
@@ -905,7 +965,7 @@ __global__ void __launch_bounds__(192, 1)
             } else {
                 mma_commit_pair(drain_bar, 0x1);
             }
-            wait_phase<false>(drain_bar, 0, wctx, kWhereDrain);
+            wait_phase<false>(drain_bar, 0, dctx, kWhereDrain);
         }
     } else {
         // --------------------------------------------------- epilogue --
@@ -926,8 +986,9 @@ __global__ void __launch_bounds__(192, 1)
         bool aborted = false;
         uint32_t acc = 0, acc_phase = 0;
         uint32_t xph = 0;  // KS = 2: parity of the next exchange
+        grid_dependency_wait();  // as the producer: after the previous kernel on the stream
         UnitIter it(cluster_id, num_clusters);
-            it.start(p);
+        it.start(p);
         WorkUnit u;
         while (!aborted && it.next(p, u)) {
             int tm, tn;
@@ -1137,7 +1198,15 @@ __global__ void __launch_bounds__(192, 1)
                             cold_phase ^= 1u << b;
                             if (okc == 0u) {
                                 wok = false;
-                                if (i + 1 < nch) tmem_ld_wait32(rn);
+                                if (i + 1 < nch) {
+                                    tmem_ld_wait32(rn);
+                                    // The next chunk's load of C is in flight:
+                                    // it lands before the CTA moves on.
+                                    if (lane == 0)
+                                        (void)wait_phase<false>(cold_bar(q, b ^ 1u), (cold_phase >> (b ^ 1u)) & 1u,
+                                                                dctx, kWhereDrain);
+                                    __syncwarp();
+                                }
                                 break;
                             }
                         } else {

@@ -140,6 +140,7 @@ struct Plan {
     uint64_t ws_bytes = 0;    // workspace this plan needs (0 without stream-K)
     int ks = 1;               // CTAs of a cluster that split each tile's k-blocks (2: variant 7)
     int hilbert = 0;          // visiting order: 0 grouped bands, k > 0 the Hilbert curve of a 2^k square
+    int ns = 1;               // MMAs per K step sharing the A operand (2: two half-width MMAs)
     void* ws_ptr = nullptr;   // the workspace of this launch
 };
 
@@ -189,6 +190,16 @@ int order_override() {
     return v;
 }
 constexpr bool kHilbertDefault = false;
+
+// MMAs per K step for the CTA-pair tiles: TCGEMM_NSPLIT=1 or =2 in the
+// environment chooses for every launch (A/B measurements); unset, 1.
+int nsplit_choice() {
+    static const int v = [] {
+        const char* s = std::getenv("TCGEMM_NSPLIT");
+        return (s && s[0] == '2') ? 2 : 1;
+    }();
+    return v;
+}
 
 // TCGEMM_SPLIT=0 in the environment turns the tail split off (for A/B timing).
 bool split_enabled() {
@@ -370,6 +381,8 @@ bool make_plan(int64_t M, int64_t N, int64_t K, int variant, int sms, int max_pa
     int g = 1;
     while (g * 2 <= ideal) g *= 2;
     pl.group_m = std::max(1, std::min(g, pl.grid_m));
+    if (in_kind == 0 && ((pl.cta_group == 2 && !pl.swap) || (pl.swap && pl.ks == 2 && pl.bn == 64)))
+        pl.ns = nsplit_choice();
     const int ov = order_override();
     if (ov == 1 || (ov < 0 && kHilbertDefault)) {
         int k = 0;
@@ -452,13 +465,13 @@ bool encode_mnmajor(CUtensorMap* m, const void* ptr, int64_t mn_extent, int64_t 
 
 // The dynamic shared-memory opt-in is a per-kernel attribute; it is set once
 // per device for each kernel instantiation.
-template <int CG, int BN, int ST, int AR, bool SW, typename OutT, int IN = 0, int KS = 1>
+template <int CG, int BN, int ST, int AR, bool SW, typename OutT, int IN = 0, int KS = 1, int NS = 1>
 bool ensure_smem_attr(int dev) {
     static std::mutex mu;
     static bool done[kMaxDevices] = {};
     std::lock_guard<std::mutex> lk(mu);
     if (done[dev]) return true;
-    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, AR, SW, OutT, IN, KS>;
+    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, AR, SW, OutT, IN, KS, NS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(tcg::GemmCfg<CG, BN, ST, AR, IN, KS>::kSmemBytes));
     if (e != cudaSuccess) {
@@ -469,25 +482,30 @@ bool ensure_smem_attr(int dev) {
     return true;
 }
 
-template <int CG, int BN, int ST, int AR, bool SW, typename OutT, int IN = 0, int KS = 1>
+template <int CG, int BN, int ST, int AR, bool SW, typename OutT, int IN = 0, int KS = 1, int NS = 1>
 int launch_gemm(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tcm,
                 const CUtensorMap& twm, const tcg::GemmParams& gp, cudaStream_t stream, int dev) {
-    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, AR, SW, OutT, IN, KS>;
-    if (!ensure_smem_attr<CG, BN, ST, AR, SW, OutT, IN, KS>(dev)) return TCGEMM_ERR_CUDA;
+    auto kern = tcg::gemm_bf16_tn_kernel<CG, BN, ST, AR, SW, OutT, IN, KS, NS>;
+    if (!ensure_smem_attr<CG, BN, ST, AR, SW, OutT, IN, KS, NS>(dev)) return TCGEMM_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(pl.grid), 1, 1);
     cfg.blockDim = dim3(tcg::GemmCfg<CG, BN, ST, AR>::kThreads, 1, 1);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    cfg.numAttrs = 0;
+    // A programmatic dependent of the previous kernel on the stream: the
+    // launch and the set-up (barriers, TMEM, the first unit) overlap that
+    // kernel's tail; the kernel reads no global memory before it completes.
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (CG * KS > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = CG * KS;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = CG * KS;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     }
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tcm, twm, gp);
     if (e != cudaSuccess) {
@@ -804,7 +822,8 @@ int tuned_variant(const TuneKey& k) {
 int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
              int64_t ldc, float alpha, float beta, int out_dtype, void* stream_v, int variant,
              int ws_mode = kWsInternal, void* ws = nullptr, int64_t ws_bytes = 0, const Epilogue& ep = Epilogue(),
-             int in_kind = 0, int in_fmt = 0, bool a_col = false, bool b_row = false) {
+             int in_kind = 0, int in_fmt = 0, bool a_col = false, bool b_row = false, int withhold_kb = -1,
+             uint64_t timeout_override_ns = 0) {
     t_last_error[0] = '\0';
     if (!variant_known(variant)) {
         set_error("unknown variant %d", variant);
@@ -914,10 +933,14 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
             if (rc != TCGEMM_OK) return rc;
         }
     }
-    // Box heights: a CTA pair loads half of the B tile per CTA.
+    // The split-MMA kernels are built for bf16 operands with fp32 or bf16
+    // output; the others issue one MMA per K step.
+    if (out_dtype == TCGEMM_OUT_I8) pl.ns = 1;
+    // Box heights: a CTA pair loads half of the B tile per CTA (in pl.ns
+    // boxes).
     const uint32_t a_box_rows = (pl.arows == 64 || (pl.swap && pl.cta_group == 2)) ? static_cast<uint32_t>(pl.arows)
                                                                                     : 128u;
-    const uint32_t b_box_rows = static_cast<uint32_t>(pl.bn / pl.cta_group);
+    const uint32_t b_box_rows = static_cast<uint32_t>(pl.cta_group == 2 ? pl.bn / 2 / pl.ns : pl.bn);
     // The transposed product multiplies B^T (N x K, rows of B contiguous in
     // k) by A^T: the operands trade places.
     const void* opA = pl.swap ? B : A;
@@ -973,7 +996,8 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     gp.sk_tiles = pl.sk_tiles;
     gp.sk_iters = pl.sk_iters;
     gp.rows_a = pl.arows;
-    gp.timeout_ns = timeout_ns();
+    gp.timeout_ns = timeout_override_ns > 0 ? timeout_override_ns : timeout_ns();
+    gp.withhold_kb = withhold_kb;
 
     const bool bf16 = out_dtype == TCGEMM_OUT_BF16;
     if (out_dtype == TCGEMM_OUT_I8) {
@@ -1026,6 +1050,9 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     if (pl.swap && pl.ks == 2 && pl.bn == 128)
         return bf16 ? launch_gemm<1, 128, kStagesS128, 128, true, __nv_bfloat16, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
                     : launch_gemm<1, 128, kStagesS128, 128, true, float, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
+    if (pl.swap && pl.ks == 2 && pl.ns == 2)
+        return bf16 ? launch_gemm<1, 64, kStagesN64, 128, true, __nv_bfloat16, 0, 2, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
+                    : launch_gemm<1, 64, kStagesN64, 128, true, float, 0, 2, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
     if (pl.swap && pl.ks == 2)
         return bf16 ? launch_gemm<1, 64, kStagesN64, 128, true, __nv_bfloat16, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
                     : launch_gemm<1, 64, kStagesN64, 128, true, float, 0, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
@@ -1033,7 +1060,13 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     if (pl.bn == 64 && pl.arows == 64) TCGEMM_LAUNCH(1, 64, kStagesN64h, 64, false);
     if (pl.bn == 64) TCGEMM_LAUNCH(1, 64, kStagesN64, 128, false);
     if (pl.cta_group == 1) TCGEMM_LAUNCH(1, 256, kStages1, 128, false);
+    if (pl.bn == 224 && pl.ns == 2)
+        return bf16 ? launch_gemm<2, 224, kStages2n, 128, false, __nv_bfloat16, 0, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
+                    : launch_gemm<2, 224, kStages2n, 128, false, float, 0, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
     if (pl.bn == 224) TCGEMM_LAUNCH(2, 224, kStages2n, 128, false);
+    if (pl.ns == 2)
+        return bf16 ? launch_gemm<2, 256, kStages2, 128, false, __nv_bfloat16, 0, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev)
+                    : launch_gemm<2, 256, kStages2, 128, false, float, 0, 1, 2>(pl, ta, tb, tcm, twm, gp, stream, dev);
     TCGEMM_LAUNCH(2, 256, kStages2, 128, false);
 #undef TCGEMM_LAUNCH
 }
@@ -1400,6 +1433,26 @@ int tcgemm_selftest_timeout(void* stream, uint64_t timeout_ns_arg) {
         return TCGEMM_ERR_CUDA;
     }
     g_launches.fetch_add(1, std::memory_order_relaxed);
+    return tcgemm_check_device_status(stream, nullptr);
+}
+
+int tcgemm_selftest_withheld_load(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                                  int64_t ldb, void* C, int64_t ldc, int variant, uint64_t timeout_ns_arg,
+                                  void* stream) {
+    t_last_error[0] = '\0';
+    if (variant != TCGEMM_VARIANT_1CTA && variant != TCGEMM_VARIANT_2CTA && variant != TCGEMM_VARIANT_1CTA_N64 &&
+        variant != TCGEMM_VARIANT_2CTA_W256) {
+        set_error("the withheld-load self test runs the plain-product variants 1, 2, 4 and 5");
+        return TCGEMM_ERR_INVALID_ARG;
+    }
+    if (M <= 0 || N <= 0 || K <= 0 || timeout_ns_arg == 0 || timeout_ns_arg > 10ull * 1000 * 1000 * 1000) {
+        set_error("self test: sizes must be positive and the limit in (0, 10 s]");
+        return TCGEMM_ERR_INVALID_ARG;
+    }
+    // No split: the withheld k-block is the first one CTA 0 loads, in a whole tile.
+    const int rc = run_gemm(M, N, K, A, lda, B, ldb, C, ldc, 1.0f, 0.0f, TCGEMM_OUT_F32, stream, variant, kWsNone,
+                            nullptr, 0, Epilogue(), 0, 0, false, false, 0, timeout_ns_arg);
+    if (rc != TCGEMM_OK) return rc;
     return tcgemm_check_device_status(stream, nullptr);
 }
 

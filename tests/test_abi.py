@@ -413,6 +413,19 @@ def test_swap_pair_refusals(tc):
         tc.binding.autotune_set(64, 4096, 256, 8, in_type=1)
 
 
+def test_withheld_load_selftest_argument_errors(tc):
+    """The GEMM give-up self test checks its arguments on the host: only the
+    plain-product variants, positive sizes, a limit in (0, 10 s]."""
+    L = tc.lib()
+    args = (256, 256, 512, FAKE, 512, FAKE * 2, 512, FAKE * 4, 256)
+    assert L.tcgemm_selftest_withheld_load(*args, 6, 20_000_000, None) == 1
+    assert L.tcgemm_selftest_withheld_load(*args, 3, 20_000_000, None) == 1
+    assert L.tcgemm_selftest_withheld_load(*args, 2, 0, None) == 1
+    assert L.tcgemm_selftest_withheld_load(*args, 2, 11_000_000_000, None) == 1
+    assert L.tcgemm_selftest_withheld_load(0, 256, 512, FAKE, 512, FAKE * 2, 512, FAKE * 4, 256, 2,
+                                           20_000_000, None) == 1
+
+
 def test_noalloc_fit_decision(tc):
     """The test gemm_bf16_noalloc applies before launching: a plan fits its
     fixed scratch array when its workspace does.  Every plan of a 152-SM

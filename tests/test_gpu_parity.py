@@ -182,6 +182,30 @@ def test_hang_guard_selftest():
     H.run_case(case)
 
 
+@pytest.mark.parametrize("variant", [4, 1, 2])
+def test_gemm_gives_up_on_withheld_load(oracle_lib, variant):
+    """The GEMM's own hang guard: the producer of CTA 0 withholds its first
+    k-block, the MMA thread's wait for it runs out after 20 ms, every role of
+    every CTA gives up or finishes, drains its copies and MMAs and exits; the
+    call reports TCGEMM_ERR_TIMEOUT within a bounded time, the status word is
+    cleared, and the same GEMM run normally afterwards matches the oracle."""
+    import time
+
+    import tensor_core_matmul_gb300 as tc
+    case = gi.make_case("withheld", 256, 256, 512, alpha=1.0, beta=0.0, out_dtype=gi.OUT_F32, seed=5)
+    A, B = case.A.cuda(), case.B.cuda()
+    C = torch.zeros((case.N, case.ldc), dtype=torch.float32, device="cuda")
+    t0 = time.perf_counter()
+    st = tc.binding.selftest_withheld_load(A, B, C, M=case.M, N=case.N, K=case.K, variant=variant,
+                                           timeout_ns=20_000_000)
+    elapsed = time.perf_counter() - t0
+    assert st == 5, (st, tc.binding.last_error())
+    assert elapsed < 5.0, elapsed
+    assert tc.check_device_status()[0] == 0
+    g = H.run_case(case, variant)
+    H.compare_full(oracle_lib, case, g.result_np(), what=f"after withheld load v{variant}")
+
+
 def _split_case():
     # A handful of pair tiles and K = 8192: stream-K shares their k-blocks out
     # over all the pairs.
