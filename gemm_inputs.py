@@ -64,7 +64,7 @@ class GemmCase:
     A: torch.Tensor  # (M, lda) bf16 or FP8, host
     B: torch.Tensor  # (N, ldb) bf16 or FP8, host
     C_in: Optional[torch.Tensor]  # (N, ldc) out dtype, host; None when beta == 0
-    in_format: str = "bf16"  # "bf16", "e4m3" or "e5m2" (A and B)
+    in_format: object = "bf16"  # "bf16", "e4m3" or "e5m2" (A and B), or a pair of FP8 formats (A's, B's)
     a_col: bool = False  # A stored column-major: A is (K, lda), A[i, k] = A[k, i]
     b_row: bool = False  # B stored row-major: B is (K, ldb), B[k, j] = B[k, j]
 
@@ -201,12 +201,13 @@ def make_case(name: str, M: int, N: int, K: int, *, alpha: float = 1.0, beta: fl
     esz = 4 if out_dtype == OUT_F32 else 2
     ldc = round_up(max(M, 1), 16 // esz) if ldc is None else ldc
     if in_format != "bf16":
+        fa, fb = (in_format, in_format) if isinstance(in_format, str) else tuple(in_format)
         if kind == "normal":
-            A = normal_fp8(M, K, seed * 1000 + 1, in_format, lda)
-            B = normal_fp8(N, K, seed * 1000 + 2, in_format, ldb)
+            A = normal_fp8(M, K, seed * 1000 + 1, fa, lda)
+            B = normal_fp8(N, K, seed * 1000 + 2, fb, ldb)
         elif kind == "integer":
-            A = integer_fp8(M, K, seed * 1000 + 1, in_format, ld=lda)
-            B = integer_fp8(N, K, seed * 1000 + 2, in_format, ld=ldb)
+            A = integer_fp8(M, K, seed * 1000 + 1, fa, ld=lda)
+            B = integer_fp8(N, K, seed * 1000 + 2, fb, ld=ldb)
         else:
             raise ValueError(kind)
     elif kind == "normal":

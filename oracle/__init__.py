@@ -37,7 +37,10 @@ _lock = threading.Lock()
 # Activation codes of gemm_oracle.c (its own numbering; callers use the names).
 ACTIVATIONS = {"none": 0, "relu": 1, "gelu": 2, "gelu_tanh": 3}
 # Input kinds of gemm_oracle.c: bf16 (uint16 bit arrays) or an FP8 format (uint8 arrays).
-FP8_KINDS = {"e4m3": 1, "e5m2": 2}
+# in_format is one format name for both operands, or a pair (format of A,
+# format of B).
+FP8_KINDS = {"e4m3": 1, "e5m2": 2, ("e4m3", "e4m3"): 1, ("e5m2", "e5m2"): 2, ("e4m3", "e5m2"): 3,
+             ("e5m2", "e4m3"): 4}
 
 
 def lib_path(mutant: int = 0, build_dir: Optional[str] = None) -> str:
@@ -149,9 +152,10 @@ class Oracle:
         A = np.ascontiguousarray(A)
         B = np.ascontiguousarray(B)
         if A.dtype == np.uint8 and B.dtype == np.uint8:
-            if in_format not in FP8_KINDS:
-                raise ValueError("uint8 operands need in_format 'e4m3' or 'e5m2'")
-            return A, B, FP8_KINDS[in_format]
+            key = tuple(in_format) if isinstance(in_format, (list, tuple)) else in_format
+            if key not in FP8_KINDS:
+                raise ValueError("uint8 operands need in_format 'e4m3', 'e5m2' or a pair of them (A, B)")
+            return A, B, FP8_KINDS[key]
         if in_format not in (None, "bf16"):
             raise ValueError("in_format given for bf16 operands")
         return np.ascontiguousarray(A, dtype=np.uint16), np.ascontiguousarray(B, dtype=np.uint16), 0

@@ -66,7 +66,9 @@
  * point specification (Micikevicius et al., "FP8 Formats for Deep Learning",
  * 2022): E4M3 (bias 7, no infinities, S.1111.111 is NaN, largest 448) or E5M2
  * (bias 15, IEEE-style infinities and NaNs, largest 57344); both operands in
- * the same format; same layouts and definition as above, with per-tensor
+ * the same format, or A in one and B in the other (the two formats have
+ * different range and precision; a product of one code of each is still
+ * exact in double); same layouts and definition as above, with per-tensor
  * scale factors folded into alpha.  Every FP8 value decodes exactly to double
  * and every product of two is exact in double.
  *
@@ -161,7 +163,7 @@ typedef struct {
     int64_t M, N, K;
     const void* A; int64_t lda;
     const void* B; int64_t ldb;
-    int in_kind;        /* 0 bf16, 1 FP8 E4M3, 2 FP8 E5M2 (both operands) */
+    int in_kind;        /* 0 bf16; FP8: 1 both E4M3, 2 both E5M2, 3 A E4M3 and B E5M2, 4 A E5M2 and B E4M3 */
     int a_col, b_row;   /* 1: A column-major (A[k*lda + i]); 1: B row-major (B[k*ldb + j]) */
     const void* Cin; int64_t ldc; int cin_bf16; /* C_in dtype: 0 fp32, 1 bf16 */
     double alpha, beta;
@@ -249,15 +251,23 @@ double oracle_fp8_to_double(uint8_t v, int format) {
     return format == 0 ? e4m3_to_double(v) : e5m2_to_double(v);
 }
 
+/* The FP8 format of A (0 E4M3, 1 E5M2) and of B under an input kind. */
+static int a_fp8_format(int kind) { return (kind == 2 || kind == 4) ? 1 : 0; }
+static int b_fp8_format(int kind) {
+#if ORACLE_MUTANT == 22
+    return (kind == 2 || kind == 4) ? 1 : 0;            /* planted: B decoded in A's format */
+#else
+    return (kind == 2 || kind == 3) ? 1 : 0;
+#endif
+}
+
 static double a_at(const problem_t* p, int64_t idx) {
-    if (p->in_kind == 1) return e4m3_to_double(((const uint8_t*)p->A)[idx]);
-    if (p->in_kind == 2) return e5m2_to_double(((const uint8_t*)p->A)[idx]);
+    if (p->in_kind != 0) return oracle_fp8_to_double(((const uint8_t*)p->A)[idx], a_fp8_format(p->in_kind));
     return bf16_to_double(((const uint16_t*)p->A)[idx]);
 }
 
 static double b_at(const problem_t* p, int64_t idx) {
-    if (p->in_kind == 1) return e4m3_to_double(((const uint8_t*)p->B)[idx]);
-    if (p->in_kind == 2) return e5m2_to_double(((const uint8_t*)p->B)[idx]);
+    if (p->in_kind != 0) return oracle_fp8_to_double(((const uint8_t*)p->B)[idx], b_fp8_format(p->in_kind));
     return bf16_to_double(((const uint16_t*)p->B)[idx]);
 }
 
@@ -390,7 +400,7 @@ int oracle_gemm_epi_f64(int64_t M, int64_t N, int64_t K,
     if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || ldc < M) return -1;
     if (beta != 0.0f && Cin == NULL) return -1;
     if (bias_kind < 0 || bias_kind > 2 || (bias_kind != 0 && bias == NULL) || act < 0 || act > 3) return -1;
-    if (in_kind < 0 || in_kind > 2) return -1;
+    if (in_kind < 0 || in_kind > 4) return -1;
     problem_t p = {M, N, K, A, lda, B, ldb, in_kind, 0, 0, Cin, ldc, cin_bf16, (double)alpha, (double)beta, 0,
                    bias, bias_kind, act};
     return run_full(&p, D, nthreads);
@@ -441,7 +451,7 @@ int oracle_gemm_epi_sampled_f64(int64_t M, int64_t N, int64_t K,
     if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || ldc < M) return -1;
     if (beta != 0.0f && Cin == NULL) return -1;
     if (bias_kind < 0 || bias_kind > 2 || (bias_kind != 0 && bias == NULL) || act < 0 || act > 3) return -1;
-    if (in_kind < 0 || in_kind > 2) return -1;
+    if (in_kind < 0 || in_kind > 4) return -1;
     problem_t p = {M, N, K, A, lda, B, ldb, in_kind, 0, 0, Cin, ldc, cin_bf16, (double)alpha, (double)beta, 0,
                    bias, bias_kind, act};
     for (int64_t s = 0; s < count; ++s) {
@@ -459,7 +469,7 @@ int oracle_absdot_kind_sampled_f64(int64_t M, int64_t N, int64_t K,
                                    const void* A, int64_t lda, const void* B, int64_t ldb, int in_kind,
                                    int64_t count, const int64_t* rows, const int64_t* cols,
                                    double* out) {
-    if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || in_kind < 0 || in_kind > 2) return -1;
+    if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || in_kind < 0 || in_kind > 4) return -1;
     problem_t p = {M, N, K, A, lda, B, ldb, in_kind, 0, 0, NULL, M, 0, 1.0, 0.0, 1, NULL, 0, 0};
     for (int64_t s = 0; s < count; ++s) {
         if (rows[s] < 0 || rows[s] >= M || cols[s] < 0 || cols[s] >= N) return -1;

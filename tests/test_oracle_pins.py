@@ -445,11 +445,35 @@ def pin_layouts(o):
                     assert Di[j, i] == float(want), (a_col, b_row, i, j)
 
 
+def pin_fp8_mixed_formats(o):
+    """A in one FP8 format and B in the other: each operand is decoded in its
+    own format.  Every FP8 value is exactly a bf16 value, so D must equal, bit
+    for bit, the bf16 definition run on the torch-decoded values; and
+    integer inputs give the exact rational result."""
+    for n, (fa, fb) in enumerate((("e4m3", "e5m2"), ("e5m2", "e4m3"))):
+        M, N, K = 9, 11, 70
+        case = gi.make_case(f"f8mix{n}", M, N, K, alpha=1.25, beta=0.0, out_dtype=gi.OUT_F32, seed=720 + n,
+                            in_format=(fa, fb))
+        A8, B8 = gi.as_u8(case.A), gi.as_u8(case.B)
+        D = o.gemm_f64(M, N, K, A8, B8, None, 1.25, 0.0, in_format=(fa, fb))
+        A16 = gi.as_u16(torch.from_numpy(_fp8_values(A8[:, :K], fa).astype(np.float32)).to(torch.bfloat16))
+        B16 = gi.as_u16(torch.from_numpy(_fp8_values(B8[:, :K], fb).astype(np.float32)).to(torch.bfloat16))
+        assert np.array_equal(D, o.gemm_f64(M, N, K, A16, B16, None, 1.25, 0.0)), (fa, fb)
+        icase = gi.make_case(f"f8mixi{n}", 4, 5, 33, alpha=1.0, beta=0.0, out_dtype=gi.OUT_F32, seed=730 + n,
+                             kind="integer", in_format=(fa, fb))
+        Ai, Bi = gi.as_u8(icase.A), gi.as_u8(icase.B)
+        Di = o.gemm_f64(4, 5, 33, Ai, Bi, None, 1.0, 0.0, in_format=(fa, fb))
+        Av, Bv = _fp8_values(Ai[:, :33], fa), _fp8_values(Bi[:, :33], fb)
+        for i in range(4):
+            for j in range(5):
+                assert Di[j, i] == float(sum(Fraction(int(Av[i, k])) * Fraction(int(Bv[j, k])) for k in range(33)))
+
+
 PINS = [pin_integer_bruteforce, pin_numpy_f64, pin_identity_and_permutation, pin_closed_forms,
         pin_bf16_rounding, pin_beta_zero_ignores_c, pin_k_zero, pin_statistics,
         pin_sampled_matches_full, pin_epilogue_integer_bruteforce, pin_activations_library,
         pin_activation_odd_identity, pin_fp8_codes, pin_fp8_integer_bruteforce, pin_fp8_numpy_f64,
-        pin_quant_table, pin_quant_gemm_integer, pin_layouts]
+        pin_quant_table, pin_quant_gemm_integer, pin_layouts, pin_fp8_mixed_formats]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -479,6 +503,7 @@ MUTANTS = {
     19: "quantisation wraps instead of saturating",
     20: "zero point added after rounding",
     21: "column-major A read as row-major",
+    22: "mixed FP8 formats: B decoded in A's format",
 }
 
 
