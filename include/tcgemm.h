@@ -256,6 +256,37 @@ int gemm_fp8(int64_t M, int64_t N, int64_t K,
              float alpha, float beta, int out_dtype, int in_format,
              void* stream, int variant);
 
+/* gemm_fp8 with each operand in its own 8-bit format and a caller-owned
+ * split workspace.  a_format is A's tcgemm_fp8_format_t, b_format B's; they
+ * may differ (E4M3 x E5M2 either way: kind::f8f6f4 takes a format per
+ * operand; products stay exact and accumulate in fp32).  workspace NULL: as
+ * gemm_fp8 (the library's own split workspace when the plan needs one);
+ * otherwise, as gemm_bf16_ws: a device buffer of at least
+ * tcgemm_workspace_bytes(M, N, K, variant, SMs) bytes for 8-bit operands
+ * (tcgemm_plan_kind with in_kind 1 reports it), 256-byte aligned, owned by
+ * the caller, used by this call only until `stream` has completed it.  The
+ * automatic choice consults the tuned-choice table only when both formats
+ * agree.  Other rules and errors as gemm_fp8; an unknown format in either
+ * position -> TCGEMM_ERR_INVALID_ARG. */
+int gemm_fp8_ex(int64_t M, int64_t N, int64_t K,
+                const void* A, int64_t lda, int a_format,
+                const void* B, int64_t ldb, int b_format,
+                void* C, int64_t ldc,
+                float alpha, float beta, int out_dtype,
+                void* stream, int variant, void* workspace, int64_t workspace_bytes);
+
+/* gemm_bf16_host for 8-bit operands: A, B (both in in_format, one byte per
+ * element; lda, ldb in elements, rows multiples of 16 bytes) and C on HOST
+ * memory, copied in, multiplied with the automatic variant and C copied back
+ * on `stream`, with the device copies, ownership and completion rules of
+ * gemm_bf16_host.  Errors as gemm_bf16_host; an unknown in_format ->
+ * TCGEMM_ERR_INVALID_ARG. */
+int gemm_fp8_host(int64_t M, int64_t N, int64_t K,
+                  const void* A, int64_t lda,
+                  const void* B, int64_t ldb,
+                  void* C, int64_t ldc,
+                  float alpha, float beta, int out_dtype, int in_format, void* stream);
+
 
 
 /* Operand types of gemm_quant_i8. */

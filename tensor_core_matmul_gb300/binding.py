@@ -88,6 +88,10 @@ def lib() -> ctypes.CDLL:
     L.tcgemm_autotune_load.restype = i64
     L.gemm_fp8.argtypes = gemm_args[:-1] + [i32, p, i32]
     L.gemm_fp8.restype = i32
+    L.gemm_fp8_ex.argtypes = [i64, i64, i64, p, i64, i32, p, i64, i32, p, i64, f32, f32, i32, p, i32, p, i64]
+    L.gemm_fp8_ex.restype = i32
+    L.gemm_fp8_host.argtypes = gemm_args[:-1] + [i32, p]
+    L.gemm_fp8_host.restype = i32
     L.tcgemm_plan_kind.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int64)]
     L.tcgemm_plan_kind.restype = i32
     L.gemm_bf16_noalloc.argtypes = gemm_args + [i32]
@@ -308,6 +312,54 @@ def gemm_fp8(A, B, C, alpha: float = 1.0, beta: float = 0.0, *, M: Optional[int]
     st = gemm_fp8_raw(M, N, K, A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0), C.data_ptr(), C.stride(0),
                       float(alpha), float(beta), out, fmts[A.dtype], _stream_ptr(stream), variant)
     _check(st)
+    return C
+
+
+def gemm_fp8_ex(A, B, C, alpha: float = 1.0, beta: float = 0.0, *, M: Optional[int] = None,
+                N: Optional[int] = None, K: Optional[int] = None, stream=None, variant: int = 0, workspace=None):
+    """gemm_fp8 with A and B each in its own 8-bit format (float8_e4m3fn or
+    float8_e5m2, which may differ) and an optional caller workspace (a CUDA
+    tensor, or None for the library's own)."""
+    import torch
+    fmts = {torch.float8_e4m3fn: FP8_E4M3, torch.float8_e5m2: FP8_E5M2}
+    if not (A.is_cuda and B.is_cuda and C.is_cuda):
+        raise ValueError("A, B and C must be CUDA tensors")
+    if A.dtype not in fmts or B.dtype not in fmts:
+        raise ValueError("A and B must be float8_e4m3fn or float8_e5m2")
+    if C.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("C must be float32 or bfloat16")
+    for t in (A, B, C):
+        if t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError("A, B, C must be 2-D with unit inner stride")
+    M = C.shape[1] if M is None else M
+    N = C.shape[0] if N is None else N
+    K = A.shape[1] if K is None else K
+    out = OUT_F32 if C.dtype == torch.float32 else OUT_BF16
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().gemm_fp8_ex(M, N, K, A.data_ptr(), A.stride(0), fmts[A.dtype], B.data_ptr(), B.stride(0),
+                             fmts[B.dtype], C.data_ptr(), C.stride(0), float(alpha), float(beta), out,
+                             _stream_ptr(stream), variant, ws_ptr, ws_bytes))
+    return C
+
+
+def gemm_fp8_host(A, B, C, alpha: float = 1.0, beta: float = 0.0, *, M: Optional[int] = None,
+                  N: Optional[int] = None, K: Optional[int] = None, stream=None):
+    """The host-buffer entry point for 8-bit operands: A, B, C are CPU torch
+    tensors (A, B float8_e4m3fn or both float8_e5m2; C float32 or
+    bfloat16), pinned for asynchronous copies."""
+    import torch
+    fmts = {torch.float8_e4m3fn: FP8_E4M3, torch.float8_e5m2: FP8_E5M2}
+    if A.is_cuda or B.is_cuda or C.is_cuda:
+        raise ValueError("A, B and C must be host tensors")
+    if A.dtype not in fmts or B.dtype != A.dtype:
+        raise ValueError("A and B must both be float8_e4m3fn or both float8_e5m2")
+    M = C.shape[1] if M is None else M
+    N = C.shape[0] if N is None else N
+    K = A.shape[1] if K is None else K
+    out = OUT_F32 if C.dtype == torch.float32 else OUT_BF16
+    _check(lib().gemm_fp8_host(M, N, K, A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0), C.data_ptr(),
+                               C.stride(0), float(alpha), float(beta), out, fmts[A.dtype], _stream_ptr(stream)))
     return C
 
 

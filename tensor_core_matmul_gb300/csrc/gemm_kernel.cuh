@@ -183,7 +183,7 @@ struct GemmParams {
     int64_t ldc;
     void* C;
     float alpha, beta;
-    int in_fmt;          // 8-bit operands: 0 = E4M3, 1 = E5M2 (unused for bf16)
+    int in_fmt;          // 8-bit operands: bit 0 the MMA's A operand, bit 1 its B operand: 0 = E4M3, 1 = E5M2
     int a_mn, b_mn;      // MMA operand A / B stored MN-major (M or N contiguous; bf16 only)
     // Fused epilogue: out = act(alpha*acc + beta*C + bias[column of C]).
     const void* bias;    // one value per column of C (per row of D in the transposed product), or null
@@ -889,7 +889,8 @@ __global__ void __launch_bounds__(192, 1)
             auto issue_units = [&](auto mn_tag) {
             constexpr bool MN = decltype(mn_tag)::value;
             // Bits 15 / 16 of the instruction descriptor: A / B MN-major.
-            const uint32_t kIdesc = (IN == 1 ? idesc_f8_f32(Cfg::kBM, BN / NS, static_cast<uint32_t>(p.in_fmt) & 1u)
+            const uint32_t kIdesc = (IN == 1 ? idesc_f8_f32(Cfg::kBM, BN / NS, static_cast<uint32_t>(p.in_fmt) & 1u,
+                                                            (static_cast<uint32_t>(p.in_fmt) >> 1) & 1u)
                                              : idesc_bf16_f32(Cfg::kBM, BN / NS)) |
                                     (MN && p.a_mn ? (1u << 15) : 0u) | (MN && p.b_mn ? (1u << 16) : 0u);
             // Descriptor step per MMA: 32 bytes along a K-major row, two

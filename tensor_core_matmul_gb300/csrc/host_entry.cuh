@@ -1,6 +1,6 @@
-// The C ABI's host-buffer entry point: gemm_bf16_host copies A, B (and C
-// when beta != 0) from host memory to the library's device copies, runs the
-// GEMM there and copies C back, all on the caller's stream.  Included once,
+// The C ABI's host-buffer entry points: gemm_bf16_host and gemm_fp8_host copy
+// A, B (and C when beta != 0) from host memory to the library's device copies,
+// run the GEMM there and copy C back, all on the caller's stream.  Included once,
 // at the end of tcgemm.cu (it uses that file's validation, device probe and
 // launch path).
 #pragma once
@@ -54,20 +54,22 @@ cudaError_t copy_matrix(void* dst, const void* src, int64_t pitch, int64_t width
                              static_cast<size_t>(width), static_cast<size_t>(rows), kind, s);
 }
 
-}  // namespace
-
-extern "C" {
-
-int gemm_bf16_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
-                   void* C, int64_t ldc, float alpha, float beta, int out_dtype, void* stream) {
+// in_kind 0: bf16 operands; 1: 8-bit operands in format in_fmt (both).
+int host_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+              int64_t ldc, float alpha, float beta, int out_dtype, void* stream, int in_kind, int in_fmt) {
     t_last_error[0] = '\0';
     if (out_dtype != TCGEMM_OUT_F32 && out_dtype != TCGEMM_OUT_BF16) {
         set_error("out_dtype must be TCGEMM_OUT_F32 (0) or TCGEMM_OUT_BF16 (1), got %d", out_dtype);
         return TCGEMM_ERR_INVALID_ARG;
     }
+    if (in_kind == 1 && in_fmt != TCGEMM_FP8_E4M3 && in_fmt != TCGEMM_FP8_E5M2) {
+        set_error("unknown FP8 format %d", in_fmt);
+        return TCGEMM_ERR_INVALID_ARG;
+    }
+    const int64_t isz = in_kind == 1 ? 1 : 2;  // bytes per operand element
     // The host buffers follow the device entry points' rules (sizes, leading
     // dimensions, 16-byte alignment, no overlap of C with A or B).
-    int rc = validate(M, N, K, A, lda, B, ldb, C, ldc, out_dtype);
+    int rc = validate(M, N, K, A, lda, B, ldb, C, ldc, out_dtype, isz);
     if (rc != TCGEMM_OK) return rc;
     if (M == 0 || N == 0) return TCGEMM_OK;
     int dev = 0;
@@ -76,8 +78,8 @@ int gemm_bf16_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
     if (rc != TCGEMM_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const uint64_t esz = out_dtype == TCGEMM_OUT_F32 ? 4 : 2;
-    const uint64_t need[3] = {K > 0 ? static_cast<uint64_t>((M - 1) * lda + K) * 2 : 0,
-                              K > 0 ? static_cast<uint64_t>((N - 1) * ldb + K) * 2 : 0,
+    const uint64_t need[3] = {K > 0 ? static_cast<uint64_t>(((M - 1) * lda + K) * isz) : 0,
+                              K > 0 ? static_cast<uint64_t>(((N - 1) * ldb + K) * isz) : 0,
                               static_cast<uint64_t>((N - 1) * ldc + M) * esz};
     void* d[3] = {nullptr, nullptr, nullptr};
     rc = host_stage(dev, s, need, d);
@@ -87,15 +89,16 @@ int gemm_bf16_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
     // so C's padding on the host is never written.
     cudaError_t e = cudaSuccess;
     if (K > 0) {
-        e = copy_matrix(d[0], A, lda * 2, K * 2, M, cudaMemcpyHostToDevice, s);
-        if (e == cudaSuccess) e = copy_matrix(d[1], B, ldb * 2, K * 2, N, cudaMemcpyHostToDevice, s);
+        e = copy_matrix(d[0], A, lda * isz, K * isz, M, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = copy_matrix(d[1], B, ldb * isz, K * isz, N, cudaMemcpyHostToDevice, s);
     }
     if (e == cudaSuccess && beta != 0.0f) e = copy_matrix(d[2], C, ldc * esz, M * esz, N, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) {
         set_error("host-to-device copy: %s", cudaGetErrorString(e));
         return TCGEMM_ERR_CUDA;
     }
-    rc = run_gemm(M, N, K, d[0], lda, d[1], ldb, d[2], ldc, alpha, beta, out_dtype, stream, TCGEMM_VARIANT_AUTO);
+    rc = run_gemm(M, N, K, d[0], lda, d[1], ldb, d[2], ldc, alpha, beta, out_dtype, stream, TCGEMM_VARIANT_AUTO,
+                  kWsInternal, nullptr, 0, Epilogue(), in_kind, in_fmt);
     if (rc != TCGEMM_OK) return rc;
     e = copy_matrix(C, d[2], ldc * esz, M * esz, N, cudaMemcpyDeviceToHost, s);
     if (e != cudaSuccess) {
@@ -103,6 +106,20 @@ int gemm_bf16_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
         return TCGEMM_ERR_CUDA;
     }
     return TCGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_bf16_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                   void* C, int64_t ldc, float alpha, float beta, int out_dtype, void* stream) {
+    return host_gemm(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, stream, 0, 0);
+}
+
+int gemm_fp8_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                  void* C, int64_t ldc, float alpha, float beta, int out_dtype, int in_format, void* stream) {
+    return host_gemm(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, stream, 1, in_format);
 }
 
 }  // extern "C"

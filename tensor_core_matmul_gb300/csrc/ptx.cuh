@@ -311,10 +311,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
-// The same for kind::f8f6f4 with both operands in one 8-bit format: A and B
-// format fields 0 = E4M3, 1 = E5M2.
-__host__ __device__ constexpr uint32_t idesc_f8_f32(uint32_t M, uint32_t N, uint32_t fmt) {
-    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+// The same for kind::f8f6f4 with 8-bit float operands: the A and B format
+// fields (0 = E4M3, 1 = E5M2) are set independently, so the two operands may
+// be in different formats.
+__host__ __device__ constexpr uint32_t idesc_f8_f32(uint32_t M, uint32_t N, uint32_t fmt_a, uint32_t fmt_b) {
+    return (1u << 4) | (fmt_a << 7) | (fmt_b << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread (bf16 operands).

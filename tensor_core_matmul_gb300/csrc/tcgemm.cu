@@ -823,15 +823,17 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
              int64_t ldc, float alpha, float beta, int out_dtype, void* stream_v, int variant,
              int ws_mode = kWsInternal, void* ws = nullptr, int64_t ws_bytes = 0, const Epilogue& ep = Epilogue(),
              int in_kind = 0, int in_fmt = 0, bool a_col = false, bool b_row = false, int withhold_kb = -1,
-             uint64_t timeout_override_ns = 0) {
+             uint64_t timeout_override_ns = 0, int in_fmt_b = -1) {
     t_last_error[0] = '\0';
     if (!variant_known(variant)) {
         set_error("unknown variant %d", variant);
         return TCGEMM_ERR_INVALID_ARG;
     }
     if (in_kind == 1) {
-        if (in_fmt != TCGEMM_FP8_E4M3 && in_fmt != TCGEMM_FP8_E5M2) {
-            set_error("unknown FP8 format %d", in_fmt);
+        if (in_fmt_b < 0) in_fmt_b = in_fmt;  // both operands in one format
+        if ((in_fmt != TCGEMM_FP8_E4M3 && in_fmt != TCGEMM_FP8_E5M2) ||
+            (in_fmt_b != TCGEMM_FP8_E4M3 && in_fmt_b != TCGEMM_FP8_E5M2)) {
+            set_error("unknown FP8 format %d / %d", in_fmt, in_fmt_b);
             return TCGEMM_ERR_INVALID_ARG;
         }
         if (variant == TCGEMM_VARIANT_1CTA || variant == TCGEMM_VARIANT_SWAP_PAIR) {
@@ -863,7 +865,8 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     rc = probe_device(dev, info);
     if (rc != TCGEMM_OK) return rc;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
-    if (variant == TCGEMM_VARIANT_AUTO) {
+    // The tuned-choice table holds problems whose operands share one format.
+    if (variant == TCGEMM_VARIANT_AUTO && (in_kind == 0 || in_fmt_b == in_fmt)) {
         const TuneKey key{dev, M, N, K, in_kind, in_kind == 1 ? in_fmt : 0, out_dtype, a_col ? 1 : 0, b_row ? 1 : 0,
                           beta != 0.0f ? 1 : 0};
         variant = tuned_variant(key);
@@ -987,7 +990,11 @@ int run_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
     gp.bias = ep.bias;
     gp.bias_kind = ep.bias_kind;
     gp.act = ep.act;
-    gp.in_fmt = in_fmt;
+    // The MMA's operand formats: A's and B's, exchanged in the transposed product.
+    if (in_kind == 1) {
+        const int fa = pl.swap ? in_fmt_b : in_fmt, fb = pl.swap ? in_fmt : in_fmt_b;
+        gp.in_fmt = (fa & 1) | ((fb & 1) << 1);
+    }
     gp.qscale = ep.qscale;
     gp.qzero = static_cast<float>(ep.qzero);
     gp.a_mn = mma_a_mn ? 1 : 0;
@@ -1112,6 +1119,14 @@ int gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
              int64_t ldc, float alpha, float beta, int out_dtype, int in_format, void* stream, int variant) {
     return run_gemm(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, stream, variant, kWsInternal, nullptr, 0,
                     Epilogue(), 1, in_format);
+}
+
+int gemm_fp8_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, int a_format, const void* B,
+                int64_t ldb, int b_format, void* C, int64_t ldc, float alpha, float beta, int out_dtype, void* stream,
+                int variant, void* workspace, int64_t workspace_bytes) {
+    return run_gemm(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, stream, variant,
+                    workspace ? kWsCaller : kWsInternal, workspace, workspace_bytes, Epilogue(), 1, a_format, false,
+                    false, -1, 0, b_format);
 }
 
 int gemm_quant_i8(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,

@@ -113,6 +113,20 @@ def test_fp8_argument_errors(tc, args, fmt, variant, status):
     assert st == status, (st, tc.binding.last_error())
 
 
+@pytest.mark.parametrize("fa,fb,status", [(2, 0, 1), (0, 2, 1), (-1, 1, 1), (1, 7, 1)])
+def test_fp8_ex_argument_errors(tc, fa, fb, status):
+    """gemm_fp8_ex checks each operand's format on the host."""
+    st = tc.lib().gemm_fp8_ex(8, 8, 16, FAKE, 16, fa, FAKE * 2, 16, fb, FAKE * 4, 8, 1.0, 0.0, 0, None, 0, None, 0)
+    assert st == status, (st, tc.binding.last_error())
+    assert b"FP8 format" in tc.lib().tcgemm_last_error()
+
+
+def test_fp8_host_argument_errors(tc):
+    L = tc.lib()
+    assert L.gemm_fp8_host(8, 8, 16, FAKE, 16, FAKE * 2, 16, FAKE * 4, 8, 1.0, 0.0, 0, 5, None) == 1
+    assert L.gemm_fp8_host(8, 8, 16, FAKE, 16, FAKE * 2, 16, FAKE * 4, 8, 1.0, 0.0, 2, 0, None) == 1   # int8 out
+
+
 @pytest.mark.parametrize("in_type,scale,variant,status", [
     (3, FAKE * 16, 0, 1),          # unknown operand type
     (0, None, 0, 1),               # no row scales

@@ -126,3 +126,76 @@ def test_fp8_full_size_sampled(oracle_lib, config, fmt):
     got = run_fp8(case)
     rows, cols = gi.cell_sample_indices(case.M, case.N, 128, 128, 2, seed=9)
     compare(oracle_lib, case, got, rows=rows, cols=cols, what=f"{config} {fmt}")
+
+
+def run_fp8_ex(case: gi.GemmCase, variant: int = 0, workspace=None) -> np.ndarray:
+    import tensor_core_matmul_gb300 as tc
+    g = H.GuardedC(case)
+    tc.gemm_fp8_ex(case.A.cuda(), case.B.cuda(), g.C, case.alpha, case.beta, M=case.M, N=case.N, K=case.K,
+                   variant=variant, workspace=workspace)
+    torch.cuda.synchronize()
+    st, where = tc.check_device_status()
+    assert st == 0, f"device status {st} (role {where})"
+    g.check_guards()
+    return g.result_np()
+
+
+MIXED = [("e4m3", "e5m2"), ("e5m2", "e4m3")]
+
+
+@pytest.mark.parametrize("variant", FP8_VARIANTS)
+@pytest.mark.parametrize("fmts", MIXED, ids=["e4m3xe5m2", "e5m2xe4m3"])
+@pytest.mark.parametrize("out", [gi.OUT_F32, gi.OUT_BF16], ids=["f32", "bf16"])
+def test_fp8_mixed_formats(oracle_lib, variant, fmts, out):
+    """A in one 8-bit format and B in the other (gemm_fp8_ex): ragged shapes
+    through every FP8 kernel, the plain and the transposed product (whose
+    MMA operands are B and A, so the formats swap places too)."""
+    for n, (M, N, K, beta) in enumerate([(200, 300, 320, 0.0), (129, 520, 200, 0.5), (48, 260, 1000, 0.0)]):
+        case = gi.make_case(f"f8mix_{n}", M, N, K, alpha=0.5, beta=beta, out_dtype=out, seed=850 + 10 * n + out,
+                            in_format=fmts)
+        compare(oracle_lib, case, run_fp8_ex(case, variant), what=f"v{variant} {fmts} {case.name}")
+
+
+@pytest.mark.parametrize("variant", FP8_VARIANTS)
+@pytest.mark.parametrize("fmts", MIXED, ids=["e4m3xe5m2", "e5m2xe4m3"])
+def test_fp8_mixed_integer_exact(oracle_lib, variant, fmts):
+    case = gi.make_case("f8mix_int", 300, 270, 700, alpha=1.0, beta=0.5, out_dtype=gi.OUT_F32, seed=870,
+                        kind="integer", in_format=fmts)
+    compare(oracle_lib, case, run_fp8_ex(case, variant), exact=True, what=f"v{variant} {fmts} integer")
+
+
+def test_fp8_caller_workspace(oracle_lib):
+    """A stream-K FP8 plan with the caller's workspace equals the library's
+    own workspace bit for bit; too small a workspace is refused."""
+    import tensor_core_matmul_gb300 as tc
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    M, N, K = 600, 700, 8192
+    p = tc.plan(M, N, K, 0, sms, in_kind=1)
+    assert p["stream_k"] == 1 and p["ws_bytes"] > 0
+    case = gi.make_case("f8_ws", M, N, K, alpha=0.5, beta=0.25, out_dtype=gi.OUT_F32, seed=880,
+                        in_format=("e4m3", "e5m2"))
+    ws = torch.empty(p["ws_bytes"] + 4096, dtype=torch.uint8, device="cuda")
+    mine = run_fp8_ex(case, 0, workspace=ws)
+    theirs = run_fp8_ex(case, 0)
+    assert np.array_equal(mine.view(np.uint32), theirs.view(np.uint32))
+    compare(oracle_lib, case, mine, what="fp8 caller workspace")
+    small = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(tc.TcgemmError):
+        run_fp8_ex(case, 0, workspace=small)
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_fp8_host_buffers(oracle_lib, fmt):
+    """gemm_fp8_host on pinned host tensors equals gemm_fp8 on the device bit
+    for bit, and the oracle within the usual bound."""
+    import tensor_core_matmul_gb300 as tc
+    case = gi.make_case(f"f8host_{fmt}", 300, 520, 640, alpha=0.75, beta=0.5, out_dtype=gi.OUT_BF16, seed=890,
+                        in_format=fmt)
+    C = case.C_in.clone().pin_memory()
+    tc.gemm_fp8_host(case.A.pin_memory(), case.B.pin_memory(), C, case.alpha, case.beta, M=case.M, N=case.N,
+                     K=case.K)
+    torch.cuda.current_stream().synchronize()
+    got = C[:, :case.M].contiguous().view(torch.int16).numpy().view(np.uint16)
+    dev = run_fp8(case)
+    assert np.array_equal(got, dev), "host and device entry points differ"
+    compare(oracle_lib, case, got, what=f"fp8 host {fmt}")
