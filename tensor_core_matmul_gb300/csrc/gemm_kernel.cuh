@@ -1038,11 +1038,15 @@ __global__ void __launch_bounds__(192, 1)
 
             if (KS == 2) {
                 // K-split tile: each CTA finishes half of the tile's columns
-                // (D columns = rows of C).  It stages the fp32 partial of the
-                // other half for its peer, then adds the peer's partial of
-                // its own half (read through distributed shared memory) to
-                // its accumulator and stores.  Two partials, so the sum does
-                // not depend on which CTA adds it up.
+                // (D columns = rows of C).  It writes the fp32 partial of the
+                // other half into its peer's staging area (distributed
+                // shared memory: posted stores, one contiguous 128-byte run
+                // per warp and column), then adds the partial its peer wrote
+                // into its own staging area to its accumulator and stores.
+                // Two partials, so the sum does not depend on which CTA adds
+                // it up.  xfree: the peer has read its staging area (this
+                // CTA may write it again); xfull: the peer's partial is in
+                // this CTA's staging area.
                 const uint32_t peer = ks_rank ^ 1u;
                 const int half = ncols / 2;
                 const int mine = static_cast<int>(ks_rank) * half, theirs = static_cast<int>(peer) * half;
@@ -1050,14 +1054,16 @@ __global__ void __launch_bounds__(192, 1)
                 if (lane == 0) okx = wait_phase<true>(xfree_bar, xph ^ 1u, wctx, kWhereEpilogue) ? 1u : 0u;
                 okx = __shfl_sync(0xffffffffu, okx, 0);
                 if (!named_barrier_and(kEpiBarrier, kEpiThreads, okx != 0u)) break;
-                float* xb = reinterpret_cast<float*>(smem + Cfg::kEpiOff) + row_local;
+                const float* xb = reinterpret_cast<const float*>(smem + Cfg::kEpiOff) + row_local;
+                const uint32_t xpeer = map_to_cta(base + Cfg::kEpiOff, peer) + row_local * 4u;
 #pragma unroll 1
                 for (int c = 0; c < half; c += 32) {
                     uint32_t r[32];
                     tmem_ld32(tbase + theirs + c, r);
                     tmem_ld_wait32(r);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) xb[(c + j) * 128] = __uint_as_float(r[j]);
+                    for (int j = 0; j < 32; ++j)
+                        st_dsmem_f32(xpeer + static_cast<uint32_t>(c + j) * 512u, __uint_as_float(r[j]));
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(map_to_cta(xfull_bar, peer));
@@ -1065,7 +1071,6 @@ __global__ void __launch_bounds__(192, 1)
                 if (lane == 0) okx = wait_phase<true>(xfull_bar, xph, wctx, kWhereEpilogue) ? 1u : 0u;
                 okx = __shfl_sync(0xffffffffu, okx, 0);
                 if (!named_barrier_and(kEpiBarrier, kEpiThreads, okx != 0u)) break;
-                const uint32_t xrow = map_to_cta(base + Cfg::kEpiOff, peer) + row_local * 4u;
 #pragma unroll 1
                 for (int c = 0; c < half; c += 32) {
                     const int64_t col0 = colt + mine + c;
@@ -1074,7 +1079,7 @@ __global__ void __launch_bounds__(192, 1)
                     tmem_ld32(tbase + mine + c, r);
                     float x[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) x[j] = ld_dsmem_f32(xrow + static_cast<uint32_t>(c + j) * 512u);
+                    for (int j = 0; j < 32; ++j) x[j] = xb[(c + j) * 128];
                     tmem_ld_wait32(r);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + x[j]);

@@ -76,12 +76,10 @@ __device__ __forceinline__ uint32_t map_to_cta(uint32_t local_addr, uint32_t ran
     return r;
 }
 
-// Load one fp32 value from the shared memory of a CTA of this cluster (a
+// Store one fp32 value to the shared memory of a CTA of this cluster (a
 // shared::cluster address, from map_to_cta).
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
-    return v;
+__device__ __forceinline__ void st_dsmem_f32(uint32_t cluster_addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
 }
 
 // Arrive on a barrier given by its shared::cluster address (may be a peer's).
