@@ -724,21 +724,24 @@ __global__ void __launch_bounds__(192, 1)
         tma_prefetch_desc(&tmB);
     }
     if (warp == 2 && lane == 0) tma_prefetch_desc(&tmC);
-    // The producer's first unit is worked out before the set-up, so that the
-    // kernel parameters it reads (first reads of the launch, from memory)
-    // arrive while the barriers are initialised and TMEM is allocated.
+    // The producer's first unit.  Its parameter reads are the first of the
+    // launch and come from memory (about a microsecond): a single-CTA
+    // producer works it out before the set-up; a CTA pair's producer between
+    // arriving at the cluster barrier and waiting on it, so that the two
+    // latencies overlap.
     UnitIter pit(cluster_id, num_clusters);
     WorkUnit pu{};
     bool p_have = false;
     int p_tm = 0, p_tn = 0;
-    if (warp == 0 && lane == 0) {
+    auto first_unit = [&]() {
         pit.start(p);
         p_have = pit.next(p, pu);
         if (p_have) {
             ks_range(pu);
             tile_of(pu.tile, p_tm, p_tn);
         }
-    }
+    };
+    if (kEarlyProducer && warp == 0 && lane == 0) first_unit();
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
@@ -774,7 +777,10 @@ __global__ void __launch_bounds__(192, 1)
                 __syncthreads();
             }
         } else {
-            cluster_sync();
+            cluster_arrive();
+            if (!kEarlyProducer && warp == 0 && lane == 0) first_unit();
+            __syncwarp();
+            cluster_wait();
         }
         tc_fence_after_sync();
     }
