@@ -278,15 +278,29 @@ __device__ __forceinline__ float2 activation2(float2 v, int act) {
 // gives the same bits for the same input.
 __device__ __forceinline__ float activation(float x, int act) { return activation2(f2(x), act).x; }
 
-// In place on an even number of values held in registers.
+// In place on an even number of values held in registers.  The (warp-
+// uniform) choice of activation is taken once, outside the loops, so that no
+// code path computes an activation it does not return.
 template <int W>
 __device__ __forceinline__ void activation_n(float (&v)[W], int act) {
     static_assert(W % 2 == 0, "pairs");
+    if (act == kActRelu) {
 #pragma unroll
-    for (int j = 0; j < W; j += 2) {
-        const float2 r = activation2(make_float2(v[j], v[j + 1]), act);
-        v[j] = r.x;
-        v[j + 1] = r.y;
+        for (int j = 0; j < W; ++j) v[j] = relu(v[j]);
+    } else if (act == kActGelu) {
+#pragma unroll
+        for (int j = 0; j < W; j += 2) {
+            const float2 r = gelu_erf2(make_float2(v[j], v[j + 1]));
+            v[j] = r.x;
+            v[j + 1] = r.y;
+        }
+    } else if (act == kActGeluTanh) {
+#pragma unroll
+        for (int j = 0; j < W; j += 2) {
+            const float2 r = gelu_tanh2(make_float2(v[j], v[j + 1]));
+            v[j] = r.x;
+            v[j + 1] = r.y;
+        }
     }
 }
 
