@@ -56,19 +56,36 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+KERNEL_SOURCES = ("tensor_core_matmul_gb300/csrc/gemm_kernel.cuh", "tensor_core_matmul_gb300/csrc/ptx.cuh",
+                  "tensor_core_matmul_gb300/csrc/tcgemm.cu")
+
+
+def code_only(text: str) -> str:
+    """C++ source without its comments and blank or trailing space, so that
+    a change to a comment does not count as a change to the kernel."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
+def kernel_source_hash() -> str:
+    """sha256[:16] over the kernel sources' code (comments stripped)."""
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode())
+    return h.hexdigest()[:16]
+
+
 def profile_traffic(kernel_tag: str):
     """Per-launch DRAM bytes of the dominant kernel from the committed ncu
-    summary, or None if the kernel source changed since it was captured."""
-    import hashlib
+    summary, or None if the kernel's code changed since it was captured."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    h = hashlib.sha256()
-    for rel in ("tensor_core_matmul_gb300/csrc/gemm_kernel.cuh", "tensor_core_matmul_gb300/csrc/ptx.cuh",
-                "tensor_core_matmul_gb300/csrc/tcgemm.cu"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
-    src = h.hexdigest()[:16]
+    src = kernel_source_hash()
     for line in open(path):
         parts = line.split()
         if len(parts) >= 3 and parts[0] == kernel_tag and parts[1] == src:

@@ -647,19 +647,19 @@ constexpr uint32_t kEpiThreads = 128;
 // contiguous run of one column of C (D row-major with leading dimension ldc).
 // KS = 2 (transposed product only): a cluster of two CTAs computes each tile,
 // CTA 0 over the first half of its k-blocks and CTA 1 over the second half.
-// Each CTA then finishes half of the tile's columns: it leaves its fp32
-// partial of the other half in its shared memory (the epilogue staging area,
-// [column][row]), adds the peer's partial of its own half to its accumulator
-// through distributed shared memory, and stores.  Per CTA, xfull (one arrival
-// per epilogue warp of the peer) says the peer's partial is staged, xfree
-// says the peer has read this CTA's.
+// Each CTA then finishes half of the tile's columns: it writes its fp32
+// partial of the other half into the peer's epilogue staging area
+// ([column][row], through distributed shared memory), adds the partial the
+// peer wrote into its own staging area to its accumulator, and stores.  Per
+// CTA, xfull (one arrival per epilogue warp of the peer) says the peer's
+// partial is in this CTA's staging area, xfree says the peer has read its
+// own (so this CTA may write it again).
 // NS: MMAs per K step.  NS = 2 issues each K step as two MMAs of width
 // BN/2 that share the A operand and write the two column halves of the
-// accumulator.  Measured on GB300, a K step with one MMA into one
-// accumulator costs 150-175 clocks whatever its width (an N = 224 MMA does
-// 112 clocks of work), while two that share A and write different columns
-// overlap and run at the full rate of 8192 FLOP per clock per SM once they
-// cover 256 columns.  For a CTA pair the halves of the tile that each MMA
+// accumulator.  It doubles the MMA instructions; measured on GB300 one MMA
+// per K step already runs at the full rate of 8192 FLOP per clock per SM
+// when the K step holds at least about 116 clocks of work, so NS = 2 is an
+// option that measured slower.  For a CTA pair the halves of the tile that each MMA
 // reads must sit at the same shared-memory offset in both CTAs, so each CTA
 // loads its B rows as NS boxes: box h holds tile columns
 // [h*BN/NS + rank*BN/(2*NS), ...), and the accumulator columns stay in tile
@@ -704,8 +704,8 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
     // C chunk loads of epilogue warp q (0..3) into its buffer b.
     auto cold_bar = [&](uint32_t q, uint32_t b) { return bar0 + 8u * (2 * STAGES + 5 + 2 * q + b); };
-    const uint32_t xfull_bar = bar0 + 8u * (2 * STAGES + 13);  // KS = 2: the peer's partial is staged
-    const uint32_t xfree_bar = bar0 + 8u * (2 * STAGES + 14);  // KS = 2: the peer has read this CTA's
+    const uint32_t xfull_bar = bar0 + 8u * (2 * STAGES + 13);  // KS = 2: the peer's partial is in this CTA's area
+    const uint32_t xfree_bar = bar0 + 8u * (2 * STAGES + 14);  // KS = 2: the peer has read its own area
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kBarOff + Cfg::kNumBars * 8);
     volatile uint32_t* abort_flag = tmem_slot + 1;
     volatile uint32_t* never_flag = tmem_slot + 2;  // stays 0: drains wait for copies even after an abort
